@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Decode benchmark: one decode step of B=4 sequences through an interleaved
+8-layer CSA/HCA stack at a context of 2**20 tokens (stack_1m), on one B300.
+
+A step, for every layer in order: append the new token of each sequence to the
+layer's cache (dsv4_compress_append), then CSA layers (even) run
+dsv4_index_topk + dsv4_csa_decode and HCA layers (odd) run dsv4_hca_decode.
+Each step's launch sequence is captured once as a CUDA graph and replayed; the
+caches (2.8 GB) and every step's inputs are resident in HBM before timing. A
+step moves 393.5 MB of algorithmic bytes, more than the 126 MB L2, so no L2
+flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun every rank runs its own four
+sequences (weak scaling, no data-path collective); `value` is the tokens/s of
+all ranks. `--impl reference` times the float64 CPU oracle on a bounded sample
+of the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from compressed_sparse_kv_05_b300 import accounting, synth  # noqa: E402
+from compressed_sparse_kv_05_b300 import workloads as W  # noqa: E402
+
+METRIC = "decode tokens/s per CSA/HCA layer at 128K-1M ctx; achieved HBM GB/s vs roofline"
+WORKLOAD = "stack_1m"
+FALLBACK_HBM_GBS = 6400.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- peaks, clocks
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- device workload
+
+
+class Stack:
+    """The eight layers' caches, biases and per-step inputs, all on the device."""
+
+    def __init__(self, dsv4, layers, steps_total, seed):
+        self.dsv4 = dsv4
+        self.layers = layers
+        self.steps_total = steps_total
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed)
+        self.g = g
+        self.descs, self.caches, self.bias, self.bias_u = [], [], [], []
+        for li, L in enumerate(layers):
+            cap = L.n_comp + steps_total // L.ratio + 2
+            desc = dsv4.layer_desc(L, cap)
+            cache = dsv4.Cache(desc)
+            self._fill(L, desc, cache)
+            self.descs.append(desc)
+            self.caches.append(cache)
+            self.bias.append(0.1 * torch.randn((L.ratio, L.dim), generator=g, device="cuda"))
+            self.bias_u.append(0.1 * torch.randn((L.ratio, L.idx_dim), generator=g, device="cuda")
+                               if L.kind == "csa" else None)
+        ws_bytes = max(dsv4.dsv4_workspace_size(d, L.heads, L.idx_heads, L.topk) for d, L in zip(self.descs, layers))
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        self.topk = [torch.zeros((L.batch, max(L.topk, 1)), dtype=torch.int32, device="cuda") for L in layers]
+        # per-step inputs: one contiguous buffer per step (for one H2D copy in the end-to-end run)
+        self.in_specs = []
+        for li, L in enumerate(layers):
+            spec = [("k", (L.batch, 1, L.dim), torch.int16), ("z", (L.batch, 1, L.dim), torch.int16),
+                    ("q", (L.batch, L.heads, L.dim), torch.int16)]
+            if L.kind == "csa":
+                spec += [("u", (L.batch, 1, L.idx_dim), torch.int16), ("zu", (L.batch, 1, L.idx_dim), torch.int16),
+                         ("q_idx", (L.batch, L.idx_heads, L.idx_dim), torch.int16),
+                         ("w", (L.batch, L.idx_heads), torch.float32)]
+            self.in_specs.append(spec)
+        self.in_bytes = 0
+        self.offsets = []
+        for spec in self.in_specs:
+            offs = {}
+            for name, shape, dt in spec:
+                self.in_bytes = (self.in_bytes + 255) // 256 * 256
+                offs[name] = (self.in_bytes, shape, dt)
+                self.in_bytes += int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
+            self.offsets.append(offs)
+        self.in_bytes = (self.in_bytes + 255) // 256 * 256
+        self.inbuf = torch.empty((steps_total, self.in_bytes), dtype=torch.uint8, device="cuda")
+        for s in range(steps_total):
+            for li, L in enumerate(layers):
+                for name, (off, shape, dt) in self.offsets[li].items():
+                    t = self.view(s, li, name)
+                    if dt == torch.float32:
+                        t.copy_(torch.rand(shape, generator=g, device="cuda"))
+                    else:
+                        t.copy_(torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16).view(torch.int16))
+        self.plant_keys()
+        H_max = max(L.heads for L in layers)
+        D_max = max(L.dim for L in layers)
+        B = layers[0].batch
+        self.out = torch.zeros((len(layers), B, H_max, D_max), dtype=torch.float32, device="cuda")
+        self.lse = torch.zeros((len(layers), B, H_max), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+
+    def view(self, step, li, name):
+        off, shape, dt = self.offsets[li][name]
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
+        return self.inbuf[step, off:off + n].view(dt).view(shape)
+
+    def _fill(self, L, desc, cache):
+        """Cache contents drawn directly: pooled rows ~N(0,1) quantised by the
+        library's own quantisers, window tokens ~N(0,1) bf16, n_tokens = context."""
+        d = self.dsv4
+        g = self.g
+        n_c = L.n_comp
+        for b in range(L.batch):
+            for r0 in range(0, n_c, 65536):
+                r1 = min(n_c, r0 + 65536)
+                y = torch.randn((r1 - r0, L.dim), generator=g, device="cuda")
+                d.dsv4_quantize_kv_rows(y, r1 - r0, L.d_nope, L.d_rope, cache.k_nope[b, r0:r1], cache.k_scale[b, r0:r1],
+                                        cache.k_rope[b, r0:r1])
+                if L.kind == "csa":
+                    yi = torch.randn((r1 - r0, L.idx_dim), generator=g, device="cuda")
+                    d.dsv4_quantize_fp4_rows(yi, r1 - r0, L.idx_dim, cache.idx_codes[b, r0:r1],
+                                             cache.idx_scales[b, r0:r1])
+            cache.win_k[b].copy_(torch.randn((L.window, L.dim), generator=g, device="cuda")
+                                 .to(torch.bfloat16).view(torch.int16))
+        cache.n_tokens.fill_(L.n_tokens)
+
+    def plant_keys(self):
+        """1% of each CSA cache's blocks get a key aligned with the step-0 indexer
+        query (4 * qbar / rms(qbar), qbar = sum_h w_h q_h), quantised to FP4."""
+        d = self.dsv4
+        for li, L in enumerate(self.layers):
+            if L.kind != "csa" or L.planted_frac <= 0:
+                continue
+            cache = self.caches[li]
+            cnt = max(1, math.ceil(L.planted_frac * L.n_comp))
+            qi = self.view(0, li, "q_idx").view(torch.bfloat16).float()
+            w = self.view(0, li, "w")
+            for b in range(L.batch):
+                qbar = (w[b][:, None] * qi[b]).sum(0)
+                key = 4.0 * qbar / qbar.pow(2).mean().sqrt()
+                idx = torch.randperm(L.n_comp, generator=self.g, device="cuda")[:cnt].sort().values
+                rows = key[None].expand(cnt, -1).contiguous()
+                codes = torch.empty((cnt, L.idx_dim // 2), dtype=torch.uint8, device="cuda")
+                scales = torch.empty((cnt, L.idx_dim // 16), dtype=torch.uint8, device="cuda")
+                d.dsv4_quantize_fp4_rows(rows, cnt, L.idx_dim, codes, scales)
+                cache.idx_codes[b, idx] = codes
+                cache.idx_scales[b, idx] = scales
+
+    def step(self, s, events=None):
+        """Launch one decode step (inputs of step slot s). events: dict call -> list of (start, end)."""
+        d = self.dsv4
+        for li, L in enumerate(self.layers):
+            desc, cache = self.descs[li], self.caches[li]
+            v = lambda n: self.view(s, li, n)  # noqa: E731
+            H = L.heads
+            out = self.out[li, :, :H, :L.dim]
+            lse = self.lse[li, :, :H]
+
+            def timed(call, fn):
+                if events is None:
+                    fn()
+                    return
+                e0 = torch.cuda.Event(enable_timing=True, external=True)
+                e1 = torch.cuda.Event(enable_timing=True, external=True)
+                e0.record()
+                fn()
+                e1.record()
+                events.setdefault(call, []).append((e0, e1))
+
+            if L.kind == "csa":
+                timed("append", lambda: d.dsv4_compress_append(desc, cache, 1, v("k"), None, v("z"), self.bias[li],
+                                                               v("u"), v("zu"), self.bias_u[li]))
+                timed("index_topk", lambda: d.dsv4_index_topk(desc, cache, L.idx_heads, v("q_idx"), v("w"), L.topk,
+                                                              self.topk[li], None, self.ws))
+                timed("csa_decode", lambda: d.dsv4_csa_decode(desc, cache, H, v("q"), L.sm_scale, self.topk[li],
+                                                              L.topk, out, lse, self.ws))
+            else:
+                timed("append", lambda: d.dsv4_compress_append(desc, cache, 1, v("k"), None, v("z"), self.bias[li],
+                                                               None, None, None))
+                timed("hca_decode", lambda: d.dsv4_hca_decode(desc, cache, H, v("q"), L.sm_scale, out, lse, self.ws))
+
+
+def count_kernel_nodes(graph):
+    """Kernel nodes in a captured graph (None when the graph handle is not reachable)."""
+    try:
+        from cuda.bindings import runtime as rt
+        h = graph.raw_cuda_graph()
+        err, _, n = rt.cudaGraphGetNodes(h, 0)
+        err, nodes, n = rt.cudaGraphGetNodes(h, n)
+        kernels = 0
+        for node in nodes:
+            e, t = rt.cudaGraphNodeGetType(node)
+            if t == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+                kernels += 1
+        return kernels
+    except Exception:
+        return None
+
+
+def traffic_for(call):
+    """DRAM bytes per launch from a committed ncu capture, when the kernel source
+    has not changed since (profiles/traffic.json records the source hash)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(call)
+        if not rec:
+            return None
+        src = os.path.join(ROOT, rec["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return rec["bytes_per_launch"] if h == rec["source_sha"] else None
+    except Exception:
+        return None
+
+
+def run_ours(args, rank, world):
+    from compressed_sparse_kv_05_b300 import dsv4
+    layers = W.STACK_1M
+    B = layers[0].batch
+    K, Wm = args.steps, args.warmup
+    total = K + Wm
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    st = Stack(dsv4, layers, total + K + 2, seed=1234 + rank)
+    stream = torch.cuda.Stream()
+    # eager warm-up of every call (kernel attributes are set outside capture)
+    with torch.cuda.stream(stream):
+        st.step(total + K)
+    stream.synchronize()
+    graphs, events = [], []
+    for s in range(total):
+        g = torch.cuda.CUDAGraph()
+        ev = {}
+        with torch.cuda.graph(g, stream=stream):
+            st.step(s, ev if s >= Wm else None)
+        graphs.append(g)
+        events.append(ev)
+    probe = torch.cuda.CUDAGraph(keep_graph=True)       # captured only to count its kernel nodes
+    with torch.cuda.graph(probe, stream=stream):
+        st.step(total + K + 1)
+    kernels_per_step = count_kernel_nodes(probe)
+    for s in range(Wm):
+        graphs[s].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(Wm, total):
+        with torch.cuda.stream(stream):
+            graphs[s].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / K
+    value = world * B * 1000.0 / ms_step
+
+    # per-call durations over the timed steps
+    per_call = {}
+    for ev in events[Wm:]:
+        for call, pairs in ev.items():
+            per_call.setdefault(call, []).extend(a.elapsed_time(b) for a, b in pairs)
+    call_layer = {"append": layers[0], "index_topk": W.STACK_CSA, "csa_decode": W.STACK_CSA, "hca_decode": W.STACK_HCA}
+    share = {c: sum(v) for c, v in per_call.items()}
+    dominant = max(share, key=share.get)
+    mean_ms = statistics.mean(per_call[dominant])
+    alg = accounting.call_bytes(call_layer[dominant], dominant)
+    peak, peak_kind = hbm_peak()
+    achieved = alg / (mean_ms * 1e-3) / 1e9
+    calls = {c: {"mean_us": round(statistics.mean(v) * 1e3, 2), "launches": len(v),
+                 "GB/s": round(accounting.call_bytes(call_layer[c], c) / (statistics.mean(v) * 1e-3) / 1e9, 1)}
+             for c, v in per_call.items()}
+    step_bytes = sum(accounting.decode_step_bytes(L) + accounting.call_bytes(L, "append") for L in layers)
+
+    # end to end: per step, H2D of that step's inputs from pinned host memory,
+    # the step, and a D2H read of every layer's output
+    in_host = torch.empty((K, st.in_bytes), dtype=torch.uint8, pin_memory=True)
+    in_host.copy_(st.inbuf[Wm:total].cpu())
+    out_host = torch.empty((K,) + tuple(st.out.shape), dtype=torch.float32, pin_memory=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K):
+            s = Wm + i
+            st.inbuf[s].copy_(in_host[i], non_blocking=True)
+            graphs[s].replay()
+            out_host[i].copy_(st.out, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    wall = (time.perf_counter() - w0) * 1e3
+    e2e_ms = max(e0.elapsed_time(e1), wall)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e = {"value": round(world * B * 1000.0 / (e2e_ms / K), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(st.in_bytes), "d2h_bytes_per_step": int(st.out.numel() * 4)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3/bf16/fp4-e2m1 storage, f32 compute", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": "8 (CSA even, HCA odd)", "batch_per_gpu": B,
+                   "context": layers[0].n_tokens, "heads": 64, "kv_dim": "448 fp8 + 64 bf16",
+                   "csa": "ratio 4, indexer 64x128 fp4, top-512, window 128",
+                   "hca": "ratio 128, dense over 8192 entries, window 128",
+                   "l2": f"inputs {step_bytes / 1e6:.1f} MB per step > 126 MB L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "step_bytes": int(step_bytes),
+        "step_GBps": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
+        "step_roofline_frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "calls": calls,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic_for(dominant), "algorithmic_bytes_per_launch": int(alg)},
+        "e2e": e2e,
+        "gpu_launches": (kernels_per_step * K) if kernels_per_step is not None else None,
+        "clocks": clk,
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------- the oracle on the host
+
+
+def oracle_sample_setup():
+    """One sequence of one CSA layer and one HCA layer of stack_1m (full context),
+    caches quantised by the oracle from the seeded rows."""
+    import oracle as O
+    tag = "bench"
+    out = []
+    for li in (0, 1):
+        L = W.STACK_1M[li]
+        rows = synth.direct_rows(tag, li, L, 0)
+        p = {}
+        p["k_nope"], p["k_scale"], p["k_rope"] = O.quantize_kv_rows(rows["kv"], L.d_nope)
+        if L.kind == "csa":
+            p["idx_codes"], p["idx_scales"] = O.quantize_fp4_rows(rows["idx"])
+        win = synth.window_tokens(tag, li, L, 0)["k"]
+        ring = np.zeros((L.window, L.dim), np.uint16)
+        pos = np.arange(L.n_tokens - L.window, L.n_tokens)
+        ring[pos % L.window] = win
+        p["ring"] = ring
+        p["dec"] = synth.decode_inputs(tag, li, L)
+        out.append((L, p))
+    return out
+
+
+def oracle_sample_step(sample):
+    import oracle as O
+    for L, p in sample:
+        dec = p["dec"]
+        if L.kind == "csa":
+            sc = O.index_scores(p["idx_codes"], p["idx_scales"], dec["q_idx"][0], dec["w"][0])
+            sel = O.topk_blocks(sc, L.topk)
+            O.csa_attend(dec["q"][0], np.float32(L.sm_scale), sel, L.n_tokens, L.ratio, L.window,
+                         p["k_nope"], p["k_scale"], p["k_rope"], p["ring"])
+        else:
+            O.hca_attend(dec["q"][0], np.float32(L.sm_scale), L.n_tokens, L.ratio, L.window,
+                         p["k_nope"], p["k_scale"], p["k_rope"], p["ring"])
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        return 1
+
+
+SAMPLE_DESC = ("one sequence x (one CSA + one HCA layer) of stack_1m at the full 2**20 context per step; "
+               "tokens/s scaled to the 8-layer stack (x 1/4)")
+
+
+def cpu_baseline(steps=2):
+    sample = oracle_sample_setup()
+    oracle_sample_step(sample)
+    t = time.perf_counter()
+    for _ in range(steps):
+        oracle_sample_step(sample)
+    dt = (time.perf_counter() - t) / steps
+    return {"value": round(1.0 / (4 * dt), 4), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": SAMPLE_DESC, "s_per_sample_step": round(dt, 3)}
+
+
+def run_reference(args):
+    sample = oracle_sample_setup()
+    for _ in range(args.warmup):
+        oracle_sample_step(sample)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(sample)
+    dt = (time.perf_counter() - t) / args.steps
+    value = 1.0 / (4 * dt)
+    cb = {"value": round(value, 4), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+          "sample": SAMPLE_DESC}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 4 * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": SAMPLE_DESC}, "cpu_baseline": cb,
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

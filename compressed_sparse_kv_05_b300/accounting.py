@@ -45,3 +45,36 @@ def decode_step_bytes(layer, n_tokens=None):
     else:
         body = n_c * entry_bytes(layer)
     return layer.batch * (body + win + q + out)
+
+
+def call_bytes(layer, call, n_tokens=None):
+    """Algorithmic bytes of one library call of one decode step (all sequences).
+
+    append      : the new token's k, z (v, u, zu) read + its window-ring and
+                  pending writes, plus the entry written when it completes a
+                  block (amortised: one in `ratio` steps)
+    index_topk  : all indexer keys + indexer query and weights + top-k indices written
+    csa_decode  : selected entries + window + query + output
+    hca_decode  : every entry + window + query + output
+    """
+    n = layer.n_tokens if n_tokens is None else n_tokens
+    n_c = n // layer.ratio
+    B = layer.batch
+    per_kv = 2 if layer.separate_v else 1
+    D = layer.dim
+    win = min(layer.window, n) * D * 2 * per_kv
+    q = layer.heads * D * 2
+    out = layer.heads * D * 4
+    if call == "append":
+        tok = D * 2 * (1 + per_kv) + (2 * layer.idx_dim * 2 if layer.kind == "csa" else 0)
+        writes = D * 2 * per_kv * 2 + (2 * layer.idx_dim * 2 if layer.kind == "csa" else 0)
+        entry = (entry_bytes(layer) + (idx_key_bytes(layer) if layer.kind == "csa" else 0)) / layer.ratio
+        return B * (tok + writes + entry)
+    if call == "index_topk":
+        return B * (n_c * idx_key_bytes(layer) + layer.idx_heads * layer.idx_dim * 2 + layer.idx_heads * 4
+                    + layer.topk * 4)
+    if call == "csa_decode":
+        return B * (min(layer.topk, n_c) * entry_bytes(layer) + win + q + out)
+    if call == "hca_decode":
+        return B * (n_c * entry_bytes(layer) + win + q + out)
+    raise ValueError(call)

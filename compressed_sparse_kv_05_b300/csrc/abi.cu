@@ -1,0 +1,317 @@
+// extern "C" entry points of libdsv4 (declared in include/dsv4.h): argument
+// validation on the host, workspace carving, kernel launches on the caller's
+// stream. No entry point allocates or frees device memory.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/dsv4.h"
+#include "kernels.h"
+
+namespace dsv4 {
+namespace {
+
+constexpr int kSplitTarget = 2 * 148;  // CTAs the split-K attention aims for (2 per SM of a B300)
+constexpr int kRowTile = 16;
+constexpr int kHeadGroup = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_desc(const dsv4_layer_desc* d) {
+  if (!d) return DSV4_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->capacity < 1 || d->d_nope < 0 || d->d_rope < 0 || d->ratio < 1 || d->window < 0 ||
+      d->idx_dim < 0)
+    return DSV4_ERR_INVALID_ARG;
+  if (d->d_nope < 16 || d->d_nope > 512 || d->d_nope % 16) return DSV4_ERR_UNSUPPORTED;
+  if (d->d_rope > 128 || d->d_rope % 8) return DSV4_ERR_UNSUPPORTED;
+  if (d->d_nope + d->d_rope > 576) return DSV4_ERR_UNSUPPORTED;
+  if (d->ratio > 256 || d->window > 4096) return DSV4_ERR_UNSUPPORTED;
+  if (d->idx_dim && (d->idx_dim % 32 || d->idx_dim > 256)) return DSV4_ERR_UNSUPPORTED;
+  return DSV4_OK;
+}
+
+#define DSV4_REQ(p)                                      \
+  do {                                                   \
+    if (!(p)) return DSV4_ERR_INVALID_ARG;               \
+    if (!aligned16(p)) return DSV4_ERR_MISALIGNED;       \
+  } while (0)
+
+int check_kv_planes(const dsv4_kv_planes& p, const dsv4_layer_desc* d) {
+  DSV4_REQ(p.nope);
+  DSV4_REQ(p.scale);
+  if (d->d_rope) DSV4_REQ(p.rope);
+  return DSV4_OK;
+}
+
+int check_cache_read(const dsv4_layer_desc* d, const dsv4_cache* c) {
+  if (!c) return DSV4_ERR_INVALID_ARG;
+  int e = check_kv_planes(c->k, d);
+  if (e) return e;
+  if (d->separate_v && (e = check_kv_planes(c->v, d))) return e;
+  if (d->window) {
+    DSV4_REQ(c->win_k);
+    if (d->separate_v) DSV4_REQ(c->win_v);
+  }
+  DSV4_REQ(c->n_tokens);
+  DSV4_REQ(c->status);
+  return DSV4_OK;
+}
+
+struct AttnPlan {
+  int head_groups, splits, rows_per_split;
+  size_t ws_bytes;
+};
+
+AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
+  AttnPlan p{};
+  p.head_groups = (H + kHeadGroup - 1) / kHeadGroup;
+  const int64_t rmax = static_cast<int64_t>(n_sel > 0 ? n_sel : d->capacity) + d->window;
+  const int64_t want = (kSplitTarget + d->batch * p.head_groups - 1) / (d->batch * p.head_groups);
+  const int64_t max_splits = (rmax + kRowTile - 1) / kRowTile;
+  int64_t s = want < max_splits ? want : max_splits;
+  if (s < 1) s = 1;
+  int64_t rps = (rmax + s - 1) / s;
+  rps = (rps + kRowTile - 1) / kRowTile * kRowTile;
+  s = (rmax + rps - 1) / rps;
+  if (s < 1) s = 1;
+  p.splits = static_cast<int>(s);
+  p.rows_per_split = static_cast<int>(rps);
+  const size_t Dv = static_cast<size_t>(d->d_nope + d->d_rope);
+  p.ws_bytes = static_cast<size_t>(d->batch) * H * p.splits * (Dv + 1) * sizeof(float) + 256;
+  return p;
+}
+
+size_t index_ws_bytes(const dsv4_layer_desc* d, int Hi) {
+  return static_cast<size_t>(d->batch) * Hi * d->idx_dim * sizeof(float) + 256 +
+         static_cast<size_t>(d->batch) * d->capacity * sizeof(float) + 256;
+}
+
+template <typename F>
+void set_smem_once(std::once_flag& flag, F func, int bytes) {
+  std::call_once(flag, [&] { cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
+}
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA; }
+
+int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const uint16_t* q, float sm_scale,
+                  const int32_t* topk, int k, float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  int e = check_desc(d);
+  if (e) return e;
+  if ((e = check_cache_read(d, c))) return e;
+  if (H < 1) return DSV4_ERR_INVALID_ARG;
+  if (H > 128) return DSV4_ERR_UNSUPPORTED;
+  DSV4_REQ(q);
+  DSV4_REQ(out);
+  DSV4_REQ(ws);
+  if (lse && !aligned16(lse)) return DSV4_ERR_MISALIGNED;
+  if (!(sm_scale == sm_scale)) return DSV4_ERR_INVALID_ARG;
+  const AttnPlan p = attn_plan(d, H, k);
+  if (ws_bytes < p.ws_bytes) return DSV4_ERR_WORKSPACE;
+  AttnArgs a{};
+  a.B = d->batch; a.H = H; a.D = d->d_nope + d->d_rope; a.Dv = a.D; a.d_nope = d->d_nope; a.d_rope = d->d_rope;
+  a.ratio = d->ratio; a.window = d->window; a.capacity = d->capacity; a.separate_v = d->separate_v ? 1 : 0;
+  a.n_sel = k; a.splits = p.splits; a.rows_per_split = p.rows_per_split; a.sm_scale = sm_scale;
+  a.q = q; a.topk = topk;
+  a.k_nope = c->k.nope; a.k_scale = c->k.scale; a.k_rope = c->k.rope; a.win_k = c->win_k;
+  a.v_nope = c->v.nope; a.v_scale = c->v.scale; a.v_rope = c->v.rope; a.win_v = c->win_v;
+  a.n_tokens = c->n_tokens; a.status = c->status;
+  char* w = static_cast<char*>(ws);
+  a.part_o = reinterpret_cast<float*>(w);
+  size_t off = static_cast<size_t>(a.B) * H * p.splits * a.Dv * sizeof(float);
+  off = (off + 255) & ~static_cast<size_t>(255);
+  a.part_lse = reinterpret_cast<float*>(w + off);
+  a.out = out; a.lse = lse;
+  return launch_attention(a, p.head_groups, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace dsv4
+
+using namespace dsv4;
+
+extern "C" {
+
+int dsv4_compress_append(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t T, const uint16_t* k,
+                         const uint16_t* v, const uint16_t* z, const float* b, const uint16_t* u,
+                         const uint16_t* zu, const float* bu, void* stream) {
+  int e = check_desc(d);
+  if (e) return e;
+  if (!c || T < 0) return DSV4_ERR_INVALID_ARG;
+  if ((e = check_kv_planes(c->k, d))) return e;
+  if (d->separate_v && (e = check_kv_planes(c->v, d))) return e;
+  DSV4_REQ(c->n_tokens);
+  DSV4_REQ(c->status);
+  if (d->window) {
+    DSV4_REQ(c->win_k);
+    if (d->separate_v) DSV4_REQ(c->win_v);
+  }
+  if (d->ratio > 1) {
+    DSV4_REQ(c->pend_k);
+    DSV4_REQ(c->pend_z);
+    if (d->separate_v) DSV4_REQ(c->pend_v);
+    if (d->idx_dim) {
+      DSV4_REQ(c->pend_u);
+      DSV4_REQ(c->pend_zu);
+    }
+  }
+  if (d->idx_dim) {
+    DSV4_REQ(c->idx_codes);
+    DSV4_REQ(c->idx_scales);
+  }
+  if (T == 0) return DSV4_OK;
+  DSV4_REQ(k);
+  DSV4_REQ(z);
+  DSV4_REQ(b);
+  if (d->separate_v) DSV4_REQ(v);
+  if (d->idx_dim) {
+    DSV4_REQ(u);
+    DSV4_REQ(zu);
+    DSV4_REQ(bu);
+  }
+  AppendArgs a{};
+  a.T = T; a.ratio = d->ratio; a.window = d->window; a.capacity = d->capacity; a.d_nope = d->d_nope;
+  a.d_rope = d->d_rope; a.idx_dim = d->idx_dim; a.separate_v = d->separate_v ? 1 : 0;
+  a.k = k; a.v = v; a.z = z; a.u = u; a.zu = zu; a.bias = b; a.bias_u = bu;
+  a.k_nope = c->k.nope; a.k_scale = c->k.scale; a.k_rope = c->k.rope;
+  a.v_nope = c->v.nope; a.v_scale = c->v.scale; a.v_rope = c->v.rope;
+  a.idx_codes = c->idx_codes; a.idx_scales = c->idx_scales;
+  a.win_k = c->win_k; a.win_v = c->win_v; a.pend_k = c->pend_k; a.pend_v = c->pend_v; a.pend_z = c->pend_z;
+  a.pend_u = c->pend_u; a.pend_zu = c->pend_zu; a.n_tokens = c->n_tokens; a.status = c->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int D = d->d_nope + d->d_rope;
+  const int blocks = (d->ratio - 1 + T) / d->ratio;
+  if (blocks > 0) {
+    const size_t smem = (2 * D + d->idx_dim + 32) * sizeof(float);
+    pool_append_kernel<<<dim3(blocks, d->batch), 256, smem, st>>>(a);
+    if ((e = launch_status())) return e;
+  }
+  append_tail_kernel<<<d->batch, 256, 0, st>>>(a);
+  return launch_status();
+}
+
+int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, const uint16_t* q_idx,
+                    const float* w, int32_t k, int32_t* topk, float* scores, void* ws, size_t ws_bytes,
+                    void* stream) {
+  int e = check_desc(d);
+  if (e) return e;
+  if (!c) return DSV4_ERR_INVALID_ARG;
+  if (d->idx_dim == 0) return DSV4_ERR_INVALID_ARG;
+  if (Hi < 1 || k < 1) return DSV4_ERR_INVALID_ARG;
+  if (Hi > 128 || k > 2048) return DSV4_ERR_UNSUPPORTED;
+  DSV4_REQ(c->idx_codes);
+  DSV4_REQ(c->idx_scales);
+  DSV4_REQ(c->n_tokens);
+  DSV4_REQ(q_idx);
+  DSV4_REQ(w);
+  DSV4_REQ(topk);
+  DSV4_REQ(ws);
+  if (scores && !aligned16(scores)) return DSV4_ERR_MISALIGNED;
+  if (ws_bytes < index_ws_bytes(d, Hi)) return DSV4_ERR_WORKSPACE;
+  IndexArgs a{};
+  a.B = d->batch; a.Hi = Hi; a.Di = d->idx_dim; a.k = k; a.capacity = d->capacity; a.ratio = d->ratio;
+  a.q_idx = q_idx; a.w = w; a.idx_codes = c->idx_codes; a.idx_scales = c->idx_scales; a.n_tokens = c->n_tokens;
+  char* wp = static_cast<char*>(ws);
+  a.qdec = reinterpret_cast<float*>(wp);
+  size_t off = (static_cast<size_t>(a.B) * Hi * a.Di * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  a.scores = scores ? scores : reinterpret_cast<float*>(wp + off);
+  a.topk = topk;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  quant_query_fp4_kernel<<<a.B * Hi, 32, 0, st>>>(a);
+  if ((e = launch_status())) return e;
+  const int hp = (Hi + 15) & ~15;
+  const size_t smem = static_cast<size_t>(hp) * (a.Di + 1) * sizeof(float);
+  static std::once_flag flag;
+  set_smem_once(flag, index_scores_kernel, 200 * 1024);
+  int tiles = (d->capacity + 127) / 128;
+  const int per_seq = (4 * 148 + a.B - 1) / a.B;
+  if (tiles > per_seq) tiles = per_seq;
+  index_scores_kernel<<<dim3(tiles, a.B), 128, smem, st>>>(a);
+  if ((e = launch_status())) return e;
+  topk_select_kernel<<<a.B, 1024, 0, st>>>(a);
+  return launch_status();
+}
+
+int dsv4_csa_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q, float sm_scale,
+                    const int32_t* topk, int32_t k, float* out, float* lse, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (k < 1) return DSV4_ERR_INVALID_ARG;
+  if (k > 2048) return DSV4_ERR_UNSUPPORTED;
+  if (!topk) return DSV4_ERR_INVALID_ARG;
+  if (!aligned16(topk)) return DSV4_ERR_MISALIGNED;
+  return decode_common(d, c, H, q, sm_scale, topk, k, out, lse, ws, ws_bytes, stream);
+}
+
+int dsv4_hca_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q, float sm_scale,
+                    float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return decode_common(d, c, H, q, sm_scale, nullptr, 0, out, lse, ws, ws_bytes, stream);
+}
+
+size_t dsv4_workspace_size(const dsv4_layer_desc* d, int32_t H, int32_t Hi, int32_t k) {
+  if (check_desc(d) || H < 1 || H > 128 || Hi < 0 || Hi > 128 || k < 0 || k > 2048) return 0;
+  size_t need = attn_plan(d, H, 0).ws_bytes;
+  if (k > 0) {
+    const size_t csa = attn_plan(d, H, k).ws_bytes;
+    if (csa > need) need = csa;
+  }
+  if (d->idx_dim && Hi > 0) {
+    const size_t idx = index_ws_bytes(d, Hi);
+    if (idx > need) need = idx;
+  }
+  return need;
+}
+
+int dsv4_read_status(const dsv4_cache* c, void* stream) {
+  if (!c || !c->status) return DSV4_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, c->status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DSV4_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DSV4_ERR_CUDA;
+  if (cudaMemsetAsync(c->status, 0, sizeof(int32_t), st) != cudaSuccess) return DSV4_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DSV4_ERR_CUDA;
+  return h;
+}
+
+int dsv4_quantize_kv_rows(const float* y, int64_t rows, int32_t d_nope, int32_t d_rope, uint8_t* nope, float* scale,
+                          uint16_t* rope, void* stream) {
+  if (rows < 0) return DSV4_ERR_INVALID_ARG;
+  if (d_nope < 16 || d_nope > 512 || d_nope % 16 || d_rope < 0 || d_rope > 128 || d_rope % 8)
+    return DSV4_ERR_UNSUPPORTED;
+  if (rows == 0) return DSV4_OK;
+  DSV4_REQ(y);
+  DSV4_REQ(nope);
+  DSV4_REQ(scale);
+  if (d_rope) DSV4_REQ(rope);
+  const int64_t blocks = (rows + 7) / 8;
+  quant_kv_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      y, rows, d_nope, d_rope, nope, scale, rope);
+  return launch_status();
+}
+
+int dsv4_quantize_fp4_rows(const float* y, int64_t rows, int32_t cols, uint8_t* codes, uint8_t* scales,
+                           void* stream) {
+  if (rows < 0) return DSV4_ERR_INVALID_ARG;
+  if (cols < 32 || cols % 32 || cols > 4096) return DSV4_ERR_UNSUPPORTED;
+  if (rows == 0) return DSV4_OK;
+  DSV4_REQ(y);
+  DSV4_REQ(codes);
+  DSV4_REQ(scales);
+  const int64_t n = rows * (cols / 16);
+  quant_fp4_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      y, rows, cols, codes, scales);
+  return launch_status();
+}
+
+int dsv4_pool_rows(const uint16_t* x, const uint16_t* z, const float* b, int64_t blocks, int32_t ratio, int32_t dim,
+                   float* y, void* stream) {
+  if (blocks < 0 || ratio < 1 || dim < 1) return DSV4_ERR_INVALID_ARG;
+  if (ratio > 256 || dim % 8 || blocks > 0x7FFFFFFF) return DSV4_ERR_UNSUPPORTED;
+  if (blocks == 0) return DSV4_OK;
+  DSV4_REQ(x);
+  DSV4_REQ(z);
+  DSV4_REQ(b);
+  DSV4_REQ(y);
+  pool_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(x, z, b, ratio, dim, y);
+  return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,235 @@
+// CSA / HCA decode attention: one softmax over (selected or all) compressed
+// entries together with the raw sliding-window tokens.
+//
+// vibecoco.ai, "DeepSeek V4 agent architecture", section
+// "混合注意力：两种压缩，交替使用": CSA attends over the top-k compressed blocks
+// plus a sliding-window branch of recent raw tokens; HCA attends densely over
+// every compressed entry. pnsm.cn, "DeepSeek V4 架构深度解析…", section 2.1
+// "CSA：压缩稀疏注意力": the window and the compressed KV feed one attention.
+//
+// Rows of sequence b are numbered: first the compressed entries (the top-k
+// list for CSA, every entry for HCA), then the window tokens oldest first.
+// attn_split_kernel gives each CTA a contiguous range of rows (a split) and
+// all heads of a head group, runs an online softmax over it in fp32 and writes
+// the normalised partial output with its log-sum-exp; attn_merge_kernel
+// combines the splits: o = sum_s exp(lse_s - lse) o_s, lse = log sum_s exp(lse_s).
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dsv4 {
+
+namespace {
+constexpr int RT = 16;        // rows per tile
+constexpr int NT = 256;       // threads per CTA
+constexpr int HG = 64;        // max heads per CTA (head group)
+
+// Value of element d of row r of sequence b (K or V side).
+struct RowSrc {
+  const uint8_t* nope;
+  const float* scale;
+  const uint16_t* rope;
+  const uint16_t* win;
+};
+}  // namespace
+
+// grid (splits, B, head groups), block 256.
+// dynamic smem: q bf16 [HP][D], kT fp32 [D][RT], v fp32 [RT][Dv], s fp32 [HP][RT], row ids
+template <int HP, int ACC>
+__global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  constexpr int TPH = NT / HP;
+  const int D = a.D, Dv = a.Dv;
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smraw);
+  float* kT = reinterpret_cast<float*>(smraw + ((HP * D * 2 + 15) & ~15));
+  float* vs = kT + D * RT;
+  float* ss = vs + RT * Dv;
+  int64_t* rowid = reinterpret_cast<int64_t*>(ss + HP * RT);   // >= 0: entry, < 0: -(window slot) - 1
+
+  const int split = blockIdx.x, b = blockIdx.y;
+  const int h0 = blockIdx.z * HG;
+  const int tid = threadIdx.x;
+
+  const int64_t n_tok = a.n_tokens[b];
+  const int64_t n_c = n_tok / a.ratio < a.capacity ? n_tok / a.ratio : a.capacity;
+  const int64_t n_win = n_tok < a.window ? n_tok : a.window;
+  const int64_t n_main = a.n_sel > 0 ? a.n_sel : n_c;
+  const int64_t R = n_main + n_win;
+  const int64_t r0 = static_cast<int64_t>(split) * a.rows_per_split;
+  int64_t r1 = r0 + a.rows_per_split;
+  if (r1 > R) r1 = R;
+
+  for (int i = tid; i < HP * D; i += NT) {
+    const int h = h0 + i / D;
+    qs[i] = h < a.H ? a.q[(static_cast<int64_t>(b) * a.H + h) * D + (i % D)] : 0;
+  }
+
+  const RowSrc K{a.k_nope, a.k_scale, a.k_rope, a.win_k};
+  const RowSrc V = a.separate_v ? RowSrc{a.v_nope, a.v_scale, a.v_rope, a.win_v} : K;
+
+  const int my_h = tid / TPH, my_u = tid % TPH;
+  float m = -INFINITY, l = 0.f;
+  float acc[ACC];
+#pragma unroll
+  for (int i = 0; i < ACC; ++i) acc[i] = 0.f;
+
+  for (int64_t t0 = r0; t0 < r1; t0 += RT) {
+    __syncthreads();
+    if (tid < RT) {
+      const int64_t r = t0 + tid;
+      int64_t id = INT64_MIN;   // masked row
+      if (r < r1) {
+        if (r < n_main) {
+          int64_t e = a.n_sel > 0 ? a.topk[static_cast<int64_t>(b) * a.n_sel + r] : r;
+          if (e < -1 || e >= n_c) {
+            atomicOr(a.status, DSV4_STATUS_BAD_INDEX);
+            e = -1;
+          }
+          if (e >= 0) id = e;
+        } else {
+          const int64_t pos = n_tok - n_win + (r - n_main);
+          id = -(pos % a.window) - 1;
+        }
+      }
+      rowid[tid] = id;
+    }
+    __syncthreads();
+    // dequantise the tile: kT[d][r], vs[r][d]
+    for (int i = tid; i < RT * D; i += NT) {
+      const int r = i / D, d = i % D;
+      const int64_t id = rowid[r];
+      float kval = 0.f, vval = 0.f;
+      if (id >= 0) {
+        const int64_t e = static_cast<int64_t>(b) * a.capacity + id;
+        if (d < a.d_nope) {
+          kval = e4m3_to_f32(K.nope[e * a.d_nope + d]) * K.scale[e];
+          vval = a.separate_v ? e4m3_to_f32(V.nope[e * a.d_nope + d]) * V.scale[e] : kval;
+        } else {
+          kval = bf16_to_f32(K.rope[e * a.d_rope + (d - a.d_nope)]);
+          vval = a.separate_v ? bf16_to_f32(V.rope[e * a.d_rope + (d - a.d_nope)]) : kval;
+        }
+      } else if (id != INT64_MIN) {
+        const int64_t slot = static_cast<int64_t>(b) * a.window + (-id - 1);
+        kval = bf16_to_f32(K.win[slot * D + d]);
+        vval = a.separate_v ? bf16_to_f32(V.win[slot * D + d]) : kval;
+      }
+      kT[d * RT + r] = kval;
+      if (d < Dv) vs[r * Dv + d] = vval;
+    }
+    __syncthreads();
+    // scores: thread -> row (tid % RT), heads tid / RT + 16 j
+    {
+      const int r = tid % RT;
+      const bool valid = rowid[r] != INT64_MIN;
+      for (int h = tid / RT; h < HP; h += NT / RT) {
+        const uint16_t* qr = qs + h * D;
+        float dot = 0.f;
+        for (int d = 0; d < D; ++d) dot = fmaf(bf16_to_f32(qr[d]), kT[d * RT + r], dot);
+        ss[h * RT + r] = valid ? dot * a.sm_scale : -INFINITY;
+      }
+    }
+    __syncthreads();
+    // online softmax + PV for (my_h, my dims)
+    {
+      const float* sr = ss + my_h * RT;
+      float mx = m;
+#pragma unroll
+      for (int r = 0; r < RT; ++r) mx = fmaxf(mx, sr[r]);
+      if (mx != -INFINITY) {
+        const float alpha = expf(m - mx);   // m = -inf -> 0
+        float p[RT];
+        float psum = 0.f;
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          p[r] = expf(sr[r] - mx);
+          psum += p[r];
+        }
+        l = l * alpha + psum;
+        m = mx;
+#pragma unroll
+        for (int i = 0; i < ACC; ++i) {
+          const int d = my_u + TPH * i;
+          float v = acc[i] * alpha;
+          if (d < Dv) {
+#pragma unroll
+            for (int r = 0; r < RT; ++r) v = fmaf(p[r], vs[r * Dv + d], v);
+          }
+          acc[i] = v;
+        }
+      }
+    }
+  }
+  const int h = h0 + my_h;
+  if (h < a.H && my_h < HP) {
+    const int64_t base = (static_cast<int64_t>(b) * a.H + h) * a.splits + split;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int i = 0; i < ACC; ++i) {
+      const int d = my_u + TPH * i;
+      if (d < Dv) a.part_o[base * Dv + d] = acc[i] * inv;
+    }
+    if (my_u == 0) a.part_lse[base] = l > 0.f ? m + logf(l) : -INFINITY;
+  }
+}
+
+// grid (B * H), block 128
+__global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+  const int64_t bh = blockIdx.x;
+  const float* lse = a.part_lse + bh * a.splits;
+  float mx = -INFINITY;
+  for (int s = 0; s < a.splits; ++s) mx = fmaxf(mx, lse[s]);
+  float tot = 0.f;
+  if (mx != -INFINITY)
+    for (int s = 0; s < a.splits; ++s) tot += expf(lse[s] - mx);
+  for (int d = threadIdx.x; d < a.Dv; d += blockDim.x) {
+    float o = 0.f;
+    if (tot > 0.f) {
+      for (int s = 0; s < a.splits; ++s) {
+        const float w = expf(lse[s] - mx);
+        if (w > 0.f) o = fmaf(w, a.part_o[(bh * a.splits + s) * a.Dv + d], o);
+      }
+      o /= tot;
+    }
+    a.out[bh * a.Dv + d] = o;
+  }
+  if (threadIdx.x == 0 && a.lse) a.lse[bh] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+}
+
+namespace {
+int launch_status() { return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA; }
+
+template <int HP, int ACC>
+int launch_split(const AttnArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
+  static std::once_flag flag;
+  std::call_once(flag, [] {
+    cudaFuncSetAttribute(attn_split_kernel<HP, ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  });
+  attn_split_kernel<HP, ACC><<<grid, NT, smem, st>>>(a);
+  return launch_status();
+}
+}  // namespace
+
+int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
+  const int hp = a.H >= 64 ? 64 : (a.H > 16 ? 32 : 16);
+  const int tph = NT / hp;
+  const int need = (a.Dv + tph - 1) / tph;
+  const size_t smem = ((static_cast<size_t>(hp) * a.D * 2 + 15) & ~static_cast<size_t>(15)) +
+                      (static_cast<size_t>(a.D) * RT + RT * a.Dv + hp * RT) * sizeof(float) + RT * sizeof(int64_t);
+  const dim3 grid(a.splits, a.B, head_groups);
+  int e;
+  if (hp == 16)
+    e = need <= 8 ? launch_split<16, 8>(a, grid, smem, st)
+        : need <= 16 ? launch_split<16, 16>(a, grid, smem, st) : launch_split<16, 36>(a, grid, smem, st);
+  else if (hp == 32)
+    e = need <= 16 ? launch_split<32, 16>(a, grid, smem, st)
+        : need <= 32 ? launch_split<32, 32>(a, grid, smem, st) : launch_split<32, 72>(a, grid, smem, st);
+  else
+    e = need <= 32 ? launch_split<64, 32>(a, grid, smem, st)
+        : need <= 64 ? launch_split<64, 64>(a, grid, smem, st) : launch_split<64, 144>(a, grid, smem, st);
+  if (e) return e;
+  attn_merge_kernel<<<a.B * a.H, 128, 0, st>>>(a);
+  return launch_status();
+}
+
+}  // namespace dsv4

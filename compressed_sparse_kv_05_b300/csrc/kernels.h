@@ -1,0 +1,71 @@
+// Internal declarations shared by the libdsv4 translation units: argument
+// blocks handed to the kernels and the kernels themselves.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsv4 {
+
+struct AppendArgs {
+  int T, ratio, window, capacity, d_nope, d_rope, idx_dim, separate_v;
+  const uint16_t *k, *v, *z, *u, *zu;
+  const float *bias, *bias_u;
+  uint8_t* k_nope;
+  float* k_scale;
+  uint16_t* k_rope;
+  uint8_t* v_nope;
+  float* v_scale;
+  uint16_t* v_rope;
+  uint8_t *idx_codes, *idx_scales;
+  uint16_t *win_k, *win_v, *pend_k, *pend_v, *pend_z, *pend_u, *pend_zu;
+  int64_t* n_tokens;
+  int32_t* status;
+};
+
+__global__ void pool_append_kernel(AppendArgs a);
+__global__ void append_tail_kernel(AppendArgs a);
+__global__ void quant_kv_rows_kernel(const float* y, int64_t rows, int d_nope, int d_rope, uint8_t* nope,
+                                     float* scale, uint16_t* rope);
+__global__ void quant_fp4_rows_kernel(const float* y, int64_t rows, int cols, uint8_t* codes, uint8_t* scales);
+__global__ void pool_rows_kernel(const uint16_t* x, const uint16_t* z, const float* bias, int ratio, int dim,
+                                 float* y);
+
+// ---- indexer + top-k
+struct IndexArgs {
+  int B, Hi, Di, k, capacity, ratio;
+  const uint16_t* q_idx;   // [B][Hi][Di] bf16
+  const float* w;          // [B][Hi]
+  const uint8_t* idx_codes;
+  const uint8_t* idx_scales;
+  const int64_t* n_tokens;
+  float* qdec;             // [B][Hi][Di] decoded FP4 query (workspace)
+  float* scores;           // [B][capacity]
+  int32_t* topk;           // [B][k]
+};
+__global__ void quant_query_fp4_kernel(IndexArgs a);
+__global__ void index_scores_kernel(IndexArgs a);
+__global__ void topk_select_kernel(IndexArgs a);
+
+// ---- attention
+struct AttnArgs {
+  int B, H, D, Dv, d_nope, d_rope, ratio, window, capacity, separate_v;
+  int n_sel;               // top-k width (CSA) or 0 for HCA (every entry)
+  int splits, rows_per_split;
+  float sm_scale;
+  const uint16_t* q;
+  const int32_t* topk;
+  const uint8_t *k_nope, *v_nope;
+  const float *k_scale, *v_scale;
+  const uint16_t *k_rope, *v_rope, *win_k, *win_v;
+  const int64_t* n_tokens;
+  int32_t* status;
+  float* part_o;           // [B][H][splits][Dv]
+  float* part_lse;         // [B][H][splits]
+  float* out;              // [B][H][Dv]
+  float* lse;              // [B][H] or null
+};
+// launches the split kernel over (splits, B, head_groups) and the merge; returns a DSV4 status
+int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st);
+
+}  // namespace dsv4

@@ -82,7 +82,7 @@ def quantize_kv_rows(y, d_nope):
     """
     y = np.asarray(y, np.float32)
     yn = y[:, :d_nope]
-    amax = np.abs(yn).max(axis=1) if d_nope else np.zeros(len(y), np.float32)
+    amax = np.abs(yn).max(axis=1, initial=np.float32(0))
     s = (amax / np.float32(448.0)).astype(np.float32)
     safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
     q = (yn / safe[:, None]).astype(np.float32)
@@ -102,7 +102,7 @@ def quantize_fp4_rows(y):
     y = np.asarray(y, np.float32)
     R, C = y.shape
     blocks = y.reshape(R, C // 16, 16)
-    amax = np.abs(blocks).max(axis=2)
+    amax = np.abs(blocks).max(axis=2, initial=np.float32(0))
     s_code = e4m3_encode((amax / np.float32(6.0)).astype(np.float32))
     s = e4m3_decode(s_code).astype(np.float32)
     safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)

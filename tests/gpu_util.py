@@ -1,0 +1,246 @@
+"""Helpers for the GPU parity tests: build caches on the device through the C ABI
+and on the host through the oracle from the same seeded inputs, and compare.
+
+No value computed by the CUDA path is ever fed to the oracle: device caches are
+either built by the library from the synthetic tokens (and compared with the
+oracle's own cache built from the same tokens), or filled with planes the
+oracle quantised from synthetic rows.
+"""
+import multiprocessing as mp
+
+import numpy as np
+import torch
+
+import oracle as O
+from compressed_sparse_kv_05_b300 import dsv4, synth
+
+DEV = "cuda"
+
+
+def to_dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(DEV)
+
+
+def to_host(t, dtype=None):
+    a = t.detach().cpu().numpy()
+    if dtype is not None:
+        a = a.view(dtype)
+    return a
+
+
+# ----------------------------------------------------------------------------- comparisons
+
+
+def row_rel_err(got, ref):
+    """max_d |g - o| / max_d |o| per row (last axis); 0 for an all-zero reference row equal to got."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    num = np.abs(got - ref).max(axis=-1)
+    den = np.abs(ref).max(axis=-1)
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+
+
+def _near_boundary(q, encode, rel=2.0 ** -20):
+    """True where an encoder's decision flips within a relative perturbation of q."""
+    q = np.asarray(q, np.float32)
+    lo = (q.astype(np.float64) * (1 - rel)).astype(np.float32)
+    hi = (q.astype(np.float64) * (1 + rel)).astype(np.float32)
+    return encode(lo) != encode(hi)
+
+
+def compare_fp8_entries(g_codes, g_scale, o_codes, o_scale, o_pooled, d_nope, max_frac=1e-4):
+    """Byte comparison of FP8 entries with the stated exceptions: a code may differ
+    only where the oracle's own value y/s sits within 2^-20 of a rounding
+    boundary; a scale may differ only within 2^-20 relative (an amax that
+    differs in its last bit), and such a row's decoded values must stay within
+    one code step of the oracle's pooled value. Returns (mismatched codes,
+    mismatched rows)."""
+    g_codes = np.asarray(g_codes).reshape(-1, d_nope)
+    o_codes = np.asarray(o_codes).reshape(-1, d_nope)
+    g_scale = np.asarray(g_scale, np.float32).reshape(-1)
+    o_scale = np.asarray(o_scale, np.float32).reshape(-1)
+    y = np.asarray(o_pooled, np.float32).reshape(-1, o_pooled.shape[-1])[:, :d_nope]
+    same_s = g_scale == o_scale
+    bad_rows = np.nonzero(~same_s)[0]
+    for r in bad_rows:
+        assert abs(float(g_scale[r]) / float(o_scale[r]) - 1) <= 2.0 ** -20, (r, g_scale[r], o_scale[r])
+        deq = O.e4m3_decode(g_codes[r]) * float(g_scale[r])
+        step = np.maximum(np.abs(y[r]) * 2.0 ** -3, 2.0 ** -9 * float(o_scale[r]))
+        assert (np.abs(deq - y[r]) <= step).all(), r
+    diff = (g_codes != o_codes) & same_s[:, None]
+    rows, cols = np.nonzero(diff)
+    if rows.size:
+        s = o_scale[rows]
+        q = (y[rows, cols] / s).astype(np.float32)
+        assert _near_boundary(q, O.e4m3_encode).all(), "FP8 code differs away from a rounding boundary"
+        lo = O.e4m3_encode((q.astype(np.float64) * (1 - 2.0 ** -20)).astype(np.float32))
+        hi = O.e4m3_encode((q.astype(np.float64) * (1 + 2.0 ** -20)).astype(np.float32))
+        gc = g_codes[rows, cols]
+        assert ((gc == lo) | (gc == hi)).all()
+    assert rows.size + bad_rows.size * d_nope <= max(8, max_frac * g_codes.size), (rows.size, bad_rows.size)
+    return rows.size, bad_rows.size
+
+
+def compare_fp4_rows(g_codes, g_scales, o_codes, o_scales, o_pooled, max_frac=1e-4):
+    """As compare_fp8_entries for FP4 rows (per-16 e4m3 scales)."""
+    R = o_pooled.shape[0]
+    C = o_pooled.shape[1]
+    g_codes = np.asarray(g_codes).reshape(R, C // 2)
+    o_codes = np.asarray(o_codes).reshape(R, C // 2)
+    g_scales = np.asarray(g_scales).reshape(R, C // 16)
+    o_scales = np.asarray(o_scales).reshape(R, C // 16)
+    y = np.asarray(o_pooled, np.float32).reshape(R, C // 16, 16)
+    amax6 = (np.abs(y).max(axis=2) / np.float32(6.0)).astype(np.float32)
+    sdiff = g_scales != o_scales
+    if sdiff.any():
+        assert _near_boundary(amax6[sdiff], O.e4m3_encode).all(), "FP4 scale differs away from a boundary"
+    gn = np.stack([g_codes & 0xF, g_codes >> 4], axis=-1).reshape(R, C // 16, 16)
+    on = np.stack([o_codes & 0xF, o_codes >> 4], axis=-1).reshape(R, C // 16, 16)
+    diff = (gn != on) & ~sdiff[:, :, None]
+    r, b, i = np.nonzero(diff)
+    if r.size:
+        s = O.e4m3_decode(o_scales[r, b]).astype(np.float32)
+        q = (y[r, b, i] / s).astype(np.float32)
+        assert _near_boundary(q, O.e2m1_encode).all(), "FP4 code differs away from a rounding boundary"
+    assert r.size + int(sdiff.sum()) * 16 <= max(8, max_frac * gn.size), (r.size, int(sdiff.sum()))
+    return r.size, int(sdiff.sum())
+
+
+def compare_bf16(g_bits, o_bits, o_pooled, max_frac=1e-4):
+    """bf16 bytes identical except where the oracle's pooled value sits within
+    2^-20 of a bf16 rounding boundary (the two sides pool in different precision)."""
+    g = np.asarray(g_bits).reshape(-1)
+    o = np.asarray(o_bits).reshape(-1)
+    y = np.asarray(o_pooled, np.float32).reshape(-1)
+    diff = g != o
+    if diff.any():
+        assert _near_boundary(y[diff], O.bf16_encode).all(), "bf16 differs away from a rounding boundary"
+    assert diff.sum() <= max(8, max_frac * g.size)
+    return int(diff.sum())
+
+
+def check_topk(g_topk, o_scores, o_topk, k, gap_rel=1e-6):
+    """Top-k set parity: identical, except when the oracle's k-th score gap is
+    below gap_rel relative; then every differing member must lie in the tied
+    boundary band. Order must be ascending with -1 padding at the end."""
+    g = np.asarray(g_topk)
+    valid = g[g >= 0]
+    assert (np.diff(valid) > 0).all(), "top-k not strictly ascending"
+    assert (g[len(valid):] == -1).all()
+    if np.array_equal(g, o_topk):
+        return 0
+    gap = O.topk_boundary_gap(o_scores, k)
+    assert gap < gap_rel, f"top-k differs with boundary gap {gap}"
+    kth = np.sort(o_scores)[::-1][k - 1]
+    band = np.abs(o_scores - kth) <= gap_rel * abs(kth) * 4
+    sym = set(valid.tolist()) ^ set(o_topk[o_topk >= 0].tolist())
+    assert all(band[i] for i in sym)
+    return len(sym)
+
+
+# ----------------------------------------------------------------------------- caches built by the library from tokens
+
+
+def gpu_stream_cache(layer, tag, layer_id, n_tokens, chunks, capacity=None):
+    """Append synthetic tokens [0, n_tokens) in the given chunk sizes (cycled)
+    through dsv4_compress_append. Returns (desc, cache)."""
+    cap = capacity if capacity is not None else max(1, n_tokens // layer.ratio + 1)
+    desc = dsv4.layer_desc(layer, cap)
+    cache = dsv4.Cache(desc)
+    b = to_dev(synth.position_bias(tag, layer_id, layer, "b"))
+    bu = to_dev(synth.position_bias(tag, layer_id, layer, "bu")) if desc.idx_dim else None
+    t0, ci = 0, 0
+    while t0 < n_tokens:
+        t1 = min(n_tokens, t0 + chunks[ci % len(chunks)])
+        ci += 1
+        toks = {k: to_dev(v) for k, v in synth.token_stream(tag, layer_id, layer, layer.batch, t0, t1).items()}
+        dsv4.dsv4_compress_append(desc, cache, t1 - t0, toks["k"], toks.get("v"), toks["z"], b,
+                                  toks.get("u"), toks.get("zu"), bu)
+        t0 = t1
+    torch.cuda.synchronize()
+    return desc, cache
+
+
+def oracle_stream_cache(layer, tag, layer_id, n_tokens, seq):
+    toks = synth.token_stream(tag, layer_id, layer, layer.batch, 0, n_tokens)
+    b = synth.position_bias(tag, layer_id, layer, "b")
+    bu = synth.position_bias(tag, layer_id, layer, "bu") if layer.idx_dim else None
+    c = O.build_cache(toks["k"][seq], toks["z"][seq], b, layer.ratio, layer.d_nope, layer.window,
+                      toks["v"][seq] if layer.separate_v else None,
+                      toks["u"][seq] if layer.idx_dim else None, toks["zu"][seq] if layer.idx_dim else None, bu)
+    D = layer.dim
+    W = layer.window
+    ring = np.zeros((max(W, 1), D), np.uint16)
+    for s, tok in c["win_k"].items():
+        ring[s] = tok
+    c["ring_k"] = ring
+    if layer.separate_v:
+        ringv = np.zeros((max(W, 1), D), np.uint16)
+        for s, tok in c["win_v"].items():
+            ringv[s] = tok
+        c["ring_v"] = ringv
+    c["tokens"] = {k: v[seq] for k, v in toks.items()}
+    return c
+
+
+# ----------------------------------------------------------------------------- caches drawn directly
+
+
+def _oracle_direct_planes(args):
+    tag, layer_id, layer, seq = args
+    rows = synth.direct_rows(tag, layer_id, layer, seq)
+    out = {}
+    out["k_nope"], out["k_scale"], out["k_rope"] = O.quantize_kv_rows(rows["kv"], layer.d_nope)
+    if layer.separate_v:
+        out["v_nope"], out["v_scale"], out["v_rope"] = O.quantize_kv_rows(rows["v"], layer.d_nope)
+    if layer.kind == "csa":
+        out["idx_codes"], out["idx_scales"] = O.quantize_fp4_rows(rows["idx"])
+        out["planted"] = rows["planted"]
+    win = synth.window_tokens(tag, layer_id, layer, seq)
+    W, n = layer.window, layer.n_tokens
+    pos = np.arange(n - min(W, n), n)
+    ring = np.zeros((max(W, 1), layer.dim), np.uint16)
+    ring[pos % max(W, 1)] = win["k"]
+    out["ring_k"] = ring
+    if layer.separate_v:
+        ringv = np.zeros((max(W, 1), layer.dim), np.uint16)
+        ringv[pos % max(W, 1)] = win["v"]
+        out["ring_v"] = ringv
+    return out
+
+
+def oracle_direct_planes(layer, tag, layer_id, seqs, processes=None):
+    """Oracle-quantised planes of directly drawn caches for the given sequences
+    (a spawn process pool when several are asked for)."""
+    args = [(tag, layer_id, layer, s) for s in seqs]
+    if processes is None or processes <= 1 or len(args) == 1:
+        return [_oracle_direct_planes(a) for a in args]
+    with mp.get_context("spawn").Pool(processes) as pool:
+        return pool.map(_oracle_direct_planes, args)
+
+
+def gpu_cache_from_planes(layer, planes, capacity=None, extra=0):
+    """Device cache holding the given per-sequence oracle planes, n_tokens set."""
+    cap = capacity if capacity is not None else layer.capacity(extra)
+    desc = dsv4.layer_desc(layer, cap)
+    cache = dsv4.Cache(desc)
+    n_c = layer.n_comp
+    for b, p in enumerate(planes):
+        cache.k_nope[b, :n_c] = to_dev(p["k_nope"])
+        cache.k_scale[b, :n_c] = to_dev(p["k_scale"])
+        cache.k_rope[b, :n_c] = to_dev(p["k_rope"])
+        cache.win_k[b] = to_dev(p["ring_k"])
+        if layer.separate_v:
+            cache.v_nope[b, :n_c] = to_dev(p["v_nope"])
+            cache.v_scale[b, :n_c] = to_dev(p["v_scale"])
+            cache.v_rope[b, :n_c] = to_dev(p["v_rope"])
+            cache.win_v[b] = to_dev(p["ring_v"])
+        if layer.kind == "csa":
+            cache.idx_codes[b, :n_c] = to_dev(p["idx_codes"])
+            cache.idx_scales[b, :n_c] = to_dev(p["idx_scales"])
+    cache.n_tokens.fill_(layer.n_tokens)
+    torch.cuda.synchronize()
+    return desc, cache
