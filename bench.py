@@ -124,7 +124,7 @@ class Stack:
         self.g = g
         self.descs, self.caches, self.bias, self.bias_u = [], [], [], []
         for li, L in enumerate(layers):
-            cap = L.n_comp + steps_total // L.ratio + 2
+            cap = L.capacity(steps_total)
             desc = dsv4.layer_desc(L, cap)
             cache = dsv4.Cache(desc)
             self._fill(L, desc, cache)

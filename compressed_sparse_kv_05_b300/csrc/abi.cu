@@ -26,7 +26,7 @@ int check_desc(const dsv4_layer_desc* d) {
   if (d->d_rope > 128 || d->d_rope % 8) return DSV4_ERR_UNSUPPORTED;
   if (d->d_nope + d->d_rope > 576) return DSV4_ERR_UNSUPPORTED;
   if (d->ratio > 256 || d->window > 4096) return DSV4_ERR_UNSUPPORTED;
-  if (d->idx_dim && (d->idx_dim % 32 || d->idx_dim > 256)) return DSV4_ERR_UNSUPPORTED;
+  if (d->idx_dim && d->idx_dim != 64 && d->idx_dim != 128 && d->idx_dim != 256) return DSV4_ERR_UNSUPPORTED;
   return DSV4_OK;
 }
 
@@ -81,10 +81,25 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
   return p;
 }
 
-size_t index_ws_bytes(const dsv4_layer_desc* d, int Hi) {
-  return static_cast<size_t>(d->batch) * Hi * d->idx_dim * sizeof(float) + 256 +
-         static_cast<size_t>(d->batch) * d->capacity * sizeof(float) + 256;
+int index_heads_padded(int Hi) { return Hi <= 64 ? 64 : 128; }
+
+struct IndexWs {
+  size_t q_codes, q_scales, wpad, scores, total;
+};
+
+IndexWs index_ws(const dsv4_layer_desc* d, int Hi) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t N = index_heads_padded(Hi);
+  IndexWs w{};
+  w.q_codes = 0;
+  w.q_scales = up(w.q_codes + d->batch * N * (d->idx_dim / 2));
+  w.wpad = up(w.q_scales + d->batch * N * (d->idx_dim / 16));
+  w.scores = up(w.wpad + d->batch * N * sizeof(float));
+  w.total = up(w.scores + static_cast<size_t>(d->batch) * d->capacity * sizeof(float));
+  return w;
 }
+
+size_t index_ws_bytes(const dsv4_layer_desc* d, int Hi) { return index_ws(d, Hi).total; }
 
 template <typename F>
 void set_smem_once(std::once_flag& flag, F func, int bytes) {
@@ -201,32 +216,40 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   DSV4_REQ(c->idx_codes);
   DSV4_REQ(c->idx_scales);
   DSV4_REQ(c->n_tokens);
+  DSV4_REQ(c->status);
   DSV4_REQ(q_idx);
   DSV4_REQ(w);
   DSV4_REQ(topk);
   DSV4_REQ(ws);
   if (scores && !aligned16(scores)) return DSV4_ERR_MISALIGNED;
   if (ws_bytes < index_ws_bytes(d, Hi)) return DSV4_ERR_WORKSPACE;
-  IndexArgs a{};
-  a.B = d->batch; a.Hi = Hi; a.Di = d->idx_dim; a.k = k; a.capacity = d->capacity; a.ratio = d->ratio;
-  a.q_idx = q_idx; a.w = w; a.idx_codes = c->idx_codes; a.idx_scales = c->idx_scales; a.n_tokens = c->n_tokens;
+  const int N = index_heads_padded(Hi);
+  const IndexWs wl = index_ws(d, Hi);
   char* wp = static_cast<char*>(ws);
-  a.qdec = reinterpret_cast<float*>(wp);
-  size_t off = (static_cast<size_t>(a.B) * Hi * a.Di * sizeof(float) + 255) & ~static_cast<size_t>(255);
-  a.scores = scores ? scores : reinterpret_cast<float*>(wp + off);
+  IndexArgs a{};
+  a.B = d->batch; a.Hi = Hi; a.N = N; a.Di = d->idx_dim; a.k = k; a.capacity = d->capacity; a.ratio = d->ratio;
+  a.q_idx = q_idx; a.w = w; a.n_tokens = c->n_tokens;
+  a.q_codes = reinterpret_cast<uint8_t*>(wp + wl.q_codes);
+  a.q_scales = reinterpret_cast<uint8_t*>(wp + wl.q_scales);
+  a.wpad = reinterpret_cast<float*>(wp + wl.wpad);
+  a.scores = scores ? scores : reinterpret_cast<float*>(wp + wl.scores);
   a.topk = topk;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  quant_query_fp4_kernel<<<a.B * Hi, 32, 0, st>>>(a);
+  quant_query_fp4_kernel<<<a.B * N, 32, 0, st>>>(a);
   if ((e = launch_status())) return e;
-  const int hp = (Hi + 15) & ~15;
-  const size_t smem = static_cast<size_t>(hp) * (a.Di + 1) * sizeof(float);
-  static std::once_flag flag;
-  set_smem_once(flag, index_scores_kernel, 200 * 1024);
-  int tiles = (d->capacity + 127) / 128;
-  const int per_seq = (4 * 148 + a.B - 1) / a.B;
-  if (tiles > per_seq) tiles = per_seq;
-  index_scores_kernel<<<dim3(tiles, a.B), 128, smem, st>>>(a);
-  if ((e = launch_status())) return e;
+  IndexTcArgs t{};
+  t.B = a.B; t.N = N; t.Di = a.Di; t.capacity = a.capacity; t.ratio = a.ratio;
+  const int tiles = (d->capacity + 127) / 128;
+  int per_seq = kSplitTarget / a.B;
+  if (per_seq < 1) per_seq = 1;
+  t.ctas_per_seq = per_seq < tiles ? per_seq : tiles;
+  uint32_t need = 2 * N + 3 * 4 * (a.Di / 64);
+  uint32_t cols = 32;
+  while (cols < need) cols <<= 1;
+  t.tmem_cols = cols;
+  t.n_tokens = c->n_tokens; t.idx_scales = c->idx_scales; t.q_scales = a.q_scales; t.wpad = a.wpad;
+  t.scores = a.scores; t.status = c->status;
+  if ((e = launch_index_scores_tc(t, c->idx_codes, a.q_codes, st))) return e;
   topk_select_kernel<<<a.B, 1024, 0, st>>>(a);
   return launch_status();
 }
@@ -277,10 +300,11 @@ int dsv4_quantize_kv_rows(const float* y, int64_t rows, int32_t d_nope, int32_t 
   if (d_nope < 16 || d_nope > 512 || d_nope % 16 || d_rope < 0 || d_rope > 128 || d_rope % 8)
     return DSV4_ERR_UNSUPPORTED;
   if (rows == 0) return DSV4_OK;
-  DSV4_REQ(y);
-  DSV4_REQ(nope);
-  DSV4_REQ(scale);
-  if (d_rope) DSV4_REQ(rope);
+  if (!y || !nope || !scale || (d_rope && !rope)) return DSV4_ERR_INVALID_ARG;
+  // natural alignment only: rows are read as floats, codes written in pairs
+  if ((reinterpret_cast<uintptr_t>(y) & 3) || (reinterpret_cast<uintptr_t>(nope) & 1) ||
+      (reinterpret_cast<uintptr_t>(scale) & 3) || (d_rope && (reinterpret_cast<uintptr_t>(rope) & 1)))
+    return DSV4_ERR_MISALIGNED;
   const int64_t blocks = (rows + 7) / 8;
   quant_kv_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       y, rows, d_nope, d_rope, nope, scale, rope);
@@ -293,8 +317,8 @@ int dsv4_quantize_fp4_rows(const float* y, int64_t rows, int32_t cols, uint8_t* 
   if (cols < 32 || cols % 32 || cols > 4096) return DSV4_ERR_UNSUPPORTED;
   if (rows == 0) return DSV4_OK;
   DSV4_REQ(y);
-  DSV4_REQ(codes);
-  DSV4_REQ(scales);
+  if (!codes || !scales) return DSV4_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(codes) & 3) return DSV4_ERR_MISALIGNED;
   const int64_t n = rows * (cols / 16);
   quant_fp4_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       y, rows, cols, codes, scales);

@@ -13,75 +13,28 @@
 
 namespace dsv4 {
 
-// grid (B * Hi), block Di/16: quantise the query to FP4 and store its exact decoded values.
+// grid (B * N), block Di/16: quantise one query head to FP4 (the same rule as the
+// keys) into the operand layout of the scoring MMA; padding heads (h >= Hi) get
+// zero codes, zero scales and zero weight.
 __global__ void quant_query_fp4_kernel(IndexArgs a) {
-  const int row = blockIdx.x;
+  const int row = blockIdx.x;               // b * N + h
+  const int b = row / a.N, h = row % a.N;
   const int blk = threadIdx.x;
-  if (blk >= a.Di / 16) return;
-  const uint16_t* src = a.q_idx + static_cast<int64_t>(row) * a.Di + blk * 16;
-  float v[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = bf16_to_f32(src[i]);
-  __align__(8) uint8_t codes[8];
-  const uint32_t sc = quant_fp4_block16(v, codes);
-  const float s = e4m3_to_f32(sc);
-  float* dst = a.qdec + static_cast<int64_t>(row) * a.Di + blk * 16;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    dst[2 * i] = e2m1_to_f32(codes[i] & 0xF) * s;
-    dst[2 * i + 1] = e2m1_to_f32(codes[i] >> 4) * s;
-  }
-}
-
-// grid (tile-strided, B), block 128: one thread per compressed block.
-// dynamic smem: Hp*Di floats of decoded query (Hp = Hi rounded up to 16, zero
-// padded) + Hp weights.
-__global__ void __launch_bounds__(128) index_scores_kernel(IndexArgs a) {
-  extern __shared__ float sm[];
-  const int b = blockIdx.y;
-  const int Hp = (a.Hi + 15) & ~15;
-  float* q = sm;
-  float* w = sm + Hp * a.Di;
-  for (int i = threadIdx.x; i < Hp * a.Di; i += blockDim.x)
-    q[i] = i < a.Hi * a.Di ? a.qdec[static_cast<int64_t>(b) * a.Hi * a.Di + i] : 0.f;
-  for (int i = threadIdx.x; i < Hp; i += blockDim.x) w[i] = i < a.Hi ? a.w[b * a.Hi + i] : 0.f;
-  __syncthreads();
-  int64_t n_c = a.n_tokens[b] / a.ratio;
-  if (n_c > a.capacity) n_c = a.capacity;
   const int nblk = a.Di / 16;
-  for (int64_t s0 = static_cast<int64_t>(blockIdx.x) * 128; s0 < n_c; s0 += static_cast<int64_t>(gridDim.x) * 128) {
-    const int64_t s = s0 + threadIdx.x;
-    if (s >= n_c) continue;
-    const int64_t e = static_cast<int64_t>(b) * a.capacity + s;
-    const uint8_t* kc = a.idx_codes + e * (a.Di / 2);
-    const uint8_t* ks = a.idx_scales + e * nblk;
-    float score = 0.f;
-    for (int hc = 0; hc < Hp; hc += 16) {
-      float acc[16];
+  if (blk >= nblk) return;
+  uint8_t* codes = a.q_codes + static_cast<int64_t>(row) * (a.Di / 2) + blk * 8;
+  uint8_t* scale = a.q_scales + static_cast<int64_t>(row) * nblk + blk;
+  if (h >= a.Hi) {
+    reinterpret_cast<uint2*>(codes)[0] = make_uint2(0u, 0u);
+    *scale = 0;
+  } else {
+    const uint16_t* src = a.q_idx + (static_cast<int64_t>(b) * a.Hi + h) * a.Di + blk * 16;
+    float v[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) acc[h] = 0.f;
-      for (int blk = 0; blk < nblk; ++blk) {
-        const uint2 packed = *reinterpret_cast<const uint2*>(kc + blk * 8);
-        const float sc = e4m3_to_f32(ks[blk]);
-        float kv[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t byte = ((i < 4 ? packed.x : packed.y) >> (8 * (i & 3))) & 0xFF;
-          kv[2 * i] = e2m1_to_f32(byte & 0xF) * sc;
-          kv[2 * i + 1] = e2m1_to_f32(byte >> 4) * sc;
-        }
-#pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const float* qr = q + (hc + h) * a.Di + blk * 16;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) acc[h] = fmaf(qr[i], kv[i], acc[h]);
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < 16; ++h) score = fmaf(w[hc + h], fmaxf(acc[h], 0.f), score);
-    }
-    a.scores[static_cast<int64_t>(b) * a.capacity + s] = score;
+    for (int i = 0; i < 16; ++i) v[i] = bf16_to_f32(src[i]);
+    *scale = static_cast<uint8_t>(quant_fp4_block16(v, codes));
   }
+  if (blk == 0) a.wpad[row] = h < a.Hi ? a.w[b * a.Hi + h] : 0.f;
 }
 
 namespace {

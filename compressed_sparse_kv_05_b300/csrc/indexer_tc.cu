@@ -1,0 +1,291 @@
+// Lightning-indexer scores on the 5th-generation tensor cores (tcgen05,
+// kind::mxf4nvf4 block-scaled FP4 MMA).
+//
+// vibecoco.ai, "DeepSeek V4 agent architecture", section
+// "混合注意力：两种压缩，交替使用": the lightning indexer of CSA runs in FP4 and
+// scores every compressed block with ReLU-scored multi-head dot products:
+//   I_s = sum_h w_h * max(0, q_h . k_s).
+// The contraction q_h . k_s is dense (all blocks x all indexer heads), so it
+// runs as D[128 keys][N heads] = K_tile[128][Di] x Q[N][Di]^T per tile of 128
+// compressed blocks, with the per-16 e4m3 scales of keys and query applied by
+// the MMA itself (UE4M3 block scales). The epilogue applies ReLU and the head
+// weights and writes one fp32 score per block.
+//
+// CTA roles (192 threads): warp 0 allocates tensor memory and streams key tiles
+// with TMA into an S-stage ring; warp 1 issues the MMAs (one thread); warps 2-5
+// (one per 32-lane quarter of tensor memory) load the block scales into tensor
+// memory ahead of the MMA and turn finished accumulators into scores. The
+// accumulator and the key-scale slots are double-buffered so that the MMA of
+// tile i+1 overlaps the epilogue of tile i.
+//
+// Block scales in tensor memory: row r's four scale bytes of one K=64 step (one
+// byte per 16 elements, the first block in the lowest byte) are stored in lane r
+// in each of four consecutive columns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace dsv4 {
+
+namespace {
+
+constexpr int kTile = 128;     // compressed blocks per MMA tile (M)
+constexpr int kThreads = 192;
+
+template <int ROWB>
+struct TcCfg {
+  static constexpr int KSTEPS = ROWB / 32;                   // K = 64 e2m1 values = 32 bytes per MMA
+  static constexpr int STAGES = ROWB <= 64 ? 8 : 6;
+  static constexpr int STAGE_BYTES = kTile * ROWB;
+  static constexpr uint32_t SWIZZLE = ROWB == 32 ? tc::kSwizzle32B : ROWB == 64 ? tc::kSwizzle64B : tc::kSwizzle128B;
+  static constexpr int SF_COLS = 4 * KSTEPS;                  // tensor-memory columns of one tile's scales
+};
+
+struct SmemTail {
+  uint64_t full[8], empty[8], acc_full[2], acc_empty[2], sf_full[2], q_full, drain;
+  uint32_t taddr;
+  int abort;
+};
+
+}  // namespace
+
+template <int ROWB>
+__global__ void __launch_bounds__(kThreads, 1)
+    index_scores_tc_kernel(const __grid_constant__ CUtensorMap keys, const __grid_constant__ CUtensorMap qmap,
+                           IndexTcArgs a) {
+  using C = TcCfg<ROWB>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte alignment for the swizzled tiles
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stages = base;
+  unsigned char* qbuf = stages + C::STAGES * C::STAGE_BYTES;
+  SmemTail* t = reinterpret_cast<SmemTail*>(qbuf + ((a.N * ROWB + 1023) & ~1023));
+  float* wsm = reinterpret_cast<float*>(t + 1);
+
+  const int b = blockIdx.y;
+  int64_t n_c = a.n_tokens[b] / a.ratio;
+  if (n_c > a.capacity) n_c = a.capacity;
+  const int tiles = static_cast<int>((n_c + kTile - 1) / kTile);
+  const int per = (tiles + a.ctas_per_seq - 1) / a.ctas_per_seq;
+  const int t0 = blockIdx.x * per;
+  const int t1 = t0 + per < tiles ? t0 + per : tiles;
+  if (t0 >= t1) return;                                    // uniform across the CTA
+  const int ntile = t1 - t0;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const uint32_t ncols = a.tmem_cols;
+  const uint32_t acc_col0 = 0, sfa_col0 = 2 * N, sfb_col = 2 * N + 2 * C::SF_COLS;
+  volatile int* abort = &t->abort;
+
+  if (warp == 0) tc::tmem_alloc(&t->taddr, ncols);
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      tc::mbar_init(&t->full[i], 1);
+      tc::mbar_init(&t->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&t->acc_full[i], 1);
+      tc::mbar_init(&t->acc_empty[i], 4);
+      tc::mbar_init(&t->sf_full[i], 4);
+    }
+    tc::mbar_init(&t->q_full, 1);
+    tc::mbar_init(&t->drain, 1);
+    t->abort = 0;
+    tc::fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < N; i += blockDim.x) wsm[i] = a.wpad[static_cast<int64_t>(b) * N + i];
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t taddr = t->taddr;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tensormap(&keys);
+      tc::prefetch_tensormap(&qmap);
+      tc::mbar_arrive_expect_tx(&t->q_full, N * ROWB);
+      tc::tma_load_2d(qbuf, &qmap, &t->q_full, 0, b * N);
+      int issued = 0;
+      for (int i = 0; i < ntile; ++i) {
+        const int stage = i % C::STAGES, round = i / C::STAGES;
+        if (!tc::mbar_wait(&t->empty[stage], (round & 1) ^ 1, abort)) break;
+        tc::mbar_arrive_expect_tx(&t->full[stage], C::STAGE_BYTES);
+        tc::tma_load_2d(stages + stage * C::STAGE_BYTES, &keys, &t->full[stage], 0,
+                        static_cast<int>(static_cast<int64_t>(b) * a.capacity + static_cast<int64_t>(t0 + i) * kTile));
+        ++issued;
+      }
+      if (*abort) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        for (int i = issued - C::STAGES > 0 ? issued - C::STAGES : 0; i < issued; ++i) {
+          const int stage = i % C::STAGES, round = i / C::STAGES;
+          for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->full[stage], round & 1); ++it) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_mxf4nvf4(kTile, N);
+      const uint32_t q_addr = tc::smem_u32(qbuf);
+      bool ok = tc::mbar_wait(&t->q_full, 0, abort);
+      for (int i = 0; ok && i < ntile; ++i) {
+        const int stage = i % C::STAGES, round = i / C::STAGES;
+        const int ab = i & 1, ra = i >> 1;
+        if (!tc::mbar_wait(&t->full[stage], round & 1, abort)) break;
+        if (!tc::mbar_wait(&t->sf_full[ab], ra & 1, abort)) break;
+        if (!tc::mbar_wait(&t->acc_empty[ab], (ra & 1) ^ 1, abort)) break;
+        tc::tc_fence_after();
+        const uint32_t a_addr = tc::smem_u32(stages + stage * C::STAGE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+          const uint64_t adesc = tc::smem_desc(a_addr + kk * 32, 8 * ROWB, C::SWIZZLE);
+          const uint64_t bdesc = tc::smem_desc(q_addr + kk * 32, 8 * ROWB, C::SWIZZLE);
+          tc::mma_mxf4nvf4(taddr + acc_col0 + ab * N, adesc, bdesc, idesc, taddr + sfa_col0 + ab * C::SF_COLS + kk * 4,
+                           taddr + sfb_col + kk * 4, kk > 0 ? 1u : 0u);
+        }
+        tc::tc_commit(&t->empty[stage]);
+        tc::tc_commit(&t->acc_full[ab]);
+      }
+      // every MMA issued must finish before tensor memory is released
+      tc::tc_commit(&t->drain);
+      for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->drain, 0); ++it) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ scales + epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;                  // tensor-memory lane == tile row
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int nblk = ROWB / 8;                            // Di/16 scale bytes per row
+    auto write_sfa = [&](int j) {
+      const int64_t s = static_cast<int64_t>(t0 + j) * kTile + row;
+      const uint8_t* src = a.idx_scales + (static_cast<int64_t>(b) * a.capacity + s) * nblk;
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        const uint32_t w = s < n_c ? *reinterpret_cast<const uint32_t*>(src + kk * 4) : 0u;
+        tc::tmem_st_x4_same(taddr + lane_base + sfa_col0 + (j & 1) * C::SF_COLS + kk * 4, w);
+      }
+    };
+    // query scales (rows >= N are padding heads: zero)
+    {
+      const uint8_t* src = a.q_scales + (static_cast<int64_t>(b) * N + row) * nblk;
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        const uint32_t w = row < N ? *reinterpret_cast<const uint32_t*>(src + kk * 4) : 0u;
+        tc::tmem_st_x4_same(taddr + lane_base + sfb_col + kk * 4, w);
+      }
+    }
+    for (int j = 0; j < 2 && j < ntile; ++j) {
+      write_sfa(j);
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&t->sf_full[j]);
+    }
+    float* out = a.scores + static_cast<int64_t>(b) * a.capacity;
+    for (int i = 0; i < ntile; ++i) {
+      const int ab = i & 1, ra = i >> 1;
+      if (!tc::mbar_wait(&t->acc_full[ab], ra & 1, abort)) break;
+      tc::tc_fence_after();
+      float score = 0.f;
+      for (int c = 0; c < N; c += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(taddr + lane_base + acc_col0 + ab * N + c, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h) score = fmaf(wsm[c + h], fmaxf(__uint_as_float(v[h]), 0.f), score);
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&t->acc_empty[ab]);
+      const int64_t s = static_cast<int64_t>(t0 + i) * kTile + row;
+      if (s < n_c) out[s] = score;
+      if (i + 2 < ntile) {
+        write_sfa(i + 2);
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&t->sf_full[ab]);
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(taddr, ncols);
+  }
+  if (threadIdx.x == 0 && t->abort) atomicOr(a.status, DSV4_STATUS_TIMEOUT);
+}
+
+// ------------------------------------------------------------------------------ host side
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_rows(CUtensorMap* map, const void* base, int rowbytes, int64_t rows, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rowbytes), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rowbytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(rowbytes), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = rowbytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                : rowbytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int ROWB>
+int launch_tc(const IndexTcArgs& a, const CUtensorMap& keys, const CUtensorMap& qmap, cudaStream_t st) {
+  using C = TcCfg<ROWB>;
+  size_t smem = 1024 + C::STAGES * C::STAGE_BYTES + ((a.N * ROWB + 1023) & ~1023) + sizeof(SmemTail) + a.N * 4;
+  // keep at most two CTAs per SM so that their tensor-memory allocations always fit
+  const size_t floor_bytes = a.tmem_cols > 256 ? 120 * 1024 : 80 * 1024;
+  if (smem < floor_bytes) smem = floor_bytes;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(index_scores_tc_kernel<ROWB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  });
+  index_scores_tc_kernel<ROWB><<<dim3(a.ctas_per_seq, a.B), kThreads, smem, st>>>(keys, qmap, a);
+  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_index_scores_tc(const IndexTcArgs& a, const uint8_t* key_codes, const uint8_t* q_codes, cudaStream_t st) {
+  const int rowb = a.Di / 2;
+  CUtensorMap keys, qmap;
+  if (!encode_rows(&keys, key_codes, rowb, static_cast<int64_t>(a.B) * a.capacity, kTile)) return DSV4_ERR_CUDA;
+  if (!encode_rows(&qmap, q_codes, rowb, static_cast<int64_t>(a.B) * a.N, a.N)) return DSV4_ERR_CUDA;
+  switch (rowb) {
+    case 32: return launch_tc<32>(a, keys, qmap, st);
+    case 64: return launch_tc<64>(a, keys, qmap, st);
+    case 128: return launch_tc<128>(a, keys, qmap, st);
+    default: return DSV4_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace dsv4

@@ -33,19 +33,31 @@ __global__ void pool_rows_kernel(const uint16_t* x, const uint16_t* z, const flo
 
 // ---- indexer + top-k
 struct IndexArgs {
-  int B, Hi, Di, k, capacity, ratio;
+  int B, Hi, N, Di, k, capacity, ratio;
   const uint16_t* q_idx;   // [B][Hi][Di] bf16
   const float* w;          // [B][Hi]
-  const uint8_t* idx_codes;
-  const uint8_t* idx_scales;
   const int64_t* n_tokens;
-  float* qdec;             // [B][Hi][Di] decoded FP4 query (workspace)
+  uint8_t* q_codes;        // [B][N][Di/2] FP4 query, heads padded to N with zeros (workspace)
+  uint8_t* q_scales;       // [B][N][Di/16]
+  float* wpad;             // [B][N] head weights, zero for padding heads
   float* scores;           // [B][capacity]
   int32_t* topk;           // [B][k]
 };
 __global__ void quant_query_fp4_kernel(IndexArgs a);
-__global__ void index_scores_kernel(IndexArgs a);
 __global__ void topk_select_kernel(IndexArgs a);
+
+struct IndexTcArgs {
+  int B, N, Di, capacity, ratio, ctas_per_seq;
+  uint32_t tmem_cols;
+  const int64_t* n_tokens;
+  const uint8_t* idx_scales;   // [B][capacity][Di/16]
+  const uint8_t* q_scales;     // [B][N][Di/16]
+  const float* wpad;           // [B][N]
+  float* scores;               // [B][capacity]
+  int32_t* status;
+};
+// tcgen05 block-scaled FP4 scores; key_codes [B][capacity][Di/2], q_codes [B][N][Di/2]
+int launch_index_scores_tc(const IndexTcArgs& a, const uint8_t* key_codes, const uint8_t* q_codes, cudaStream_t st);
 
 // ---- attention
 struct AttnArgs {

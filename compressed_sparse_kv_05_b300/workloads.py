@@ -55,8 +55,11 @@ class Layer:
         return 1.0 / math.sqrt(self.dim)
 
     def capacity(self, extra_tokens=0):
-        """Compressed-entry capacity that holds the context plus extra_tokens appends."""
-        return (self.n_tokens + extra_tokens) // self.ratio + 1
+        """Compressed-entry capacity that holds the context plus extra_tokens
+        appends, rounded up to a multiple of 128 so that every sequence's slice
+        of every plane starts on a 16-byte boundary."""
+        need = (self.n_tokens + extra_tokens) // self.ratio + 1
+        return (need + 127) // 128 * 128
 
 
 CSA_4K = Layer("csa", 1, 4096, 16, 64, 64, True, 4, 128, idx_heads=4, idx_dim=64, topk=64)

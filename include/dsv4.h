@@ -53,13 +53,14 @@ enum {
 /* Bits of the device status word (sticky until dsv4_read_status clears them). */
 enum {
   DSV4_STATUS_CAPACITY = 1, /* an append would pass `capacity`: that sequence was left unchanged */
-  DSV4_STATUS_BAD_INDEX = 2 /* a top-k index outside [-1, n_c) was ignored */
+  DSV4_STATUS_BAD_INDEX = 2, /* a top-k index outside [-1, n_c) was ignored */
+  DSV4_STATUS_TIMEOUT = 4    /* a bounded wait inside a kernel expired; that kernel's output is incomplete */
 };
 
 /* Shape of one attention layer's cache. Supported: 16 <= d_nope <= 512 and a
  * multiple of 16; 0 <= d_rope <= 128 and a multiple of 8; 1 <= ratio <= 256;
- * 0 <= window <= 4096; idx_dim 0 (no indexer, HCA) or 32..256 in steps of 32;
- * capacity >= 1. */
+ * d_nope + d_rope <= 576; 0 <= window <= 4096; idx_dim 0 (no indexer, HCA),
+ * 64, 128 or 256; capacity >= 1 and batch * capacity < 2^31. */
 typedef struct {
   int32_t batch;      /* B sequences */
   int32_t d_nope;     /* FP8 dims of an entry */
@@ -128,6 +129,7 @@ int dsv4_compress_append(const dsv4_layer_desc* desc, const dsv4_cache* cache, i
  *   topk   : [B][k] int32 output
  *   scores : [B][capacity] fp32 output of I (entries >= n_c untouched), or NULL
  *   ws     : device workspace of at least dsv4_workspace_size() bytes
+ * The contraction runs on the tensor cores (block-scaled FP4 MMA, fp32 accumulate).
  * Supported: 1 <= Hi <= 128, 1 <= k <= 2048, layer with idx_dim > 0. */
 int dsv4_index_topk(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_t Hi,
                     const uint16_t* q_idx, const float* w, int32_t k, int32_t* topk, float* scores,
@@ -164,12 +166,14 @@ int dsv4_read_status(const dsv4_cache* cache, void* stream);
 /* The quantisation step of an append on rows pooled elsewhere [HYB]:
  * y [rows][d_nope + d_rope] fp32 -> nope [rows][d_nope] e4m3, scale [rows],
  * rope [rows][d_rope] bf16, with the same rule and rounding as
- * dsv4_compress_append. */
+ * dsv4_compress_append. Alignment: y, scale 4 bytes; nope, rope 2 bytes (so that
+ * one sequence's slice of a cache plane can be filled directly). */
 int dsv4_quantize_kv_rows(const float* y, int64_t rows, int32_t d_nope, int32_t d_rope,
                           uint8_t* nope, float* scale, uint16_t* rope, void* stream);
 
 /* FP4 quantisation of rows [HYB]: y [rows][cols] fp32 (cols a multiple of 32)
- * -> codes [rows][cols/2] e2m1, scales [rows][cols/16] e4m3. */
+ * -> codes [rows][cols/2] e2m1, scales [rows][cols/16] e4m3. Alignment: y 16 bytes,
+ * codes 4 bytes, scales none. */
 int dsv4_quantize_fp4_rows(const float* y, int64_t rows, int32_t cols, uint8_t* codes,
                            uint8_t* scales, void* stream);
 

@@ -133,6 +133,7 @@ def test_quantizers_and_pool_reject_bad_arguments_on_host(dsv4):
     assert L.dsv4_quantize_kv_rows(FAKE, 0, 448, 64, None, None, None, None) == dsv4.OK     # nothing to do
     assert L.dsv4_quantize_fp4_rows(FAKE, 10, 48, FAKE, FAKE, None) == dsv4.ERR_UNSUPPORTED
     assert L.dsv4_quantize_fp4_rows(FAKE, 10, 128, FAKE + 1, FAKE, None) == dsv4.ERR_MISALIGNED
+    assert L.dsv4_quantize_kv_rows(FAKE + 2, 10, 448, 64, FAKE, FAKE, FAKE, None) == dsv4.ERR_MISALIGNED
     assert L.dsv4_pool_rows(FAKE, FAKE, FAKE, 10, 0, 128, FAKE, None) == dsv4.ERR_INVALID_ARG
     assert L.dsv4_pool_rows(FAKE, FAKE, FAKE, 10, 4, 100, FAKE, None) == dsv4.ERR_UNSUPPORTED
     assert L.dsv4_read_status(None, None) == dsv4.ERR_INVALID_ARG
