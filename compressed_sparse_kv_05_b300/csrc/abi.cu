@@ -84,22 +84,28 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
 int index_heads_padded(int Hi) { return Hi <= 64 ? 64 : 128; }
 
 struct IndexWs {
-  size_t q_codes, q_scales, wpad, scores, total;
+  size_t q_codes, q_scales, wpad, scores, hist1, hist2, cnt, above, cand, total;
 };
 
-IndexWs index_ws(const dsv4_layer_desc* d, int Hi) {
+IndexWs index_ws(const dsv4_layer_desc* d, int Hi, int k) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t N = index_heads_padded(Hi);
+  const size_t B = d->batch, cap = d->capacity;
   IndexWs w{};
   w.q_codes = 0;
-  w.q_scales = up(w.q_codes + d->batch * N * (d->idx_dim / 2));
-  w.wpad = up(w.q_scales + d->batch * N * (d->idx_dim / 16));
-  w.scores = up(w.wpad + d->batch * N * sizeof(float));
-  w.total = up(w.scores + static_cast<size_t>(d->batch) * d->capacity * sizeof(float));
+  w.q_scales = up(w.q_codes + B * N * (d->idx_dim / 2));
+  w.wpad = up(w.q_scales + B * N * (d->idx_dim / 16));
+  w.scores = up(w.wpad + B * N * sizeof(float));
+  w.hist1 = up(w.scores + B * cap * sizeof(float));
+  w.hist2 = up(w.hist1 + B * 4096 * sizeof(uint32_t));
+  w.cnt = up(w.hist2 + B * 4096 * sizeof(uint32_t));
+  w.above = up(w.cnt + B * 4 * sizeof(uint32_t));
+  w.cand = up(w.above + B * static_cast<size_t>(k) * sizeof(int32_t));
+  w.total = up(w.cand + B * cap * sizeof(uint64_t));
   return w;
 }
 
-size_t index_ws_bytes(const dsv4_layer_desc* d, int Hi) { return index_ws(d, Hi).total; }
+size_t index_ws_bytes(const dsv4_layer_desc* d, int Hi, int k) { return index_ws(d, Hi, k).total; }
 
 template <typename F>
 void set_smem_once(std::once_flag& flag, F func, int bytes) {
@@ -222,9 +228,9 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   DSV4_REQ(topk);
   DSV4_REQ(ws);
   if (scores && !aligned16(scores)) return DSV4_ERR_MISALIGNED;
-  if (ws_bytes < index_ws_bytes(d, Hi)) return DSV4_ERR_WORKSPACE;
+  if (ws_bytes < index_ws_bytes(d, Hi, k)) return DSV4_ERR_WORKSPACE;
   const int N = index_heads_padded(Hi);
-  const IndexWs wl = index_ws(d, Hi);
+  const IndexWs wl = index_ws(d, Hi, k);
   char* wp = static_cast<char*>(ws);
   IndexArgs a{};
   a.B = d->batch; a.Hi = Hi; a.N = N; a.Di = d->idx_dim; a.k = k; a.capacity = d->capacity; a.ratio = d->ratio;
@@ -234,6 +240,11 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   a.wpad = reinterpret_cast<float*>(wp + wl.wpad);
   a.scores = scores ? scores : reinterpret_cast<float*>(wp + wl.scores);
   a.topk = topk;
+  a.hist1 = reinterpret_cast<uint32_t*>(wp + wl.hist1);
+  a.hist2 = reinterpret_cast<uint32_t*>(wp + wl.hist2);
+  a.cnt = reinterpret_cast<uint32_t*>(wp + wl.cnt);
+  a.above = reinterpret_cast<int32_t*>(wp + wl.above);
+  a.cand = reinterpret_cast<uint64_t*>(wp + wl.cand);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   quant_query_fp4_kernel<<<a.B * N, 32, 0, st>>>(a);
   if ((e = launch_status())) return e;
@@ -248,9 +259,13 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   while (cols < need) cols <<= 1;
   t.tmem_cols = cols;
   t.n_tokens = c->n_tokens; t.idx_scales = c->idx_scales; t.q_scales = a.q_scales; t.wpad = a.wpad;
-  t.scores = a.scores; t.status = c->status;
+  t.scores = a.scores; t.hist1 = a.hist1; t.status = c->status;
   if ((e = launch_index_scores_tc(t, c->idx_codes, a.q_codes, st))) return e;
-  topk_select_kernel<<<a.B, 1024, 0, st>>>(a);
+  int sel = (4 * 148) / a.B;
+  const int sel_max = (d->capacity + 511) / 512;
+  if (sel > sel_max) sel = sel_max;
+  if (sel < 1) sel = 1;
+  topk_select_kernel<<<dim3(sel, a.B), 512, 0, st>>>(a);
   return launch_status();
 }
 
@@ -277,7 +292,7 @@ size_t dsv4_workspace_size(const dsv4_layer_desc* d, int32_t H, int32_t Hi, int3
     if (csa > need) need = csa;
   }
   if (d->idx_dim && Hi > 0) {
-    const size_t idx = index_ws_bytes(d, Hi);
+    const size_t idx = index_ws_bytes(d, Hi, k > 0 ? k : 1);
     if (idx > need) need = idx;
   }
   return need;

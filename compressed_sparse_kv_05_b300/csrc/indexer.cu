@@ -35,94 +35,244 @@ __global__ void quant_query_fp4_kernel(IndexArgs a) {
     *scale = static_cast<uint8_t>(quant_fp4_block16(v, codes));
   }
   if (blk == 0) a.wpad[row] = h < a.Hi ? a.w[b * a.Hi + h] : 0.f;
+  // zero this sequence's top-k histograms and counters (the N blocks of a sequence share the work)
+  const int words = 2 * 4096 + 4;
+  const int per = (words + a.N - 1) / a.N;
+  for (int i = h * per + blk; i < (h + 1) * per && i < words; i += nblk) {
+    if (i < 4096) a.hist1[static_cast<int64_t>(b) * 4096 + i] = 0;
+    else if (i < 8192) a.hist2[static_cast<int64_t>(b) * 4096 + (i - 4096)] = 0;
+    else a.cnt[b * 4 + (i - 8192)] = 0;
+  }
 }
 
 namespace {
-// block-wide exclusive prefix count of `flag` over 1024 threads; returns the
-// prefix and stores the block total in *total (shared, read after a sync).
-DSV4_DEV int block_prefix(bool flag, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned bal = __ballot_sync(0xffffffffu, flag);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) warp_tot[warp] = __popc(bal);
+
+constexpr int kBins = 4096;          // 12-bit digit histograms
+constexpr int kSelThreads = 512;
+constexpr int kMaxK = 2048;
+
+// Suffix search over a 4096-bin histogram held in shared memory: the largest
+// bin t with sum_{j >= t} h[j] >= need. Returns t and writes sum_{j > t} h[j]
+// to *above. `part` is >= kSelThreads ints of scratch. Every thread returns the same.
+DSV4_DEV int suffix_select(const uint32_t* h, uint32_t need, uint32_t* above, uint32_t* part) {
+  constexpr int per = kBins / kSelThreads;    // 8 bins per thread, thread t owns bins [t*per, (t+1)*per)
+  const int t = threadIdx.x;
+  uint32_t mine = 0;
+#pragma unroll
+  for (int i = 0; i < per; ++i) mine += h[t * per + i];
+  part[t] = mine;
   __syncthreads();
-  if (warp == 0) {
-    int v = warp_tot[lane];
-    int incl = v;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+  // inclusive suffix scan over threads (Hillis-Steele on shared memory)
+  for (int off = 1; off < kSelThreads; off <<= 1) {
+    const uint32_t v = t + off < kSelThreads ? part[t + off] : 0u;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  if (t == 0) { s_bin = 0; s_above = 0; }
+  __syncthreads();
+  const uint32_t incl = part[t];                              // bins >= t*per
+  const uint32_t excl = t + 1 < kSelThreads ? part[t + 1] : 0u;   // bins >= (t+1)*per
+  if (excl < need && incl >= need) {
+    uint32_t acc = excl;
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t c = h[t * per + i];
+      if (acc + c >= need) {
+        s_bin = t * per + i;
+        s_above = acc;
+        break;
+      }
+      acc += c;
     }
-    warp_tot[lane] = incl - v;
-    if (lane == 31) *total = incl;
   }
   __syncthreads();
-  const int r = warp_tot[warp] + in_warp;
+  *above = s_above;
+  const int r = s_bin;
   __syncthreads();
   return r;
 }
+
+// Append `flag`-ed values of a warp to list[*counter ...] with one atomic per
+// warp; positions at or beyond `cap` are dropped.
+DSV4_DEV void warp_append_i32(bool flag, int32_t v, uint32_t* counter, int32_t* list, uint32_t cap) {
+  const unsigned bal = __ballot_sync(0xffffffffu, flag);
+  if (!bal) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(bal) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(bal)));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
+  if (flag && pos < cap) list[pos] = v;
+}
+
+DSV4_DEV void warp_append_u64(bool flag, uint64_t v, uint32_t* counter, uint64_t* list, uint32_t cap) {
+  const unsigned bal = __ballot_sync(0xffffffffu, flag);
+  if (!bal) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(bal) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(bal)));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
+  if (flag && pos < cap) list[pos] = v;
+}
+
 }  // namespace
 
-// grid (B), block 1024: radix select of the k-th largest score key (MSB-first,
-// 8 bits a pass), then one pass in index order that keeps every key above the
-// threshold and the lowest-index `need` keys equal to it.
-__global__ void __launch_bounds__(1024) topk_select_kernel(IndexArgs a) {
-  __shared__ int hist[256];
-  __shared__ int warp_tot[32];
-  __shared__ int total;
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
-  const int b = blockIdx.x;
+// Top-k selection, grid (sel_ctas, B), block 512. The scoring kernel has
+// already histogrammed the top 12 bits of every score key (hist1). Each CTA
+// finds the threshold bin T1 (the bin holding the k-th largest key), scans its
+// slice of the scores, appends every block above T1 to `above` and every block
+// in T1 to `cand` (key, index) while histogramming the next 12 key bits
+// (hist2). The last CTA of the sequence to finish (a completion counter, no
+// waiting) resolves the boundary: blocks of cand above the second-level
+// threshold bin are taken, the remaining ties are settled by the low 8 key bits
+// and then the lower index, and the k indices are sorted ascending.
+__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
+  __shared__ uint32_t h[kBins];
+  __shared__ uint32_t part[kSelThreads];
+  __shared__ int32_t fin[kMaxK];
+  __shared__ uint32_t s_nfin, s_last;
+  __shared__ uint32_t s_d, s_rem;
+  const int b = blockIdx.y;
   int64_t n_c = a.n_tokens[b] / a.ratio;
   if (n_c > a.capacity) n_c = a.capacity;
-  const float* sc = a.scores + static_cast<int64_t>(b) * a.capacity;
   int32_t* out = a.topk + static_cast<int64_t>(b) * a.k;
-  if (n_c <= a.k) {
-    for (int i = threadIdx.x; i < a.k; i += blockDim.x) out[i] = i < n_c ? i : -1;
+  const int k = a.k;
+  if (n_c <= k) {
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < n_c ? i : -1;
     return;
   }
-  uint32_t prefix = 0, mask = 0;
-  int need = a.k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (threadIdx.x < 256) hist[threadIdx.x] = 0;
-    __syncthreads();
-    for (int64_t s = threadIdx.x; s < n_c; s += blockDim.x) {
-      const uint32_t key = score_key(sc[s]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFF], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int cum = 0, d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= need) break;
-        cum += hist[d];
-      }
-      s_need = need - cum;
-      s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
-    }
-    __syncthreads();
-    need = s_need;
-    prefix = s_prefix;
-    mask |= 0xFFu << shift;
-    __syncthreads();
-  }
-  // prefix is now the exact key of the k-th largest score; take `need` of its ties.
-  int taken = 0, ties = 0;
-  for (int64_t base = 0; base < n_c; base += blockDim.x) {
+  const float* sc = a.scores + static_cast<int64_t>(b) * a.capacity;
+  uint32_t* cnt = a.cnt + b * 4;      // [0] above, [1] cand, [2] finished CTAs
+  int32_t* above = a.above + static_cast<int64_t>(b) * k;
+  uint64_t* cand = a.cand + static_cast<int64_t>(b) * a.capacity;
+  uint32_t* hist2 = a.hist2 + static_cast<int64_t>(b) * kBins;
+
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = a.hist1[static_cast<int64_t>(b) * kBins + i];
+  __syncthreads();
+  uint32_t n_gt1;
+  const uint32_t T1 = static_cast<uint32_t>(suffix_select(h, static_cast<uint32_t>(k), &n_gt1, part));
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+
+  const int64_t chunk = (n_c + gridDim.x - 1) / gridDim.x;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
+  const int64_t c1 = c0 + chunk < n_c ? c0 + chunk : n_c;
+  for (int64_t base = c0; base < c1; base += blockDim.x) {
     const int64_t s = base + threadIdx.x;
-    const uint32_t key = s < n_c ? score_key(sc[s]) : 0u;
-    const bool eq = s < n_c && key == prefix;
-    const bool gt = s < n_c && key > prefix;
-    const int tie_rank = ties + block_prefix(eq, warp_tot, &total);
-    const int tie_total = total;
-    const bool take = gt || (eq && tie_rank < need);
-    const int pos = taken + block_prefix(take, warp_tot, &total);
-    if (take && pos < a.k) out[pos] = static_cast<int32_t>(s);
-    taken += total;
-    ties += tie_total;
-    __syncthreads();
+    const bool in = s < c1;
+    const uint32_t key = in ? score_key(sc[s]) : 0u;
+    const uint32_t bin = key >> 20;
+    const bool gt = in && bin > T1;
+    const bool eq = in && bin == T1;
+    warp_append_i32(gt, static_cast<int32_t>(s), &cnt[0], above, static_cast<uint32_t>(k));
+    warp_append_u64(eq, (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(s), &cnt[1], cand,
+                    static_cast<uint32_t>(a.capacity));
+    if (eq) atomicAdd(&h[(key >> 8) & 0xFFF], 1u);
   }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x)
+    if (h[i]) atomicAdd(&hist2[i], h[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&cnt[2], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- the last CTA of sequence b resolves the boundary
+  uint32_t n_above = *reinterpret_cast<volatile uint32_t*>(&cnt[0]);
+  uint32_t n_cand = *reinterpret_cast<volatile uint32_t*>(&cnt[1]);
+  if (n_above > static_cast<uint32_t>(k)) n_above = k;                      // only on inconsistent input
+  if (n_cand > static_cast<uint32_t>(a.capacity)) n_cand = a.capacity;
+  const uint32_t need1 = static_cast<uint32_t>(k) - n_above;                 // taken from cand
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = reinterpret_cast<volatile uint32_t*>(hist2)[i];
+  for (uint32_t i = threadIdx.x; i < n_above; i += blockDim.x) fin[i] = reinterpret_cast<volatile int32_t*>(above)[i];
+  if (threadIdx.x == 0) s_nfin = n_above;
+  __syncthreads();
+  uint32_t n_gt2;
+  const uint32_t T2 = static_cast<uint32_t>(suffix_select(h, need1, &n_gt2, part));
+  const uint32_t need2 = need1 - n_gt2;                                      // taken among the keys of bin (T1, T2)
+  // Candidates strictly above T2 are in; ties at (T1, T2) are ranked by the low
+  // 8 key bits, then the lower index: radix select of the need2-th largest
+  // 40-bit rank (low8 << 32 | ~index) among them.
+  uint64_t thr_rank = 0;
+  const uint32_t n_eq2 = h[T2];
+  if (need2 < n_eq2) {
+    uint64_t prefix = 0, mask = 0;
+    uint32_t remaining = need2;
+    for (int pass = 0; pass < 5; ++pass) {
+      const int shift = 32 - 8 * pass;                                       // bits 39..32, 31..24, ..., 7..0
+      __syncthreads();
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
+        const uint64_t v = reinterpret_cast<volatile uint64_t*>(cand)[i];
+        const uint32_t key = static_cast<uint32_t>(v >> 32);
+        if (((key >> 8) & 0xFFF) != T2) continue;
+        const uint64_t rank = (static_cast<uint64_t>(key & 0xFF) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(v));
+        if ((rank & mask) == prefix) atomicAdd(&h[(rank >> shift) & 0xFF], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        uint32_t cum = 0;
+        int d = 255;
+        for (; d > 0; --d) {
+          if (cum + h[d] >= remaining) break;
+          cum += h[d];
+        }
+        s_d = static_cast<uint32_t>(d);
+        s_rem = remaining - cum;
+      }
+      __syncthreads();
+      prefix |= static_cast<uint64_t>(s_d) << shift;
+      mask |= static_cast<uint64_t>(0xFF) << shift;
+      remaining = s_rem;
+    }
+    thr_rank = prefix;                                                       // exactly need2 ranks are >= prefix
+  }
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
+    const uint64_t v = reinterpret_cast<volatile uint64_t*>(cand)[i];
+    const uint32_t key = static_cast<uint32_t>(v >> 32);
+    const uint32_t b2 = (key >> 8) & 0xFFF;
+    bool take = b2 > T2;
+    if (b2 == T2) {
+      const uint64_t rank = (static_cast<uint64_t>(key & 0xFF) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(v));
+      take = need2 > 0 && rank >= thr_rank;
+    }
+    if (take) {
+      const uint32_t pos = atomicAdd(&s_nfin, 1u);
+      if (pos < static_cast<uint32_t>(k)) fin[pos] = static_cast<int32_t>(static_cast<uint32_t>(v));
+    }
+  }
+  __syncthreads();
+  // bitonic sort of the k indices (padded to a power of two with INT_MAX), ascending
+  int P = 1;
+  while (P < k) P <<= 1;
+  for (int i = threadIdx.x + k; i < P; i += blockDim.x) fin[i] = 0x7FFFFFFF;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const int32_t x = fin[lo], y = fin[hi];
+        if ((x > y) == asc) {
+          fin[lo] = y;
+          fin[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = fin[i];
 }
 
 }  // namespace dsv4

@@ -9,18 +9,20 @@
 // runs as D[128 keys][N heads] = K_tile[128][Di] x Q[N][Di]^T per tile of 128
 // compressed blocks, with the per-16 e4m3 scales of keys and query applied by
 // the MMA itself (UE4M3 block scales). The epilogue applies ReLU and the head
-// weights and writes one fp32 score per block.
+// weights, writes one fp32 score per block and histograms the top 12 bits of
+// the score keys for the top-k selection that follows.
 //
-// CTA roles (192 threads): warp 0 allocates tensor memory and streams key tiles
-// with TMA into an S-stage ring; warp 1 issues the MMAs (one thread); warps 2-5
-// (one per 32-lane quarter of tensor memory) load the block scales into tensor
-// memory ahead of the MMA and turn finished accumulators into scores. The
-// accumulator and the key-scale slots are double-buffered so that the MMA of
-// tile i+1 overlaps the epilogue of tile i.
+// CTA roles (256 threads): warp 0 allocates tensor memory and streams key tiles
+// with TMA into an S-stage ring; warp 1 issues tcgen05.cp (block scales) and
+// the MMAs (one thread); warps 2-3 rearrange each tile's key scales in shared
+// memory into the 32-row x 16-byte blocks that tcgen05.cp moves to tensor
+// memory; warps 4-7 (one per 32-lane quarter of tensor memory) turn finished
+// accumulators into scores. The accumulator and the scale slots are
+// double-buffered so the MMA of tile i+1 overlaps the epilogue of tile i.
 //
-// Block scales in tensor memory: row r's four scale bytes of one K=64 step (one
-// byte per 16 elements, the first block in the lowest byte) are stored in lane r
-// in each of four consecutive columns.
+// Scale block layout (one per 128 rows and K=64 step): row r's four scale bytes
+// (one per 16 elements, the first in the lowest byte) form the 32-bit word at
+// word index (r % 32) * 4 + r / 32.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,22 +37,28 @@ namespace dsv4 {
 namespace {
 
 constexpr int kTile = 128;     // compressed blocks per MMA tile (M)
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
+constexpr int kSfBlock = 512;  // bytes of one scale block (128 rows x 4 scales)
 
 template <int ROWB>
 struct TcCfg {
   static constexpr int KSTEPS = ROWB / 32;                   // K = 64 e2m1 values = 32 bytes per MMA
   static constexpr int STAGES = ROWB <= 64 ? 8 : 6;
   static constexpr int STAGE_BYTES = kTile * ROWB;
+  static constexpr int SF_BYTES = KSTEPS * kSfBlock;          // one tile's key scales
   static constexpr uint32_t SWIZZLE = ROWB == 32 ? tc::kSwizzle32B : ROWB == 64 ? tc::kSwizzle64B : tc::kSwizzle128B;
   static constexpr int SF_COLS = 4 * KSTEPS;                  // tensor-memory columns of one tile's scales
 };
 
 struct SmemTail {
-  uint64_t full[8], empty[8], acc_full[2], acc_empty[2], sf_full[2], q_full, drain;
+  uint64_t full[8], empty[8], sf_full[8], acc_full[2], acc_empty[2], q_full, qsf_full, drain;
   uint32_t taddr;
   int abort;
+  uint32_t hist[4096];   // histogram of score-key bits 31..20 of this CTA's blocks
 };
+
+// named barrier among the four epilogue warps
+DSV4_DEV void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 }  // namespace
 
@@ -60,11 +68,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                            IndexTcArgs a) {
   using C = TcCfg<ROWB>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // 1024-byte alignment for the swizzled tiles
-  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* stages = base;
-  unsigned char* qbuf = stages + C::STAGES * C::STAGE_BYTES;
-  SmemTail* t = reinterpret_cast<SmemTail*>(qbuf + ((a.N * ROWB + 1023) & ~1023));
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stages = base;                                           // S x 128 x ROWB key codes
+  unsigned char* qbuf = stages + C::STAGES * C::STAGE_BYTES;              // N x ROWB query codes
+  unsigned char* sfbuf = qbuf + ((a.N * ROWB + 1023) & ~1023);           // S x SF_BYTES key scale blocks
+  unsigned char* qsf = sfbuf + C::STAGES * C::SF_BYTES;                   // query scale blocks (N <= 128 rows)
+  SmemTail* t = reinterpret_cast<SmemTail*>(qsf + C::SF_BYTES);
   float* wsm = reinterpret_cast<float*>(t + 1);
 
   const int b = blockIdx.y;
@@ -79,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
+  const int nblk = ROWB / 8;                               // Di/16 scale bytes per row
   const uint32_t ncols = a.tmem_cols;
   const uint32_t acc_col0 = 0, sfa_col0 = 2 * N, sfb_col = 2 * N + 2 * C::SF_COLS;
   volatile int* abort = &t->abort;
@@ -88,13 +99,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::STAGES; ++i) {
       tc::mbar_init(&t->full[i], 1);
       tc::mbar_init(&t->empty[i], 1);
+      tc::mbar_init(&t->sf_full[i], 2);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&t->acc_full[i], 1);
       tc::mbar_init(&t->acc_empty[i], 4);
-      tc::mbar_init(&t->sf_full[i], 4);
     }
     tc::mbar_init(&t->q_full, 1);
+    tc::mbar_init(&t->qsf_full, 2);
     tc::mbar_init(&t->drain, 1);
     t->abort = 0;
     tc::fence_mbar_init();
@@ -121,75 +133,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                         static_cast<int>(static_cast<int64_t>(b) * a.capacity + static_cast<int64_t>(t0 + i) * kTile));
         ++issued;
       }
-      if (*abort) {
-        // let the copies already issued land before the CTA's shared memory goes away
-        for (int i = issued - C::STAGES > 0 ? issued - C::STAGES : 0; i < issued; ++i) {
-          const int stage = i % C::STAGES, round = i / C::STAGES;
-          for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->full[stage], round & 1); ++it) {
-          }
+      // every copy issued must land before the CTA's shared memory goes away
+      for (int i = issued - C::STAGES > 0 ? issued - C::STAGES : 0; i < issued; ++i) {
+        const int stage = i % C::STAGES, round = i / C::STAGES;
+        for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->full[stage], round & 1); ++it) {
         }
+      }
+      for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->q_full, 0); ++it) {
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ tcgen05.cp + MMA issuer
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_mxf4nvf4(kTile, N);
       const uint32_t q_addr = tc::smem_u32(qbuf);
-      bool ok = tc::mbar_wait(&t->q_full, 0, abort);
+      bool ok = tc::mbar_wait(&t->q_full, 0, abort) && tc::mbar_wait(&t->qsf_full, 0, abort);
+      if (ok) {
+        tc::tc_fence_after();
+        for (int kk = 0; kk < C::KSTEPS; ++kk)
+          tc::tmem_cp_32x128b_warpx4(taddr + sfb_col + kk * 4, tc::smem_desc_rows16(tc::smem_u32(qsf + kk * kSfBlock)));
+      }
       for (int i = 0; ok && i < ntile; ++i) {
         const int stage = i % C::STAGES, round = i / C::STAGES;
         const int ab = i & 1, ra = i >> 1;
         if (!tc::mbar_wait(&t->full[stage], round & 1, abort)) break;
-        if (!tc::mbar_wait(&t->sf_full[ab], ra & 1, abort)) break;
+        if (!tc::mbar_wait(&t->sf_full[stage], round & 1, abort)) break;
         if (!tc::mbar_wait(&t->acc_empty[ab], (ra & 1) ^ 1, abort)) break;
         tc::tc_fence_after();
         const uint32_t a_addr = tc::smem_u32(stages + stage * C::STAGE_BYTES);
+        const uint32_t sf_addr = tc::smem_u32(sfbuf + stage * C::SF_BYTES);
+        const uint32_t sfa = taddr + sfa_col0 + ab * C::SF_COLS;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk)
+          tc::tmem_cp_32x128b_warpx4(sfa + kk * 4, tc::smem_desc_rows16(sf_addr + kk * kSfBlock));
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
           const uint64_t adesc = tc::smem_desc(a_addr + kk * 32, 8 * ROWB, C::SWIZZLE);
           const uint64_t bdesc = tc::smem_desc(q_addr + kk * 32, 8 * ROWB, C::SWIZZLE);
-          tc::mma_mxf4nvf4(taddr + acc_col0 + ab * N, adesc, bdesc, idesc, taddr + sfa_col0 + ab * C::SF_COLS + kk * 4,
-                           taddr + sfb_col + kk * 4, kk > 0 ? 1u : 0u);
+          tc::mma_mxf4nvf4(taddr + acc_col0 + ab * N, adesc, bdesc, idesc, sfa + kk * 4, taddr + sfb_col + kk * 4,
+                           kk > 0 ? 1u : 0u);
         }
         tc::tc_commit(&t->empty[stage]);
         tc::tc_commit(&t->acc_full[ab]);
       }
-      // every MMA issued must finish before tensor memory is released
+      // every tcgen05 operation issued must finish before tensor memory is released
       tc::tc_commit(&t->drain);
       for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->drain, 0); ++it) {
       }
     }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ scale-block builders (64 threads)
+    const int tid = threadIdx.x - 64;
+    // query scales: rows >= N (padding heads) are zero
+    for (int r = tid; r < kTile; r += 64) {
+      const uint8_t* src = a.q_scales + (static_cast<int64_t>(b) * N + r) * nblk;
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        const uint32_t w = r < N ? *reinterpret_cast<const uint32_t*>(src + kk * 4) : 0u;
+        reinterpret_cast<uint32_t*>(qsf + kk * kSfBlock)[(r & 31) * 4 + (r >> 5)] = w;
+      }
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&t->qsf_full);
+    for (int i = 0; i < ntile; ++i) {
+      const int stage = i % C::STAGES, round = i / C::STAGES;
+      if (!tc::mbar_wait(&t->empty[stage], (round & 1) ^ 1, abort)) break;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(sfbuf + stage * C::SF_BYTES);
+      for (int r = tid; r < kTile; r += 64) {
+        const int64_t s = static_cast<int64_t>(t0 + i) * kTile + r;
+        const uint8_t* src = a.idx_scales + (static_cast<int64_t>(b) * a.capacity + s) * nblk;
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+          const uint32_t w = s < n_c ? *reinterpret_cast<const uint32_t*>(src + kk * 4) : 0u;
+          dst[kk * (kSfBlock / 4) + (r & 31) * 4 + (r >> 5)] = w;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&t->sf_full[stage]);
+    }
   } else {
-    // ------------------------------------------------------------ scales + epilogue
+    // ------------------------------------------------------------ epilogue (warps 4-7)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                  // tensor-memory lane == tile row
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int nblk = ROWB / 8;                            // Di/16 scale bytes per row
-    auto write_sfa = [&](int j) {
-      const int64_t s = static_cast<int64_t>(t0 + j) * kTile + row;
-      const uint8_t* src = a.idx_scales + (static_cast<int64_t>(b) * a.capacity + s) * nblk;
-#pragma unroll
-      for (int kk = 0; kk < C::KSTEPS; ++kk) {
-        const uint32_t w = s < n_c ? *reinterpret_cast<const uint32_t*>(src + kk * 4) : 0u;
-        tc::tmem_st_x4_same(taddr + lane_base + sfa_col0 + (j & 1) * C::SF_COLS + kk * 4, w);
-      }
-    };
-    // query scales (rows >= N are padding heads: zero)
-    {
-      const uint8_t* src = a.q_scales + (static_cast<int64_t>(b) * N + row) * nblk;
-#pragma unroll
-      for (int kk = 0; kk < C::KSTEPS; ++kk) {
-        const uint32_t w = row < N ? *reinterpret_cast<const uint32_t*>(src + kk * 4) : 0u;
-        tc::tmem_st_x4_same(taddr + lane_base + sfb_col + kk * 4, w);
-      }
-    }
-    for (int j = 0; j < 2 && j < ntile; ++j) {
-      write_sfa(j);
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&t->sf_full[j]);
-    }
+    for (int i = row; i < 4096; i += 128) t->hist[i] = 0;
+    epilogue_sync();
     float* out = a.scores + static_cast<int64_t>(b) * a.capacity;
     for (int i = 0; i < ntile; ++i) {
       const int ab = i & 1, ra = i >> 1;
@@ -207,15 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t->acc_empty[ab]);
       const int64_t s = static_cast<int64_t>(t0 + i) * kTile + row;
-      if (s < n_c) out[s] = score;
-      if (i + 2 < ntile) {
-        write_sfa(i + 2);
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&t->sf_full[ab]);
+      if (s < n_c) {
+        out[s] = score;
+        atomicAdd(&t->hist[score_key(score) >> 20], 1u);
       }
     }
+    epilogue_sync();
+    uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * 4096;
+    for (int i = row; i < 4096; i += 128)
+      if (t->hist[i]) atomicAdd(&gh[i], t->hist[i]);
   }
 
   tc::tc_fence_before();
@@ -261,7 +289,8 @@ bool encode_rows(CUtensorMap* map, const void* base, int rowbytes, int64_t rows,
 template <int ROWB>
 int launch_tc(const IndexTcArgs& a, const CUtensorMap& keys, const CUtensorMap& qmap, cudaStream_t st) {
   using C = TcCfg<ROWB>;
-  size_t smem = 1024 + C::STAGES * C::STAGE_BYTES + ((a.N * ROWB + 1023) & ~1023) + sizeof(SmemTail) + a.N * 4;
+  size_t smem = 1024 + C::STAGES * (C::STAGE_BYTES + C::SF_BYTES) + ((a.N * ROWB + 1023) & ~1023) + C::SF_BYTES +
+                sizeof(SmemTail) + a.N * 4;
   // keep at most two CTAs per SM so that their tensor-memory allocations always fit
   const size_t floor_bytes = a.tmem_cols > 256 ? 120 * 1024 : 80 * 1024;
   if (smem < floor_bytes) smem = floor_bytes;

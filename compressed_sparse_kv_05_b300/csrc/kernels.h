@@ -42,6 +42,11 @@ struct IndexArgs {
   float* wpad;             // [B][N] head weights, zero for padding heads
   float* scores;           // [B][capacity]
   int32_t* topk;           // [B][k]
+  uint32_t* hist1;         // [B][4096] histogram of score-key bits 31..20 (filled while scoring)
+  uint32_t* hist2;         // [B][4096] histogram of key bits 19..8 inside the threshold bin
+  uint32_t* cnt;           // [B][4] above count, candidate count, finished select CTAs
+  int32_t* above;          // [B][k] blocks above the threshold bin
+  uint64_t* cand;          // [B][capacity] (key << 32 | index) of the blocks in the threshold bin
 };
 __global__ void quant_query_fp4_kernel(IndexArgs a);
 __global__ void topk_select_kernel(IndexArgs a);
@@ -54,6 +59,7 @@ struct IndexTcArgs {
   const uint8_t* q_scales;     // [B][N][Di/16]
   const float* wpad;           // [B][N]
   float* scores;               // [B][capacity]
+  uint32_t* hist1;             // [B][4096]
   int32_t* status;
 };
 // tcgen05 block-scaled FP4 scores; key_codes [B][capacity][Di/2], q_codes [B][N][Di/2]

@@ -112,7 +112,19 @@ DSV4_DEV void tmem_st_x4_same(uint32_t taddr, uint32_t w) {
 
 DSV4_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// ---- shared-memory matrix descriptor (K-major operand, swizzled rows)
+// Copy a 32-row x 16-byte shared-memory block (described by `desc`) into tensor
+// memory at `taddr`, the same data in each of the four 32-lane quarters: row l
+// lands in lane l of every quarter, its four 32-bit words in four consecutive
+// columns. This is the form block-scale factors take in tensor memory.
+DSV4_DEV void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tcgen05.cp, tcgen05.mma operand reads).
+DSV4_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---- shared-memory matrix descriptors
 // bits 0-13 start address >> 4, 16-29 leading byte offset >> 4 (unused for a
 // swizzled K-major tile whose K extent fits one swizzle atom), 32-45 stride byte
 // offset >> 4 (distance between 8-row groups), 46-47 descriptor version (1),
@@ -132,6 +144,19 @@ DSV4_DEV uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes, uint32_t swizzle
 // Instruction descriptor of kind::mxf4nvf4 (e2m1 x e2m1, UE4M3 block scales,
 // fp32 accumulate), both operands K-major: a/b format E2M1 (bits 7-9, 10-12),
 // N >> 3 (bits 17-22), scale type UE4M3 (bit 23 = 0), M >> 4 (bits 24-28).
+// Descriptor of an unswizzled block of 16-byte rows stored back to back (the
+// scale-factor blocks): core matrices of 8 rows x 16 bytes, 128 bytes apart.
+// The leading and stride offsets are both 128 bytes (only one core matrix
+// along the 16-byte direction exists, so the leading offset is never used).
+DSV4_DEV uint64_t smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
