@@ -14,8 +14,9 @@ import oracle as O
 from compressed_sparse_kv_05_b300 import dsv4, synth
 from compressed_sparse_kv_05_b300 import workloads as W
 
-from .gpu_util import (check_topk, compare_bf16, compare_fp4_rows, compare_fp8_entries, gpu_cache_from_planes, gpu_stream_cache,
-                       oracle_direct_planes, oracle_stream_cache, row_rel_err, to_dev, to_host)
+from .gpu_util import (check_topk, compare_bf16, compare_fp4_rows, compare_fp8_entries, gpu_cache_from_planes,
+                       gpu_stream_cache, oracle_direct_planes, oracle_stream_cache, pooling_error_bound, row_rel_err,
+                       to_dev, to_host)
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
@@ -116,15 +117,20 @@ def test_append_builds_oracle_cache(layer, n):
     oc = oracle_stream_cache(layer, "append", 0, n, 0)
     n_c = n // layer.ratio
     assert to_host(cache.n_tokens)[0] == n
+    dk = pooling_error_bound(oc["tokens"]["k"], layer.ratio)
     compare_fp8_entries(to_host(cache.k_nope)[0, :n_c], to_host(cache.k_scale)[0, :n_c], oc["k_nope"], oc["k_scale"],
-                        oc["pooled_k"], layer.d_nope)
-    compare_bf16(to_host(cache.k_rope, np.uint16)[0, :n_c], oc["k_rope"], oc["pooled_k"][:, layer.d_nope:])
+                        oc["pooled_k"], layer.d_nope, dk)
+    compare_bf16(to_host(cache.k_rope, np.uint16)[0, :n_c], oc["k_rope"], oc["pooled_k"][:, layer.d_nope:],
+                 dk[:, layer.d_nope:])
     if layer.separate_v:
+        dv = pooling_error_bound(oc["tokens"]["v"], layer.ratio)
         compare_fp8_entries(to_host(cache.v_nope)[0, :n_c], to_host(cache.v_scale)[0, :n_c], oc["v_nope"],
-                            oc["v_scale"], oc["pooled_v"], layer.d_nope)
+                            oc["v_scale"], oc["pooled_v"], layer.d_nope, dv)
+        compare_bf16(to_host(cache.v_rope, np.uint16)[0, :n_c], oc["v_rope"], oc["pooled_v"][:, layer.d_nope:],
+                     dv[:, layer.d_nope:])
     if layer.idx_dim:
         compare_fp4_rows(to_host(cache.idx_codes)[0, :n_c], to_host(cache.idx_scales)[0, :n_c], oc["idx_codes"],
-                         oc["idx_scales"], oc["pooled_u"])
+                         oc["idx_scales"], oc["pooled_u"], pooling_error_bound(oc["tokens"]["u"], layer.ratio))
     ring = to_host(cache.win_k, np.uint16)[0]
     for slot, tok in oc["ring_slots"].items():
         assert np.array_equal(ring[slot], oc["tokens"]["k"][tok])
