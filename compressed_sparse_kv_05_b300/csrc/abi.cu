@@ -11,7 +11,9 @@
 namespace dsv4 {
 namespace {
 
-constexpr int kSplitTarget = 2 * 148;  // CTAs the split-K attention aims for (2 per SM of a B300)
+constexpr int kSms = 148;                // streaming multiprocessors of a B300
+constexpr int kSplitTarget = 2 * kSms;  // CTAs the CUDA-core split-K attention aims for
+constexpr int kTcTile = 128;            // rows per tile of the tensor-core attention
 constexpr int kRowTile = 16;
 constexpr int kHeadGroup = 64;
 
@@ -59,6 +61,7 @@ int check_cache_read(const dsv4_layer_desc* d, const dsv4_cache* c) {
 
 struct AttnPlan {
   int head_groups, splits, rows_per_split;
+  bool tc;
   size_t ws_bytes;
 };
 
@@ -66,6 +69,20 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
   AttnPlan p{};
   p.head_groups = (H + kHeadGroup - 1) / kHeadGroup;
   const int64_t rmax = static_cast<int64_t>(n_sel > 0 ? n_sel : d->capacity) + d->window;
+  const size_t Dv = static_cast<size_t>(d->d_nope + d->d_rope);
+  p.tc = attention_tc_supported(H, d->d_nope, d->d_rope, d->separate_v);
+  if (p.tc) {
+    // tiles of 128 rows spread evenly over one wave of CTAs (one per SM)
+    const int64_t tiles = (rmax + kTcTile - 1) / kTcTile;
+    const int64_t total = tiles * d->batch * p.head_groups;
+    const int64_t per_cta = (total + kSms - 1) / kSms;
+    const int64_t rps = per_cta * kTcTile;
+    p.rows_per_split = static_cast<int>(rps);
+    p.splits = static_cast<int>((rmax + rps - 1) / rps);
+    if (p.splits < 1) p.splits = 1;
+    p.ws_bytes = static_cast<size_t>(d->batch) * H * p.splits * (Dv + 1) * sizeof(float) + 256;
+    return p;
+  }
   const int64_t want = (kSplitTarget + d->batch * p.head_groups - 1) / (d->batch * p.head_groups);
   const int64_t max_splits = (rmax + kRowTile - 1) / kRowTile;
   int64_t s = want < max_splits ? want : max_splits;
@@ -76,7 +93,6 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
   if (s < 1) s = 1;
   p.splits = static_cast<int>(s);
   p.rows_per_split = static_cast<int>(rps);
-  const size_t Dv = static_cast<size_t>(d->d_nope + d->d_rope);
   p.ws_bytes = static_cast<size_t>(d->batch) * H * p.splits * (Dv + 1) * sizeof(float) + 256;
   return p;
 }
@@ -142,6 +158,7 @@ int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const ui
   off = (off + 255) & ~static_cast<size_t>(255);
   a.part_lse = reinterpret_cast<float*>(w + off);
   a.out = out; a.lse = lse;
+  if (p.tc) return launch_attention_tc(a, p.head_groups, static_cast<cudaStream_t>(stream));
   return launch_attention(a, p.head_groups, static_cast<cudaStream_t>(stream));
 }
 

@@ -228,6 +228,10 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
     e = need <= 32 ? launch_split<64, 32>(a, grid, smem, st)
         : need <= 64 ? launch_split<64, 64>(a, grid, smem, st) : launch_split<64, 144>(a, grid, smem, st);
   if (e) return e;
+  return launch_attention_merge(a, st);
+}
+
+int launch_attention_merge(const AttnArgs& a, cudaStream_t st) {
   attn_merge_kernel<<<a.B * a.H, 128, 0, st>>>(a);
   return launch_status();
 }

@@ -1,0 +1,596 @@
+// CSA / HCA decode attention on the 5th-generation tensor cores (tcgen05
+// kind::f16, fp32 accumulators in tensor memory).
+//
+// vibecoco.ai, "DeepSeek V4 agent architecture", section
+// "混合注意力：两种压缩，交替使用": CSA attends over the top-k compressed blocks
+// plus a sliding window of recent raw tokens, HCA densely over every
+// compressed entry plus the window; every query head shares the one KV head.
+// pnsm.cn, "DeepSeek V4 架构深度解析…", section 2.1 "CSA：压缩稀疏注意力": the
+// window and the compressed KV feed one attention (one softmax over the union).
+//
+// All query heads read the same rows, so a decode step is a pair of dense
+// contractions per tile of 128 rows:
+//   X   [128 rows][D]  f16: each row's dequantised key (code * scale || rope, or
+//                      the raw window token); it is also the value row when K = V
+//   S^T [128][64]      = X . Q^T             (M = 128 rows, N = 64 heads, K = D)
+//   P   [128][64]      = exp2(S^T * c - m)   (f16, the running max m per head)
+//   O^T [D][64]       += X^T . P             (M = 128 dims per block, N = 64, K = 128 rows)
+// X is written once per tile in the 128-byte-swizzled layout that serves as a
+// K-major operand for the first product and as an MN-major operand for the
+// second; S^T and O^T live in tensor memory (lane = row / dim, column = head).
+//
+// CTA roles (384 threads, one CTA per SM for D = 512):
+//   warp 0      allocates tensor memory, prefetches the CTA's rows into L2, and
+//               one lane issues every MMA;
+//   warps 1-3, 8-11  (224 threads) dequantise rows into X, chunk by chunk of
+//               128 dims, as soon as the previous tile's P.V no longer reads it;
+//   warps 4-7   (one per 32-lane quarter of tensor memory, one row each) turn
+//               S^T into P. The running max per head only moves when a score
+//               exceeds it by more than 2^8 (then the tile's column max is
+//               reduced and O^T, l rescaled), so P <= 256 always fits f16.
+//               After the last tile they normalise O^T and write this split's
+//               partial output and log-sum-exp.
+// Splits are merged by attn_merge_kernel (attention.cu).
+//
+// Precision: K, V and P are rounded to f16 (relative error <= 2^-11 each), the
+// bf16 query converts to f16 exactly for |q| in [2^-14, 65504]; products and
+// sums are fp32. A value that does not fit f16 (|x| >= 65504) raises
+// DSV4_STATUS_RANGE.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace dsv4 {
+
+namespace {
+
+constexpr int kRows = 128;                     // rows per tile
+constexpr int kHeads = 64;                     // heads per CTA (MMA N), zero-padded
+constexpr int kThreads = 384;
+constexpr int kConvThreads = 7 * 32;           // warps 1-3 and 8-11
+constexpr int kGroups = kRows * 16;            // 8-dim groups of one 128-dim chunk
+constexpr int kItems = (kGroups + kConvThreads - 1) / kConvThreads;
+constexpr int kAtomBytes = kRows * 128;        // 128 rows x 64 dims f16
+constexpr int kChunkBytes = 2 * kAtomBytes;    // 128 rows x 128 dims f16
+constexpr int kQAtomBytes = kHeads * 128;      // 64 heads x 64 dims f16
+constexpr int kPBytes = kRows * kHeads * 2;
+constexpr int kMaxChunks = 4;                  // D <= 512
+constexpr int kBarSoftmax = 1, kBarConv = 2;   // named barriers (0 is __syncthreads)
+constexpr float kRescale = 8.f;                // lazy-rescale threshold (log2 units)
+constexpr float kF16Max = 65504.f;
+
+struct TcTail {
+  uint64_t xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, drain;
+  uint32_t taddr;
+  int abort;
+  int32_t rt[2][kRows];     // row sources of a tile, by tile parity
+  float sk[2][kRows];       // key scale of each row
+  float sv[2][kRows];       // value scale (separate V)
+  float m_used[kHeads];     // running max per head, log2 domain
+  float alpha[kHeads];
+  float lsum[kHeads];
+  float red[4][kHeads];
+};
+
+DSV4_DEV uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two e4m3 codes (low byte first) times s, rounded to two f16.
+DSV4_DEV uint32_t e4m3x2_scaled_to_f16x2(uint32_t pair, float s) {
+  uint32_t out;
+  asm("{\n"
+      ".reg .b32 h2;\n"
+      ".reg .b16 l, u, p;\n"
+      ".reg .f32 f0, f1;\n"
+      "cvt.u16.u32 p, %1;\n"
+      "cvt.rn.f16x2.e4m3x2 h2, p;\n"
+      "mov.b32 {l, u}, h2;\n"
+      "cvt.f32.f16 f0, l;\n"
+      "cvt.f32.f16 f1, u;\n"
+      "mul.rn.f32 f0, f0, %2;\n"
+      "mul.rn.f32 f1, f1, %2;\n"
+      "cvt.rn.f16x2.f32 %0, f1, f0;\n"
+      "}"
+      : "=r"(out)
+      : "r"(pair), "f"(s));
+  return out;
+}
+
+DSV4_DEV uint32_t bf16x2_to_f16x2(uint32_t w, float& mx) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+  return f32x2_to_f16x2(lo, hi);
+}
+
+DSV4_DEV uint4 bf16x8_to_f16x8(uint4 w, float& mx) {
+  return make_uint4(bf16x2_to_f16x2(w.x, mx), bf16x2_to_f16x2(w.y, mx), bf16x2_to_f16x2(w.z, mx),
+                    bf16x2_to_f16x2(w.w, mx));
+}
+
+DSV4_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+DSV4_DEV uint4 ldg16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+DSV4_DEV uint2 ldg8(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+// Rows of sequence b are numbered: first the compressed entries (the top-k list
+// for CSA, every entry for HCA), then the window tokens, oldest first.
+struct RowSpace {
+  int64_t n_tok, n_c, n_win, n_main, R;
+};
+
+DSV4_DEV RowSpace row_space(const AttnArgs& a, int b) {
+  RowSpace s;
+  s.n_tok = a.n_tokens[b];
+  s.n_c = s.n_tok / a.ratio < a.capacity ? s.n_tok / a.ratio : a.capacity;
+  s.n_win = s.n_tok < a.window ? s.n_tok : a.window;
+  s.n_main = a.n_sel > 0 ? a.n_sel : s.n_c;
+  s.R = s.n_main + s.n_win;
+  return s;
+}
+
+// Source of row r: >= 0 entry index into the planes (b * capacity + e), -1 no
+// row (past the split, a -1 top-k slot or an invalid index), <= -2 window ring
+// slot (-2 - slot).
+DSV4_DEV int32_t row_source(const AttnArgs& a, const RowSpace& s, int b, int64_t r, int64_t r1, bool flag_bad) {
+  if (r >= r1) return -1;
+  if (r < s.n_main) {
+    const int64_t e = a.n_sel > 0 ? static_cast<int64_t>(a.topk[static_cast<int64_t>(b) * a.n_sel + r]) : r;
+    if (e < -1 || e >= s.n_c) {
+      if (flag_bad) atomicOr(a.status, DSV4_STATUS_BAD_INDEX);
+      return -1;
+    }
+    if (e < 0) return -1;
+    return static_cast<int32_t>(static_cast<int64_t>(b) * a.capacity + e);
+  }
+  const int64_t pos = s.n_tok - s.n_win + (r - s.n_main);
+  return static_cast<int32_t>(-2 - pos % a.window);
+}
+
+// [p, p + bytes) into L2, both ends rounded down to 16 bytes (never past the range).
+DSV4_DEV void prefetch_range(const void* p, int64_t bytes) {
+  const uintptr_t lo = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes) & ~static_cast<uintptr_t>(15);
+  for (uintptr_t x = lo; x < hi; x += (1u << 20)) {
+    const uintptr_t n = hi - x < (1u << 20) ? hi - x : (1u << 20);
+    tc::prefetch_l2_bulk(reinterpret_cast<const void*>(x), static_cast<uint32_t>(n));
+  }
+}
+
+// Warp 0: hint L2 to fetch every byte this CTA's rows [r0, r1) read.
+DSV4_DEV void prefetch_rows(const AttnArgs& a, const RowSpace& s, int b, int64_t r0, int64_t r1, bool sep, int lane) {
+  const int64_t m1 = r1 < s.n_main ? r1 : s.n_main;
+  const int64_t base = static_cast<int64_t>(b) * a.capacity;
+  if (m1 > r0) {
+    if (a.n_sel == 0) {
+      const int64_t e0 = base + r0, n = m1 - r0;
+      if (lane == 0) prefetch_range(a.k_nope + e0 * a.d_nope, n * a.d_nope);
+      if (lane == 1 && a.d_rope) prefetch_range(a.k_rope + e0 * a.d_rope, n * a.d_rope * 2);
+      if (lane == 2) prefetch_range(a.k_scale + e0, n * 4);
+      if (sep && lane == 3) prefetch_range(a.v_nope + e0 * a.d_nope, n * a.d_nope);
+      if (sep && lane == 4 && a.d_rope) prefetch_range(a.v_rope + e0 * a.d_rope, n * a.d_rope * 2);
+      if (sep && lane == 5) prefetch_range(a.v_scale + e0, n * 4);
+    } else {
+      for (int64_t r = r0 + lane; r < m1; r += 32) {
+        const int64_t e = a.topk[static_cast<int64_t>(b) * a.n_sel + r];
+        if (e < 0 || e >= s.n_c) continue;
+        const int64_t row = base + e;
+        prefetch_range(a.k_nope + row * a.d_nope, a.d_nope);
+        if (a.d_rope) prefetch_range(a.k_rope + row * a.d_rope, a.d_rope * 2);
+        if (sep) {
+          prefetch_range(a.v_nope + row * a.d_nope, a.d_nope);
+          if (a.d_rope) prefetch_range(a.v_rope + row * a.d_rope, a.d_rope * 2);
+        }
+      }
+    }
+  }
+  const int64_t w0 = r0 > s.n_main ? r0 : s.n_main;
+  if (r1 > w0 && lane < (sep ? 4 : 2)) {
+    const int64_t pos0 = s.n_tok - s.n_win + (w0 - s.n_main);
+    const int64_t cnt = r1 - w0, s0 = pos0 % a.window;
+    const int64_t seg1 = cnt < a.window - s0 ? cnt : a.window - s0;
+    const uint16_t* win = (lane >> 1) ? a.win_v : a.win_k;
+    const int64_t rowb = static_cast<int64_t>(a.D) * 2;
+    if ((lane & 1) == 0) prefetch_range(win + (static_cast<int64_t>(b) * a.window + s0) * a.D, seg1 * rowb);
+    else if (cnt > seg1) prefetch_range(win + static_cast<int64_t>(b) * a.window * a.D, (cnt - seg1) * rowb);
+  }
+}
+
+// Dequantise dims [128c, 128c + 128) of the tile's 128 rows into one X chunk
+// (two 64-dim swizzle atoms). Returns the largest |bf16 value| met (range check).
+DSV4_DEV float convert_chunk(const AttnArgs& a, int b, int c, const int32_t* rt, const float* sc,
+                             const uint8_t* nope, const uint16_t* rope, const uint16_t* win, unsigned char* xc,
+                             int ctid) {
+  uint4 raw[kItems];
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int i = ctid + it * kConvThreads;
+    raw[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < kGroups) {
+      const int j = i >> 4, d0 = c * 128 + (i & 15) * 8;
+      const int32_t src = rt[j];
+      if (src >= 0) {
+        if (d0 < a.d_nope) {
+          const uint2 w = ldg8(nope + static_cast<int64_t>(src) * a.d_nope + d0);
+          raw[it].x = w.x;
+          raw[it].y = w.y;
+        } else {
+          raw[it] = ldg16(rope + static_cast<int64_t>(src) * a.d_rope + (d0 - a.d_nope));
+        }
+      } else if (src <= -2) {
+        raw[it] = ldg16(win + (static_cast<int64_t>(b) * a.window + (-2 - src)) * a.D + d0);
+      }
+    }
+  }
+  float mx = 0.f;
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int i = ctid + it * kConvThreads;
+    if (i < kGroups) {
+      const int j = i >> 4, g = i & 15, d0 = c * 128 + g * 8;
+      const int32_t src = rt[j];
+      uint4 h;
+      if (src >= 0 && d0 < a.d_nope) {
+        const float s = sc[j];
+        h = make_uint4(e4m3x2_scaled_to_f16x2(raw[it].x, s), e4m3x2_scaled_to_f16x2(raw[it].x >> 16, s),
+                       e4m3x2_scaled_to_f16x2(raw[it].y, s), e4m3x2_scaled_to_f16x2(raw[it].y >> 16, s));
+      } else {
+        h = bf16x8_to_f16x8(raw[it], mx);
+      }
+      const int atom = g >> 3, gg = g & 7;
+      *reinterpret_cast<uint4*>(xc + atom * kAtomBytes + j * 128 + ((gg ^ (j & 7)) << 4)) = h;
+    }
+  }
+  return mx;
+}
+
+// In-warp reduce-scatter of N values per lane (one per head, N = 32 or 64):
+// afterwards v[0 .. N/32) hold the max (or sum) over the warp's 32 lanes for
+// heads (N/32)*lane + i. Each step keeps half of the values and takes the other
+// half from the partner lane.
+template <int N, bool MAX>
+DSV4_DEV void warp_reduce_scatter(float* v, int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int o = 16 >> step;
+    const int half = (N / 2) >> step;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+}
+
+// 32 scores (heads [col, col + 32)) of this thread's row, scaled to the log2
+// domain; -inf for a row that does not exist.
+DSV4_DEV void load_scores32(uint32_t taddr, float c2, bool valid, float* s) {
+  uint32_t v[32];
+  tc::tmem_ld32(taddr, v);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) s[i] = valid ? __uint_as_float(v[i]) * c2 : -INFINITY;
+}
+
+}  // namespace
+
+// grid (splits, B, head groups), block 384. See the top of the file.
+template <bool SEP>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int D = a.D;
+  const int nch = D / 128;
+  unsigned char* qs = base;                                  // D/64 atoms of [64 heads][128 B]
+  unsigned char* pb = qs + D * 128;                          // [128 rows][64 heads] f16
+  unsigned char* xk = pb + kPBytes;                          // nch chunks of [2 atoms][128 rows][128 B]
+  unsigned char* xv = SEP ? xk + nch * kChunkBytes : xk;
+  TcTail* t = reinterpret_cast<TcTail*>(xk + (SEP ? 2 : 1) * nch * kChunkBytes);
+
+  const int split = blockIdx.x, b = blockIdx.y;
+  const int h0 = blockIdx.z * kHeads;
+  const int hcount = a.H - h0 < kHeads ? a.H - h0 : kHeads;
+  const RowSpace rs = row_space(a, b);
+  const int64_t r0 = static_cast<int64_t>(split) * a.rows_per_split;
+  const int64_t r1 = r0 + a.rows_per_split < rs.R ? r0 + a.rows_per_split : rs.R;
+  const int nt = r1 > r0 ? static_cast<int>((r1 - r0 + kRows - 1) / kRows) : 0;
+  if (nt == 0) {   // uniform: nothing to attend in this split
+    for (int h = threadIdx.x; h < hcount; h += blockDim.x)
+      a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + h) * a.splits + split] = -INFINITY;
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(kHeads * (1 + nch))) cols <<= 1;
+  volatile int* abort = &t->abort;
+
+  if (warp == 0) tc::tmem_alloc(&t->taddr, cols);
+  if (threadIdx.x == 32) {
+    for (int c = 0; c < kMaxChunks; ++c) {
+      tc::mbar_init(&t->xfull[c], kConvThreads / 32);
+      tc::mbar_init(&t->xfree[c], 1);
+    }
+    tc::mbar_init(&t->sfull, 1);
+    tc::mbar_init(&t->pfull, 4);
+    tc::mbar_init(&t->pvdone, 1);
+    tc::mbar_init(&t->drain, 1);
+    t->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (threadIdx.x < kHeads) t->m_used[threadIdx.x] = -INFINITY;
+  // the query, bf16 -> f16, heads beyond H zero
+  {
+    float qmax = 0.f;
+    const int gpr = D / 8;   // 8-dim groups per head
+    for (int i = threadIdx.x; i < kHeads * gpr; i += kThreads) {
+      const int h = i / gpr, d0 = (i % gpr) * 8;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (h < hcount) w = ldg16(a.q + (static_cast<int64_t>(b) * a.H + h0 + h) * D + d0);
+      const uint4 f = bf16x8_to_f16x8(w, qmax);
+      const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
+      *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) = f;
+    }
+    if (qmax >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
+  }
+  if (warp == 0) prefetch_rows(a, rs, b, r0, r1, SEP, lane);
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t taddr = t->taddr;
+  const uint32_t s_tmem = taddr, o_tmem = taddr + kHeads;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_f16_f32(kRows, kHeads, 0, 0);
+      const uint32_t id_pv = tc::idesc_f16_f32(kRows, kHeads, 1, 1);
+      const uint32_t q_sa = tc::smem_u32(qs), p_sa = tc::smem_u32(pb);
+      const uint32_t xk_sa = tc::smem_u32(xk), xv_sa = tc::smem_u32(xv);
+      for (int tt = 0; tt < nt; ++tt) {
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+          if (!(ok = tc::mbar_wait(&t->xfull[c], tt & 1, abort))) break;
+          tc::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+            const uint64_t ad = tc::smem_desc(xk_sa + c * kChunkBytes + koff, 1024, tc::kSwizzle128B);
+            const uint64_t bd =
+                tc::smem_desc(q_sa + (2 * c + (kk >> 2)) * kQAtomBytes + (kk & 3) * 32, 1024, tc::kSwizzle128B);
+            tc::mma_f16(s_tmem, ad, bd, id_qk, (c | kk) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
+        tc::tc_commit(&t->sfull);
+        if (!tc::mbar_wait(&t->pfull, tt & 1, abort)) break;
+        tc::tc_fence_after();
+        for (int c = 0; c < nch; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad =
+                tc::smem_desc_lbo(xv_sa + c * kChunkBytes + kk * 2048, kAtomBytes, 1024, tc::kSwizzle128B);
+            const uint64_t bd = tc::smem_desc_lbo(p_sa + kk * 2048, kAtomBytes, 1024, tc::kSwizzle128B);
+            tc::mma_f16(o_tmem + c * kHeads, ad, bd, id_pv, (tt | kk) ? 1u : 0u);
+          }
+          tc::tc_commit(&t->xfree[c]);
+        }
+        tc::tc_commit(&t->pvdone);
+      }
+      // every MMA issued must finish before tensor memory is released
+      tc::tc_commit(&t->drain);
+      for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->drain, 0); ++it) {
+      }
+    }
+  } else if (warp < 4 || warp >= 8) {
+    // ------------------------------------------------------------ dequantisation into X
+    const int ctid = (warp < 4 ? warp - 1 : warp - 5) * 32 + lane;
+    float mx = 0.f;
+    bool range_bad = false;
+    for (int tt = 0; tt < nt; ++tt) {
+      const int par = tt & 1;
+      if (ctid < kRows) {
+        const int32_t src = row_source(a, rs, b, r0 + static_cast<int64_t>(tt) * kRows + ctid, r1, true);
+        float sk = 0.f, sv = 0.f;
+        if (src >= 0) {
+          sk = a.k_scale[src];
+          if (SEP) sv = a.v_scale[src];
+        }
+        range_bad |= fabsf(sk) * 448.f > kF16Max || fabsf(sv) * 448.f > kF16Max;
+        t->rt[par][ctid] = src;
+        t->sk[par][ctid] = sk;
+        t->sv[par][ctid] = sv;
+      }
+      bool ok = tc::bar_and(kBarConv, kConvThreads, *abort == 0);
+      for (int c = 0; ok && c < nch; ++c) {
+        if (tt > 0) ok = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
+        ok = tc::bar_and(kBarConv, kConvThreads, ok);
+        if (!ok) break;
+        mx = fmaxf(mx, convert_chunk(a, b, c, t->rt[par], t->sk[par], a.k_nope, a.k_rope, a.win_k,
+                                     xk + c * kChunkBytes, ctid));
+        if (SEP)
+          mx = fmaxf(mx, convert_chunk(a, b, c, t->rt[par], t->sv[par], a.v_nope, a.v_rope, a.win_v,
+                                       xv + c * kChunkBytes, ctid));
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&t->xfull[c]);
+      }
+      if (!ok) break;
+    }
+    if (range_bad || mx >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
+  } else {
+    // ------------------------------------------------------------ softmax, then the epilogue
+    const int qd = warp - 4;                       // tensor-memory lane quarter
+    const int j = qd * 32 + lane;                  // row of the tile / dim of an O^T block
+    const int st = threadIdx.x - 128;              // 0..127 within the group
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const float c2 = a.sm_scale * 1.4426950408889634f;
+    // l of head hb + lane over this warp's rows, hb = 0 and 32
+    float lw[2] = {0.f, 0.f};
+    bool ok = true;
+    for (int tt = 0; tt < nt; ++tt) {
+      const bool valid = row_source(a, rs, b, r0 + static_cast<int64_t>(tt) * kRows + j, r1, false) != -1;
+      ok = tc::bar_and(kBarSoftmax, 128, tc::mbar_wait(&t->sfull, tt & 1, abort));
+      if (!ok) break;
+      if (tt > 0) {   // the previous P.V must be done with P and O^T
+        ok = tc::bar_and(kBarSoftmax, 128, tc::mbar_wait(&t->pvdone, (tt - 1) & 1, abort));
+        if (!ok) break;
+      }
+      tc::tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int hb = half * 32;
+        float s[32];
+        load_scores32(s_tmem + lane_off + hb, c2, valid, s);
+        bool need = false;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) need |= s[i] > t->m_used[hb + i] + kRescale;
+        if (tc::bar_or(kBarSoftmax, 128, need)) {
+          // the running max of some head moves: reduce this tile's column max
+          warp_reduce_scatter<32, true>(s, lane);
+          t->red[qd][lane] = s[0];
+          tc::bar_named(kBarSoftmax, 128);
+          if (st < 32) {
+            const float tm = fmaxf(fmaxf(t->red[0][st], t->red[1][st]), fmaxf(t->red[2][st], t->red[3][st]));
+            const float mo = t->m_used[hb + st];
+            const float mn = fmaxf(mo, tm);
+            t->alpha[hb + st] = mn == -INFINITY ? 1.f : ex2(mo - mn);
+            t->m_used[hb + st] = mn;
+          }
+          tc::bar_named(kBarSoftmax, 128);
+          lw[half] *= t->alpha[hb + lane];
+          if (tt > 0) {
+            for (int c = 0; c < nch; ++c) {
+              uint32_t v[32];
+              const uint32_t addr = o_tmem + lane_off + c * kHeads + hb;
+              tc::tmem_ld32(addr, v);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * t->alpha[hb + i]);
+              tc::tmem_st32(addr, v);
+            }
+            tc::tmem_wait_st();
+          }
+          load_scores32(s_tmem + lane_off + hb, c2, valid, s);   // the reduction consumed s
+        }
+        // probabilities of this row, f16, into P (row j, 16-byte chunks, swizzled)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = valid ? ex2(s[i] - t->m_used[hb + i]) : 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int i = g * 8, gc = half * 4 + g;
+          *reinterpret_cast<uint4*>(pb + j * 128 + ((gc ^ (j & 7)) << 4)) =
+              make_uint4(f32x2_to_f16x2(s[i], s[i + 1]), f32x2_to_f16x2(s[i + 2], s[i + 3]),
+                         f32x2_to_f16x2(s[i + 4], s[i + 5]), f32x2_to_f16x2(s[i + 6], s[i + 7]));
+        }
+        warp_reduce_scatter<32, false>(s, lane);
+        lw[half] += s[0];
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&t->pfull);
+    }
+    if (ok) ok = tc::mbar_wait(&t->pvdone, (nt - 1) & 1, abort);
+    ok = tc::bar_and(kBarSoftmax, 128, ok);
+    if (ok) {
+      tc::tc_fence_after();
+      t->red[qd][lane] = lw[0];
+      t->red[qd][32 + lane] = lw[1];
+      tc::bar_named(kBarSoftmax, 128);
+      if (st < kHeads) t->lsum[st] = (t->red[0][st] + t->red[1][st]) + (t->red[2][st] + t->red[3][st]);
+      tc::bar_named(kBarSoftmax, 128);
+      const int64_t row0 = static_cast<int64_t>(b) * a.H + h0;
+      const int64_t hstride = static_cast<int64_t>(a.splits) * a.Dv;   // between heads of part_o
+      if (st < kHeads) t->alpha[st] = t->lsum[st] > 0.f ? 1.f / t->lsum[st] : 0.f;
+      tc::bar_named(kBarSoftmax, 128);
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c) {
+        float* po = a.part_o + (row0 * a.splits + split) * a.Dv + c * 128 + j;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tc::tmem_ld32(o_tmem + lane_off + c * kHeads + half * 32, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int h = half * 32 + i;
+            if (h < hcount) po[h * hstride] = __uint_as_float(v[i]) * t->alpha[h];
+          }
+        }
+      }
+      if (st < hcount) {
+        const float l = t->lsum[st];
+        a.part_lse[(row0 + st) * a.splits + split] =
+            l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(taddr, cols);
+  }
+  if (threadIdx.x == 0 && t->abort) atomicOr(a.status, DSV4_STATUS_TIMEOUT);
+}
+
+namespace {
+
+size_t tc_smem_bytes(int D, bool sep) {
+  return 1024 + static_cast<size_t>(D) * 128 + kPBytes + (sep ? 2 : 1) * static_cast<size_t>(D / 128) * kChunkBytes +
+         sizeof(TcTail);
+}
+
+template <bool SEP>
+int launch_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(attn_tc_kernel<SEP>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  const size_t smem = tc_smem_bytes(a.D, SEP);
+  attn_tc_kernel<SEP><<<dim3(a.splits, a.B, head_groups), kThreads, smem, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+}  // namespace
+
+bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v) {
+  const int D = d_nope + d_rope;
+  if (H < 1 || H > 128 || D % 128 || D > 128 * kMaxChunks || d_nope % 8 || d_rope % 8) return false;
+  if (separate_v && D > 256) return false;
+  return tc_smem_bytes(D, separate_v != 0) <= 227 * 1024;
+}
+
+int launch_attention_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
+  const int e = a.separate_v ? launch_tc<true>(a, head_groups, st) : launch_tc<false>(a, head_groups, st);
+  if (e) return e;
+  return launch_attention_merge(a, st);
+}
+
+}  // namespace dsv4

@@ -85,5 +85,9 @@ struct AttnArgs {
 };
 // launches the split kernel over (splits, B, head_groups) and the merge; returns a DSV4 status
 int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st);
+// the tensor-core split kernel (tiles of 128 rows, up to 64 heads per CTA) and the merge
+bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v);
+int launch_attention_tc(const AttnArgs& a, int head_groups, cudaStream_t st);
+int launch_attention_merge(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace dsv4

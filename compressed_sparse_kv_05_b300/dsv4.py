@@ -19,7 +19,7 @@ if not os.path.exists(_LIB_PATH):
 lib = ctypes.CDLL(_LIB_PATH)
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA = 0, -1, -2, -3, -4, -5
-STATUS_CAPACITY, STATUS_BAD_INDEX, STATUS_TIMEOUT = 1, 2, 4
+STATUS_CAPACITY, STATUS_BAD_INDEX, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4, 8
 _ERR_NAMES = {-1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "MISALIGNED", -4: "WORKSPACE", -5: "CUDA"}
 
 

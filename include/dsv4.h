@@ -54,7 +54,9 @@ enum {
 enum {
   DSV4_STATUS_CAPACITY = 1, /* an append would pass `capacity`: that sequence was left unchanged */
   DSV4_STATUS_BAD_INDEX = 2, /* a top-k index outside [-1, n_c) was ignored */
-  DSV4_STATUS_TIMEOUT = 4    /* a bounded wait inside a kernel expired; that kernel's output is incomplete */
+  DSV4_STATUS_TIMEOUT = 4,   /* a bounded wait inside a kernel expired; that kernel's output is incomplete */
+  DSV4_STATUS_RANGE = 8      /* attention met a query, key or value of magnitude >= 65504, outside the f16
+                                range of its tensor-core operands; that call's output is unreliable */
 };
 
 /* Shape of one attention layer's cache. Supported: 16 <= d_nope <= 512 and a
