@@ -38,7 +38,15 @@ from compressed_sparse_kv_05_b300 import accounting, synth  # noqa: E402
 from compressed_sparse_kv_05_b300 import workloads as W  # noqa: E402
 
 METRIC = "decode tokens/s per CSA/HCA layer at 128K-1M ctx; achieved HBM GB/s vs roofline"
-WORKLOAD = "stack_1m"
+# workload name -> layers of one decode step. stack_1m is the headline line; the
+# others are single layers of it (per-layer figures, small profiling cases) and
+# the batched CSA configuration.
+WORKLOADS = {
+    "stack_1m": W.STACK_1M,
+    "stack_1m_csa": (W.STACK_CSA,),
+    "stack_1m_hca": (W.STACK_HCA,),
+    "csa_b32_128k": (W.CSA_B32_128K,),
+}
 FALLBACK_HBM_GBS = 6400.0
 
 
@@ -49,6 +57,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack_1m")
     return ap.parse_args()
 
 
@@ -254,6 +263,26 @@ class Stack:
                 timed("hca_decode", lambda: d.dsv4_hca_decode(desc, cache, H, v("q"), L.sm_scale, out, lse, self.ws))
 
 
+def workload_config(name, layers, world, step_bytes):
+    kinds = [L.kind for L in layers]
+    c = {"workload": name, "layers": len(layers) if len(layers) > 1 else kinds[0],
+         "batch_per_gpu": layers[0].batch, "context": layers[0].n_tokens, "heads": layers[0].heads,
+         "kv_dim": f"{layers[0].d_nope} fp8 + {layers[0].d_rope} bf16"}
+    if len(layers) > 1:
+        c["order"] = "CSA even, HCA odd"
+    for L in layers:
+        if L.kind == "csa" and "csa" not in c:
+            c["csa"] = (f"ratio {L.ratio}, {L.n_comp} entries, indexer {L.idx_heads}x{L.idx_dim} fp4, "
+                        f"top-{L.topk}, window {L.window}")
+        if L.kind == "hca" and "hca" not in c:
+            c["hca"] = f"ratio {L.ratio}, dense over {L.n_comp} entries, window {L.window}"
+    c["l2"] = (f"inputs {step_bytes / 1e6:.1f} MB per step > 126 MB L2 (no flush)" if step_bytes > 126e6 else
+               f"inputs {step_bytes / 1e6:.1f} MB per step < 126 MB L2: steps rotate over "
+               f"distinct input slots but the caches stay L2-resident (upper bound)")
+    c["parallelism"] = f"replicas x{world}"
+    return c
+
+
 def count_kernel_nodes(graph):
     """Kernel nodes in a captured graph (None when the graph handle is not reachable)."""
     try:
@@ -289,7 +318,7 @@ def traffic_for(call):
 
 def run_ours(args, rank, world):
     from compressed_sparse_kv_05_b300 import dsv4
-    layers = W.STACK_1M
+    layers = WORKLOADS[args.workload]
     B = layers[0].batch
     K, Wm = args.steps, args.warmup
     total = K + Wm
@@ -343,7 +372,11 @@ def run_ours(args, rank, world):
     for ev in events[Wm:]:
         for call, pairs in ev.items():
             per_call.setdefault(call, []).extend(a.elapsed_time(b) for a, b in pairs)
-    call_layer = {"append": layers[0], "index_topk": W.STACK_CSA, "csa_decode": W.STACK_CSA, "hca_decode": W.STACK_HCA}
+    call_layer = {"append": layers[0]}
+    for L in layers:
+        call_layer.setdefault("index_topk" if L.kind == "csa" else "hca_decode", L)
+        if L.kind == "csa":
+            call_layer.setdefault("csa_decode", L)
     share = {c: sum(v) for c, v in per_call.items()}
     dominant = max(share, key=share.get)
     mean_ms = statistics.mean(per_call[dominant])
@@ -388,12 +421,7 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8-e4m3/bf16/fp4-e2m1 storage, f32 compute", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": "8 (CSA even, HCA odd)", "batch_per_gpu": B,
-                   "context": layers[0].n_tokens, "heads": 64, "kv_dim": "448 fp8 + 64 bf16",
-                   "csa": "ratio 4, indexer 64x128 fp4, top-512, window 128",
-                   "hca": "ratio 128, dense over 8192 entries, window 128",
-                   "l2": f"inputs {step_bytes / 1e6:.1f} MB per step > 126 MB L2 (no flush)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload, layers, world, step_bytes),
         "step_bytes": int(step_bytes),
         "step_GBps": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
         "step_roofline_frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
@@ -411,14 +439,17 @@ def run_ours(args, rank, world):
 # ----------------------------------------------------------------------------- the oracle on the host
 
 
-def oracle_sample_setup():
-    """One sequence of one CSA layer and one HCA layer of stack_1m (full context),
+def oracle_sample_setup(layers):
+    """One sequence of one layer of each kind in the workload (full context),
     caches quantised by the oracle from the seeded rows."""
     import oracle as O
     tag = "bench"
     out = []
-    for li in (0, 1):
-        L = W.STACK_1M[li]
+    seen = set()
+    for li, L in enumerate(layers):
+        if L.kind in seen:
+            continue
+        seen.add(L.kind)
         rows = synth.direct_rows(tag, li, L, 0)
         p = {}
         p["k_nope"], p["k_scale"], p["k_rope"] = O.quantize_kv_rows(rows["kv"], L.d_nope)
@@ -432,6 +463,13 @@ def oracle_sample_setup():
         p["dec"] = synth.decode_inputs(tag, li, L)
         out.append((L, p))
     return out
+
+
+def sample_scale(layers):
+    """Sequences-times-layers of one step per sample step (one sequence of each kind)."""
+    n_csa = sum(L.kind == "csa" for L in layers)
+    n_hca = len(layers) - n_csa
+    return max(n_csa, n_hca)
 
 
 def oracle_sample_step(sample):
@@ -456,36 +494,41 @@ def oracle_threads():
         return 1
 
 
-SAMPLE_DESC = ("one sequence x (one CSA + one HCA layer) of stack_1m at the full 2**20 context per step; "
-               "tokens/s scaled to the 8-layer stack (x 1/4)")
+def sample_desc(name, layers):
+    kinds = sorted({L.kind.upper() for L in layers})
+    return (f"one sequence x (one {' + one '.join(kinds)} layer) of {name} at the full context per sample step; "
+            f"tokens/s = 1 / (sample-step time x {sample_scale(layers)})")
 
 
-def cpu_baseline(steps=2):
-    sample = oracle_sample_setup()
-    oracle_sample_step(sample)
+def time_oracle(layers, steps, warmup):
+    sample = oracle_sample_setup(layers)
+    for _ in range(warmup):
+        oracle_sample_step(sample)
     t = time.perf_counter()
     for _ in range(steps):
         oracle_sample_step(sample)
-    dt = (time.perf_counter() - t) / steps
-    return {"value": round(1.0 / (4 * dt), 4), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
-            "sample": SAMPLE_DESC, "s_per_sample_step": round(dt, 3)}
+    return (time.perf_counter() - t) / steps
+
+
+def cpu_baseline(name, layers, steps=2):
+    dt = time_oracle(layers, steps, 1)
+    return {"value": round(1.0 / (sample_scale(layers) * dt), 4), "unit": "tokens/s", "cores": oracle_threads(),
+            "kind": "oracle", "sample": sample_desc(name, layers), "s_per_sample_step": round(dt, 3)}
 
 
 def run_reference(args):
-    sample = oracle_sample_setup()
-    for _ in range(args.warmup):
-        oracle_sample_step(sample)
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_sample_step(sample)
-    dt = (time.perf_counter() - t) / args.steps
-    value = 1.0 / (4 * dt)
-    cb = {"value": round(value, 4), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
-          "sample": SAMPLE_DESC}
+    layers = WORKLOADS[args.workload]
+    dt = time_oracle(layers, args.steps, args.warmup)
+    scale = sample_scale(layers)
+    value = 1.0 / (scale * dt)
+    desc = sample_desc(args.workload, layers)
+    cb = {"value": round(value, 4), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle", "sample": desc}
+    config = workload_config(args.workload, layers, 1, sum(accounting.decode_step_bytes(L) for L in layers))
+    config["sample"] = desc
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 4 * 1e3, 2),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * scale * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": SAMPLE_DESC}, "cpu_baseline": cb,
+            "config": config, "cpu_baseline": cb,
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -502,7 +545,7 @@ def main():
     line = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(args.workload, WORKLOADS[args.workload])
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()

@@ -14,6 +14,7 @@ namespace {
 constexpr int kSms = 148;                // streaming multiprocessors of a B300
 constexpr int kSplitTarget = 2 * kSms;  // CTAs the CUDA-core split-K attention aims for
 constexpr int kTcTile = 128;            // rows per tile of the tensor-core attention
+constexpr int kTcMaxTiles = 8;          // tiles per CTA of the tensor-core attention, at most
 constexpr int kRowTile = 16;
 constexpr int kHeadGroup = 64;
 
@@ -75,7 +76,8 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
     // tiles of 128 rows spread evenly over one wave of CTAs (one per SM)
     const int64_t tiles = (rmax + kTcTile - 1) / kTcTile;
     const int64_t total = tiles * d->batch * p.head_groups;
-    const int64_t per_cta = (total + kSms - 1) / kSms;
+    int64_t per_cta = (total + kSms - 1) / kSms;
+    if (per_cta > kTcMaxTiles) per_cta = kTcMaxTiles;   // a CTA keeps its rows' sources in shared memory
     const int64_t rps = per_cta * kTcTile;
     p.rows_per_split = static_cast<int>(rps);
     p.splits = static_cast<int>((rmax + rps - 1) / rps);

@@ -173,27 +173,47 @@ __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
   }
 }
 
-// grid (B * H), block 128
+// grid (B * H, ceil(Dv / 128)), block 128: one (sequence, head) and 128 dims
+// per CTA. Warp g sums splits g, g + 4, ... for 4 dims per lane, with several
+// splits' loads in flight; the four warps' sums are then added.
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   const int64_t bh = blockIdx.x;
   const float* lse = a.part_lse + bh * a.splits;
+  const int sg = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float mx = -INFINITY;
-  for (int s = 0; s < a.splits; ++s) mx = fmaxf(mx, lse[s]);
+  for (int s = lane; s < a.splits; s += 32) mx = fmaxf(mx, lse[s]);
+  mx = warp_max(mx);
   float tot = 0.f;
   if (mx != -INFINITY)
-    for (int s = 0; s < a.splits; ++s) tot += expf(lse[s] - mx);
-  for (int d = threadIdx.x; d < a.Dv; d += blockDim.x) {
-    float o = 0.f;
-    if (tot > 0.f) {
-      for (int s = 0; s < a.splits; ++s) {
-        const float w = expf(lse[s] - mx);
-        if (w > 0.f) o = fmaf(w, a.part_o[(bh * a.splits + s) * a.Dv + d], o);
+    for (int s = lane; s < a.splits; s += 32) tot += expf(lse[s] - mx);
+  tot = warp_sum(tot);
+  const int d0 = blockIdx.y * 128 + lane * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tot > 0.f && d0 < a.Dv) {
+    const float* po = a.part_o + bh * a.splits * a.Dv + d0;
+#pragma unroll 4
+    for (int s = sg; s < a.splits; s += 4) {
+      const float w = expf(lse[s] - mx);
+      const float4 v = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * a.Dv);
+      if (w > 0.f) {   // a split without rows may leave its partial unwritten
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
       }
-      o /= tot;
     }
-    a.out[bh * a.Dv + d] = o;
   }
-  if (threadIdx.x == 0 && a.lse) a.lse[bh] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  __shared__ float4 red[4][32];
+  red[sg][lane] = acc;
+  __syncthreads();
+  if (sg == 0 && d0 < a.Dv) {
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    const float4 r1 = red[1][lane], r2 = red[2][lane], r3 = red[3][lane];
+    *reinterpret_cast<float4*>(a.out + bh * a.Dv + d0) =
+        make_float4(((acc.x + r1.x) + (r2.x + r3.x)) * inv, ((acc.y + r1.y) + (r2.y + r3.y)) * inv,
+                    ((acc.z + r1.z) + (r2.z + r3.z)) * inv, ((acc.w + r1.w) + (r2.w + r3.w)) * inv);
+  }
+  if (threadIdx.x == 0 && blockIdx.y == 0 && a.lse) a.lse[bh] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
 namespace {
@@ -232,7 +252,7 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
 }
 
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st) {
-  attn_merge_kernel<<<a.B * a.H, 128, 0, st>>>(a);
+  attn_merge_kernel<<<dim3(a.B * a.H, (a.Dv + 127) / 128), 128, 0, st>>>(a);
   return launch_status();
 }
 

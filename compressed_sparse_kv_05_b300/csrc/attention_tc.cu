@@ -19,23 +19,28 @@
 // K-major operand for the first product and as an MN-major operand for the
 // second; S^T and O^T live in tensor memory (lane = row / dim, column = head).
 //
-// CTA roles (384 threads, one CTA per SM for D = 512):
+// CTA roles (512 threads, one CTA per SM for D = 512):
 //   warp 0      allocates tensor memory, prefetches the CTA's rows into L2, and
 //               one lane issues every MMA;
-//   warps 1-3, 8-11  (224 threads) dequantise rows into X, chunk by chunk of
-//               128 dims, as soon as the previous tile's P.V no longer reads it;
-//   warps 4-7   (one per 32-lane quarter of tensor memory, one row each) turn
-//               S^T into P. The running max per head only moves when a score
-//               exceeds it by more than 2^8 (then the tile's column max is
-//               reduced and O^T, l rescaled), so P <= 256 always fits f16.
-//               After the last tile they normalise O^T and write this split's
-//               partial output and log-sum-exp.
+//   warps 1-3, 8-11   (224 threads) dequantise rows into X, chunk by chunk of
+//               128 dims, with the loads of the next chunk in flight. An e4m3
+//               code becomes f16 by integer operations (its bit pattern shifted
+//               into an f16 is exactly code * 2^-8) and one f16 multiply by the
+//               row's scale * 2^8;
+//   warps 4-7, 12-15  (two per 32-lane quarter of tensor memory: one row each,
+//               heads 0-31 or 32-63) convert the query, then turn S^T into P.
+//               The running max of a head only moves when a score exceeds it by
+//               more than 2^8 (then the tile's column max is reduced and O^T
+//               and l are rescaled), so P <= 256 always fits f16. After the
+//               last tile they normalise O^T, stage it in shared memory and
+//               store this split's partial output with bulk copies.
 // Splits are merged by attn_merge_kernel (attention.cu).
 //
-// Precision: K, V and P are rounded to f16 (relative error <= 2^-11 each), the
-// bf16 query converts to f16 exactly for |q| in [2^-14, 65504]; products and
-// sums are fp32. A value that does not fit f16 (|x| >= 65504) raises
-// DSV4_STATUS_RANGE.
+// Precision: K, V and P are rounded to f16 (relative error <= 2^-11 each; a
+// row's scale is rounded to f16 once), the bf16 query converts to f16 exactly
+// for |q| in [2^-14, 65504]; products and sums are fp32. A value that does not
+// fit f16 (|x| >= 65504) raises DSV4_STATUS_RANGE. The two e4m3 NaN codes, which
+// the quantiser never writes, read as +-480.
 #include <mutex>
 
 #include "common.cuh"
@@ -48,8 +53,9 @@ namespace {
 
 constexpr int kRows = 128;                     // rows per tile
 constexpr int kHeads = 64;                     // heads per CTA (MMA N), zero-padded
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kConvThreads = 7 * 32;           // warps 1-3 and 8-11
+constexpr int kSoftThreads = 8 * 32;           // warps 4-7 and 12-15
 constexpr int kGroups = kRows * 16;            // 8-dim groups of one 128-dim chunk
 constexpr int kItems = (kGroups + kConvThreads - 1) / kConvThreads;
 constexpr int kAtomBytes = kRows * 128;        // 128 rows x 64 dims f16
@@ -57,18 +63,17 @@ constexpr int kChunkBytes = 2 * kAtomBytes;    // 128 rows x 128 dims f16
 constexpr int kQAtomBytes = kHeads * 128;      // 64 heads x 64 dims f16
 constexpr int kPBytes = kRows * kHeads * 2;
 constexpr int kMaxChunks = 4;                  // D <= 512
-constexpr int kBarSoftmax = 1, kBarConv = 2;   // named barriers (0 is __syncthreads)
+constexpr int kMaxTiles = 8;                   // rows per CTA <= 1024 (the host plan keeps to it)
+constexpr int kBarSoft = 1, kBarConv = 2;      // named barriers (0 is __syncthreads)
 constexpr float kRescale = 8.f;                // lazy-rescale threshold (log2 units)
 constexpr float kF16Max = 65504.f;
 
 struct TcTail {
-  uint64_t xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, drain;
+  uint64_t xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, qready, drain;
   uint32_t taddr;
   int abort;
-  int32_t rt[2][kRows];     // row sources of a tile, by tile parity
-  float sk[2][kRows];       // key scale of each row
-  float sv[2][kRows];       // value scale (separate V)
-  float m_used[kHeads];     // running max per head, log2 domain
+  int32_t src[kMaxTiles * kRows];   // row sources of every row of the split (see row_source)
+  float m_used[kHeads];             // running max per head, log2 domain
   float alpha[kHeads];
   float lsum[kHeads];
   float red[4][kHeads];
@@ -80,25 +85,16 @@ DSV4_DEV uint32_t f32x2_to_f16x2(float lo, float hi) {
   return r;
 }
 
-// Two e4m3 codes (low byte first) times s, rounded to two f16.
-DSV4_DEV uint32_t e4m3x2_scaled_to_f16x2(uint32_t pair, float s) {
-  uint32_t out;
-  asm("{\n"
-      ".reg .b32 h2;\n"
-      ".reg .b16 l, u, p;\n"
-      ".reg .f32 f0, f1;\n"
-      "cvt.u16.u32 p, %1;\n"
-      "cvt.rn.f16x2.e4m3x2 h2, p;\n"
-      "mov.b32 {l, u}, h2;\n"
-      "cvt.f32.f16 f0, l;\n"
-      "cvt.f32.f16 f1, u;\n"
-      "mul.rn.f32 f0, f0, %2;\n"
-      "mul.rn.f32 f1, f1, %2;\n"
-      "cvt.rn.f16x2.f32 %0, f1, f0;\n"
-      "}"
-      : "=r"(out)
-      : "r"(pair), "f"(s));
-  return out;
+// Two e4m3 codes (bytes 0 and 1 of w after `sel`) as two f16 times f16x2 `sc`:
+// placing code c in the low byte of a halfword, (c + (c & 0x80)) << 7 is the
+// f16 bit pattern of e4m3(c) * 2^-8 (the sign moves to bit 15, the exponent and
+// mantissa land under f16's, subnormals included).
+DSV4_DEV uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t sel, uint32_t sc) {
+  uint32_t h, r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(h) : "r"(w), "r"(sel));
+  h = (h + (h & 0x00800080u)) << 7;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc));
+  return r;
 }
 
 DSV4_DEV uint32_t bf16x2_to_f16x2(uint32_t w, float& mx) {
@@ -215,64 +211,76 @@ DSV4_DEV void prefetch_rows(const AttnArgs& a, const RowSpace& s, int b, int64_t
   }
 }
 
-// Dequantise dims [128c, 128c + 128) of the tile's 128 rows into one X chunk
-// (two 64-dim swizzle atoms). Returns the largest |bf16 value| met (range check).
-DSV4_DEV float convert_chunk(const AttnArgs& a, int b, int c, const int32_t* rt, const float* sc,
-                             const uint8_t* nope, const uint16_t* rope, const uint16_t* win, unsigned char* xc,
-                             int ctid) {
-  uint4 raw[kItems];
+// Raw bytes of one 128-dim chunk of a tile, as this thread's share of the
+// 2048 8-dim groups (group i = row i / 16, dims 8 * (i % 16) of the chunk):
+// 8 e4m3 codes with the row's scale, or 8 bf16 values.
+struct ChunkRaw {
+  uint4 v[kItems];
+  float s[kItems];
+};
+
+// Issue the global loads of chunk c of tile tt (rows src[tt * 128 ...]).
+DSV4_DEV void load_chunk(const AttnArgs& a, int b, const int32_t* src, int tt, int c, const uint8_t* nope,
+                         const float* scale, const uint16_t* rope, const uint16_t* win, int ctid, ChunkRaw& r) {
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
     const int i = ctid + it * kConvThreads;
-    raw[it] = make_uint4(0u, 0u, 0u, 0u);
+    r.v[it] = make_uint4(0u, 0u, 0u, 0u);
+    r.s[it] = 0.f;
     if (i < kGroups) {
-      const int j = i >> 4, d0 = c * 128 + (i & 15) * 8;
-      const int32_t src = rt[j];
-      if (src >= 0) {
+      const int d0 = c * 128 + (i & 15) * 8;
+      const int32_t sr = src[tt * kRows + (i >> 4)];
+      if (sr >= 0) {
         if (d0 < a.d_nope) {
-          const uint2 w = ldg8(nope + static_cast<int64_t>(src) * a.d_nope + d0);
-          raw[it].x = w.x;
-          raw[it].y = w.y;
+          const uint2 w = ldg8(nope + static_cast<int64_t>(sr) * a.d_nope + d0);
+          r.v[it].x = w.x;
+          r.v[it].y = w.y;
+          r.s[it] = __ldg(scale + sr);
         } else {
-          raw[it] = ldg16(rope + static_cast<int64_t>(src) * a.d_rope + (d0 - a.d_nope));
+          r.v[it] = ldg16(rope + static_cast<int64_t>(sr) * a.d_rope + (d0 - a.d_nope));
         }
-      } else if (src <= -2) {
-        raw[it] = ldg16(win + (static_cast<int64_t>(b) * a.window + (-2 - src)) * a.D + d0);
+      } else if (sr <= -2) {
+        r.v[it] = ldg16(win + (static_cast<int64_t>(b) * a.window + (-2 - sr)) * a.D + d0);
       }
     }
   }
-  float mx = 0.f;
+}
+
+// Convert a loaded chunk to f16 and store it into X chunk `xc` (two 64-dim
+// swizzle atoms). Tracks the largest |value| that must fit f16 (range check).
+DSV4_DEV void store_chunk(const AttnArgs& a, const int32_t* src, int tt, int c, const ChunkRaw& r, unsigned char* xc,
+                          int ctid, float& mx) {
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
     const int i = ctid + it * kConvThreads;
     if (i < kGroups) {
       const int j = i >> 4, g = i & 15, d0 = c * 128 + g * 8;
-      const int32_t src = rt[j];
       uint4 h;
-      if (src >= 0 && d0 < a.d_nope) {
-        const float s = sc[j];
-        h = make_uint4(e4m3x2_scaled_to_f16x2(raw[it].x, s), e4m3x2_scaled_to_f16x2(raw[it].x >> 16, s),
-                       e4m3x2_scaled_to_f16x2(raw[it].y, s), e4m3x2_scaled_to_f16x2(raw[it].y >> 16, s));
+      if (d0 < a.d_nope && src[tt * kRows + j] >= 0) {   // e4m3 codes times the row's scale
+        const float sc = r.s[it];
+        mx = fmaxf(mx, fabsf(sc) * 448.f);
+        uint32_t s2;
+        asm("{\n.reg .b16 t;\ncvt.rn.f16.f32 t, %1;\nmov.b32 %0, {t, t};\n}" : "=r"(s2) : "f"(sc * 256.f));
+        h = make_uint4(e4m3x2_to_f16x2_scaled(r.v[it].x, 0x4140u, s2), e4m3x2_to_f16x2_scaled(r.v[it].x, 0x4342u, s2),
+                       e4m3x2_to_f16x2_scaled(r.v[it].y, 0x4140u, s2), e4m3x2_to_f16x2_scaled(r.v[it].y, 0x4342u, s2));
       } else {
-        h = bf16x8_to_f16x8(raw[it], mx);
+        h = bf16x8_to_f16x8(r.v[it], mx);
       }
       const int atom = g >> 3, gg = g & 7;
       *reinterpret_cast<uint4*>(xc + atom * kAtomBytes + j * 128 + ((gg ^ (j & 7)) << 4)) = h;
     }
   }
-  return mx;
 }
 
-// In-warp reduce-scatter of N values per lane (one per head, N = 32 or 64):
-// afterwards v[0 .. N/32) hold the max (or sum) over the warp's 32 lanes for
-// heads (N/32)*lane + i. Each step keeps half of the values and takes the other
-// half from the partner lane.
-template <int N, bool MAX>
-DSV4_DEV void warp_reduce_scatter(float* v, int lane) {
+// In-warp reduce-scatter of 32 values per lane (one per head): afterwards v[0]
+// holds the max (or sum) over the warp's 32 lanes for head `lane`. Each step
+// keeps half of the values and takes the other half from the partner lane.
+template <bool MAX>
+DSV4_DEV void warp_reduce_scatter32(float* v, int lane) {
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
     const int o = 16 >> step;
-    const int half = (N / 2) >> step;
+    const int half = 16 >> step;
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
@@ -296,7 +304,7 @@ DSV4_DEV void load_scores32(uint32_t taddr, float c2, bool valid, float* s) {
 
 }  // namespace
 
-// grid (splits, B, head groups), block 384. See the top of the file.
+// grid (splits, B, head groups), block 512. See the top of the file.
 template <bool SEP>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -308,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   unsigned char* pb = qs + D * 128;                          // [128 rows][64 heads] f16
   unsigned char* xk = pb + kPBytes;                          // nch chunks of [2 atoms][128 rows][128 B]
   unsigned char* xv = SEP ? xk + nch * kChunkBytes : xk;
+  float* stage = reinterpret_cast<float*>(xk);               // epilogue: [64 heads][D] fp32, after the last P.V
   TcTail* t = reinterpret_cast<TcTail*>(xk + (SEP ? 2 : 1) * nch * kChunkBytes);
 
   const int split = blockIdx.x, b = blockIdx.y;
@@ -327,7 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(kHeads * (1 + nch))) cols <<= 1;
   volatile int* abort = &t->abort;
+  const int nrows = nt * kRows;   // <= kMaxTiles * kRows (host plan)
 
+  if (a.n_sel == 0 && warp == 0) prefetch_rows(a, rs, b, r0, r1, SEP, lane);   // HCA: known ranges, start now
   if (warp == 0) tc::tmem_alloc(&t->taddr, cols);
   if (threadIdx.x == 32) {
     for (int c = 0; c < kMaxChunks; ++c) {
@@ -335,34 +346,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
       tc::mbar_init(&t->xfree[c], 1);
     }
     tc::mbar_init(&t->sfull, 1);
-    tc::mbar_init(&t->pfull, 4);
+    tc::mbar_init(&t->pfull, kSoftThreads / 32);
     tc::mbar_init(&t->pvdone, 1);
+    tc::mbar_init(&t->qready, kSoftThreads / 32);
     tc::mbar_init(&t->drain, 1);
     t->abort = 0;
     tc::fence_mbar_init();
   }
   if (threadIdx.x < kHeads) t->m_used[threadIdx.x] = -INFINITY;
-  // the query, bf16 -> f16, heads beyond H zero
   {
-    float qmax = 0.f;
-    const int gpr = D / 8;   // 8-dim groups per head
-    for (int i = threadIdx.x; i < kHeads * gpr; i += kThreads) {
-      const int h = i / gpr, d0 = (i % gpr) * 8;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (h < hcount) w = ldg16(a.q + (static_cast<int64_t>(b) * a.H + h0 + h) * D + d0);
-      const uint4 f = bf16x8_to_f16x8(w, qmax);
-      const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
-      *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) = f;
+    // row sources of the whole split (CSA: one round trip for the top-k indices)
+    int32_t sv[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      sv[k] = i < nrows ? row_source(a, rs, b, r0 + i, r1, true) : -1;
     }
-    if (qmax >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      if (i < nrows) t->src[i] = sv[k];
+    }
   }
-  if (warp == 0) prefetch_rows(a, rs, b, r0, r1, SEP, lane);
-  tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t taddr = t->taddr;
   const uint32_t s_tmem = taddr, o_tmem = taddr + kHeads;
+  const int32_t* src = t->src;
+  if (a.n_sel > 0 && warp == 0) {   // CSA: prefetch the selected rows and the window, now that they are known
+    for (int i = lane; i < nrows; i += 32) {
+      const int32_t sr = src[i];
+      if (sr >= 0) {
+        tc::prefetch_l2_bulk(a.k_nope + static_cast<int64_t>(sr) * a.d_nope, a.d_nope);
+        if (a.d_rope) tc::prefetch_l2_bulk(a.k_rope + static_cast<int64_t>(sr) * a.d_rope, a.d_rope * 2);
+        if (SEP) {
+          tc::prefetch_l2_bulk(a.v_nope + static_cast<int64_t>(sr) * a.d_nope, a.d_nope);
+          if (a.d_rope) tc::prefetch_l2_bulk(a.v_rope + static_cast<int64_t>(sr) * a.d_rope, a.d_rope * 2);
+        }
+      }
+    }
+    if (lane < (SEP ? 4 : 2)) prefetch_rows(a, rs, b, r0 > rs.n_main ? r0 : rs.n_main, r1, SEP, lane);
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -371,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
       const uint32_t id_pv = tc::idesc_f16_f32(kRows, kHeads, 1, 1);
       const uint32_t q_sa = tc::smem_u32(qs), p_sa = tc::smem_u32(pb);
       const uint32_t xk_sa = tc::smem_u32(xk), xv_sa = tc::smem_u32(xv);
-      for (int tt = 0; tt < nt; ++tt) {
-        bool ok = true;
+      bool ok = tc::mbar_wait(&t->qready, 0, abort);
+      for (int tt = 0; ok && tt < nt; ++tt) {
         for (int c = 0; c < nch; ++c) {
           if (!(ok = tc::mbar_wait(&t->xfull[c], tt & 1, abort))) break;
           tc::tc_fence_after();
@@ -387,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
         }
         if (!ok) break;
         tc::tc_commit(&t->sfull);
-        if (!tc::mbar_wait(&t->pfull, tt & 1, abort)) break;
+        if (!(ok = tc::mbar_wait(&t->pfull, tt & 1, abort))) break;
         tc::tc_fence_after();
         for (int c = 0; c < nch; ++c) {
 #pragma unroll
@@ -403,150 +428,173 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
       }
       // every MMA issued must finish before tensor memory is released
       tc::tc_commit(&t->drain);
-      for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->drain, 0); ++it) {
-      }
+      tc::mbar_wait_drain(&t->drain, 0);
     }
-  } else if (warp < 4 || warp >= 8) {
+  } else if (warp < 4 || (warp >= 8 && warp < 12)) {
     // ------------------------------------------------------------ dequantisation into X
+    // Stages q = (tile, chunk, K/V) in order; the loads of stage q + 1 are in
+    // flight while stage q waits for its X chunk and converts.
     const int ctid = (warp < 4 ? warp - 1 : warp - 5) * 32 + lane;
+    const int per = SEP ? 2 : 1;
+    const int nstage = nt * nch * per;
     float mx = 0.f;
-    bool range_bad = false;
-    for (int tt = 0; tt < nt; ++tt) {
-      const int par = tt & 1;
-      if (ctid < kRows) {
-        const int32_t src = row_source(a, rs, b, r0 + static_cast<int64_t>(tt) * kRows + ctid, r1, true);
-        float sk = 0.f, sv = 0.f;
-        if (src >= 0) {
-          sk = a.k_scale[src];
-          if (SEP) sv = a.v_scale[src];
-        }
-        range_bad |= fabsf(sk) * 448.f > kF16Max || fabsf(sv) * 448.f > kF16Max;
-        t->rt[par][ctid] = src;
-        t->sk[par][ctid] = sk;
-        t->sv[par][ctid] = sv;
+    ChunkRaw ra, rb;
+    auto issue = [&](int q, ChunkRaw& r) {
+      const int kv = q % per, c = (q / per) % nch, tt = q / (per * nch);
+      if (kv == 0) load_chunk(a, b, src, tt, c, a.k_nope, a.k_scale, a.k_rope, a.win_k, ctid, r);
+      else load_chunk(a, b, src, tt, c, a.v_nope, a.v_scale, a.v_rope, a.win_v, ctid, r);
+    };
+    auto finish = [&](int q, const ChunkRaw& r) -> bool {
+      const int kv = q % per, c = (q / per) % nch, tt = q / (per * nch);
+      if (kv == 0) {
+        const bool ok = tt == 0 || tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
+        if (!tc::bar_and(kBarConv, kConvThreads, ok)) return false;
       }
-      bool ok = tc::bar_and(kBarConv, kConvThreads, *abort == 0);
-      for (int c = 0; ok && c < nch; ++c) {
-        if (tt > 0) ok = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
-        ok = tc::bar_and(kBarConv, kConvThreads, ok);
-        if (!ok) break;
-        mx = fmaxf(mx, convert_chunk(a, b, c, t->rt[par], t->sk[par], a.k_nope, a.k_rope, a.win_k,
-                                     xk + c * kChunkBytes, ctid));
-        if (SEP)
-          mx = fmaxf(mx, convert_chunk(a, b, c, t->rt[par], t->sv[par], a.v_nope, a.v_rope, a.win_v,
-                                       xv + c * kChunkBytes, ctid));
+      store_chunk(a, src, tt, c, r, (kv ? xv : xk) + c * kChunkBytes, ctid, mx);
+      if (kv == per - 1) {
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&t->xfull[c]);
       }
-      if (!ok) break;
+      return true;
+    };
+    issue(0, ra);
+    for (int q = 0; q < nstage; q += 2) {
+      if (q + 1 < nstage) issue(q + 1, rb);
+      if (!finish(q, ra)) break;
+      if (q + 1 >= nstage) break;
+      if (q + 2 < nstage) issue(q + 2, ra);
+      if (!finish(q + 1, rb)) break;
     }
-    if (range_bad || mx >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
+    if (mx >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
   } else {
-    // ------------------------------------------------------------ softmax, then the epilogue
-    const int qd = warp - 4;                       // tensor-memory lane quarter
+    // ------------------------------------------------------------ query, softmax, epilogue
+    const int qd = warp & 3;                       // tensor-memory lane quarter
+    const int hb = warp >= 12 ? 32 : 0;            // this warp's heads [hb, hb + 32)
     const int j = qd * 32 + lane;                  // row of the tile / dim of an O^T block
-    const int st = threadIdx.x - 128;              // 0..127 within the group
+    const int st = (warp >= 12 ? 128 : 0) + qd * 32 + lane;   // 0..255 within the group
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float c2 = a.sm_scale * 1.4426950408889634f;
-    // l of head hb + lane over this warp's rows, hb = 0 and 32
-    float lw[2] = {0.f, 0.f};
+    {
+      // the query, bf16 -> f16 into the K-major operand (heads beyond H zero)
+      const int gpr = D / 8;   // 8-dim groups per head
+      float qmax = 0.f;
+      for (int i0 = 0; i0 < kHeads * gpr; i0 += 8 * kSoftThreads) {
+        uint4 qw[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + st + u * kSoftThreads, h = i / gpr;
+          qw[u] = make_uint4(0u, 0u, 0u, 0u);
+          if (i < kHeads * gpr && h < hcount)
+            qw[u] = ldg16(a.q + (static_cast<int64_t>(b) * a.H + h0 + h) * D + (i % gpr) * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + st + u * kSoftThreads, h = i / gpr;
+          if (i < kHeads * gpr) {
+            const int d0 = (i % gpr) * 8, atom = d0 >> 6, gg = (d0 >> 3) & 7;
+            *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) =
+                bf16x8_to_f16x8(qw[u], qmax);
+          }
+        }
+      }
+      if (qmax >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&t->qready);
+    }
+    float lw = 0.f;   // l of head hb + lane over this warp's rows
     bool ok = true;
     for (int tt = 0; tt < nt; ++tt) {
-      const bool valid = row_source(a, rs, b, r0 + static_cast<int64_t>(tt) * kRows + j, r1, false) != -1;
-      ok = tc::bar_and(kBarSoftmax, 128, tc::mbar_wait(&t->sfull, tt & 1, abort));
+      const bool valid = src[tt * kRows + j] != -1;
+      ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->sfull, tt & 1, abort));
       if (!ok) break;
       if (tt > 0) {   // the previous P.V must be done with P and O^T
-        ok = tc::bar_and(kBarSoftmax, 128, tc::mbar_wait(&t->pvdone, (tt - 1) & 1, abort));
+        ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->pvdone, (tt - 1) & 1, abort));
         if (!ok) break;
       }
       tc::tc_fence_after();
+      float s[32];
+      load_scores32(s_tmem + lane_off + hb, c2, valid, s);
+      bool need = false;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int hb = half * 32;
-        float s[32];
-        load_scores32(s_tmem + lane_off + hb, c2, valid, s);
-        bool need = false;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) need |= s[i] > t->m_used[hb + i] + kRescale;
-        if (tc::bar_or(kBarSoftmax, 128, need)) {
-          // the running max of some head moves: reduce this tile's column max
-          warp_reduce_scatter<32, true>(s, lane);
-          t->red[qd][lane] = s[0];
-          tc::bar_named(kBarSoftmax, 128);
-          if (st < 32) {
-            const float tm = fmaxf(fmaxf(t->red[0][st], t->red[1][st]), fmaxf(t->red[2][st], t->red[3][st]));
-            const float mo = t->m_used[hb + st];
-            const float mn = fmaxf(mo, tm);
-            t->alpha[hb + st] = mn == -INFINITY ? 1.f : ex2(mo - mn);
-            t->m_used[hb + st] = mn;
-          }
-          tc::bar_named(kBarSoftmax, 128);
-          lw[half] *= t->alpha[hb + lane];
-          if (tt > 0) {
-            for (int c = 0; c < nch; ++c) {
-              uint32_t v[32];
-              const uint32_t addr = o_tmem + lane_off + c * kHeads + hb;
-              tc::tmem_ld32(addr, v);
-              tc::tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * t->alpha[hb + i]);
-              tc::tmem_st32(addr, v);
-            }
-            tc::tmem_wait_st();
-          }
-          load_scores32(s_tmem + lane_off + hb, c2, valid, s);   // the reduction consumed s
+      for (int i = 0; i < 32; ++i) need |= s[i] > t->m_used[hb + i] + kRescale;
+      if (tc::bar_or(kBarSoft, kSoftThreads, need)) {
+        // the running max of some head moves: reduce this tile's column max
+        warp_reduce_scatter32<true>(s, lane);
+        t->red[qd][hb + lane] = s[0];
+        tc::bar_named(kBarSoft, kSoftThreads);
+        if (st < kHeads) {
+          const float tm = fmaxf(fmaxf(t->red[0][st], t->red[1][st]), fmaxf(t->red[2][st], t->red[3][st]));
+          const float mo = t->m_used[st];
+          const float mn = fmaxf(mo, tm);
+          t->alpha[st] = mn == -INFINITY ? 1.f : ex2(mo - mn);
+          t->m_used[st] = mn;
         }
-        // probabilities of this row, f16, into P (row j, 16-byte chunks, swizzled)
+        tc::bar_named(kBarSoft, kSoftThreads);
+        lw *= t->alpha[hb + lane];
+        if (tt > 0) {
+          for (int c = 0; c < nch; ++c) {
+            uint32_t v[32];
+            const uint32_t addr = o_tmem + lane_off + c * kHeads + hb;
+            tc::tmem_ld32(addr, v);
+            tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = valid ? ex2(s[i] - t->m_used[hb + i]) : 0.f;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int i = g * 8, gc = half * 4 + g;
-          *reinterpret_cast<uint4*>(pb + j * 128 + ((gc ^ (j & 7)) << 4)) =
-              make_uint4(f32x2_to_f16x2(s[i], s[i + 1]), f32x2_to_f16x2(s[i + 2], s[i + 3]),
-                         f32x2_to_f16x2(s[i + 4], s[i + 5]), f32x2_to_f16x2(s[i + 6], s[i + 7]));
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * t->alpha[hb + i]);
+            tc::tmem_st32(addr, v);
+          }
+          tc::tmem_wait_st();
         }
-        warp_reduce_scatter<32, false>(s, lane);
-        lw[half] += s[0];
+        load_scores32(s_tmem + lane_off + hb, c2, valid, s);   // the reduction consumed s
       }
+      // probabilities of this row and heads, f16, into P (row j, 16-byte chunks, swizzled)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] = valid ? ex2(s[i] - t->m_used[hb + i]) : 0.f;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int i = g * 8, gc = (hb >> 3) + g;
+        *reinterpret_cast<uint4*>(pb + j * 128 + ((gc ^ (j & 7)) << 4)) =
+            make_uint4(f32x2_to_f16x2(s[i], s[i + 1]), f32x2_to_f16x2(s[i + 2], s[i + 3]),
+                       f32x2_to_f16x2(s[i + 4], s[i + 5]), f32x2_to_f16x2(s[i + 6], s[i + 7]));
+      }
+      warp_reduce_scatter32<false>(s, lane);
+      lw += s[0];
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t->pfull);
     }
     if (ok) ok = tc::mbar_wait(&t->pvdone, (nt - 1) & 1, abort);
-    ok = tc::bar_and(kBarSoftmax, 128, ok);
+    ok = tc::bar_and(kBarSoft, kSoftThreads, ok);
     if (ok) {
       tc::tc_fence_after();
-      t->red[qd][lane] = lw[0];
-      t->red[qd][32 + lane] = lw[1];
-      tc::bar_named(kBarSoftmax, 128);
-      if (st < kHeads) t->lsum[st] = (t->red[0][st] + t->red[1][st]) + (t->red[2][st] + t->red[3][st]);
-      tc::bar_named(kBarSoftmax, 128);
-      const int64_t row0 = static_cast<int64_t>(b) * a.H + h0;
-      const int64_t hstride = static_cast<int64_t>(a.splits) * a.Dv;   // between heads of part_o
-      if (st < kHeads) t->alpha[st] = t->lsum[st] > 0.f ? 1.f / t->lsum[st] : 0.f;
-      tc::bar_named(kBarSoftmax, 128);
-#pragma unroll 1
-      for (int c = 0; c < nch; ++c) {
-        float* po = a.part_o + (row0 * a.splits + split) * a.Dv + c * 128 + j;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-          tc::tmem_ld32(o_tmem + lane_off + c * kHeads + half * 32, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int h = half * 32 + i;
-            if (h < hcount) po[h * hstride] = __uint_as_float(v[i]) * t->alpha[h];
-          }
-        }
+      t->red[qd][hb + lane] = lw;
+      tc::bar_named(kBarSoft, kSoftThreads);
+      if (st < kHeads) {
+        const float l = (t->red[0][st] + t->red[1][st]) + (t->red[2][st] + t->red[3][st]);
+        t->lsum[st] = l;
+        t->alpha[st] = l > 0.f ? 1.f / l : 0.f;
       }
+      tc::bar_named(kBarSoft, kSoftThreads);
+      // normalised O^T -> stage[h][d] (fp32, d contiguous), then one bulk copy per head
+      for (int c = 0; c < nch; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld32(o_tmem + lane_off + c * kHeads + hb, v);
+        tc::tmem_wait_ld();
+        const int d = c * 128 + j;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) stage[(hb + i) * D + d] = __uint_as_float(v[i]) * t->alpha[hb + i];
+      }
+      tc::fence_proxy_async_smem();
+      tc::bar_named(kBarSoft, kSoftThreads);
+      const int64_t row0 = static_cast<int64_t>(b) * a.H + h0;
       if (st < hcount) {
+        tc::bulk_store(a.part_o + ((row0 + st) * a.splits + split) * a.Dv, stage + st * D, D * 4);
+        tc::bulk_commit();
         const float l = t->lsum[st];
         a.part_lse[(row0 + st) * a.splits + split] =
             l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        tc::bulk_wait();   // shared memory must outlive the copy, and its writes precede the merge
       }
     }
   }

@@ -136,11 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every copy issued must land before the CTA's shared memory goes away
       for (int i = issued - C::STAGES > 0 ? issued - C::STAGES : 0; i < issued; ++i) {
         const int stage = i % C::STAGES, round = i / C::STAGES;
-        for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->full[stage], round & 1); ++it) {
-        }
+        tc::mbar_wait_drain(&t->full[stage], round & 1);
       }
-      for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->q_full, 0); ++it) {
-      }
+      tc::mbar_wait_drain(&t->q_full, 0);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ tcgen05.cp + MMA issuer
@@ -178,8 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every tcgen05 operation issued must finish before tensor memory is released
       tc::tc_commit(&t->drain);
-      for (uint32_t it = 0; it < tc::kWaitLimit && !tc::mbar_try_wait(&t->drain, 0); ++it) {
-      }
+      tc::mbar_wait_drain(&t->drain, 0);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ scale-block builders (64 threads)

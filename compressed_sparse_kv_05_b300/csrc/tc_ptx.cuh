@@ -1,6 +1,6 @@
 // Inline-PTX helpers for the sm_100-family tensor-core path: mbarriers, TMA,
 // tensor memory (tcgen05.alloc/ld/st), shared-memory matrix descriptors and the
-// block-scaled FP4 MMA. Every wait is bounded: after kWaitLimit polls it raises
+// block-scaled FP4 MMA. Every wait is bounded: after kWaitNs it raises
 // the CTA's abort flag and returns false, so no kernel can spin forever.
 #pragma once
 
@@ -12,9 +12,16 @@
 namespace dsv4 {
 namespace tc {
 
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint64_t kWaitNs = 2000000000ull;   // a wait gives up after 2 s
+constexpr uint32_t kSuspendNs = 100000;       // a waiting thread sleeps up to 100 us per poll
 
 DSV4_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+DSV4_DEV uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 DSV4_DEV void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -22,29 +29,44 @@ DSV4_DEV void mbar_init(uint64_t* bar, uint32_t count) {
 
 DSV4_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
+// Test the phase of `bar` with parity `parity`; while it is incomplete the
+// thread is suspended (it resumes when the phase completes, or after
+// kSuspendNs), so waiting warps take no issue slots or shared-memory bandwidth.
 DSV4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n"
       ".reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n"
       "}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete. Gives up (and
-// raises *abort) after kWaitLimit polls, or as soon as another warp raised it.
+// raises *abort) after kWaitNs, or as soon as another warp raised it.
 DSV4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+  const uint64_t t0 = now_ns();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
+    if (now_ns() - t0 > kWaitNs) {
+      *abort = 1;
+      return false;
+    }
   }
-  *abort = 1;
-  return false;
+}
+
+// Wait without an abort flag (draining copies or MMAs before shared or tensor
+// memory is released); gives up after kWaitNs.
+DSV4_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = now_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (now_ns() - t0 > kWaitNs) return false;
+  return true;
 }
 
 DSV4_DEV void mbar_arrive(uint64_t* bar) {
@@ -259,6 +281,17 @@ DSV4_DEV bool bar_and(int id, int count, bool v) {
       : "memory");
   return r != 0;
 }
+
+// Bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16),
+// tracked by this thread's bulk-async groups.
+DSV4_DEV void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+DSV4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk copy of this thread has completed (its writes are performed).
+DSV4_DEV void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 DSV4_DEV void bar_named(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
 
