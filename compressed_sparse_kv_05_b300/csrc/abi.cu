@@ -164,6 +164,26 @@ int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const ui
   return launch_attention(a, p.head_groups, static_cast<cudaStream_t>(stream));
 }
 
+// Scratch of dsv4_hca_decode_static: one array per device, never allocated at run time.
+static __device__ __align__(256) unsigned char g_static_scratch[DSV4_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (cudaGetSymbolAddress with that device current). Null on failure.
+void* static_scratch() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
 }  // namespace
 }  // namespace dsv4
 
@@ -301,6 +321,19 @@ int dsv4_csa_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, co
 int dsv4_hca_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q, float sm_scale,
                     float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
   return decode_common(d, c, H, q, sm_scale, nullptr, 0, out, lse, ws, ws_bytes, stream);
+}
+
+int dsv4_hca_decode_static(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q,
+                           float sm_scale, float* out, float* lse, void* stream) {
+  int e = check_desc(d);
+  if (e) return e;
+  if (H < 1) return DSV4_ERR_INVALID_ARG;
+  if (H > 128) return DSV4_ERR_UNSUPPORTED;
+  const size_t need = attn_plan(d, H, 0).ws_bytes;
+  if (need > DSV4_STATIC_SCRATCH_BYTES) return DSV4_ERR_SCRATCH;
+  void* ws = static_scratch();
+  if (!ws) return DSV4_ERR_CUDA;
+  return decode_common(d, c, H, q, sm_scale, nullptr, 0, out, lse, ws, DSV4_STATIC_SCRATCH_BYTES, stream);
 }
 
 size_t dsv4_workspace_size(const dsv4_layer_desc* d, int32_t H, int32_t Hi, int32_t k) {

@@ -18,9 +18,10 @@ if not os.path.exists(_LIB_PATH):
 
 lib = ctypes.CDLL(_LIB_PATH)
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA = 0, -1, -2, -3, -4, -5
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_SCRATCH = 0, -1, -2, -3, -4, -5, -6
+STATIC_SCRATCH_BYTES = 32 << 20
 STATUS_CAPACITY, STATUS_BAD_INDEX, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4, 8
-_ERR_NAMES = {-1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "MISALIGNED", -4: "WORKSPACE", -5: "CUDA"}
+_ERR_NAMES = {-1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "MISALIGNED", -4: "WORKSPACE", -5: "CUDA", -6: "SCRATCH"}
 
 
 class Dsv4Error(RuntimeError):
@@ -56,6 +57,7 @@ _SIGS = {
     "dsv4_csa_decode": ([_DESC, _CACHE, _I32, _P, ctypes.c_float, _P, _I32, _P, _P, _P, ctypes.c_size_t, _P],
                         ctypes.c_int),
     "dsv4_hca_decode": ([_DESC, _CACHE, _I32, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "dsv4_hca_decode_static": ([_DESC, _CACHE, _I32, _P, ctypes.c_float, _P, _P, _P], ctypes.c_int),
     "dsv4_workspace_size": ([_DESC, _I32, _I32, _I32], ctypes.c_size_t),
     "dsv4_read_status": ([_CACHE, _P], ctypes.c_int),
     "dsv4_quantize_kv_rows": ([_P, _I64, _I32, _I32, _P, _P, _P, _P], ctypes.c_int),
@@ -159,6 +161,12 @@ def dsv4_hca_decode(desc, cache, H, q, sm_scale, out, lse, ws, stream=None):
     return _check("dsv4_hca_decode", lib.dsv4_hca_decode(
         ctypes.byref(desc), ctypes.byref(cache.struct), H, _ptr(q), float(sm_scale), _ptr(out), _ptr(lse),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dsv4_hca_decode_static(desc, cache, H, q, sm_scale, out, lse, stream=None):
+    return _check("dsv4_hca_decode_static", lib.dsv4_hca_decode_static(
+        ctypes.byref(desc), ctypes.byref(cache.struct), H, _ptr(q), float(sm_scale), _ptr(out), _ptr(lse),
+        _stream(stream)))
 
 
 def dsv4_workspace_size(desc, H, Hi, k):

@@ -47,7 +47,8 @@ enum {
   DSV4_ERR_UNSUPPORTED = -2, /* dims outside the supported ranges below */
   DSV4_ERR_MISALIGNED = -3,  /* a plane not 16-byte aligned */
   DSV4_ERR_WORKSPACE = -4,   /* ws smaller than dsv4_workspace_size() */
-  DSV4_ERR_CUDA = -5         /* a kernel launch failed */
+  DSV4_ERR_CUDA = -5,        /* a kernel launch failed */
+  DSV4_ERR_SCRATCH = -6      /* the call needs more scratch than DSV4_STATIC_SCRATCH_BYTES */
 };
 
 /* Bits of the device status word (sticky until dsv4_read_status clears them). */
@@ -156,6 +157,31 @@ int dsv4_csa_decode(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_
 int dsv4_hca_decode(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_t H,
                     const uint16_t* q, float sm_scale, float* out, float* lse,
                     void* ws, size_t ws_bytes, void* stream);
+
+/* dsv4_hca_decode for callers that cannot allocate device memory.
+ * The pages describe no such call; it exists for library users. Some callers
+ * cannot call cudaMalloc at all: code that runs while a CUDA graph is being
+ * captured, engines whose memory is fully planned up front by an allocator
+ * that owns the device, or plug-in hosts that forbid allocation on their
+ * hot path. This variant takes the same arguments as dsv4_hca_decode minus the
+ * workspace: its split partials live in one file-scope device array of
+ * DSV4_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits. The caller still passes the cache, query and outputs.
+ *   - Returns DSV4_ERR_SCRATCH (and launches nothing) when the call would need
+ *     more than DSV4_STATIC_SCRATCH_BYTES (dsv4_workspace_size(desc, H, 0, 0)
+ *     gives the need).
+ *   - The first call on a device looks up the array's device address there
+ *     (with that device current); make that first call before any stream
+ *     capture. Later calls only read the cached address.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; the kernels write every scratch word they read, so nothing needs
+ *     clearing between calls. Calls whose executions overlap on the GPU (other
+ *     streams, other threads) race on the array: order them.
+ *   - It allocates and frees nothing (no cudaMalloc, cudaFree or allocating
+ *     library routine). */
+#define DSV4_STATIC_SCRATCH_BYTES (32u << 20)
+int dsv4_hca_decode_static(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_t H,
+                           const uint16_t* q, float sm_scale, float* out, float* lse, void* stream);
 
 /* Bytes of device workspace the calls above need for this layer with H query
  * heads, Hi indexer heads and top-k k (0 when the arguments are invalid). */
