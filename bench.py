@@ -124,16 +124,17 @@ class ClockSampler:
 class Stack:
     """The eight layers' caches, biases and per-step inputs, all on the device."""
 
-    def __init__(self, dsv4, layers, steps_total, seed):
+    def __init__(self, dsv4, layers, steps_total, seed, extra_tokens=None):
         self.dsv4 = dsv4
         self.layers = layers
         self.steps_total = steps_total
+        extra_tokens = steps_total if extra_tokens is None else extra_tokens
         g = torch.Generator(device="cuda")
         g.manual_seed(seed)
         self.g = g
         self.descs, self.caches, self.bias, self.bias_u = [], [], [], []
         for li, L in enumerate(layers):
-            cap = L.capacity(steps_total)
+            cap = L.capacity(extra_tokens)
             desc = dsv4.layer_desc(L, cap)
             cache = dsv4.Cache(desc)
             self._fill(L, desc, cache)
@@ -323,19 +324,30 @@ def run_ours(args, rank, world):
     K, Wm = args.steps, args.warmup
     total = K + Wm
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-    st = Stack(dsv4, layers, total + K + 2, seed=1234 + rank)
+    # input slots: [0, total) timed run, [total, total + K) per-call event run and
+    # end-to-end run, then one eager warm-up step and one probe capture
+    # appends: eager warm-up, W + K timed, K per-call, K end-to-end steps
+    st = Stack(dsv4, layers, total + K + 2, seed=1234 + rank, extra_tokens=total + 2 * K + 2)
     stream = torch.cuda.Stream()
     # eager warm-up of every call (kernel attributes are set outside capture)
     with torch.cuda.stream(stream):
         st.step(total + K)
     stream.synchronize()
-    graphs, events = [], []
+    # timed graphs hold only the library's launches, so consecutive kernels keep
+    # their programmatic (overlapping) launch edges; a second set with an event
+    # pair around every call gives the per-call durations
+    graphs, ev_graphs, events = [], [], []
     for s in range(total):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            st.step(s)
+        graphs.append(g)
+    for i in range(K):
         g = torch.cuda.CUDAGraph()
         ev = {}
         with torch.cuda.graph(g, stream=stream):
-            st.step(s, ev if s >= Wm else None)
-        graphs.append(g)
+            st.step(total + i, ev)
+        ev_graphs.append(g)
         events.append(ev)
     probe = torch.cuda.CUDAGraph(keep_graph=True)       # captured only to count its kernel nodes
     with torch.cuda.graph(probe, stream=stream):
@@ -367,9 +379,13 @@ def run_ours(args, rank, world):
     ms_step = ms / K
     value = world * B * 1000.0 / ms_step
 
-    # per-call durations over the timed steps
+    # per-call durations: K more steps through the graphs with events
+    for g in ev_graphs:
+        with torch.cuda.stream(stream):
+            g.replay()
+    torch.cuda.synchronize()
     per_call = {}
-    for ev in events[Wm:]:
+    for ev in events:
         for call, pairs in ev.items():
             per_call.setdefault(call, []).extend(a.elapsed_time(b) for a, b in pairs)
     call_layer = {"append": layers[0]}

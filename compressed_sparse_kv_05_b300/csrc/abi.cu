@@ -7,6 +7,7 @@
 
 #include "../../include/dsv4.h"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dsv4 {
 namespace {
@@ -117,7 +118,7 @@ IndexWs index_ws(const dsv4_layer_desc* d, int Hi, int k) {
   w.hist1 = up(w.scores + B * cap * sizeof(float));
   w.hist2 = up(w.hist1 + B * 4096 * sizeof(uint32_t));
   w.cnt = up(w.hist2 + B * 4096 * sizeof(uint32_t));
-  w.above = up(w.cnt + B * 4 * sizeof(uint32_t));
+  w.above = up(w.cnt + B * kCntWords * sizeof(uint32_t));
   w.cand = up(w.above + B * static_cast<size_t>(k) * sizeof(int32_t));
   w.total = up(w.cand + B * cap * sizeof(uint64_t));
   return w;
@@ -239,14 +240,13 @@ int dsv4_compress_append(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t 
   a.pend_u = c->pend_u; a.pend_zu = c->pend_zu; a.n_tokens = c->n_tokens; a.status = c->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int D = d->d_nope + d->d_rope;
+  const size_t smem = (2 * D + d->idx_dim + 32) * sizeof(float);
+  if (T == 1) return launch_pdl(append_one_kernel, dim3(d->batch), dim3(256), smem, st, a);
   const int blocks = (d->ratio - 1 + T) / d->ratio;
   if (blocks > 0) {
-    const size_t smem = (2 * D + d->idx_dim + 32) * sizeof(float);
-    pool_append_kernel<<<dim3(blocks, d->batch), 256, smem, st>>>(a);
-    if ((e = launch_status())) return e;
+    if ((e = launch_pdl(pool_append_kernel, dim3(blocks, d->batch), dim3(256), smem, st, a))) return e;
   }
-  append_tail_kernel<<<d->batch, 256, 0, st>>>(a);
-  return launch_status();
+  return launch_pdl(append_tail_kernel, dim3(d->batch), dim3(256), 0, st, a);
 }
 
 int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, const uint16_t* q_idx,
@@ -285,8 +285,7 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   a.above = reinterpret_cast<int32_t*>(wp + wl.above);
   a.cand = reinterpret_cast<uint64_t*>(wp + wl.cand);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  quant_query_fp4_kernel<<<a.B * N, 32, 0, st>>>(a);
-  if ((e = launch_status())) return e;
+  if ((e = launch_pdl(quant_query_fp4_kernel, dim3(a.B * N), dim3(32), 0, st, a))) return e;
   IndexTcArgs t{};
   t.B = a.B; t.N = N; t.Di = a.Di; t.capacity = a.capacity; t.ratio = a.ratio;
   const int tiles = (d->capacity + 127) / 128;
@@ -298,14 +297,13 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   while (cols < need) cols <<= 1;
   t.tmem_cols = cols;
   t.n_tokens = c->n_tokens; t.idx_scales = c->idx_scales; t.q_scales = a.q_scales; t.wpad = a.wpad;
-  t.scores = a.scores; t.hist1 = a.hist1; t.status = c->status;
+  t.scores = a.scores; t.hist1 = a.hist1; t.cnt = a.cnt; t.k = k; t.status = c->status;
   if ((e = launch_index_scores_tc(t, c->idx_codes, a.q_codes, st))) return e;
-  int sel = (4 * 148) / a.B;
+  int sel = (2 * kSms) / a.B;
   const int sel_max = (d->capacity + 511) / 512;
   if (sel > sel_max) sel = sel_max;
   if (sel < 1) sel = 1;
-  topk_select_kernel<<<dim3(sel, a.B), 512, 0, st>>>(a);
-  return launch_status();
+  return launch_topk_select(a, sel, st);
 }
 
 int dsv4_csa_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q, float sm_scale,

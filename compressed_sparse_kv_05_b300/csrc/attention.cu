@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dsv4 {
 
@@ -39,6 +40,8 @@ struct RowSrc {
 template <int HP, int ACC>
 __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smraw[];
+  pdl_trigger();
+  pdl_wait();
   constexpr int TPH = NT / HP;
   const int D = a.D, Dv = a.Dv;
   uint16_t* qs = reinterpret_cast<uint16_t*>(smraw);
@@ -177,6 +180,8 @@ __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
 // per CTA. Warp g sums splits g, g + 4, ... for 4 dims per lane, with several
 // splits' loads in flight; the four warps' sums are then added.
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t bh = blockIdx.x;
   const float* lse = a.part_lse + bh * a.splits;
   const int sg = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -225,8 +230,7 @@ int launch_split(const AttnArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
   std::call_once(flag, [] {
     cudaFuncSetAttribute(attn_split_kernel<HP, ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   });
-  attn_split_kernel<HP, ACC><<<grid, NT, smem, st>>>(a);
-  return launch_status();
+  return launch_pdl(attn_split_kernel<HP, ACC>, grid, dim3(NT), smem, st, a);
 }
 }  // namespace
 
@@ -252,8 +256,7 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
 }
 
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st) {
-  attn_merge_kernel<<<dim3(a.B * a.H, (a.Dv + 127) / 128), 128, 0, st>>>(a);
-  return launch_status();
+  return launch_pdl(attn_merge_kernel, dim3(a.B * a.H, (a.Dv + 127) / 128), dim3(128), 0, st, a);
 }
 
 }  // namespace dsv4

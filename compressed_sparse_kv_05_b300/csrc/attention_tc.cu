@@ -45,6 +45,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace dsv4 {
@@ -318,6 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   unsigned char* xv = SEP ? xk + nch * kChunkBytes : xk;
   float* stage = reinterpret_cast<float*>(xk);               // epilogue: [64 heads][D] fp32, after the last P.V
   TcTail* t = reinterpret_cast<TcTail*>(xk + (SEP ? 2 : 1) * nch * kChunkBytes);
+  pdl_trigger();
+  pdl_wait();
 
   const int split = blockIdx.x, b = blockIdx.y;
   const int h0 = blockIdx.z * kHeads;
@@ -622,8 +625,7 @@ int launch_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
     cudaFuncSetAttribute(attn_tc_kernel<SEP>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   const size_t smem = tc_smem_bytes(a.D, SEP);
-  attn_tc_kernel<SEP><<<dim3(a.splits, a.B, head_groups), kThreads, smem, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+  return launch_pdl(attn_tc_kernel<SEP>, dim3(a.splits, a.B, head_groups), dim3(kThreads), smem, st, a);
 }
 
 }  // namespace

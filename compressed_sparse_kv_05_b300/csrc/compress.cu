@@ -18,6 +18,7 @@
 // kernel ahead of the pending writes of the second.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dsv4 {
 
@@ -77,6 +78,8 @@ DSV4_DEV void store_fp4_row(const float* y, int cols, uint8_t* codes, uint8_t* s
 // grid (max blocks one call can complete, B); dynamic smem: (2*D + Di) floats + 32
 __global__ void __launch_bounds__(256) pool_append_kernel(AppendArgs a) {
   extern __shared__ float smem[];
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.y;
   const int D = a.d_nope + a.d_rope;
   const int m = a.ratio;
@@ -115,6 +118,8 @@ DSV4_DEV void copy_row(uint16_t* dst, const uint16_t* src, int dim) {
 
 // grid (B); writes the window ring and the pending tokens, then advances n_tokens.
 __global__ void __launch_bounds__(256) append_tail_kernel(AppendArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int D = a.d_nope + a.d_rope;
   const int m = a.ratio;
@@ -143,6 +148,63 @@ __global__ void __launch_bounds__(256) append_tail_kernel(AppendArgs a) {
         copy_row(a.pend_u + dst * a.idx_dim, a.u + src * a.idx_dim, a.idx_dim);
         copy_row(a.pend_zu + dst * a.idx_dim, a.zu + src * a.idx_dim, a.idx_dim);
       }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.n_tokens[b] = n_new;
+}
+
+// Single-token append (T = 1), grid (B), one CTA per sequence: if the token
+// completes a block, pool it (old pending tokens + the new one) and store the
+// entry; then write the token into the window ring and, while its block stays
+// open, into the pending planes; then advance n_tokens. One CTA does all of a
+// sequence's work in this order, so the pending reads precede the writes.
+__global__ void __launch_bounds__(256) append_one_kernel(AppendArgs a) {
+  extern __shared__ float smem[];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  const int D = a.d_nope + a.d_rope;
+  const int m = a.ratio;
+  const int64_t n_old = a.n_tokens[b];
+  const int64_t n_new = n_old + 1;
+  if (n_new / m > a.capacity) {
+    if (threadIdx.x == 0) atomicOr(a.status, DSV4_STATUS_CAPACITY);
+    return;
+  }
+  if (n_new % m == 0) {
+    const int64_t j = n_old / m;
+    float* yk = smem;
+    float* yv = smem + D;
+    float* yu = smem + 2 * D;
+    float* red = yu + a.idx_dim;
+    pool_block(a, b, j, n_old, a.pend_k, a.k, a.pend_v, a.v, a.pend_z, a.z, a.bias, D, yk,
+               a.separate_v ? yv : nullptr);
+    if (a.idx_dim) pool_block(a, b, j, n_old, a.pend_u, a.u, nullptr, nullptr, a.pend_zu, a.zu, a.bias_u,
+                              a.idx_dim, yu, nullptr);
+    __syncthreads();
+    const int64_t e = static_cast<int64_t>(b) * a.capacity + j;
+    store_kv_entry(yk, a.d_nope, a.d_rope, a.k_nope + e * a.d_nope, a.k_scale + e, a.k_rope + e * a.d_rope, red);
+    if (a.separate_v)
+      store_kv_entry(yv, a.d_nope, a.d_rope, a.v_nope + e * a.d_nope, a.v_scale + e, a.v_rope + e * a.d_rope, red);
+    if (a.idx_dim)
+      store_fp4_row(yu, a.idx_dim, a.idx_codes + e * (a.idx_dim / 2), a.idx_scales + e * (a.idx_dim / 16));
+    __syncthreads();
+  }
+  const int64_t src = b;   // row b of the [B][1][.] inputs
+  if (a.window > 0) {
+    const int64_t dst = static_cast<int64_t>(b) * a.window + n_old % a.window;
+    copy_row(a.win_k + dst * D, a.k + src * D, D);
+    if (a.separate_v) copy_row(a.win_v + dst * D, a.v + src * D, D);
+  }
+  if (m > 1 && n_new % m != 0) {
+    const int64_t dst = static_cast<int64_t>(b) * m + n_old % m;
+    copy_row(a.pend_k + dst * D, a.k + src * D, D);
+    copy_row(a.pend_z + dst * D, a.z + src * D, D);
+    if (a.separate_v) copy_row(a.pend_v + dst * D, a.v + src * D, D);
+    if (a.idx_dim) {
+      copy_row(a.pend_u + dst * a.idx_dim, a.u + src * a.idx_dim, a.idx_dim);
+      copy_row(a.pend_zu + dst * a.idx_dim, a.zu + src * a.idx_dim, a.idx_dim);
     }
   }
   __syncthreads();

@@ -30,6 +30,8 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
+#include "select.cuh"
 #include "tc_ptx.cuh"
 
 namespace dsv4 {
@@ -54,7 +56,9 @@ struct SmemTail {
   uint64_t full[8], empty[8], sf_full[8], acc_full[2], acc_empty[2], q_full, qsf_full, drain;
   uint32_t taddr;
   int abort;
-  uint32_t hist[4096];   // histogram of score-key bits 31..20 of this CTA's blocks
+  uint32_t last;
+  uint32_t scratch[kThreads / 32 + 2];
+  uint32_t hist[kBins];  // histogram of score-key bits 31..20 of this CTA's blocks
 };
 
 // named barrier among the four epilogue warps
@@ -76,6 +80,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* qsf = sfbuf + C::STAGES * C::SF_BYTES;                   // query scale blocks (N <= 128 rows)
   SmemTail* t = reinterpret_cast<SmemTail*>(qsf + C::SF_BYTES);
   float* wsm = reinterpret_cast<float*>(t + 1);
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    tc::prefetch_tensormap(&keys);
+    tc::prefetch_tensormap(&qmap);
+  }
+  pdl_wait();
 
   const int b = blockIdx.y;
   int64_t n_c = a.n_tokens[b] / a.ratio;
@@ -192,21 +202,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&t->qsf_full);
-    for (int i = 0; i < ntile; ++i) {
-      const int stage = i % C::STAGES, round = i / C::STAGES;
-      if (!tc::mbar_wait(&t->empty[stage], (round & 1) ^ 1, abort)) break;
-      uint32_t* dst = reinterpret_cast<uint32_t*>(sfbuf + stage * C::SF_BYTES);
-      for (int r = tid; r < kTile; r += 64) {
-        const int64_t s = static_cast<int64_t>(t0 + i) * kTile + r;
-        const uint8_t* src = a.idx_scales + (static_cast<int64_t>(b) * a.capacity + s) * nblk;
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-          const uint32_t w = s < n_c ? *reinterpret_cast<const uint32_t*>(src + kk * 4) : 0u;
-          dst[kk * (kSfBlock / 4) + (r & 31) * 4 + (r >> 5)] = w;
+    // key scales: the global loads run kPf tiles ahead of the shared-memory
+    // writes, so no tile waits for a memory round trip
+    constexpr int kPf = 4;
+    uint32_t pf[kPf][2][C::KSTEPS];
+    auto load_scales = [&](int i, uint32_t (&w)[2][C::KSTEPS]) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int64_t s = static_cast<int64_t>(t0 + i) * kTile + tid + rr * 64;
+        const uint32_t* src =
+            reinterpret_cast<const uint32_t*>(a.idx_scales + (static_cast<int64_t>(b) * a.capacity + s) * nblk);
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) w[rr][kk] = (i < ntile && s < n_c) ? __ldg(src + kk) : 0u;
+      }
+    };
+#pragma unroll
+    for (int u = 0; u < kPf; ++u) load_scales(u, pf[u]);
+    bool ok = true;
+    for (int i0 = 0; ok && i0 < ntile; i0 += kPf) {
+#pragma unroll
+      for (int u = 0; u < kPf; ++u) {
+        const int i = i0 + u;
+        if (ok && i < ntile) {
+          const int stage = i % C::STAGES, round = i / C::STAGES;
+          ok = tc::mbar_wait(&t->empty[stage], (round & 1) ^ 1, abort);
+          if (ok) {
+            uint32_t* dst = reinterpret_cast<uint32_t*>(sfbuf + stage * C::SF_BYTES);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const int r = tid + rr * 64;
+#pragma unroll
+              for (int kk = 0; kk < C::KSTEPS; ++kk) dst[kk * (kSfBlock / 4) + (r & 31) * 4 + (r >> 5)] = pf[u][rr][kk];
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&t->sf_full[stage]);
+            load_scales(i + kPf, pf[u]);
+          }
         }
       }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&t->sf_full[stage]);
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 4-7)
@@ -250,6 +284,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_dealloc(taddr, ncols);
   }
   if (threadIdx.x == 0 && t->abort) atomicOr(a.status, DSV4_STATUS_TIMEOUT);
+
+  // The last CTA of sequence b to finish (a completion counter, no waiting)
+  // finds the first-level threshold bin of the top-k in the full histogram.
+  uint32_t* cnt = a.cnt + b * kCntWords;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int active = (tiles + per - 1) / per;   // CTAs of this sequence that had tiles
+    t->last = atomicAdd(&cnt[3], 1u) == static_cast<uint32_t>(active - 1);
+  }
+  __syncthreads();
+  if (!t->last || n_c <= a.k) return;
+  __threadfence();
+  const volatile uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) t->hist[i] = gh[i];
+  __syncthreads();
+  uint32_t n_gt1;
+  const int T1 = block_suffix_select<kThreads>(t->hist, static_cast<uint32_t>(a.k), &n_gt1, t->scratch);
+  if (threadIdx.x == 0) {
+    cnt[4] = static_cast<uint32_t>(T1);
+    cnt[5] = n_gt1;
+  }
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -295,8 +350,7 @@ int launch_tc(const IndexTcArgs& a, const CUtensorMap& keys, const CUtensorMap& 
   std::call_once(once, [] {
     cudaFuncSetAttribute(index_scores_tc_kernel<ROWB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   });
-  index_scores_tc_kernel<ROWB><<<dim3(a.ctas_per_seq, a.B), kThreads, smem, st>>>(keys, qmap, a);
-  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+  return launch_pdl(index_scores_tc_kernel<ROWB>, dim3(a.ctas_per_seq, a.B), dim3(kThreads), smem, st, keys, qmap, a);
 }
 
 }  // namespace

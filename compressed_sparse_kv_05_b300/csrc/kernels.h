@@ -25,6 +25,7 @@ struct AppendArgs {
 
 __global__ void pool_append_kernel(AppendArgs a);
 __global__ void append_tail_kernel(AppendArgs a);
+__global__ void append_one_kernel(AppendArgs a);
 __global__ void quant_kv_rows_kernel(const float* y, int64_t rows, int d_nope, int d_rope, uint8_t* nope,
                                      float* scale, uint16_t* rope);
 __global__ void quant_fp4_rows_kernel(const float* y, int64_t rows, int cols, uint8_t* codes, uint8_t* scales);
@@ -32,6 +33,10 @@ __global__ void pool_rows_kernel(const uint16_t* x, const uint16_t* z, const flo
                                  float* y);
 
 // ---- indexer + top-k
+// Per-sequence counter words of the top-k: [0] blocks above the threshold bin,
+// [1] candidates in it, [2] finished selection CTAs, [3] finished scoring CTAs,
+// [4] first-level threshold bin T1, [5] keys in bins above T1.
+constexpr int kCntWords = 8;
 struct IndexArgs {
   int B, Hi, N, Di, k, capacity, ratio;
   const uint16_t* q_idx;   // [B][Hi][Di] bf16
@@ -44,15 +49,16 @@ struct IndexArgs {
   int32_t* topk;           // [B][k]
   uint32_t* hist1;         // [B][4096] histogram of score-key bits 31..20 (filled while scoring)
   uint32_t* hist2;         // [B][4096] histogram of key bits 19..8 inside the threshold bin
-  uint32_t* cnt;           // [B][4] above count, candidate count, finished select CTAs
+  uint32_t* cnt;           // [B][kCntWords] (see kCntWords)
   int32_t* above;          // [B][k] blocks above the threshold bin
   uint64_t* cand;          // [B][capacity] (key << 32 | index) of the blocks in the threshold bin
 };
 __global__ void quant_query_fp4_kernel(IndexArgs a);
 __global__ void topk_select_kernel(IndexArgs a);
+int launch_topk_select(const IndexArgs& a, int sel_ctas, cudaStream_t st);
 
 struct IndexTcArgs {
-  int B, N, Di, capacity, ratio, ctas_per_seq;
+  int B, N, Di, capacity, ratio, ctas_per_seq, k;
   uint32_t tmem_cols;
   const int64_t* n_tokens;
   const uint8_t* idx_scales;   // [B][capacity][Di/16]
@@ -60,6 +66,7 @@ struct IndexTcArgs {
   const float* wpad;           // [B][N]
   float* scores;               // [B][capacity]
   uint32_t* hist1;             // [B][4096]
+  uint32_t* cnt;               // [B][kCntWords]
   int32_t* status;
 };
 // tcgen05 block-scaled FP4 scores; key_codes [B][capacity][Di/2], q_codes [B][N][Di/2]

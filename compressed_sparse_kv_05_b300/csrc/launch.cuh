@@ -1,0 +1,34 @@
+// Programmatic dependent launch for the library's kernels on the caller's
+// stream. A kernel launched with launch_pdl may be scheduled while the
+// previous kernel of the stream is still finishing; it calls pdl_wait() before
+// its first global-memory access, which returns once every prerequisite grid
+// has completed and its writes are visible. Each kernel calls pdl_trigger()
+// early so that the next kernel's launch overlaps its own tail. After a kernel
+// that never triggers (any other library's), the launch simply waits for it.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "../../include/dsv4.h"
+
+namespace dsv4 {
+
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+}  // namespace dsv4
