@@ -64,6 +64,7 @@ int check_cache_read(const dsv4_layer_desc* d, const dsv4_cache* c) {
 struct AttnPlan {
   int head_groups, splits, rows_per_split;
   bool tc;
+  size_t part_bytes;   // bytes of the split partials (the log-sum-exps follow)
   size_t ws_bytes;
 };
 
@@ -83,7 +84,9 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
     p.rows_per_split = static_cast<int>(rps);
     p.splits = static_cast<int>((rmax + rps - 1) / rps);
     if (p.splits < 1) p.splits = 1;
-    p.ws_bytes = static_cast<size_t>(d->batch) * H * p.splits * (Dv + 1) * sizeof(float) + 256;
+    // f16 partials [B][splits][head groups][D][64], then fp32 log-sum-exps [B][H][splits]
+    p.part_bytes = (static_cast<size_t>(d->batch) * p.splits * p.head_groups * Dv * 64 * 2 + 255) & ~size_t(255);
+    p.ws_bytes = p.part_bytes + static_cast<size_t>(d->batch) * H * p.splits * sizeof(float) + 256;
     return p;
   }
   const int64_t want = (kSplitTarget + d->batch * p.head_groups - 1) / (d->batch * p.head_groups);
@@ -96,6 +99,7 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
   if (s < 1) s = 1;
   p.splits = static_cast<int>(s);
   p.rows_per_split = static_cast<int>(rps);
+  p.part_bytes = (static_cast<size_t>(d->batch) * H * p.splits * Dv * sizeof(float) + 255) & ~size_t(255);
   p.ws_bytes = static_cast<size_t>(d->batch) * H * p.splits * (Dv + 1) * sizeof(float) + 256;
   return p;
 }
@@ -157,9 +161,7 @@ int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const ui
   a.n_tokens = c->n_tokens; a.status = c->status;
   char* w = static_cast<char*>(ws);
   a.part_o = reinterpret_cast<float*>(w);
-  size_t off = static_cast<size_t>(a.B) * H * p.splits * a.Dv * sizeof(float);
-  off = (off + 255) & ~static_cast<size_t>(255);
-  a.part_lse = reinterpret_cast<float*>(w + off);
+  a.part_lse = reinterpret_cast<float*>(w + p.part_bytes);
   a.out = out; a.lse = lse;
   if (p.tc) return launch_attention_tc(a, p.head_groups, static_cast<cudaStream_t>(stream));
   return launch_attention(a, p.head_groups, static_cast<cudaStream_t>(stream));

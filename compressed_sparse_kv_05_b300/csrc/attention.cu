@@ -15,6 +15,8 @@
 // combines the splits: o = sum_s exp(lse_s - lse) o_s, lse = log sum_s exp(lse_s).
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -221,6 +223,98 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   if (threadIdx.x == 0 && blockIdx.y == 0 && a.lse) a.lse[bh] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
+// Merge of the tensor-core kernel's splits: partials are f16 [B][splits][head
+// groups][D][64 heads] (normalised), log-sum-exps fp32 [B][H][splits].
+// grid (B * head groups, D / 16), block 128: 16 dims x 64 heads per CTA; thread
+// t handles dim d0 + t / 8 and heads 8 (t % 8) .. + 7. The split weights
+// exp(lse_s - max) are computed once per CTA, 64 splits at a time.
+__global__ void __launch_bounds__(128) attn_merge_tc_kernel(AttnArgs a) {
+  constexpr int kS = 64;   // splits per pass over the weights
+  constexpr int kU = 8;    // partial loads in flight per thread
+  pdl_trigger();
+  pdl_wait();
+  const int hgs = (a.H + 63) / 64;
+  const int b = blockIdx.x / hgs, hg = blockIdx.x % hgs;
+  const int h0 = hg * 64;
+  const int hcount = a.H - h0 < 64 ? a.H - h0 : 64;
+  __shared__ float s_mx[64], s_inv[64];
+  __shared__ float s_w[kS][64];
+  __shared__ float s_out[64][17];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const float* lse0 = a.part_lse + (static_cast<int64_t>(b) * a.H + h0) * a.splits;
+  {
+    // head t / 2: max and sum of exp over its splits, each of the two threads
+    // taking every other split (all loads of a pass in flight together)
+    const int h = t >> 1, par = t & 1;
+    float mx = -INFINITY, tot = 0.f;
+    if (h < hcount) {
+      const float* lse = lse0 + static_cast<int64_t>(h) * a.splits;
+#pragma unroll 8
+      for (int s = par; s < a.splits; s += 2) mx = fmaxf(mx, lse[s]);
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    if (h < hcount && mx != -INFINITY) {
+      const float* lse = lse0 + static_cast<int64_t>(h) * a.splits;
+#pragma unroll 8
+      for (int s = par; s < a.splits; s += 2) tot += __expf(lse[s] - mx);
+    }
+    tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+    if (par == 0) {
+      s_mx[h] = mx;
+      s_inv[h] = tot > 0.f ? 1.f / tot : 0.f;
+      if (blockIdx.y == 0 && a.lse && h < hcount)
+        a.lse[static_cast<int64_t>(b) * a.H + h0 + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+    }
+  }
+  const int dl = t >> 3, hq = (t & 7) * 8;
+  const int d = blockIdx.y * 16 + dl;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const uint16_t* part = reinterpret_cast<const uint16_t*>(a.part_o) +
+                         ((static_cast<int64_t>(b) * a.splits * hgs + hg) * a.D + (d < a.D ? d : 0)) * 64 + hq;
+  const int64_t sstride = static_cast<int64_t>(hgs) * a.D * 64;   // between splits
+  for (int s0 = 0; s0 < a.splits; s0 += kS) {
+    const int ns = a.splits - s0 < kS ? a.splits - s0 : kS;
+    __syncthreads();
+    for (int i = t; i < ns * 64; i += blockDim.x) {
+      const int s = i >> 6, h = i & 63;
+      // normalised weight of split s for head h; a split without rows (lse
+      // -inf) gets 0 and may have left its partial unwritten
+      s_w[s][h] = h < hcount && s_mx[h] != -INFINITY
+                      ? __expf(lse0[static_cast<int64_t>(h) * a.splits + s0 + s] - s_mx[h]) * s_inv[h]
+                      : 0.f;
+    }
+    __syncthreads();
+    for (int s = 0; s < ns; s += kU) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        v[u] = s + u < ns ? __ldcg(reinterpret_cast<const uint4*>(part + (s0 + s + u) * sstride)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (s + u < ns) {
+          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float w = s_w[s + u][hq + i];
+            const uint16_t bits = static_cast<uint16_t>((i & 1) ? w4[i >> 1] >> 16 : w4[i >> 1] & 0xFFFFu);
+            const float x = __half2float(__ushort_as_half(bits));
+            acc[i] = w > 0.f ? fmaf(w, x, acc[i]) : acc[i];
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s_out[hq + i][dl] = acc[i];
+  __syncthreads();
+  for (int r = warp * 2 + (lane >> 4); r < hcount; r += 8) {   // 16 dims of head r per half-warp
+    const int dd = blockIdx.y * 16 + (lane & 15);
+    if (dd < a.D) a.out[(static_cast<int64_t>(b) * a.H + h0 + r) * a.Dv + dd] = s_out[r][lane & 15];
+  }
+}
+
 namespace {
 int launch_status() { return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA; }
 
@@ -253,6 +347,10 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
         : need <= 64 ? launch_split<64, 64>(a, grid, smem, st) : launch_split<64, 144>(a, grid, smem, st);
   if (e) return e;
   return launch_attention_merge(a, st);
+}
+
+int launch_attention_merge_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
+  return launch_pdl(attn_merge_tc_kernel, dim3(a.B * head_groups, (a.D + 15) / 16), dim3(128), 0, st, a);
 }
 
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st) {

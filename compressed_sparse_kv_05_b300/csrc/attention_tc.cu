@@ -70,10 +70,12 @@ constexpr float kRescale = 8.f;                // lazy-rescale threshold (log2 u
 constexpr float kF16Max = 65504.f;
 
 struct TcTail {
-  uint64_t xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, qready, drain;
+  uint64_t xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, qready, qraw, drain;
   uint32_t taddr;
   int abort;
   int32_t src[kMaxTiles * kRows];   // row sources of every row of the split (see row_source)
+  float sk[kMaxTiles * kRows];      // key (or shared entry) scale of every row, 0 for others
+  float sv[kMaxTiles * kRows];      // value scale (separate V)
   float m_used[kHeads];             // running max per head, log2 domain
   float alpha[kHeads];
   float lsum[kHeads];
@@ -113,20 +115,6 @@ DSV4_DEV float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-DSV4_DEV uint4 ldg16(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-DSV4_DEV uint2 ldg8(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
 }
 
 // Rows of sequence b are numbered: first the compressed entries (the top-k list
@@ -212,60 +200,104 @@ DSV4_DEV void prefetch_rows(const AttnArgs& a, const RowSpace& s, int b, int64_t
   }
 }
 
-// Raw bytes of one 128-dim chunk of a tile, as this thread's share of the
-// 2048 8-dim groups (group i = row i / 16, dims 8 * (i % 16) of the chunk):
-// 8 e4m3 codes with the row's scale, or 8 bf16 values.
-struct ChunkRaw {
-  uint4 v[kItems];
-  float s[kItems];
-};
+DSV4_DEV void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+DSV4_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most n of this thread's committed groups are pending (n < 4)
+DSV4_DEV void cp_async_wait(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+  }
+}
 
-// Issue the global loads of chunk c of tile tt (rows src[tt * 128 ...]).
-DSV4_DEV void load_chunk(const AttnArgs& a, int b, const int32_t* src, int tt, int c, const uint8_t* nope,
-                         const float* scale, const uint16_t* rope, const uint16_t* win, int ctid, ChunkRaw& r) {
+// Dims [128c, 128c + 128) of a row: nn FP8 dims (codes), the rest RoPE (bf16).
+struct ChunkSplit {
+  int nn, rope0;   // nope dims in the chunk; first RoPE dim (index into the row's RoPE part)
+};
+DSV4_DEV ChunkSplit chunk_split(const AttnArgs& a, int c) {
+  const int n0 = c * 128;
+  int nn = a.d_nope - n0;
+  nn = nn < 0 ? 0 : (nn > 128 ? 128 : nn);
+  return ChunkSplit{nn, n0 + nn - a.d_nope};
+}
+
+// Issue the asynchronous copies of chunk c of tile tt into the X chunk region
+// `xc`: row j's raw bytes land at xc + 256 j, as the chunk's FP8 codes followed
+// by its RoPE dims (bf16) for an entry, or its 128 bf16 values for a window
+// token; rows that do not exist get nothing. Thread ctid copies 16-byte
+// granules (row i / 16, granule i % 16) of its items.
+DSV4_DEV void issue_chunk(const AttnArgs& a, int b, const int32_t* src, int tt, int c, const uint8_t* nope,
+                          const uint16_t* rope, const uint16_t* win, unsigned char* xc, int ctid) {
+  const ChunkSplit cs = chunk_split(a, c);
+  const int ng = cs.nn / 16, ngr = (128 - cs.nn) / 8;
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
     const int i = ctid + it * kConvThreads;
-    r.v[it] = make_uint4(0u, 0u, 0u, 0u);
-    r.s[it] = 0.f;
     if (i < kGroups) {
-      const int d0 = c * 128 + (i & 15) * 8;
-      const int32_t sr = src[tt * kRows + (i >> 4)];
+      const int j = i >> 4, k = i & 15;
+      const int32_t sr = src[tt * kRows + j];
+      unsigned char* dst = xc + j * 256 + k * 16;
       if (sr >= 0) {
-        if (d0 < a.d_nope) {
-          const uint2 w = ldg8(nope + static_cast<int64_t>(sr) * a.d_nope + d0);
-          r.v[it].x = w.x;
-          r.v[it].y = w.y;
-          r.s[it] = __ldg(scale + sr);
-        } else {
-          r.v[it] = ldg16(rope + static_cast<int64_t>(sr) * a.d_rope + (d0 - a.d_nope));
-        }
+        if (k < ng) cp_async16(dst, nope + static_cast<int64_t>(sr) * a.d_nope + c * 128 + k * 16);
+        else if (k < ng + ngr) cp_async16(dst, rope + static_cast<int64_t>(sr) * a.d_rope + cs.rope0 + (k - ng) * 8);
       } else if (sr <= -2) {
-        r.v[it] = ldg16(win + (static_cast<int64_t>(b) * a.window + (-2 - sr)) * a.D + d0);
+        cp_async16(dst, win + (static_cast<int64_t>(b) * a.window + (-2 - sr)) * a.D + c * 128 + k * 8);
       }
     }
   }
 }
 
-// Convert a loaded chunk to f16 and store it into X chunk `xc` (two 64-dim
-// swizzle atoms). Tracks the largest |value| that must fit f16 (range check).
-DSV4_DEV void store_chunk(const AttnArgs& a, const int32_t* src, int tt, int c, const ChunkRaw& r, unsigned char* xc,
-                          int ctid, float& mx) {
+// Convert chunk c of tile tt in place: every converter thread first reads the
+// raw bytes of its 8-dim groups (group i: row i / 16, dims 8 * (i % 16) of the
+// chunk), then, after a barrier of the converter group, writes them as f16 into
+// the two 64-dim swizzle atoms of the chunk. Tracks the largest |value| that
+// must fit f16 (range check).
+DSV4_DEV void convert_chunk(const AttnArgs& a, const int32_t* src, const float* sc, int tt, int c,
+                            unsigned char* xc, int ctid, float& mx) {
+  const ChunkSplit cs = chunk_split(a, c);
+  uint4 raw[kItems];
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int i = ctid + it * kConvThreads;
+    raw[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < kGroups) {
+      const int j = i >> 4, g = i & 15;
+      const int32_t sr = src[tt * kRows + j];
+      const unsigned char* row = xc + j * 256;
+      if (sr >= 0) {
+        if (8 * g < cs.nn) {
+          const uint2 w = *reinterpret_cast<const uint2*>(row + 8 * g);
+          raw[it].x = w.x;
+          raw[it].y = w.y;
+        } else {
+          raw[it] = *reinterpret_cast<const uint4*>(row + cs.nn + 2 * (8 * g - cs.nn));
+        }
+      } else if (sr <= -2) {
+        raw[it] = *reinterpret_cast<const uint4*>(row + 16 * g);
+      }
+    }
+  }
+  tc::bar_named(kBarConv, kConvThreads);
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
     const int i = ctid + it * kConvThreads;
     if (i < kGroups) {
-      const int j = i >> 4, g = i & 15, d0 = c * 128 + g * 8;
+      const int j = i >> 4, g = i & 15;
+      const int32_t sr = src[tt * kRows + j];
       uint4 h;
-      if (d0 < a.d_nope && src[tt * kRows + j] >= 0) {   // e4m3 codes times the row's scale
-        const float sc = r.s[it];
-        mx = fmaxf(mx, fabsf(sc) * 448.f);
+      if (sr >= 0 && 8 * g < cs.nn) {   // e4m3 codes times the row's scale
+        const float scl = sc[tt * kRows + j];
+        mx = fmaxf(mx, fabsf(scl) * 448.f);
         uint32_t s2;
-        asm("{\n.reg .b16 t;\ncvt.rn.f16.f32 t, %1;\nmov.b32 %0, {t, t};\n}" : "=r"(s2) : "f"(sc * 256.f));
-        h = make_uint4(e4m3x2_to_f16x2_scaled(r.v[it].x, 0x4140u, s2), e4m3x2_to_f16x2_scaled(r.v[it].x, 0x4342u, s2),
-                       e4m3x2_to_f16x2_scaled(r.v[it].y, 0x4140u, s2), e4m3x2_to_f16x2_scaled(r.v[it].y, 0x4342u, s2));
+        asm("{\n.reg .b16 t;\ncvt.rn.f16.f32 t, %1;\nmov.b32 %0, {t, t};\n}" : "=r"(s2) : "f"(scl * 256.f));
+        h = make_uint4(e4m3x2_to_f16x2_scaled(raw[it].x, 0x4140u, s2), e4m3x2_to_f16x2_scaled(raw[it].x, 0x4342u, s2),
+                       e4m3x2_to_f16x2_scaled(raw[it].y, 0x4140u, s2), e4m3x2_to_f16x2_scaled(raw[it].y, 0x4342u, s2));
       } else {
-        h = bf16x8_to_f16x8(r.v[it], mx);
+        h = bf16x8_to_f16x8(raw[it], mx);
       }
       const int atom = g >> 3, gg = g & 7;
       *reinterpret_cast<uint4*>(xc + atom * kAtomBytes + j * 128 + ((gg ^ (j & 7)) << 4)) = h;
@@ -317,7 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   unsigned char* pb = qs + D * 128;                          // [128 rows][64 heads] f16
   unsigned char* xk = pb + kPBytes;                          // nch chunks of [2 atoms][128 rows][128 B]
   unsigned char* xv = SEP ? xk + nch * kChunkBytes : xk;
-  float* stage = reinterpret_cast<float*>(xk);               // epilogue: [64 heads][D] fp32, after the last P.V
+  uint16_t* stage16 = reinterpret_cast<uint16_t*>(xk);      // epilogue: [D][64 heads] f16, after the last P.V
+  const int xbytes = (SEP ? 2 : 1) * nch * kChunkBytes;
+  unsigned char* qstage = xk + xbytes - 128 * D;             // prologue: raw bf16 query [64][D], top of X
   TcTail* t = reinterpret_cast<TcTail*>(xk + (SEP ? 2 : 1) * nch * kChunkBytes);
   pdl_trigger();
   pdl_wait();
@@ -352,23 +386,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
     tc::mbar_init(&t->pfull, kSoftThreads / 32);
     tc::mbar_init(&t->pvdone, 1);
     tc::mbar_init(&t->qready, kSoftThreads / 32);
+    tc::mbar_init(&t->qraw, 1);
     tc::mbar_init(&t->drain, 1);
     t->abort = 0;
     tc::fence_mbar_init();
+    // the query rows of this head group, raw bf16, into the top of the X region
+    const uint32_t qbytes = static_cast<uint32_t>(hcount) * D * 2;
+    tc::mbar_arrive_expect_tx(&t->qraw, qbytes);
+    tc::bulk_load(qstage, a.q + (static_cast<int64_t>(b) * a.H + h0) * D, qbytes, &t->qraw);
   }
   if (threadIdx.x < kHeads) t->m_used[threadIdx.x] = -INFINITY;
   {
     // row sources of the whole split (CSA: one round trip for the top-k indices)
-    int32_t sv[2];
+    int32_t sr[2];
+    float ks[2], vs[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int i = threadIdx.x + k * kThreads;
-      sv[k] = i < nrows ? row_source(a, rs, b, r0 + i, r1, true) : -1;
+      sr[k] = i < nrows ? row_source(a, rs, b, r0 + i, r1, true) : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      ks[k] = sr[k] >= 0 ? __ldg(a.k_scale + sr[k]) : 0.f;
+      vs[k] = SEP && sr[k] >= 0 ? __ldg(a.v_scale + sr[k]) : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int i = threadIdx.x + k * kThreads;
-      if (i < nrows) t->src[i] = sv[k];
+      if (i < nrows) {
+        t->src[i] = sr[k];
+        t->sk[i] = ks[k];
+        if (SEP) t->sv[i] = vs[k];
+      }
     }
   }
   tc::tc_fence_before();
@@ -435,40 +484,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
     }
   } else if (warp < 4 || (warp >= 8 && warp < 12)) {
     // ------------------------------------------------------------ dequantisation into X
-    // Stages q = (tile, chunk, K/V) in order; the loads of stage q + 1 are in
-    // flight while stage q waits for its X chunk and converts.
+    // Per tile: the copies of every chunk are issued as soon as its X region is
+    // free (all of them in flight at once), then the chunks are converted in
+    // place in order. Tile 0's regions that hold the staged query wait for it.
     const int ctid = (warp < 4 ? warp - 1 : warp - 5) * 32 + lane;
-    const int per = SEP ? 2 : 1;
-    const int nstage = nt * nch * per;
+    const int qoff = xbytes - 128 * D;
     float mx = 0.f;
-    ChunkRaw ra, rb;
-    auto issue = [&](int q, ChunkRaw& r) {
-      const int kv = q % per, c = (q / per) % nch, tt = q / (per * nch);
-      if (kv == 0) load_chunk(a, b, src, tt, c, a.k_nope, a.k_scale, a.k_rope, a.win_k, ctid, r);
-      else load_chunk(a, b, src, tt, c, a.v_nope, a.v_scale, a.v_rope, a.win_v, ctid, r);
-    };
-    auto finish = [&](int q, const ChunkRaw& r) -> bool {
-      const int kv = q % per, c = (q / per) % nch, tt = q / (per * nch);
-      if (kv == 0) {
-        const bool ok = tt == 0 || tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
-        if (!tc::bar_and(kBarConv, kConvThreads, ok)) return false;
+    bool ok = true;
+    for (int tt = 0; ok && tt < nt; ++tt) {
+      for (int c = 0; c < nch; ++c) {
+        bool w = true;
+        if (tt > 0) {
+          w = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
+        } else {
+          const int lo = c * kChunkBytes, hi_k = lo + kChunkBytes;
+          const bool clash = hi_k > qoff || (SEP && lo + nch * kChunkBytes + kChunkBytes > qoff);
+          if (clash) w = tc::mbar_wait(&t->qready, 0, abort);
+        }
+        if (!(ok = tc::bar_and(kBarConv, kConvThreads, w))) break;
+        issue_chunk(a, b, src, tt, c, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, ctid);
+        if (SEP) issue_chunk(a, b, src, tt, c, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, ctid);
+        cp_async_commit();
       }
-      store_chunk(a, src, tt, c, r, (kv ? xv : xk) + c * kChunkBytes, ctid, mx);
-      if (kv == per - 1) {
+      for (int c = 0; ok && c < nch; ++c) {
+        cp_async_wait(nch - 1 - c);
+        tc::bar_named(kBarConv, kConvThreads);   // every thread's copies of chunk c have landed
+        convert_chunk(a, src, t->sk, tt, c, xk + c * kChunkBytes, ctid, mx);
+        if (SEP) {
+          tc::bar_named(kBarConv, kConvThreads);
+          convert_chunk(a, src, t->sv, tt, c, xv + c * kChunkBytes, ctid, mx);
+        }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&t->xfull[c]);
       }
-      return true;
-    };
-    issue(0, ra);
-    for (int q = 0; q < nstage; q += 2) {
-      if (q + 1 < nstage) issue(q + 1, rb);
-      if (!finish(q, ra)) break;
-      if (q + 1 >= nstage) break;
-      if (q + 2 < nstage) issue(q + 2, ra);
-      if (!finish(q + 1, rb)) break;
     }
+    cp_async_wait(0);
     if (mx >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
   } else {
     // ------------------------------------------------------------ query, softmax, epilogue
@@ -479,27 +530,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float c2 = a.sm_scale * 1.4426950408889634f;
     {
-      // the query, bf16 -> f16 into the K-major operand (heads beyond H zero)
+      // the query (staged raw by the bulk copy), bf16 -> f16 into the K-major
+      // operand; heads beyond H zero
+      const bool got = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->qraw, 0, abort));
       const int gpr = D / 8;   // 8-dim groups per head
       float qmax = 0.f;
-      for (int i0 = 0; i0 < kHeads * gpr; i0 += 8 * kSoftThreads) {
-        uint4 qw[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + st + u * kSoftThreads, h = i / gpr;
-          qw[u] = make_uint4(0u, 0u, 0u, 0u);
-          if (i < kHeads * gpr && h < hcount)
-            qw[u] = ldg16(a.q + (static_cast<int64_t>(b) * a.H + h0 + h) * D + (i % gpr) * 8);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + st + u * kSoftThreads, h = i / gpr;
-          if (i < kHeads * gpr) {
-            const int d0 = (i % gpr) * 8, atom = d0 >> 6, gg = (d0 >> 3) & 7;
-            *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) =
-                bf16x8_to_f16x8(qw[u], qmax);
-          }
-        }
+      for (int i = st; got && i < kHeads * gpr; i += kSoftThreads) {
+        const int h = i / gpr, d0 = (i % gpr) * 8;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (h < hcount) w = *reinterpret_cast<const uint4*>(qstage + (h * D + d0) * 2);
+        const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
+        *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) = bf16x8_to_f16x8(w, qmax);
       }
       if (qmax >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
       tc::fence_proxy_async_smem();
@@ -579,26 +620,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
         t->alpha[st] = l > 0.f ? 1.f / l : 0.f;
       }
       tc::bar_named(kBarSoft, kSoftThreads);
-      // normalised O^T -> stage[h][d] (fp32, d contiguous), then one bulk copy per head
+      // normalised O^T as f16 -> stage [D][64 heads] (this split's partial in
+      // the layout of the workspace), then one bulk copy
       for (int c = 0; c < nch; ++c) {
         uint32_t v[32];
         tc::tmem_ld32(o_tmem + lane_off + c * kHeads + hb, v);
         tc::tmem_wait_ld();
-        const int d = c * 128 + j;
+        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) stage[(hb + i) * D + d] = __uint_as_float(v[i]) * t->alpha[hb + i];
+        for (int i = 0; i < 16; ++i)
+          w[i] = f32x2_to_f16x2(__uint_as_float(v[2 * i]) * t->alpha[hb + 2 * i],
+                                __uint_as_float(v[2 * i + 1]) * t->alpha[hb + 2 * i + 1]);
+        uint4* dst = reinterpret_cast<uint4*>(stage16 + (c * 128 + j) * kHeads + hb);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       }
       tc::fence_proxy_async_smem();
       tc::bar_named(kBarSoft, kSoftThreads);
       const int64_t row0 = static_cast<int64_t>(b) * a.H + h0;
-      if (st < hcount) {
-        tc::bulk_store(a.part_o + ((row0 + st) * a.splits + split) * a.Dv, stage + st * D, D * 4);
+      if (st == 0) {
+        const int hgs = gridDim.z;
+        uint16_t* part = reinterpret_cast<uint16_t*>(a.part_o) +
+                         ((static_cast<int64_t>(b) * a.splits + split) * hgs + blockIdx.z) * D * kHeads;
+        tc::bulk_store(part, stage16, D * kHeads * 2);
         tc::bulk_commit();
+      }
+      if (st < hcount) {
         const float l = t->lsum[st];
         a.part_lse[(row0 + st) * a.splits + split] =
             l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-        tc::bulk_wait();   // shared memory must outlive the copy, and its writes precede the merge
       }
+      if (st == 0) tc::bulk_wait();   // shared memory must outlive the copy, and its writes precede the merge
     }
   }
 
@@ -640,7 +692,7 @@ bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v) {
 int launch_attention_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
   const int e = a.separate_v ? launch_tc<true>(a, head_groups, st) : launch_tc<false>(a, head_groups, st);
   if (e) return e;
-  return launch_attention_merge(a, st);
+  return launch_attention_merge_tc(a, head_groups, st);
 }
 
 }  // namespace dsv4

@@ -57,6 +57,7 @@ constexpr int kSelThreads = 512;
 constexpr int kMaxK = 2048;
 constexpr int kScanItems = 8;        // scores each thread loads per round trip
 constexpr int kCandCache = 4096;     // candidates the resolving CTA keeps in shared memory
+constexpr int kTopkDynSmem = kCandCache * 8 + 8192 * 4;   // candidate cache + bitmap of 2^18 blocks
 
 // Append `flag`-ed values of a warp to list[*counter ...] with one atomic per
 // warp; positions at or beyond `cap` are dropped.
@@ -130,24 +131,76 @@ DSV4_DEV void block_sort_asc(int32_t* v, int P) {
 
 }  // namespace
 
+namespace {
+
+// Block-wide exclusive prefix sum of two 16-bit counts packed in one word
+// (low: gt, high: eq); returns the exclusive prefix and writes the block total
+// to *total. `scratch` holds kSelThreads / 32 words. Every thread calls it.
+DSV4_DEV uint32_t block_excl_scan_packed(uint32_t v, uint32_t* total, uint32_t* scratch) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[w] = inc;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+  for (int ww = 0; ww < kSelThreads / 32; ++ww) {
+    const uint32_t t = scratch[ww];
+    if (ww < w) before += t;
+    all += t;
+  }
+  *total = all;
+  return before + inc - v;
+}
+
+// Load n words of a global array (written by other CTAs of this kernel or by
+// earlier kernels) into shared memory, kScanItems loads in flight per thread.
+template <typename T>
+DSV4_DEV void load_to_smem(T* dst, const T* src, uint32_t n) {
+  for (uint32_t i0 = 0; i0 < n; i0 += kScanItems * blockDim.x) {
+    T v[kScanItems];
+#pragma unroll
+    for (int u = 0; u < kScanItems; ++u) {
+      const uint32_t i = i0 + threadIdx.x + u * blockDim.x;
+      v[u] = i < n ? __ldcg(src + i) : T(0);
+    }
+#pragma unroll
+    for (int u = 0; u < kScanItems; ++u) {
+      const uint32_t i = i0 + threadIdx.x + u * blockDim.x;
+      if (i < n) dst[i] = v[u];
+    }
+  }
+}
+
+constexpr int kBitmapWords = 8192;   // the fast path's bitmap of selected blocks: n_c <= 2^18
+
+}  // namespace
+
 // Top-k selection, grid (sel_ctas, B), block 512. The scoring kernel has
 // histogrammed the top 12 bits of every score key and its last CTA stored the
 // threshold bin T1 (the bin holding the k-th largest key) and the number of keys
 // above it. Each CTA scans its slice of the scores, appends every block above
-// T1 to `above` and every block in T1 to `cand` (key, index) while
-// histogramming the next 12 key bits (hist2). The last CTA of the sequence to
-// finish (a completion counter, no waiting) resolves the boundary: candidates
-// above the second-level threshold bin are taken, the remaining ties are
-// settled by the low 8 key bits and then the lower index, and the k indices are
-// sorted ascending.
+// T1 to `above` and every block in T1 to `cand` (key, index) with one reservation
+// per CTA, while histogramming the next 12 key bits (hist2). The last CTA of the
+// sequence to finish (a completion counter, no waiting) resolves the boundary:
+// candidates above the second-level threshold bin T2 are taken; ties in T2 are
+// settled by the low 8 key bits, then by the lower index; the k blocks are
+// emitted in ascending index order.
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   __shared__ uint32_t h[kBins];
   __shared__ int32_t fin[kMaxK];
   __shared__ uint32_t scratch[kSelThreads / 32 + 2];
-  __shared__ uint32_t s_nfin, s_last, s_d, s_rem;
+  __shared__ uint32_t s_nfin, s_last, s_d, s_rem, s_base[2];
+  extern __shared__ uint64_t dyn[];   // candidate cache, then (fast path) the bitmap behind it
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
+  uint32_t* cnt = a.cnt + b * kCntWords;
+  const uint32_t T1 = cnt[4];
   int64_t n_c = a.n_tokens[b] / a.ratio;
   if (n_c > a.capacity) n_c = a.capacity;
   int32_t* out = a.topk + static_cast<int64_t>(b) * a.k;
@@ -158,11 +211,9 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
     return;
   }
   const float* sc = a.scores + static_cast<int64_t>(b) * a.capacity;
-  uint32_t* cnt = a.cnt + b * kCntWords;
   int32_t* above = a.above + static_cast<int64_t>(b) * k;
   uint64_t* cand = a.cand + static_cast<int64_t>(b) * a.capacity;
   uint32_t* hist2 = a.hist2 + static_cast<int64_t>(b) * kBins;
-  const uint32_t T1 = cnt[4];   // issued with the n_tokens load above
 
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
   __syncthreads();
@@ -170,27 +221,46 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
   const int64_t c1 = c0 + chunk < n_c ? c0 + chunk : n_c;
   for (int64_t base = c0; base < c1; base += kScanItems * blockDim.x) {
-    float v[kScanItems];
+    uint32_t key[kScanItems];
 #pragma unroll
     for (int u = 0; u < kScanItems; ++u) {
       const int64_t s = base + threadIdx.x + u * blockDim.x;
-      v[u] = s < c1 ? __ldg(sc + s) : 0.f;
+      key[u] = s < c1 ? score_key(__ldg(sc + s)) : 0u;
     }
+    uint32_t mine = 0;   // packed counts: above T1 (low 16 bits), in T1 (high 16 bits)
 #pragma unroll
     for (int u = 0; u < kScanItems; ++u) {
       const int64_t s = base + threadIdx.x + u * blockDim.x;
       const bool in = s < c1;
-      const uint32_t key = in ? score_key(v[u]) : 0u;
-      const uint32_t bin = key >> 20;
-      const bool gt = in && bin > T1;
-      const bool eq = in && bin == T1;
-      warp_append_i32(gt, static_cast<int32_t>(s), &cnt[0], above, static_cast<uint32_t>(k));
-      warp_append_u64(eq, (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(s), &cnt[1], cand,
-                      static_cast<uint32_t>(a.capacity));
-      if (eq) atomicAdd(&h[(key >> 8) & 0xFFF], 1u);
+      const uint32_t bin = key[u] >> 20;
+      mine += (in && bin > T1) ? 1u : 0u;
+      mine += (in && bin == T1) ? (1u << 16) : 0u;
+      warp_hist_add(h, (key[u] >> 8) & 0xFFF, in && bin == T1);
     }
+    uint32_t tot;
+    uint32_t pre = block_excl_scan_packed(mine, &tot, scratch);
+    if (threadIdx.x == 0) {
+      s_base[0] = (tot & 0xFFFFu) ? atomicAdd(&cnt[0], tot & 0xFFFFu) : 0u;
+      s_base[1] = (tot >> 16) ? atomicAdd(&cnt[1], tot >> 16) : 0u;
+    }
+    __syncthreads();
+    uint32_t pg = s_base[0] + (pre & 0xFFFFu), pe = s_base[1] + (pre >> 16);
+#pragma unroll
+    for (int u = 0; u < kScanItems; ++u) {
+      const int64_t s = base + threadIdx.x + u * blockDim.x;
+      const bool in = s < c1;
+      const uint32_t bin = key[u] >> 20;
+      if (in && bin > T1) {
+        if (pg < static_cast<uint32_t>(k)) above[pg] = static_cast<int32_t>(s);
+        ++pg;
+      } else if (in && bin == T1) {
+        if (pe < static_cast<uint32_t>(a.capacity))
+          cand[pe] = (static_cast<uint64_t>(key[u]) << 32) | static_cast<uint32_t>(s);
+        ++pe;
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
   for (int i = threadIdx.x; i < kBins; i += blockDim.x)
     if (h[i]) atomicAdd(&hist2[i], h[i]);
   __threadfence();
@@ -201,42 +271,139 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   __threadfence();
 
   // ---- the last CTA of sequence b resolves the boundary
-  uint32_t n_above = *reinterpret_cast<volatile uint32_t*>(&cnt[0]);
-  uint32_t n_cand = *reinterpret_cast<volatile uint32_t*>(&cnt[1]);
+  uint32_t n_above = __ldcg(&cnt[0]);
+  uint32_t n_cand = __ldcg(&cnt[1]);
   if (n_above > static_cast<uint32_t>(k)) n_above = k;                      // only on inconsistent input
   if (n_cand > static_cast<uint32_t>(a.capacity)) n_cand = a.capacity;
   const uint32_t need1 = static_cast<uint32_t>(k) - n_above;                 // taken from cand
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = reinterpret_cast<volatile uint32_t*>(hist2)[i];
-  for (uint32_t i = threadIdx.x; i < n_above; i += blockDim.x) fin[i] = reinterpret_cast<volatile int32_t*>(above)[i];
+  load_to_smem(h, hist2, kBins);
+  load_to_smem(fin, above, n_above);
   if (threadIdx.x == 0) s_nfin = n_above;
-  // the candidates, read once: into shared memory when they fit
-  extern __shared__ uint64_t cache[];
-  const volatile uint64_t* cl = reinterpret_cast<volatile uint64_t*>(cand);
-  if (n_cand <= static_cast<uint32_t>(kCandCache)) {
-    for (uint32_t i0 = 0; i0 < n_cand; i0 += kScanItems * blockDim.x) {
-      uint64_t v[kScanItems];
-#pragma unroll
-      for (int u = 0; u < kScanItems; ++u) {
-        const uint32_t i = i0 + threadIdx.x + u * blockDim.x;
-        v[u] = i < n_cand ? cl[i] : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < kScanItems; ++u) {
-        const uint32_t i = i0 + threadIdx.x + u * blockDim.x;
-        if (i < n_cand) cache[i] = v[u];
-      }
-    }
-    cl = cache;
-  }
+  uint64_t* cache = dyn;
+  const bool cached = n_cand <= static_cast<uint32_t>(kCandCache);
+  const bool fast = cached && n_c <= 32 * kBitmapWords;
+  if (cached) load_to_smem(cache, static_cast<const uint64_t*>(cand), n_cand);
+  const uint64_t* cl = cached ? cache : cand;
+  uint32_t* bm = reinterpret_cast<uint32_t*>(dyn + kCandCache);
+  if (fast)
+    for (int i = threadIdx.x; i < kBitmapWords; i += blockDim.x) bm[i] = 0;
   __syncthreads();
   uint32_t n_gt2 = 0;
   const uint32_t T2 = need1 ? static_cast<uint32_t>(block_suffix_select<kSelThreads>(h, need1, &n_gt2, scratch)) : 0xFFFFu;
   const uint32_t need2 = need1 - n_gt2;                                      // taken among the keys of bin (T1, T2)
-  // Candidates strictly above T2 are in; ties at (T1, T2) are ranked by the low
-  // 8 key bits, then the lower index: radix select of the need2-th largest
-  // 40-bit rank (low8 << 32 | ~index) among them.
-  uint64_t thr_rank = 0;
   const uint32_t n_eq2 = T2 < static_cast<uint32_t>(kBins) ? h[T2] : 0u;
+
+  if (fast) {
+    // selected blocks as bits: those above T1, candidates above T2, and the
+    // need2 best of T2 by (low 8 key bits desc, index asc)
+    for (uint32_t i = threadIdx.x; i < n_above; i += blockDim.x) {
+      const uint32_t x = static_cast<uint32_t>(fin[i]);
+      atomicOr(&bm[x >> 5], 1u << (x & 31));
+    }
+    uint32_t d8 = 0, r8 = need2;   // take low8 > d8 fully, and the r8 lowest indices with low8 == d8
+    __syncthreads();
+    if (need2 > 0 && need2 < n_eq2) {
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+      __syncthreads();
+      for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
+        const uint32_t i = i0 + threadIdx.x;
+        const uint64_t v = i < n_cand ? cl[i] : 0ull;
+        const uint32_t key = static_cast<uint32_t>(v >> 32);
+        warp_hist_add(h, key & 0xFF, i < n_cand && ((key >> 8) & 0xFFF) == T2);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) { s_d = 0; s_rem = 0; }
+      __syncthreads();
+      if (threadIdx.x < 32) warp_digit_select(h, need2, &s_d, &s_rem);
+      __syncthreads();
+      d8 = s_d;
+      r8 = need2 - s_rem;
+      // the r8-th smallest index with low8 == d8: two passes over 9-bit digits (n_c <= 2^18)
+      uint32_t prefix = 0;
+      for (int pass = 0; pass < 2; ++pass) {
+        const int shift = 9 - 9 * pass;
+        __syncthreads();
+        for (int i = threadIdx.x; i < 512; i += blockDim.x) h[i] = 0;
+        __syncthreads();
+        for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
+          const uint32_t i = i0 + threadIdx.x;
+          const uint64_t v = i < n_cand ? cl[i] : 0ull;
+          const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
+          const bool in = i < n_cand && ((key >> 8) & 0xFFF) == T2 && (key & 0xFF) == d8 &&
+                          (pass == 0 || (idx >> 9) == prefix);
+          warp_hist_add(h, (idx >> shift) & 0x1FF, in);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {   // smallest digit with prefix count >= r8
+          const int lane = threadIdx.x;
+          uint32_t mine = 0;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) mine += h[lane * 16 + q];
+          uint32_t inc = mine;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          const uint32_t excl = inc - mine;
+          if (excl < r8 && inc >= r8) {
+            uint32_t acc = excl;
+            for (int q = 0; q < 16; ++q) {
+              const uint32_t c = h[lane * 16 + q];
+              if (acc + c >= r8) {
+                s_d = static_cast<uint32_t>(lane * 16 + q);
+                s_rem = acc;
+                break;
+              }
+              acc += c;
+            }
+          }
+        }
+        __syncthreads();
+        prefix = (prefix << 9) | s_d;
+        r8 -= s_rem;
+      }
+      const uint32_t thr = prefix;   // indices <= thr with low8 == d8 are taken (exactly r8 of them before)
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
+        const uint64_t v = cl[i];
+        const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
+        const uint32_t b2 = (key >> 8) & 0xFFF;
+        const bool take = b2 > T2 || (b2 == T2 && ((key & 0xFF) > d8 || ((key & 0xFF) == d8 && idx <= thr)));
+        if (take) atomicOr(&bm[idx >> 5], 1u << (idx & 31));
+      }
+    } else {
+      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
+        const uint64_t v = cl[i];
+        const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
+        const uint32_t b2 = (key >> 8) & 0xFFF;
+        if (b2 > T2 || (b2 == T2 && need2 > 0)) atomicOr(&bm[idx >> 5], 1u << (idx & 31));
+      }
+    }
+    __syncthreads();
+    // emit the set bits in ascending order: thread t owns words [16t, 16t + 16)
+    constexpr int per = kBitmapWords / kSelThreads;
+    uint32_t cntw = 0;
+#pragma unroll
+    for (int q = 0; q < per; ++q) cntw += __popc(bm[threadIdx.x * per + q]);
+    uint32_t tot;
+    uint32_t pos = block_excl_scan_packed(cntw, &tot, scratch);
+    for (int q = 0; q < per; ++q) {
+      uint32_t wd = bm[threadIdx.x * per + q];
+      while (wd) {
+        const int bit = __ffs(wd) - 1;
+        wd &= wd - 1;
+        if (pos < static_cast<uint32_t>(k)) out[pos] = (threadIdx.x * per + q) * 32 + bit;
+        ++pos;
+      }
+    }
+    for (uint32_t i = tot + threadIdx.x; i < static_cast<uint32_t>(k); i += blockDim.x) out[i] = -1;   // inconsistent input only
+    return;
+  }
+
+  // ---- general path: radix select of the need2-th largest 40-bit rank
+  // (low8 << 32 | ~index) in bin (T1, T2), then a bitonic sort
+  uint64_t thr_rank = 0;
   if (need2 > 0 && need2 < n_eq2) {
     uint64_t prefix = 0, mask = 0;
     uint32_t remaining = need2;
@@ -245,12 +412,13 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
       __syncthreads();
       for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
       __syncthreads();
-      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
-        const uint64_t v = cl[i];
+      for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
+        const uint32_t i = i0 + threadIdx.x;
+        const uint64_t v = i < n_cand ? cl[i] : 0ull;
         const uint32_t key = static_cast<uint32_t>(v >> 32);
-        if (((key >> 8) & 0xFFF) != T2) continue;
         const uint64_t rank = (static_cast<uint64_t>(key & 0xFF) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(v));
-        if ((rank & mask) == prefix) atomicAdd(&h[(rank >> shift) & 0xFF], 1u);
+        const bool in = i < n_cand && ((key >> 8) & 0xFFF) == T2 && (rank & mask) == prefix;
+        warp_hist_add(h, static_cast<uint32_t>((rank >> shift) & 0xFF), in);
       }
       __syncthreads();
       if (threadIdx.x == 0) {
@@ -268,19 +436,17 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
     thr_rank = prefix;                                                       // exactly need2 ranks are >= prefix
   }
   __syncthreads();
-  for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
-    const uint64_t v = cl[i];
+  for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
+    const uint32_t i = i0 + threadIdx.x;
+    const uint64_t v = i < n_cand ? cl[i] : 0ull;
     const uint32_t key = static_cast<uint32_t>(v >> 32);
     const uint32_t b2 = (key >> 8) & 0xFFF;
-    bool take = need1 > 0 && b2 > T2;
-    if (b2 == T2) {
+    bool take = i < n_cand && need1 > 0 && b2 > T2;
+    if (i < n_cand && b2 == T2) {
       const uint64_t rank = (static_cast<uint64_t>(key & 0xFF) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(v));
       take = need2 > 0 && (need2 >= n_eq2 || rank >= thr_rank);
     }
-    if (take) {
-      const uint32_t pos = atomicAdd(&s_nfin, 1u);
-      if (pos < static_cast<uint32_t>(k)) fin[pos] = static_cast<int32_t>(static_cast<uint32_t>(v));
-    }
+    warp_append_i32(take, static_cast<int32_t>(static_cast<uint32_t>(v)), &s_nfin, fin, static_cast<uint32_t>(k));
   }
   __syncthreads();
   int P = 1;
@@ -294,10 +460,9 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
 int launch_topk_select(const IndexArgs& a, int sel_ctas, cudaStream_t st) {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kCandCache * static_cast<int>(sizeof(uint64_t)));
+    cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkDynSmem);
   });
-  return launch_pdl(topk_select_kernel, dim3(sel_ctas, a.B), dim3(kSelThreads), kCandCache * sizeof(uint64_t), st, a);
+  return launch_pdl(topk_select_kernel, dim3(sel_ctas, a.B), dim3(kSelThreads), kTopkDynSmem, st, a);
 }
 
 }  // namespace dsv4

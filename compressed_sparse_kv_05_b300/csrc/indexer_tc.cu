@@ -266,10 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t->acc_empty[ab]);
       const int64_t s = static_cast<int64_t>(t0 + i) * kTile + row;
-      if (s < n_c) {
-        out[s] = score;
-        atomicAdd(&t->hist[score_key(score) >> 20], 1u);
-      }
+      if (s < n_c) out[s] = score;
+      warp_hist_add(t->hist, score_key(score) >> 20, s < n_c);
     }
     epilogue_sync();
     uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * 4096;
@@ -296,8 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (!t->last || n_c <= a.k) return;
   __threadfence();
-  const volatile uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x) t->hist[i] = gh[i];
+  {
+    // every CTA's histogram atomics are done (counter above); L2 reads, all in flight
+    const uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
+    constexpr int per = kBins / kThreads;
+    uint32_t v[per];
+#pragma unroll
+    for (int u = 0; u < per; ++u) v[u] = __ldcg(gh + threadIdx.x + u * kThreads);
+#pragma unroll
+    for (int u = 0; u < per; ++u) t->hist[threadIdx.x + u * kThreads] = v[u];
+  }
   __syncthreads();
   uint32_t n_gt1;
   const int T1 = block_suffix_select<kThreads>(t->hist, static_cast<uint32_t>(a.k), &n_gt1, t->scratch);

@@ -85,7 +85,7 @@ struct AttnArgs {
   const uint16_t *k_rope, *v_rope, *win_k, *win_v;
   const int64_t* n_tokens;
   int32_t* status;
-  float* part_o;           // [B][H][splits][Dv]
+  float* part_o;           // [B][H][splits][Dv] fp32 (CUDA-core kernel); f16 [B][splits][hg][D][64] (tensor-core)
   float* part_lse;         // [B][H][splits]
   float* out;              // [B][H][Dv]
   float* lse;              // [B][H] or null
@@ -96,5 +96,7 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st);
 bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v);
 int launch_attention_tc(const AttnArgs& a, int head_groups, cudaStream_t st);
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st);
+// merge of the tensor-core kernel's f16 partials ([B][splits][head groups][D][64])
+int launch_attention_merge_tc(const AttnArgs& a, int head_groups, cudaStream_t st);
 
 }  // namespace dsv4

@@ -58,6 +58,17 @@ DSV4_DEV int block_suffix_select(const uint32_t* h, uint32_t need, uint32_t* abo
   return bin;
 }
 
+// Add 1 to h[bin] for every lane with `active`, one atomic per distinct bin of
+// the warp (lanes with equal bins are grouped), so that many equal keys do not
+// serialise on one shared-memory word. All 32 lanes must call it.
+DSV4_DEV void warp_hist_add(uint32_t* h, uint32_t bin, bool active) {
+  const unsigned act = __ballot_sync(0xffffffffu, active);
+  if (!act) return;
+  const unsigned peers = __match_any_sync(0xffffffffu, active ? bin : 0xFFFFFFFFu) & act;
+  const int lane = threadIdx.x & 31;
+  if (active && (__ffs(peers) - 1) == lane) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
+}
+
 // Warp 0 of the block: the largest digit d of a 256-bin histogram h with
 // sum_{j >= d} h[j] >= need, and sum_{j > d} h[j]. Other warps get nothing.
 DSV4_DEV void warp_digit_select(const uint32_t* h, uint32_t need, uint32_t* digit, uint32_t* above) {

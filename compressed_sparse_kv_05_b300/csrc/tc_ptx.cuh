@@ -282,6 +282,15 @@ DSV4_DEV bool bar_and(int id, int count, bool v) {
   return r != 0;
 }
 
+// Bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completing as transaction bytes on `bar`.
+DSV4_DEV void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(sdst)),
+               "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16),
 // tracked by this thread's bulk-async groups.
 DSV4_DEV void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {

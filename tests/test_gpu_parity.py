@@ -218,6 +218,29 @@ def test_index_topk_short_and_edge(n_c, k):
         check_topk(g_topk[b], o_scores, O.topk_blocks(o_scores, k), k)
 
 
+@pytest.mark.parametrize("layer", [W.scaled(W.CSA_B32_128K, batch=2), W.scaled(W.STACK_CSA, batch=1)],
+                         ids=["csa_b32_128k_shape", "stack_1m_shape"])
+def test_index_topk_full_size_planted(layer):
+    """Full-size selections with 1% planted keys: 32768 blocks (the planted keys
+    are all selected and the boundary falls among random keys) and 2^18 blocks
+    (2622 identical planted keys compete for 512 slots: the lowest indices win)."""
+    planes = oracle_direct_planes(layer, "idxfull", 0, range(layer.batch))
+    desc, cache = gpu_cache_from_planes(layer, planes)
+    dec = synth.decode_inputs("idxfull", 0, layer)
+    g_topk, g_scores = _index(desc, cache, layer, dec, layer.topk)
+    for b in range(layer.batch):
+        o_scores = O.index_scores(planes[b]["idx_codes"], planes[b]["idx_scales"], dec["q_idx"][b], dec["w"][b])
+        rel = np.abs(g_scores[b, :layer.n_comp] - o_scores) / np.abs(o_scores).max()
+        assert rel.max() <= 1e-5
+        o_sel = O.topk_blocks(o_scores, layer.topk)
+        check_topk(g_topk[b], o_scores, o_sel, layer.topk)
+        planted = set(planes[b]["planted"].tolist())
+        if len(planted) >= layer.topk:
+            assert set(g_topk[b].tolist()) == set(sorted(planted)[:layer.topk])
+        else:
+            assert planted <= set(g_topk[b].tolist())
+
+
 def test_topk_ties_go_to_lower_index():
     """All keys identical: every score ties, so the selection is the lowest k indices."""
     layer = W.scaled(W.CSA_B32_128K, batch=1, n_tokens=4 * 5000, topk=512)
