@@ -14,7 +14,8 @@ namespace {
 
 constexpr int kSms = 148;                // streaming multiprocessors of a B300
 constexpr int kSplitTarget = 2 * kSms;  // CTAs the CUDA-core split-K attention aims for
-constexpr int kTcTile = 128;            // rows per tile of the tensor-core attention
+constexpr int kTcTile = 128;            // rows per tile of the tensor-core attention, at most
+constexpr int kTcMinTile = 32;          // and at least
 constexpr int kTcMaxTiles = 8;          // tiles per CTA of the tensor-core attention, at most
 constexpr int kRowTile = 16;
 constexpr int kHeadGroup = 64;
@@ -62,7 +63,7 @@ int check_cache_read(const dsv4_layer_desc* d, const dsv4_cache* c) {
 }
 
 struct AttnPlan {
-  int head_groups, splits, rows_per_split;
+  int head_groups, splits, rows_per_split, tile_rows, tiles_per_split;
   bool tc;
   size_t part_bytes;   // bytes of the split partials (the log-sum-exps follow)
   size_t ws_bytes;
@@ -71,18 +72,27 @@ struct AttnPlan {
 AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
   AttnPlan p{};
   p.head_groups = (H + kHeadGroup - 1) / kHeadGroup;
-  const int64_t rmax = static_cast<int64_t>(n_sel > 0 ? n_sel : d->capacity) + d->window;
+  const int64_t n_main = n_sel > 0 ? n_sel : d->capacity;
+  const int64_t rmax = n_main + d->window;
   const size_t Dv = static_cast<size_t>(d->d_nope + d->d_rope);
   p.tc = attention_tc_supported(H, d->d_nope, d->d_rope, d->separate_v);
   if (p.tc) {
-    // tiles of 128 rows spread evenly over one wave of CTAs (one per SM)
-    const int64_t tiles = (rmax + kTcTile - 1) / kTcTile;
-    const int64_t total = tiles * d->batch * p.head_groups;
-    int64_t per_cta = (total + kSms - 1) / kSms;
+    // Tiles of R rows (compressed rows, then window tokens, never mixed): the
+    // largest R in {128, 64, 32} whose halving would still fit one wave of
+    // CTAs is halved, so short row sets spread over more SMs; then runs of
+    // consecutive tiles are spread evenly over one wave (one CTA per SM).
+    const int64_t units = static_cast<int64_t>(d->batch) * p.head_groups;
+    auto tiles_for = [&](int64_t r) { return (n_main + r - 1) / r + (d->window + r - 1) / r; };
+    int64_t tr = kTcTile;
+    while (tr > kTcMinTile && units * tiles_for(tr / 2) <= kSms) tr /= 2;
+    const int64_t tiles = tiles_for(tr);
+    int64_t per_cta = (tiles * units + kSms - 1) / kSms;
     if (per_cta > kTcMaxTiles) per_cta = kTcMaxTiles;   // a CTA keeps its rows' sources in shared memory
-    const int64_t rps = per_cta * kTcTile;
-    p.rows_per_split = static_cast<int>(rps);
-    p.splits = static_cast<int>((rmax + rps - 1) / rps);
+    if (per_cta < 1) per_cta = 1;
+    p.tile_rows = static_cast<int>(tr);
+    p.tiles_per_split = static_cast<int>(per_cta);
+    p.rows_per_split = static_cast<int>(per_cta * tr);
+    p.splits = static_cast<int>((tiles + per_cta - 1) / per_cta);
     if (p.splits < 1) p.splits = 1;
     // f16 partials [B][splits][head groups][D][64], then fp32 log-sum-exps [B][H][splits]
     p.part_bytes = (static_cast<size_t>(d->batch) * p.splits * p.head_groups * Dv * 64 * 2 + 255) & ~size_t(255);
@@ -155,6 +165,7 @@ int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const ui
   a.B = d->batch; a.H = H; a.D = d->d_nope + d->d_rope; a.Dv = a.D; a.d_nope = d->d_nope; a.d_rope = d->d_rope;
   a.ratio = d->ratio; a.window = d->window; a.capacity = d->capacity; a.separate_v = d->separate_v ? 1 : 0;
   a.n_sel = k; a.splits = p.splits; a.rows_per_split = p.rows_per_split; a.sm_scale = sm_scale;
+  a.tile_rows = p.tile_rows; a.tiles_per_split = p.tiles_per_split;
   a.q = q; a.topk = topk;
   a.k_nope = c->k.nope; a.k_scale = c->k.scale; a.k_rope = c->k.rope; a.win_k = c->win_k;
   a.v_nope = c->v.nope; a.v_scale = c->v.scale; a.v_rope = c->v.rope; a.win_v = c->win_v;

@@ -224,94 +224,123 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
 }
 
 // Merge of the tensor-core kernel's splits: partials are f16 [B][splits][head
-// groups][D][64 heads] (normalised), log-sum-exps fp32 [B][H][splits].
-// grid (B * head groups, D / 16), block 128: 16 dims x 64 heads per CTA; thread
-// t handles dim d0 + t / 8 and heads 8 (t % 8) .. + 7. The split weights
-// exp(lse_s - max) are computed once per CTA, 64 splits at a time.
-__global__ void __launch_bounds__(128) attn_merge_tc_kernel(AttnArgs a) {
-  constexpr int kS = 64;   // splits per pass over the weights
-  constexpr int kU = 8;    // partial loads in flight per thread
+// groups][D][64 heads] (normalised; in each 128-byte row of a dim d the
+// 16-byte granule of heads 8q .. 8q + 7 sits at granule q ^ (d & 7)),
+// log-sum-exps fp32 [B][H][splits].
+// grid (B * head groups, D / 8), block 512: 8 dims x 64 heads per CTA; thread
+// t takes split group t / 64 (splits s = t / 64 mod 8), dim t / 8 % 8 and
+// heads 8 (t % 8) .. + 7. Per pass of up to 64 splits every thread issues its
+// partial loads while the CTA stages the log-sum-exps in shared memory (one
+// round trip); the split weights exp(lse - max) / sum are then computed once
+// per CTA in place, each thread accumulates its splits, and the eight split
+// groups are summed in shared memory. With more than 64 splits the passes
+// rescale the running result (online softmax over passes).
+__global__ void __launch_bounds__(512, 2) attn_merge_tc_kernel(AttnArgs a) {
+  constexpr int kS = 64;   // splits per pass
+  constexpr int kSg = 8;   // split groups
+  constexpr int kU = kS / kSg;
   pdl_trigger();
   pdl_wait();
   const int hgs = (a.H + 63) / 64;
   const int b = blockIdx.x / hgs, hg = blockIdx.x % hgs;
   const int h0 = hg * 64;
   const int hcount = a.H - h0 < 64 ? a.H - h0 : 64;
-  __shared__ float s_mx[64], s_inv[64];
-  __shared__ float s_w[kS][64];
-  __shared__ float s_out[64][17];
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  __shared__ float s_w[64][kS + 1];          // log-sum-exps, then weights
+  __shared__ float s_m[64], s_l[64], s_r[64];   // running max and sum per head, rescale of this pass
+  __shared__ float s_acc[kSg][64][9];
+  const int t = threadIdx.x;
+  const int sg = t >> 6, dl = (t >> 3) & 7, hq = (t & 7) * 8;
+  const int d = blockIdx.y * 8 + dl;
   const float* lse0 = a.part_lse + (static_cast<int64_t>(b) * a.H + h0) * a.splits;
-  {
-    // head t / 2: max and sum of exp over its splits, each of the two threads
-    // taking every other split (all loads of a pass in flight together)
-    const int h = t >> 1, par = t & 1;
-    float mx = -INFINITY, tot = 0.f;
-    if (h < hcount) {
-      const float* lse = lse0 + static_cast<int64_t>(h) * a.splits;
-#pragma unroll 8
-      for (int s = par; s < a.splits; s += 2) mx = fmaxf(mx, lse[s]);
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    if (h < hcount && mx != -INFINITY) {
-      const float* lse = lse0 + static_cast<int64_t>(h) * a.splits;
-#pragma unroll 8
-      for (int s = par; s < a.splits; s += 2) tot += __expf(lse[s] - mx);
-    }
-    tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-    if (par == 0) {
-      s_mx[h] = mx;
-      s_inv[h] = tot > 0.f ? 1.f / tot : 0.f;
-      if (blockIdx.y == 0 && a.lse && h < hcount)
-        a.lse[static_cast<int64_t>(b) * a.H + h0 + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
-    }
+  // granule hq / 8 of dim d sits at granule (hq / 8) ^ (d & 7) of the row
+  const int dd0 = d < a.D ? d : 0;
+  const uint16_t* part = reinterpret_cast<const uint16_t*>(a.part_o) +
+                         ((static_cast<int64_t>(b) * a.splits * hgs + hg) * a.D + dd0) * 64 + (((hq >> 3) ^ (dd0 & 7)) << 3);
+  const int64_t sstride = static_cast<int64_t>(hgs) * a.D * 64;   // between splits
+  if (t < 64) {
+    s_m[t] = -INFINITY;
+    s_l[t] = 0.f;
   }
-  const int dl = t >> 3, hq = (t & 7) * 8;
-  const int d = blockIdx.y * 16 + dl;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  const uint16_t* part = reinterpret_cast<const uint16_t*>(a.part_o) +
-                         ((static_cast<int64_t>(b) * a.splits * hgs + hg) * a.D + (d < a.D ? d : 0)) * 64 + hq;
-  const int64_t sstride = static_cast<int64_t>(hgs) * a.D * 64;   // between splits
   for (int s0 = 0; s0 < a.splits; s0 += kS) {
     const int ns = a.splits - s0 < kS ? a.splits - s0 : kS;
-    __syncthreads();
-    for (int i = t; i < ns * 64; i += blockDim.x) {
-      const int s = i >> 6, h = i & 63;
-      // normalised weight of split s for head h; a split without rows (lse
-      // -inf) gets 0 and may have left its partial unwritten
-      s_w[s][h] = h < hcount && s_mx[h] != -INFINITY
-                      ? __expf(lse0[static_cast<int64_t>(h) * a.splits + s0 + s] - s_mx[h]) * s_inv[h]
-                      : 0.f;
+    uint4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int s = sg + kSg * u;
+      v[u] = s < ns ? __ldcg(reinterpret_cast<const uint4*>(part + (s0 + s) * sstride)) : make_uint4(0, 0, 0, 0);
+    }
+    for (int i = t; i < 64 * kS; i += blockDim.x) {
+      const int h = i >> 6, s = i & (kS - 1);
+      s_w[h][s] = h < hcount && s < ns ? lse0[static_cast<int64_t>(h) * a.splits + s0 + s] : -INFINITY;
     }
     __syncthreads();
-    for (int s = 0; s < ns; s += kU) {
-      uint4 v[kU];
+    {
+      // head t / 8: this pass's max and sum of exp (eight threads, eight splits each)
+      const int h = t >> 3, part8 = t & 7;
+      float mx = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kU; ++u)
-        v[u] = s + u < ns ? __ldcg(reinterpret_cast<const uint4*>(part + (s0 + s + u) * sstride)) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 8; ++u) mx = fmaxf(mx, s_w[h][part8 + 8 * u]);
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        if (s + u < ns) {
-          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float mo = s_m[h], mn = fmaxf(mo, mx);
+      float sum = 0.f;
+      if (mn != -INFINITY) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float w = s_w[s + u][hq + i];
-            const uint16_t bits = static_cast<uint16_t>((i & 1) ? w4[i >> 1] >> 16 : w4[i >> 1] & 0xFFFFu);
-            const float x = __half2float(__ushort_as_half(bits));
-            acc[i] = w > 0.f ? fmaf(w, x, acc[i]) : acc[i];
-          }
+        for (int u = 0; u < 8; ++u) sum += __expf(s_w[h][part8 + 8 * u] - mn);   // exp(-inf) = 0
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      __syncthreads();
+      if (part8 == 0) {
+        const float r = mo == -INFINITY ? 0.f : __expf(mo - mn);
+        s_r[h] = r;
+        s_l[h] = s_l[h] * r + sum;
+        s_m[h] = mn;
+      }
+      // weights relative to the running max (a split without rows gets 0)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float x = s_w[h][part8 + 8 * u];
+        s_w[h][part8 + 8 * u] = x == -INFINITY ? 0.f : __expf(x - mn);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= s_r[hq + i];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int s = sg + kSg * u;
+      if (s < ns) {
+        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float w = s_w[hq + i][s];
+          const uint16_t bits = static_cast<uint16_t>((i & 1) ? w4[i >> 1] >> 16 : w4[i >> 1] & 0xFFFFu);
+          // a split without rows may have left its partial unwritten
+          acc[i] = w > 0.f ? fmaf(w, __half2float(__ushort_as_half(bits)), acc[i]) : acc[i];
         }
       }
     }
+    __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) s_out[hq + i][dl] = acc[i];
+  for (int i = 0; i < 8; ++i) s_acc[sg][hq + i][dl] = acc[i];
   __syncthreads();
-  for (int r = warp * 2 + (lane >> 4); r < hcount; r += 8) {   // 16 dims of head r per half-warp
-    const int dd = blockIdx.y * 16 + (lane & 15);
-    if (dd < a.D) a.out[(static_cast<int64_t>(b) * a.H + h0 + r) * a.Dv + dd] = s_out[r][lane & 15];
+  {
+    const int r = t >> 3, dd = t & 7;   // head r, dim dd of the CTA's 8
+    if (r < hcount) {
+      float o = 0.f;
+#pragma unroll
+      for (int g = 0; g < kSg; ++g) o += s_acc[g][r][dd];
+      const float L = s_l[r];
+      const int dg = blockIdx.y * 8 + dd;
+      if (dg < a.D) a.out[(static_cast<int64_t>(b) * a.H + h0 + r) * a.Dv + dg] = L > 0.f ? o / L : 0.f;
+      if (blockIdx.y == 0 && dd == 0 && a.lse)
+        a.lse[static_cast<int64_t>(b) * a.H + h0 + r] = L > 0.f ? s_m[r] + logf(L) : -INFINITY;
+    }
   }
 }
 
@@ -350,7 +379,7 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
 }
 
 int launch_attention_merge_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
-  return launch_pdl(attn_merge_tc_kernel, dim3(a.B * head_groups, (a.D + 15) / 16), dim3(128), 0, st, a);
+  return launch_pdl(attn_merge_tc_kernel, dim3(a.B * head_groups, (a.D + 7) / 8), dim3(512), 0, st, a);
 }
 
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st) {

@@ -9,38 +9,45 @@
 // window and the compressed KV feed one attention (one softmax over the union).
 //
 // All query heads read the same rows, so a decode step is a pair of dense
-// contractions per tile of 128 rows:
+// contractions per tile of up to 128 rows:
 //   X   [128 rows][D]  f16: each row's dequantised key (code * scale || rope, or
 //                      the raw window token); it is also the value row when K = V
 //   S^T [128][64]      = X . Q^T             (M = 128 rows, N = 64 heads, K = D)
 //   P   [128][64]      = exp2(S^T * c - m)   (f16, the running max m per head)
-//   O^T [D][64]       += X^T . P             (M = 128 dims per block, N = 64, K = 128 rows)
+//   O^T [D][64]       += X^T . P             (M = 128 dims per block, N = 64, K = rows)
 // X is written once per tile in the 128-byte-swizzled layout that serves as a
 // K-major operand for the first product and as an MN-major operand for the
 // second; S^T and O^T live in tensor memory (lane = row / dim, column = head).
 //
+// A sequence's rows are cut into tiles of R = 32, 64 or 128 rows (the host
+// picks the largest R that still fills the GPU): first the compressed rows
+// (the top-k list for CSA, every entry for HCA), then the window tokens; a tile
+// never mixes the two. Each CTA takes a run of consecutive tiles (a split).
+// X is staged chunk by chunk, a chunk being 128 dims of every row of the tile:
+// the raw bytes land in the chunk's own region of X and are dequantised there.
+//
 // CTA roles (512 threads, one CTA per SM for D = 512):
-//   warp 0      allocates tensor memory, prefetches the CTA's rows into L2, and
-//               one lane issues every MMA;
-//   warps 1-3, 8-11   (224 threads) dequantise rows into X, chunk by chunk of
-//               128 dims, with the loads of the next chunk in flight. An e4m3
-//               code becomes f16 by integer operations (its bit pattern shifted
-//               into an f16 is exactly code * 2^-8) and one f16 multiply by the
-//               row's scale * 2^8;
-//   warps 4-7, 12-15  (two per 32-lane quarter of tensor memory: one row each,
-//               heads 0-31 or 32-63) convert the query, then turn S^T into P.
-//               The running max of a head only moves when a score exceeds it by
-//               more than 2^8 (then the tile's column max is reduced and O^T
-//               and l are rescaled), so P <= 256 always fits f16. After the
-//               last tile they normalise O^T, stage it in shared memory and
-//               store this split's partial output with bulk copies.
-// Splits are merged by attn_merge_kernel (attention.cu).
+//   warp 0      allocates tensor memory; one lane issues every MMA;
+//   warp 1      one lane streams the compressed rows of HCA tiles with TMA
+//               boxes (contiguous rows); the others prefetch later tiles into L2;
+//   warps 2-15  (448 workers) copy gathered rows (CSA, and every window token)
+//               with cp.async, convert the query, and dequantise every chunk in
+//               place: e4m3 codes become f16 by the hardware conversion, then
+//               two exact-range f16 multiplies (by 2^-8, then by scale * 2^8).
+//               Warps 4-7 and 12-15 (two per 32-lane quarter of tensor memory)
+//               also turn S^T into P: the running max of a head only moves when
+//               a score exceeds it by more than 2^8 (then O^T and l are
+//               rescaled), so P <= 256 always fits f16. After the last tile they
+//               normalise O^T and store this split's partial output as f16
+//               (rows of 64 heads per dim, 16-byte granules swizzled by dim).
+// Splits are merged by attn_merge_tc_kernel (attention.cu).
 //
 // Precision: K, V and P are rounded to f16 (relative error <= 2^-11 each; a
 // row's scale is rounded to f16 once), the bf16 query converts to f16 exactly
-// for |q| in [2^-14, 65504]; products and sums are fp32. A value that does not
-// fit f16 (|x| >= 65504) raises DSV4_STATUS_RANGE. The two e4m3 NaN codes, which
-// the quantiser never writes, read as +-480.
+// for |q| in [2^-14, 65504]; products and sums are fp32; split partials are
+// stored as f16. A value that does not fit f16 (|x| >= 65504) raises
+// DSV4_STATUS_RANGE. The two e4m3 NaN codes (never written by the quantiser)
+// decode to NaN, as the format defines them.
 #include <mutex>
 
 #include "common.cuh"
@@ -52,28 +59,29 @@ namespace dsv4 {
 
 namespace {
 
-constexpr int kRows = 128;                     // rows per tile
+constexpr int kRows = 128;                     // MMA M; the most rows a tile holds
 constexpr int kHeads = 64;                     // heads per CTA (MMA N), zero-padded
 constexpr int kThreads = 512;
-constexpr int kConvThreads = 7 * 32;           // warps 1-3 and 8-11
+constexpr int kWorkers = 14 * 32;              // warps 2-15
 constexpr int kSoftThreads = 8 * 32;           // warps 4-7 and 12-15
 constexpr int kGroups = kRows * 16;            // 8-dim groups of one 128-dim chunk
-constexpr int kItems = (kGroups + kConvThreads - 1) / kConvThreads;
+constexpr int kItems = (kGroups + kWorkers - 1) / kWorkers;
+constexpr int kQItems = (kHeads * 64 + kWorkers - 1) / kWorkers;   // 8-dim query groups (D <= 512)
 constexpr int kAtomBytes = kRows * 128;        // 128 rows x 64 dims f16
 constexpr int kChunkBytes = 2 * kAtomBytes;    // 128 rows x 128 dims f16
 constexpr int kQAtomBytes = kHeads * 128;      // 64 heads x 64 dims f16
 constexpr int kPBytes = kRows * kHeads * 2;
 constexpr int kMaxChunks = 4;                  // D <= 512
-constexpr int kMaxTiles = 8;                   // rows per CTA <= 1024 (the host plan keeps to it)
-constexpr int kBarSoft = 1, kBarConv = 2;      // named barriers (0 is __syncthreads)
+constexpr int kMaxTiles = 8;                   // tiles per CTA (the host plan keeps to it)
+constexpr int kBarWork = 1, kBarSoft = 2;      // named barriers (0 is __syncthreads)
 constexpr float kRescale = 8.f;                // lazy-rescale threshold (log2 units)
 constexpr float kF16Max = 65504.f;
 
 struct TcTail {
-  uint64_t xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, qready, qraw, drain;
+  uint64_t xland[kMaxChunks], xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, qready, drain;
   uint32_t taddr;
   int abort;
-  int32_t src[kMaxTiles * kRows];   // row sources of every row of the split (see row_source)
+  int32_t src[kMaxTiles * kRows];   // row sources of every tile of the split (see row_source), 128 per tile
   float sk[kMaxTiles * kRows];      // key (or shared entry) scale of every row, 0 for others
   float sv[kMaxTiles * kRows];      // value scale (separate V)
   float m_used[kHeads];             // running max per head, log2 domain
@@ -88,16 +96,20 @@ DSV4_DEV uint32_t f32x2_to_f16x2(float lo, float hi) {
   return r;
 }
 
-// Two e4m3 codes (bytes 0 and 1 of w after `sel`) as two f16 times f16x2 `sc`:
-// placing code c in the low byte of a halfword, (c + (c & 0x80)) << 7 is the
-// f16 bit pattern of e4m3(c) * 2^-8 (the sign moves to bit 15, the exponent and
-// mantissa land under f16's, subnormals included).
-DSV4_DEV uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t sel, uint32_t sc) {
-  uint32_t h, r;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(h) : "r"(w), "r"(sel));
-  h = (h + (h & 0x00800080u)) << 7;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc));
+DSV4_DEV uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
+}
+
+// Two e4m3 codes (the low and high byte of `two`) times the f16x2 `sc`
+// (= scale * 2^8 in both halves): the hardware conversion is exact, the
+// multiply by 2^-8 is exact too (it keeps every e4m3 value, subnormals
+// included, within f16), and the last multiply rounds once.
+DSV4_DEV uint32_t e4m3x2_to_f16x2_scaled(uint16_t two, uint32_t sc) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  return hmul2(hmul2(h, 0x1C001C00u), sc);   // 0x1C00 = f16 2^-8
 }
 
 DSV4_DEV uint32_t bf16x2_to_f16x2(uint32_t w, float& mx) {
@@ -117,10 +129,11 @@ DSV4_DEV float ex2(float x) {
   return y;
 }
 
-// Rows of sequence b are numbered: first the compressed entries (the top-k list
-// for CSA, every entry for HCA), then the window tokens, oldest first.
+// Rows of sequence b: n_main compressed rows (the top-k list for CSA, every
+// entry for HCA), then n_win window tokens, oldest first.
 struct RowSpace {
-  int64_t n_tok, n_c, n_win, n_main, R;
+  int64_t n_tok, n_c, n_win, n_main;
+  int mt, wt;   // tiles of compressed rows, tiles of window rows
 };
 
 DSV4_DEV RowSpace row_space(const AttnArgs& a, int b) {
@@ -129,25 +142,44 @@ DSV4_DEV RowSpace row_space(const AttnArgs& a, int b) {
   s.n_c = s.n_tok / a.ratio < a.capacity ? s.n_tok / a.ratio : a.capacity;
   s.n_win = s.n_tok < a.window ? s.n_tok : a.window;
   s.n_main = a.n_sel > 0 ? a.n_sel : s.n_c;
-  s.R = s.n_main + s.n_win;
+  s.mt = static_cast<int>((s.n_main + a.tile_rows - 1) / a.tile_rows);
+  s.wt = static_cast<int>((s.n_win + a.tile_rows - 1) / a.tile_rows);
   return s;
 }
 
-// Source of row r: >= 0 entry index into the planes (b * capacity + e), -1 no
-// row (past the split, a -1 top-k slot or an invalid index), <= -2 window ring
-// slot (-2 - slot).
-DSV4_DEV int32_t row_source(const AttnArgs& a, const RowSpace& s, int b, int64_t r, int64_t r1, bool flag_bad) {
-  if (r >= r1) return -1;
-  if (r < s.n_main) {
+// Tile i of a sequence: rows [r0, r0 + cnt) of the compressed rows, or of the
+// window tokens when win.
+struct Tile {
+  bool win;
+  int64_t r0;
+  int cnt;
+};
+
+DSV4_DEV Tile tile_at(const AttnArgs& a, const RowSpace& s, int i) {
+  Tile t;
+  t.win = i >= s.mt;
+  t.r0 = static_cast<int64_t>(t.win ? i - s.mt : i) * a.tile_rows;
+  const int64_t left = (t.win ? s.n_win : s.n_main) - t.r0;
+  t.cnt = static_cast<int>(left < a.tile_rows ? left : a.tile_rows);
+  return t;
+}
+
+// Source of row j of tile t: >= 0 entry index into the planes (b * capacity +
+// e), -1 no row (past the tile, a -1 top-k slot or an invalid index), <= -2
+// window ring slot (-2 - slot).
+DSV4_DEV int32_t row_source(const AttnArgs& a, const RowSpace& s, int b, const Tile& t, int j) {
+  if (j >= t.cnt) return -1;
+  const int64_t r = t.r0 + j;
+  if (!t.win) {
     const int64_t e = a.n_sel > 0 ? static_cast<int64_t>(a.topk[static_cast<int64_t>(b) * a.n_sel + r]) : r;
     if (e < -1 || e >= s.n_c) {
-      if (flag_bad) atomicOr(a.status, DSV4_STATUS_BAD_INDEX);
+      atomicOr(a.status, DSV4_STATUS_BAD_INDEX);
       return -1;
     }
     if (e < 0) return -1;
     return static_cast<int32_t>(static_cast<int64_t>(b) * a.capacity + e);
   }
-  const int64_t pos = s.n_tok - s.n_win + (r - s.n_main);
+  const int64_t pos = s.n_tok - s.n_win + r;
   return static_cast<int32_t>(-2 - pos % a.window);
 }
 
@@ -158,45 +190,6 @@ DSV4_DEV void prefetch_range(const void* p, int64_t bytes) {
   for (uintptr_t x = lo; x < hi; x += (1u << 20)) {
     const uintptr_t n = hi - x < (1u << 20) ? hi - x : (1u << 20);
     tc::prefetch_l2_bulk(reinterpret_cast<const void*>(x), static_cast<uint32_t>(n));
-  }
-}
-
-// Warp 0: hint L2 to fetch every byte this CTA's rows [r0, r1) read.
-DSV4_DEV void prefetch_rows(const AttnArgs& a, const RowSpace& s, int b, int64_t r0, int64_t r1, bool sep, int lane) {
-  const int64_t m1 = r1 < s.n_main ? r1 : s.n_main;
-  const int64_t base = static_cast<int64_t>(b) * a.capacity;
-  if (m1 > r0) {
-    if (a.n_sel == 0) {
-      const int64_t e0 = base + r0, n = m1 - r0;
-      if (lane == 0) prefetch_range(a.k_nope + e0 * a.d_nope, n * a.d_nope);
-      if (lane == 1 && a.d_rope) prefetch_range(a.k_rope + e0 * a.d_rope, n * a.d_rope * 2);
-      if (lane == 2) prefetch_range(a.k_scale + e0, n * 4);
-      if (sep && lane == 3) prefetch_range(a.v_nope + e0 * a.d_nope, n * a.d_nope);
-      if (sep && lane == 4 && a.d_rope) prefetch_range(a.v_rope + e0 * a.d_rope, n * a.d_rope * 2);
-      if (sep && lane == 5) prefetch_range(a.v_scale + e0, n * 4);
-    } else {
-      for (int64_t r = r0 + lane; r < m1; r += 32) {
-        const int64_t e = a.topk[static_cast<int64_t>(b) * a.n_sel + r];
-        if (e < 0 || e >= s.n_c) continue;
-        const int64_t row = base + e;
-        prefetch_range(a.k_nope + row * a.d_nope, a.d_nope);
-        if (a.d_rope) prefetch_range(a.k_rope + row * a.d_rope, a.d_rope * 2);
-        if (sep) {
-          prefetch_range(a.v_nope + row * a.d_nope, a.d_nope);
-          if (a.d_rope) prefetch_range(a.v_rope + row * a.d_rope, a.d_rope * 2);
-        }
-      }
-    }
-  }
-  const int64_t w0 = r0 > s.n_main ? r0 : s.n_main;
-  if (r1 > w0 && lane < (sep ? 4 : 2)) {
-    const int64_t pos0 = s.n_tok - s.n_win + (w0 - s.n_main);
-    const int64_t cnt = r1 - w0, s0 = pos0 % a.window;
-    const int64_t seg1 = cnt < a.window - s0 ? cnt : a.window - s0;
-    const uint16_t* win = (lane >> 1) ? a.win_v : a.win_k;
-    const int64_t rowb = static_cast<int64_t>(a.D) * 2;
-    if ((lane & 1) == 0) prefetch_range(win + (static_cast<int64_t>(b) * a.window + s0) * a.D, seg1 * rowb);
-    else if (cnt > seg1) prefetch_range(win + static_cast<int64_t>(b) * a.window * a.D, (cnt - seg1) * rowb);
   }
 }
 
@@ -214,93 +207,154 @@ DSV4_DEV void cp_async_wait(int n) {
   }
 }
 
-// Dims [128c, 128c + 128) of a row: nn FP8 dims (codes), the rest RoPE (bf16).
+// Dims [128c, 128c + 128) of an entry row: nn FP8 codes, then 128 - nn RoPE
+// dims (bf16) starting at RoPE element e0. Raw bytes of row j in the chunk's
+// region: codes at j * nn, RoPE at rope_off + j * rb (rope_off = 128 * nn, a
+// multiple of 128 bytes as a TMA destination needs). A window row's 128 bf16
+// values sit at j * 256.
 struct ChunkSplit {
-  int nn, rope0;   // nope dims in the chunk; first RoPE dim (index into the row's RoPE part)
+  int nn, e0, rb, rope_off;
 };
 DSV4_DEV ChunkSplit chunk_split(const AttnArgs& a, int c) {
-  const int n0 = c * 128;
-  int nn = a.d_nope - n0;
+  int nn = a.d_nope - c * 128;
   nn = nn < 0 ? 0 : (nn > 128 ? 128 : nn);
-  return ChunkSplit{nn, n0 + nn - a.d_nope};
+  return ChunkSplit{nn, c * 128 + nn - a.d_nope, 2 * (128 - nn), 128 * nn};
 }
 
-// Issue the asynchronous copies of chunk c of tile tt into the X chunk region
-// `xc`: row j's raw bytes land at xc + 256 j, as the chunk's FP8 codes followed
-// by its RoPE dims (bf16) for an entry, or its 128 bf16 values for a window
-// token; rows that do not exist get nothing. Thread ctid copies 16-byte
-// granules (row i / 16, granule i % 16) of its items.
-DSV4_DEV void issue_chunk(const AttnArgs& a, int b, const int32_t* src, int tt, int c, const uint8_t* nope,
-                          const uint16_t* rope, const uint16_t* win, unsigned char* xc, int ctid) {
+// Issue the cp.async copies of chunk c of a tile (row sources `src`, rc rows)
+// into the chunk region xc; rows without a source get nothing.
+DSV4_DEV void issue_chunk(const AttnArgs& a, int b, bool win, const int32_t* src, int c, int rc, const uint8_t* nope,
+                          const uint16_t* rope, const uint16_t* wbuf, unsigned char* xc, int wtid) {
   const ChunkSplit cs = chunk_split(a, c);
-  const int ng = cs.nn / 16, ngr = (128 - cs.nn) / 8;
+  const int ng = cs.nn / 16, nr = cs.rb / 16;
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
-    const int i = ctid + it * kConvThreads;
-    if (i < kGroups) {
-      const int j = i >> 4, k = i & 15;
-      const int32_t sr = src[tt * kRows + j];
-      unsigned char* dst = xc + j * 256 + k * 16;
-      if (sr >= 0) {
-        if (k < ng) cp_async16(dst, nope + static_cast<int64_t>(sr) * a.d_nope + c * 128 + k * 16);
-        else if (k < ng + ngr) cp_async16(dst, rope + static_cast<int64_t>(sr) * a.d_rope + cs.rope0 + (k - ng) * 8);
-      } else if (sr <= -2) {
-        cp_async16(dst, win + (static_cast<int64_t>(b) * a.window + (-2 - sr)) * a.D + c * 128 + k * 8);
+    const int i = wtid + it * kWorkers;
+    if (i < rc * 16) {
+      const int j = i >> 4, g = i & 15;
+      const int32_t sr = src[j];
+      if (!win && sr >= 0) {
+        if (g < ng)
+          cp_async16(xc + j * cs.nn + 16 * g, nope + static_cast<int64_t>(sr) * a.d_nope + c * 128 + 16 * g);
+        else if (g < ng + nr)
+          cp_async16(xc + cs.rope_off + j * cs.rb + 16 * (g - ng),
+                     rope + static_cast<int64_t>(sr) * a.d_rope + cs.e0 + 8 * (g - ng));
+      } else if (win && sr <= -2) {
+        cp_async16(xc + j * 256 + 16 * g, wbuf + (static_cast<int64_t>(b) * a.window + (-2 - sr)) * a.D + c * 128 + 8 * g);
       }
     }
   }
 }
 
-// Convert chunk c of tile tt in place: every converter thread first reads the
-// raw bytes of its 8-dim groups (group i: row i / 16, dims 8 * (i % 16) of the
-// chunk), then, after a barrier of the converter group, writes them as f16 into
-// the two 64-dim swizzle atoms of the chunk. Tracks the largest |value| that
-// must fit f16 (range check).
-DSV4_DEV void convert_chunk(const AttnArgs& a, const int32_t* src, const float* sc, int tt, int c,
-                            unsigned char* xc, int ctid, float& mx) {
+// Item it of worker wtid in chunk c: row j and 8-dim group g. With 64 code
+// dims (the chunk where the RoPE dims start in the 448 + 64 layout) each
+// aligned run of 32 items holds only code groups or only RoPE groups (four
+// rows each), so every warp takes one kind; otherwise 16 groups per row.
+DSV4_DEV void chunk_item(int nn, int i, int& j, int& g) {
+  if (nn == 64) {
+    const int q = i >> 5, l = i & 31;
+    j = ((q >> 1) << 2) + (l >> 3);
+    g = ((q & 1) << 3) + (l & 7);
+  } else {
+    j = i >> 4;
+    g = i & 15;
+  }
+}
+
+DSV4_DEV uint4 codes8_to_f16x8(uint2 w, uint32_t s2) {
+  return make_uint4(e4m3x2_to_f16x2_scaled(static_cast<uint16_t>(w.x), s2),
+                    e4m3x2_to_f16x2_scaled(static_cast<uint16_t>(w.x >> 16), s2),
+                    e4m3x2_to_f16x2_scaled(static_cast<uint16_t>(w.y), s2),
+                    e4m3x2_to_f16x2_scaled(static_cast<uint16_t>(w.y >> 16), s2));
+}
+
+DSV4_DEV uint32_t f16x2_of(float x) {
+  uint32_t s2;
+  asm("{\n.reg .b16 t;\ncvt.rn.f16.f32 t, %1;\nmov.b32 %0, {t, t};\n}" : "=r"(s2) : "f"(x));
+  return s2;
+}
+
+DSV4_DEV void store_group(unsigned char* xc, int j, int g, uint4 h) {
+  const int atom = g >> 3, gg = g & 7;
+  *reinterpret_cast<uint4*>(xc + atom * kAtomBytes + j * 128 + ((gg ^ (j & 7)) << 4)) = h;
+}
+
+// Dequantise chunk c of a tile in place: every worker first reads the raw
+// bytes of its items (8-dim groups, see chunk_item), then, after a barrier of
+// the workers, writes them as f16 into the two 64-dim swizzle atoms of the
+// chunk. Rows without a source read nothing and become zeros (their scale is
+// 0). Tracks the largest |value| that must fit f16 (range check). The
+// conversions run without per-item branches whenever a warp's items are all
+// codes or all bf16, so the items of a thread overlap.
+DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, const float* sc, int c, int rc,
+                            unsigned char* xc, int wtid, float& mx) {
   const ChunkSplit cs = chunk_split(a, c);
+  const int nn = win ? 128 : cs.nn;   // window rows: the item layout of a full chunk
+  const int n_items = rc * 16;
   uint4 raw[kItems];
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
-    const int i = ctid + it * kConvThreads;
+    const int i = wtid + it * kWorkers;
+    int j, g;
+    chunk_item(nn, i, j, g);
     raw[it] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < kGroups) {
-      const int j = i >> 4, g = i & 15;
-      const int32_t sr = src[tt * kRows + j];
-      const unsigned char* row = xc + j * 256;
-      if (sr >= 0) {
+    if (i < n_items) {
+      const int32_t sr = src[j];
+      if (win) {
+        if (sr <= -2) raw[it] = *reinterpret_cast<const uint4*>(xc + j * 256 + 16 * g);
+      } else if (sr >= 0) {
         if (8 * g < cs.nn) {
-          const uint2 w = *reinterpret_cast<const uint2*>(row + 8 * g);
+          const uint2 w = *reinterpret_cast<const uint2*>(xc + j * cs.nn + 8 * g);
           raw[it].x = w.x;
           raw[it].y = w.y;
         } else {
-          raw[it] = *reinterpret_cast<const uint4*>(row + cs.nn + 2 * (8 * g - cs.nn));
+          raw[it] = *reinterpret_cast<const uint4*>(xc + cs.rope_off + j * cs.rb + 2 * (8 * g - cs.nn));
         }
-      } else if (sr <= -2) {
-        raw[it] = *reinterpret_cast<const uint4*>(row + 16 * g);
       }
     }
   }
-  tc::bar_named(kBarConv, kConvThreads);
+  tc::bar_named(kBarWork, kWorkers);
+  // the kind of this thread's items: all codes, all bf16, or mixed
+  const int warp_q = wtid >> 5;   // items of a thread share the parity of i >> 5 (kWorkers is a multiple of 64)
+  const bool all_codes = !win && (cs.nn == 128 || (cs.nn == 64 && (warp_q & 1) == 0));
+  const bool all_bf16 = win || cs.nn == 0 || (cs.nn == 64 && (warp_q & 1) == 1);
+  if (all_codes) {
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int i = ctid + it * kConvThreads;
-    if (i < kGroups) {
-      const int j = i >> 4, g = i & 15;
-      const int32_t sr = src[tt * kRows + j];
-      uint4 h;
-      if (sr >= 0 && 8 * g < cs.nn) {   // e4m3 codes times the row's scale
-        const float scl = sc[tt * kRows + j];
-        mx = fmaxf(mx, fabsf(scl) * 448.f);
-        uint32_t s2;
-        asm("{\n.reg .b16 t;\ncvt.rn.f16.f32 t, %1;\nmov.b32 %0, {t, t};\n}" : "=r"(s2) : "f"(scl * 256.f));
-        h = make_uint4(e4m3x2_to_f16x2_scaled(raw[it].x, 0x4140u, s2), e4m3x2_to_f16x2_scaled(raw[it].x, 0x4342u, s2),
-                       e4m3x2_to_f16x2_scaled(raw[it].y, 0x4140u, s2), e4m3x2_to_f16x2_scaled(raw[it].y, 0x4342u, s2));
-      } else {
-        h = bf16x8_to_f16x8(raw[it], mx);
+    for (int it = 0; it < kItems; ++it) {
+      const int i = wtid + it * kWorkers;
+      int j, g;
+      chunk_item(nn, i, j, g);
+      const float scl = i < n_items ? sc[j] : 0.f;
+      mx = fmaxf(mx, fabsf(scl) * 448.f);
+      const uint4 h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), f16x2_of(scl * 256.f));
+      if (i < n_items) store_group(xc, j, g, h);
+    }
+  } else if (all_bf16) {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int i = wtid + it * kWorkers;
+      int j, g;
+      chunk_item(nn, i, j, g);
+      const uint4 h = bf16x8_to_f16x8(raw[it], mx);
+      if (i < n_items) store_group(xc, j, g, h);
+    }
+  } else {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int i = wtid + it * kWorkers;
+      if (i < n_items) {
+        int j, g;
+        chunk_item(nn, i, j, g);
+        uint4 h;
+        if (8 * g < cs.nn) {
+          const float scl = sc[j];
+          mx = fmaxf(mx, fabsf(scl) * 448.f);
+          h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), f16x2_of(scl * 256.f));
+        } else {
+          h = bf16x8_to_f16x8(raw[it], mx);
+        }
+        store_group(xc, j, g, h);
       }
-      const int atom = g >> 3, gg = g & 7;
-      *reinterpret_cast<uint4*>(xc + atom * kAtomBytes + j * 128 + ((gg ^ (j & 7)) << 4)) = h;
     }
   }
 }
@@ -339,7 +393,7 @@ DSV4_DEV void load_scores32(uint32_t taddr, float c2, bool valid, float* s) {
 
 // grid (splits, B, head groups), block 512. See the top of the file.
 template <bool SEP>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnMaps maps, AttnArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -349,20 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   unsigned char* pb = qs + D * 128;                          // [128 rows][64 heads] f16
   unsigned char* xk = pb + kPBytes;                          // nch chunks of [2 atoms][128 rows][128 B]
   unsigned char* xv = SEP ? xk + nch * kChunkBytes : xk;
-  uint16_t* stage16 = reinterpret_cast<uint16_t*>(xk);      // epilogue: [D][64 heads] f16, after the last P.V
-  const int xbytes = (SEP ? 2 : 1) * nch * kChunkBytes;
-  unsigned char* qstage = xk + xbytes - 128 * D;             // prologue: raw bf16 query [64][D], top of X
   TcTail* t = reinterpret_cast<TcTail*>(xk + (SEP ? 2 : 1) * nch * kChunkBytes);
   pdl_trigger();
+  if (threadIdx.x == 32 && a.tma) {
+    tc::prefetch_tensormap(&maps.nope);
+    tc::prefetch_tensormap(&maps.nope_tail);
+    tc::prefetch_tensormap(&maps.rope);
+  }
   pdl_wait();
 
   const int split = blockIdx.x, b = blockIdx.y;
   const int h0 = blockIdx.z * kHeads;
   const int hcount = a.H - h0 < kHeads ? a.H - h0 : kHeads;
   const RowSpace rs = row_space(a, b);
-  const int64_t r0 = static_cast<int64_t>(split) * a.rows_per_split;
-  const int64_t r1 = r0 + a.rows_per_split < rs.R ? r0 + a.rows_per_split : rs.R;
-  const int nt = r1 > r0 ? static_cast<int>((r1 - r0 + kRows - 1) / kRows) : 0;
+  const int tile0 = split * a.tiles_per_split;
+  const int tiles = rs.mt + rs.wt;
+  const int nt = tiles - tile0 < a.tiles_per_split ? (tiles - tile0 > 0 ? tiles - tile0 : 0) : a.tiles_per_split;
   if (nt == 0) {   // uniform: nothing to attend in this split
     for (int h = threadIdx.x; h < hcount; h += blockDim.x)
       a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + h) * a.splits + split] = -INFINITY;
@@ -370,40 +426,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // workers: the query rows of this head group (bf16), all loads in flight
+  // while the CTA sets up; converted into the MMA operand further down
+  const int gpr = D / 8;   // 8-dim groups per head
+  uint4 qw[kQItems];
+  if (warp >= 2) {
+    const int wtid = threadIdx.x - 64;
+#pragma unroll
+    for (int u = 0; u < kQItems; ++u) {
+      const int i = wtid + u * kWorkers, h = i / gpr;
+      qw[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < kHeads * gpr && h < hcount)
+        qw[u] = __ldg(reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.H + h0 + h) * D) + i % gpr);
+    }
+  }
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(kHeads * (1 + nch))) cols <<= 1;
   volatile int* abort = &t->abort;
-  const int nrows = nt * kRows;   // <= kMaxTiles * kRows (host plan)
 
-  if (a.n_sel == 0 && warp == 0) prefetch_rows(a, rs, b, r0, r1, SEP, lane);   // HCA: known ranges, start now
   if (warp == 0) tc::tmem_alloc(&t->taddr, cols);
   if (threadIdx.x == 32) {
     for (int c = 0; c < kMaxChunks; ++c) {
-      tc::mbar_init(&t->xfull[c], kConvThreads / 32);
+      tc::mbar_init(&t->xland[c], 1);
+      tc::mbar_init(&t->xfull[c], kWorkers / 32);
       tc::mbar_init(&t->xfree[c], 1);
     }
     tc::mbar_init(&t->sfull, 1);
     tc::mbar_init(&t->pfull, kSoftThreads / 32);
     tc::mbar_init(&t->pvdone, 1);
-    tc::mbar_init(&t->qready, kSoftThreads / 32);
-    tc::mbar_init(&t->qraw, 1);
+    tc::mbar_init(&t->qready, kWorkers / 32);
     tc::mbar_init(&t->drain, 1);
     t->abort = 0;
     tc::fence_mbar_init();
-    // the query rows of this head group, raw bf16, into the top of the X region
-    const uint32_t qbytes = static_cast<uint32_t>(hcount) * D * 2;
-    tc::mbar_arrive_expect_tx(&t->qraw, qbytes);
-    tc::bulk_load(qstage, a.q + (static_cast<int64_t>(b) * a.H + h0) * D, qbytes, &t->qraw);
   }
   if (threadIdx.x < kHeads) t->m_used[threadIdx.x] = -INFINITY;
   {
-    // row sources of the whole split (CSA: one round trip for the top-k indices)
+    // row sources of every tile of the split (CSA: one round trip for the top-k indices)
     int32_t sr[2];
     float ks[2], vs[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int i = threadIdx.x + k * kThreads;
-      sr[k] = i < nrows ? row_source(a, rs, b, r0 + i, r1, true) : -1;
+      const int i = threadIdx.x + k * kThreads, tt = i >> 7;
+      sr[k] = tt < nt ? row_source(a, rs, b, tile_at(a, rs, tile0 + tt), i & (kRows - 1)) : -1;
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -413,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int i = threadIdx.x + k * kThreads;
-      if (i < nrows) {
+      if ((i >> 7) < nt) {
         t->src[i] = sr[k];
         t->sk[i] = ks[k];
         if (SEP) t->sv[i] = vs[k];
@@ -426,20 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   const uint32_t taddr = t->taddr;
   const uint32_t s_tmem = taddr, o_tmem = taddr + kHeads;
   const int32_t* src = t->src;
-  if (a.n_sel > 0 && warp == 0) {   // CSA: prefetch the selected rows and the window, now that they are known
-    for (int i = lane; i < nrows; i += 32) {
-      const int32_t sr = src[i];
-      if (sr >= 0) {
-        tc::prefetch_l2_bulk(a.k_nope + static_cast<int64_t>(sr) * a.d_nope, a.d_nope);
-        if (a.d_rope) tc::prefetch_l2_bulk(a.k_rope + static_cast<int64_t>(sr) * a.d_rope, a.d_rope * 2);
-        if (SEP) {
-          tc::prefetch_l2_bulk(a.v_nope + static_cast<int64_t>(sr) * a.d_nope, a.d_nope);
-          if (a.d_rope) tc::prefetch_l2_bulk(a.v_rope + static_cast<int64_t>(sr) * a.d_rope, a.d_rope * 2);
-        }
-      }
-    }
-    if (lane < (SEP ? 4 : 2)) prefetch_rows(a, rs, b, r0 > rs.n_main ? r0 : rs.n_main, r1, SEP, lane);
-  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -450,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
       const uint32_t xk_sa = tc::smem_u32(xk), xv_sa = tc::smem_u32(xv);
       bool ok = tc::mbar_wait(&t->qready, 0, abort);
       for (int tt = 0; ok && tt < nt; ++tt) {
+        const int kk_pv = (tile_at(a, rs, tile0 + tt).cnt + 15) >> 4;   // 16-row steps holding rows
         for (int c = 0; c < nch; ++c) {
           if (!(ok = tc::mbar_wait(&t->xfull[c], tt & 1, abort))) break;
           tc::tc_fence_after();
@@ -467,8 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
         if (!(ok = tc::mbar_wait(&t->pfull, tt & 1, abort))) break;
         tc::tc_fence_after();
         for (int c = 0; c < nch; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < kk_pv; ++kk) {
             const uint64_t ad =
                 tc::smem_desc_lbo(xv_sa + c * kChunkBytes + kk * 2048, kAtomBytes, 1024, tc::kSwizzle128B);
             const uint64_t bd = tc::smem_desc_lbo(p_sa + kk * 2048, kAtomBytes, 1024, tc::kSwizzle128B);
@@ -476,87 +526,132 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
           }
           tc::tc_commit(&t->xfree[c]);
         }
-        tc::tc_commit(&t->pvdone);
       }
+      tc::tc_commit(&t->pvdone);
       // every MMA issued must finish before tensor memory is released
       tc::tc_commit(&t->drain);
       tc::mbar_wait_drain(&t->drain, 0);
     }
-  } else if (warp < 4 || (warp >= 8 && warp < 12)) {
-    // ------------------------------------------------------------ dequantisation into X
-    // Per tile: the copies of every chunk are issued as soon as its X region is
-    // free (all of them in flight at once), then the chunks are converted in
-    // place in order. Tile 0's regions that hold the staged query wait for it.
-    const int ctid = (warp < 4 ? warp - 1 : warp - 5) * 32 + lane;
-    const int qoff = xbytes - 128 * D;
-    float mx = 0.f;
-    bool ok = true;
-    for (int tt = 0; ok && tt < nt; ++tt) {
-      for (int c = 0; c < nch; ++c) {
-        bool w = true;
-        if (tt > 0) {
-          w = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
-        } else {
-          const int lo = c * kChunkBytes, hi_k = lo + kChunkBytes;
-          const bool clash = hi_k > qoff || (SEP && lo + nch * kChunkBytes + kChunkBytes > qoff);
-          if (clash) w = tc::mbar_wait(&t->qready, 0, abort);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ TMA producer (HCA compressed rows)
+    if (!SEP && a.tma) {
+      const int64_t row_base = static_cast<int64_t>(b) * a.capacity;
+      if (lane == 0) {
+        int issued = 0;
+        for (int tt = 0; tt < nt; ++tt) {
+          const Tile tl = tile_at(a, rs, tile0 + tt);
+          if (tl.win) break;   // window tiles come last and go by cp.async
+          const int y = static_cast<int>(row_base + tl.r0);
+          bool ok = true;
+          for (int c = 0; c < nch; ++c) {
+            if (tt > 0 && !(ok = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort))) break;
+            const ChunkSplit cs = chunk_split(a, c);
+            unsigned char* xc = xk + c * kChunkBytes;
+            tc::mbar_arrive_expect_tx(&t->xland[c], static_cast<uint32_t>(a.tile_rows * (cs.nn + cs.rb)));
+            if (cs.nn == 128) tc::tma_load_2d(xc, &maps.nope, &t->xland[c], c * 128, y);
+            else if (cs.nn > 0) tc::tma_load_2d(xc, &maps.nope_tail, &t->xland[c], c * 128, y);
+            if (cs.rb > 0) tc::tma_load_2d(xc + cs.rope_off, &maps.rope, &t->xland[c], 0, y);
+          }
+          if (!ok) break;
+          ++issued;
         }
-        if (!(ok = tc::bar_and(kBarConv, kConvThreads, w))) break;
-        issue_chunk(a, b, src, tt, c, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, ctid);
-        if (SEP) issue_chunk(a, b, src, tt, c, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, ctid);
-        cp_async_commit();
-      }
-      for (int c = 0; ok && c < nch; ++c) {
-        cp_async_wait(nch - 1 - c);
-        tc::bar_named(kBarConv, kConvThreads);   // every thread's copies of chunk c have landed
-        convert_chunk(a, src, t->sk, tt, c, xk + c * kChunkBytes, ctid, mx);
-        if (SEP) {
-          tc::bar_named(kBarConv, kConvThreads);
-          convert_chunk(a, src, t->sv, tt, c, xv + c * kChunkBytes, ctid, mx);
+        // every box issued must land before the CTA's shared memory goes away
+        if (issued > 0)
+          for (int c = 0; c < nch; ++c) tc::mbar_wait_drain(&t->xland[c], (issued - 1) & 1);
+      } else if (nt > 1) {
+        // later tiles' compressed rows into L2 (the first tile's boxes are on their way)
+        const Tile t1 = tile_at(a, rs, tile0 + 1);
+        const Tile tl = tile_at(a, rs, tile0 + nt - 1);
+        if (!t1.win) {
+          const int64_t e0 = row_base + t1.r0;
+          const int64_t n = (tl.win ? rs.n_main : tl.r0 + tl.cnt) - t1.r0;
+          if (lane == 1) prefetch_range(a.k_nope + e0 * a.d_nope, n * a.d_nope);
+          if (lane == 2 && a.d_rope) prefetch_range(a.k_rope + e0 * a.d_rope, n * a.d_rope * 2);
         }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&t->xfull[c]);
       }
     }
-    cp_async_wait(0);
-    if (mx >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
   } else {
-    // ------------------------------------------------------------ query, softmax, epilogue
+    // ------------------------------------------------------------ workers (warps 2-15)
+    const int wtid = threadIdx.x - 64;
+    const bool soft = (warp >= 4 && warp < 8) || warp >= 12;
     const int qd = warp & 3;                       // tensor-memory lane quarter
-    const int hb = warp >= 12 ? 32 : 0;            // this warp's heads [hb, hb + 32)
+    const int hb = warp >= 12 ? 32 : 0;            // a softmax warp's heads [hb, hb + 32)
     const int j = qd * 32 + lane;                  // row of the tile / dim of an O^T block
-    const int st = (warp >= 12 ? 128 : 0) + qd * 32 + lane;   // 0..255 within the group
+    const int st = (warp >= 12 ? 128 : 0) + qd * 32 + lane;   // 0..255 among the softmax threads
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float c2 = a.sm_scale * 1.4426950408889634f;
+    float mx = 0.f;
+
+    // tile 0's gathered rows: all copies in flight before the query work
+    const Tile first = tile_at(a, rs, tile0);
+    const bool first_cp = SEP || !a.tma || first.win;
+    if (first_cp) {
+      const int rc = (first.cnt + 15) & ~15;
+      for (int c = 0; c < nch; ++c) {
+        issue_chunk(a, b, first.win, src, c, rc, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, wtid);
+        if (SEP) issue_chunk(a, b, first.win, src, c, rc, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, wtid);
+        cp_async_commit();
+      }
+    }
     {
-      // the query (staged raw by the bulk copy), bf16 -> f16 into the K-major
-      // operand; heads beyond H zero
-      const bool got = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->qraw, 0, abort));
-      const int gpr = D / 8;   // 8-dim groups per head
+      // the query, bf16 -> f16 into the K-major operand (heads beyond H zero)
       float qmax = 0.f;
-      for (int i = st; got && i < kHeads * gpr; i += kSoftThreads) {
-        const int h = i / gpr, d0 = (i % gpr) * 8;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (h < hcount) w = *reinterpret_cast<const uint4*>(qstage + (h * D + d0) * 2);
-        const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
-        *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) = bf16x8_to_f16x8(w, qmax);
+#pragma unroll
+      for (int u = 0; u < kQItems; ++u) {
+        const int i = wtid + u * kWorkers;
+        if (i < kHeads * gpr) {
+          const int h = i / gpr, d0 = (i % gpr) * 8;
+          const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
+          *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) =
+              bf16x8_to_f16x8(qw[u], qmax);
+        }
       }
       if (qmax >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t->qready);
     }
-    float lw = 0.f;   // l of head hb + lane over this warp's rows
-    bool ok = true;
-    for (int tt = 0; tt < nt; ++tt) {
-      const bool valid = src[tt * kRows + j] != -1;
-      ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->sfull, tt & 1, abort));
-      if (!ok) break;
-      if (tt > 0) {   // the previous P.V must be done with P and O^T
-        ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->pvdone, (tt - 1) & 1, abort));
+
+    float lw = 0.f;   // softmax warps: l of head hb + lane over this warp's rows
+    // Every worker takes part in the same sequence of worker barriers; a
+    // softmax failure (a wait that gave up) reaches the others through the
+    // next one, so no worker is left waiting at a named barrier.
+    bool ok = true, soft_ok = true;
+    for (int tt = 0; ok && tt < nt; ++tt) {
+      const Tile tl = tile_at(a, rs, tile0 + tt);
+      const int rc = (tl.cnt + 15) & ~15;
+      const bool via_tma = !SEP && a.tma && !tl.win;
+      const int32_t* src_t = src + tt * kRows;
+      if (!via_tma && tt > 0) {
+        for (int c = 0; c < nch; ++c) {
+          const bool w = soft_ok && tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
+          if (!(ok = tc::bar_and(kBarWork, kWorkers, w))) break;
+          issue_chunk(a, b, tl.win, src_t, c, rc, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, wtid);
+          if (SEP) issue_chunk(a, b, tl.win, src_t, c, rc, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, wtid);
+          cp_async_commit();
+        }
         if (!ok) break;
       }
+      for (int c = 0; c < nch; ++c) {
+        bool w = soft_ok;
+        if (via_tma) w = w && tc::mbar_wait(&t->xland[c], tt & 1, abort);
+        else cp_async_wait(nch - 1 - c);
+        // every worker's copies of chunk c have landed (or the boxes have)
+        if (!(ok = tc::bar_and(kBarWork, kWorkers, w))) break;
+        convert_chunk(a, tl.win, src_t, t->sk + tt * kRows, c, rc, xk + c * kChunkBytes, wtid, mx);
+        if (SEP) {
+          tc::bar_named(kBarWork, kWorkers);
+          convert_chunk(a, tl.win, src_t, t->sv + tt * kRows, c, rc, xv + c * kChunkBytes, wtid, mx);
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&t->xfull[c]);
+      }
+      if (!ok || !soft) continue;
+
+      // ---- softmax warps: S^T -> P for this tile
+      const bool valid = src_t[j] != -1;
+      if (!(soft_ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->sfull, tt & 1, abort)))) continue;
       tc::tc_fence_after();
       float s[32];
       load_scores32(s_tmem + lane_off + hb, c2, valid, s);
@@ -608,49 +703,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t->pfull);
     }
-    if (ok) ok = tc::mbar_wait(&t->pvdone, (nt - 1) & 1, abort);
-    ok = tc::bar_and(kBarSoft, kSoftThreads, ok);
-    if (ok) {
-      tc::tc_fence_after();
-      t->red[qd][hb + lane] = lw;
-      tc::bar_named(kBarSoft, kSoftThreads);
-      if (st < kHeads) {
-        const float l = (t->red[0][st] + t->red[1][st]) + (t->red[2][st] + t->red[3][st]);
-        t->lsum[st] = l;
-        t->alpha[st] = l > 0.f ? 1.f / l : 0.f;
-      }
-      tc::bar_named(kBarSoft, kSoftThreads);
-      // normalised O^T as f16 -> stage [D][64 heads] (this split's partial in
-      // the layout of the workspace), then one bulk copy
-      for (int c = 0; c < nch; ++c) {
-        uint32_t v[32];
-        tc::tmem_ld32(o_tmem + lane_off + c * kHeads + hb, v);
-        tc::tmem_wait_ld();
-        uint32_t w[16];
+    cp_async_wait(0);
+    if (mx >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
+
+    if (soft) {
+      // ---- epilogue: normalise O^T and store this split's f16 partial [D][64 heads]
+      ok = ok && soft_ok;
+      if (ok) ok = tc::mbar_wait(&t->pvdone, 0, abort);
+      ok = tc::bar_and(kBarSoft, kSoftThreads, ok);
+      if (ok) {
+        tc::tc_fence_after();
+        t->red[qd][hb + lane] = lw;
+        tc::bar_named(kBarSoft, kSoftThreads);
+        if (st < kHeads) {
+          const float l = (t->red[0][st] + t->red[1][st]) + (t->red[2][st] + t->red[3][st]);
+          t->lsum[st] = l;
+          t->alpha[st] = l > 0.f ? 1.f / l : 0.f;
+        }
+        tc::bar_named(kBarSoft, kSoftThreads);
+        // normalised O^T as f16 rows [dim][64 heads] staged in the (now free) X
+        // region, 16-byte granule q of row r at granule q ^ (r & 7) (no bank
+        // conflicts; the merge reads the same swizzle), then one bulk copy
+        unsigned char* stage = xk;
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld32(o_tmem + lane_off + c * kHeads + hb, v);
+          tc::tmem_wait_ld();
+          uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = f32x2_to_f16x2(__uint_as_float(v[2 * i]) * t->alpha[hb + 2 * i],
-                                __uint_as_float(v[2 * i + 1]) * t->alpha[hb + 2 * i + 1]);
-        uint4* dst = reinterpret_cast<uint4*>(stage16 + (c * 128 + j) * kHeads + hb);
+          for (int i = 0; i < 16; ++i)
+            w[i] = f32x2_to_f16x2(__uint_as_float(v[2 * i]) * t->alpha[hb + 2 * i],
+                                  __uint_as_float(v[2 * i + 1]) * t->alpha[hb + 2 * i + 1]);
+          const int r = c * 128 + j;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((((hb >> 3) + q4) ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        }
+        tc::fence_proxy_async_smem();
+        tc::bar_named(kBarSoft, kSoftThreads);
+        if (st == 0) {
+          const int hgs = gridDim.z;
+          uint16_t* part = reinterpret_cast<uint16_t*>(a.part_o) +
+                           ((static_cast<int64_t>(b) * a.splits + split) * hgs + blockIdx.z) * D * kHeads;
+          tc::bulk_store(part, stage, static_cast<uint32_t>(D) * kHeads * 2);
+          tc::bulk_commit();
+        }
+        if (st < hcount) {
+          const float l = t->lsum[st];
+          a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + st) * a.splits + split] =
+              l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
+        if (st == 0) tc::bulk_wait();   // the stage must outlive the copy, and its writes precede the merge
       }
-      tc::fence_proxy_async_smem();
-      tc::bar_named(kBarSoft, kSoftThreads);
-      const int64_t row0 = static_cast<int64_t>(b) * a.H + h0;
-      if (st == 0) {
-        const int hgs = gridDim.z;
-        uint16_t* part = reinterpret_cast<uint16_t*>(a.part_o) +
-                         ((static_cast<int64_t>(b) * a.splits + split) * hgs + blockIdx.z) * D * kHeads;
-        tc::bulk_store(part, stage16, D * kHeads * 2);
-        tc::bulk_commit();
-      }
-      if (st < hcount) {
-        const float l = t->lsum[st];
-        a.part_lse[(row0 + st) * a.splits + split] =
-            l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-      }
-      if (st == 0) tc::bulk_wait();   // shared memory must outlive the copy, and its writes precede the merge
     }
   }
 
@@ -671,26 +776,44 @@ size_t tc_smem_bytes(int D, bool sep) {
 }
 
 template <bool SEP>
-int launch_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
+int launch_tc(const AttnMaps& maps, const AttnArgs& a, int head_groups, cudaStream_t st) {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(attn_tc_kernel<SEP>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   const size_t smem = tc_smem_bytes(a.D, SEP);
-  return launch_pdl(attn_tc_kernel<SEP>, dim3(a.splits, a.B, head_groups), dim3(kThreads), smem, st, a);
+  return launch_pdl(attn_tc_kernel<SEP>, dim3(a.splits, a.B, head_groups), dim3(kThreads), smem, st, maps, a);
 }
 
 }  // namespace
 
 bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v) {
   const int D = d_nope + d_rope;
-  if (H < 1 || H > 128 || D % 128 || D > 128 * kMaxChunks || d_nope % 8 || d_rope % 8) return false;
+  if (H < 1 || H > 128 || D % 128 || D > 128 * kMaxChunks || d_nope % 16 || d_rope % 8) return false;
   if (separate_v && D > 256) return false;
   return tc_smem_bytes(D, separate_v != 0) <= 227 * 1024;
 }
 
-int launch_attention_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
-  const int e = a.separate_v ? launch_tc<true>(a, head_groups, st) : launch_tc<false>(a, head_groups, st);
+bool attention_tc_tma_shape(int d_nope, int d_rope, int separate_v) {
+  // every chunk but the last holds 128 codes; the last holds the remaining
+  // codes and all RoPE dims (so three box shapes cover every load)
+  return !separate_v && d_rope <= 128 && (d_rope == 0 || d_nope % 128 + d_rope == 128);
+}
+
+int launch_attention_tc(const AttnArgs& a0, int head_groups, cudaStream_t st) {
+  AttnArgs a = a0;
+  AttnMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  a.tma = 0;
+  if (a.n_sel == 0 && attention_tc_tma_shape(a.d_nope, a.d_rope, a.separate_v)) {
+    const int64_t rows = static_cast<int64_t>(a.B) * a.capacity;
+    const int tail = a.d_nope % 128;
+    bool ok = a.d_nope < 128 || encode_u8_rows(&maps.nope, a.k_nope, rows, a.d_nope, 128, a.tile_rows);
+    if (ok && tail) ok = encode_u8_rows(&maps.nope_tail, a.k_nope, rows, a.d_nope, tail, a.tile_rows);
+    if (ok && a.d_rope) ok = encode_u8_rows(&maps.rope, a.k_rope, rows, 2 * a.d_rope, 2 * a.d_rope, a.tile_rows);
+    a.tma = ok ? 1 : 0;
+  }
+  const int e = a.separate_v ? launch_tc<true>(maps, a, head_groups, st) : launch_tc<false>(maps, a, head_groups, st);
   if (e) return e;
   return launch_attention_merge_tc(a, head_groups, st);
 }

@@ -57,23 +57,11 @@ constexpr int kSelThreads = 512;
 constexpr int kMaxK = 2048;
 constexpr int kScanItems = 8;        // scores each thread loads per round trip
 constexpr int kCandCache = 4096;     // candidates the resolving CTA keeps in shared memory
-constexpr int kTopkDynSmem = kCandCache * 8 + 8192 * 4;   // candidate cache + bitmap of 2^18 blocks
+constexpr int kTopkDynSmem = kCandCache * 8;   // candidate cache
 
 // Append `flag`-ed values of a warp to list[*counter ...] with one atomic per
 // warp; positions at or beyond `cap` are dropped.
 DSV4_DEV void warp_append_i32(bool flag, int32_t v, uint32_t* counter, int32_t* list, uint32_t cap) {
-  const unsigned bal = __ballot_sync(0xffffffffu, flag);
-  if (!bal) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(bal) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(bal)));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
-  if (flag && pos < cap) list[pos] = v;
-}
-
-DSV4_DEV void warp_append_u64(bool flag, uint64_t v, uint32_t* counter, uint64_t* list, uint32_t cap) {
   const unsigned bal = __ballot_sync(0xffffffffu, flag);
   if (!bal) return;
   const int lane = threadIdx.x & 31;
@@ -176,8 +164,6 @@ DSV4_DEV void load_to_smem(T* dst, const T* src, uint32_t n) {
   }
 }
 
-constexpr int kBitmapWords = 8192;   // the fast path's bitmap of selected blocks: n_c <= 2^18
-
 }  // namespace
 
 // Top-k selection, grid (sel_ctas, B), block 512. The scoring kernel has
@@ -188,14 +174,14 @@ constexpr int kBitmapWords = 8192;   // the fast path's bitmap of selected block
 // per CTA, while histogramming the next 12 key bits (hist2). The last CTA of the
 // sequence to finish (a completion counter, no waiting) resolves the boundary:
 // candidates above the second-level threshold bin T2 are taken; ties in T2 are
-// settled by the low 8 key bits, then by the lower index; the k blocks are
-// emitted in ascending index order.
+// settled by the low 8 key bits, then by the lower index (radix select over
+// 12-bit index digits); the k blocks are sorted into ascending index order.
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   __shared__ uint32_t h[kBins];
   __shared__ int32_t fin[kMaxK];
   __shared__ uint32_t scratch[kSelThreads / 32 + 2];
   __shared__ uint32_t s_nfin, s_last, s_d, s_rem, s_base[2];
-  extern __shared__ uint64_t dyn[];   // candidate cache, then (fast path) the bitmap behind it
+  extern __shared__ uint64_t dyn[];   // candidate cache
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
@@ -281,180 +267,84 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   if (threadIdx.x == 0) s_nfin = n_above;
   uint64_t* cache = dyn;
   const bool cached = n_cand <= static_cast<uint32_t>(kCandCache);
-  const bool fast = cached && n_c <= 32 * kBitmapWords;
   if (cached) load_to_smem(cache, static_cast<const uint64_t*>(cand), n_cand);
   const uint64_t* cl = cached ? cache : cand;
-  uint32_t* bm = reinterpret_cast<uint32_t*>(dyn + kCandCache);
-  if (fast)
-    for (int i = threadIdx.x; i < kBitmapWords; i += blockDim.x) bm[i] = 0;
   __syncthreads();
   uint32_t n_gt2 = 0;
   const uint32_t T2 = need1 ? static_cast<uint32_t>(block_suffix_select<kSelThreads>(h, need1, &n_gt2, scratch)) : 0xFFFFu;
   const uint32_t need2 = need1 - n_gt2;                                      // taken among the keys of bin (T1, T2)
   const uint32_t n_eq2 = T2 < static_cast<uint32_t>(kBins) ? h[T2] : 0u;
 
-  if (fast) {
-    // selected blocks as bits: those above T1, candidates above T2, and the
-    // need2 best of T2 by (low 8 key bits desc, index asc)
-    for (uint32_t i = threadIdx.x; i < n_above; i += blockDim.x) {
-      const uint32_t x = static_cast<uint32_t>(fin[i]);
-      atomicOr(&bm[x >> 5], 1u << (x & 31));
-    }
-    uint32_t d8 = 0, r8 = need2;   // take low8 > d8 fully, and the r8 lowest indices with low8 == d8
-    __syncthreads();
-    if (need2 > 0 && need2 < n_eq2) {
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
-      __syncthreads();
-      for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
-        const uint32_t i = i0 + threadIdx.x;
-        const uint64_t v = i < n_cand ? cl[i] : 0ull;
-        const uint32_t key = static_cast<uint32_t>(v >> 32);
-        warp_hist_add(h, key & 0xFF, i < n_cand && ((key >> 8) & 0xFFF) == T2);
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) { s_d = 0; s_rem = 0; }
-      __syncthreads();
-      if (threadIdx.x < 32) warp_digit_select(h, need2, &s_d, &s_rem);
-      __syncthreads();
-      d8 = s_d;
-      r8 = need2 - s_rem;
-      // the r8-th smallest index with low8 == d8: two passes over 9-bit digits (n_c <= 2^18)
-      uint32_t prefix = 0;
-      for (int pass = 0; pass < 2; ++pass) {
-        const int shift = 9 - 9 * pass;
-        __syncthreads();
-        for (int i = threadIdx.x; i < 512; i += blockDim.x) h[i] = 0;
-        __syncthreads();
-        for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
-          const uint32_t i = i0 + threadIdx.x;
-          const uint64_t v = i < n_cand ? cl[i] : 0ull;
-          const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
-          const bool in = i < n_cand && ((key >> 8) & 0xFFF) == T2 && (key & 0xFF) == d8 &&
-                          (pass == 0 || (idx >> 9) == prefix);
-          warp_hist_add(h, (idx >> shift) & 0x1FF, in);
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {   // smallest digit with prefix count >= r8
-          const int lane = threadIdx.x;
-          uint32_t mine = 0;
-#pragma unroll
-          for (int q = 0; q < 16; ++q) mine += h[lane * 16 + q];
-          uint32_t inc = mine;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
-          }
-          const uint32_t excl = inc - mine;
-          if (excl < r8 && inc >= r8) {
-            uint32_t acc = excl;
-            for (int q = 0; q < 16; ++q) {
-              const uint32_t c = h[lane * 16 + q];
-              if (acc + c >= r8) {
-                s_d = static_cast<uint32_t>(lane * 16 + q);
-                s_rem = acc;
-                break;
-              }
-              acc += c;
-            }
-          }
-        }
-        __syncthreads();
-        prefix = (prefix << 9) | s_d;
-        r8 -= s_rem;
-      }
-      const uint32_t thr = prefix;   // indices <= thr with low8 == d8 are taken (exactly r8 of them before)
-      __syncthreads();
-      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
-        const uint64_t v = cl[i];
-        const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
-        const uint32_t b2 = (key >> 8) & 0xFFF;
-        const bool take = b2 > T2 || (b2 == T2 && ((key & 0xFF) > d8 || ((key & 0xFF) == d8 && idx <= thr)));
-        if (take) atomicOr(&bm[idx >> 5], 1u << (idx & 31));
-      }
-    } else {
-      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
-        const uint64_t v = cl[i];
-        const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
-        const uint32_t b2 = (key >> 8) & 0xFFF;
-        if (b2 > T2 || (b2 == T2 && need2 > 0)) atomicOr(&bm[idx >> 5], 1u << (idx & 31));
-      }
-    }
-    __syncthreads();
-    // emit the set bits in ascending order: thread t owns words [16t, 16t + 16)
-    constexpr int per = kBitmapWords / kSelThreads;
-    uint32_t cntw = 0;
-#pragma unroll
-    for (int q = 0; q < per; ++q) cntw += __popc(bm[threadIdx.x * per + q]);
-    uint32_t tot;
-    uint32_t pos = block_excl_scan_packed(cntw, &tot, scratch);
-    for (int q = 0; q < per; ++q) {
-      uint32_t wd = bm[threadIdx.x * per + q];
-      while (wd) {
-        const int bit = __ffs(wd) - 1;
-        wd &= wd - 1;
-        if (pos < static_cast<uint32_t>(k)) out[pos] = (threadIdx.x * per + q) * 32 + bit;
-        ++pos;
-      }
-    }
-    for (uint32_t i = tot + threadIdx.x; i < static_cast<uint32_t>(k); i += blockDim.x) out[i] = -1;   // inconsistent input only
-    return;
-  }
-
-  // ---- general path: radix select of the need2-th largest 40-bit rank
-  // (low8 << 32 | ~index) in bin (T1, T2), then a bitonic sort
-  uint64_t thr_rank = 0;
+  // Within bin (T1, T2) the need2 best by (low 8 key bits desc, index asc):
+  // every key with low8 > d8, and the r8 lowest indices with low8 == d8, i.e.
+  // those <= thr (a radix select over 12-bit index digits, lowest first).
+  uint32_t d8 = 0, thr = 0;
   if (need2 > 0 && need2 < n_eq2) {
-    uint64_t prefix = 0, mask = 0;
-    uint32_t remaining = need2;
-    for (int pass = 0; pass < 5; ++pass) {
-      const int shift = 32 - 8 * pass;                                       // bits 39..32, 31..24, ..., 7..0
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
+      const uint32_t i = i0 + threadIdx.x;
+      const uint64_t v = i < n_cand ? cl[i] : 0ull;
+      const uint32_t key = static_cast<uint32_t>(v >> 32);
+      warp_hist_add(h, key & 0xFF, i < n_cand && ((key >> 8) & 0xFFF) == T2);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_d = 0;
+      s_rem = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) warp_digit_select(h, need2, &s_d, &s_rem);
+    __syncthreads();
+    d8 = s_d;
+    uint32_t r8 = need2 - s_rem;   // lowest indices to take among low8 == d8
+    int nbits = 1;
+    while (nbits < 31 && (static_cast<int64_t>(1) << nbits) < n_c) ++nbits;
+    const int passes = (nbits + 11) / 12;
+    uint32_t prefix = 0;
+    for (int pass = 0; pass < passes; ++pass) {
+      const int shift = 12 * (passes - 1 - pass);
       __syncthreads();
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+      for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
       __syncthreads();
       for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
         const uint32_t i = i0 + threadIdx.x;
         const uint64_t v = i < n_cand ? cl[i] : 0ull;
-        const uint32_t key = static_cast<uint32_t>(v >> 32);
-        const uint64_t rank = (static_cast<uint64_t>(key & 0xFF) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(v));
-        const bool in = i < n_cand && ((key >> 8) & 0xFFF) == T2 && (rank & mask) == prefix;
-        warp_hist_add(h, static_cast<uint32_t>((rank >> shift) & 0xFF), in);
+        const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
+        const bool in = i < n_cand && ((key >> 8) & 0xFFF) == T2 && (key & 0xFF) == d8 &&
+                        (pass == 0 || (idx >> (shift + 12)) == prefix);
+        // reversed digit: the largest reversed bin with enough keys at or above it is the smallest digit
+        warp_hist_add(h, (kBins - 1) - ((idx >> shift) & 0xFFF), in);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        s_d = 0;
-        s_rem = 0;
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) warp_digit_select(h, remaining, &s_d, &s_rem);   // s_rem: count above the digit
-      __syncthreads();
-      const uint32_t digit = s_d, above_digit = s_rem;
-      prefix |= static_cast<uint64_t>(digit) << shift;
-      mask |= static_cast<uint64_t>(0xFF) << shift;
-      remaining -= above_digit;
+      uint32_t before;
+      const uint32_t rd = static_cast<uint32_t>(block_suffix_select<kSelThreads>(h, r8, &before, scratch));
+      prefix = (prefix << 12) | ((kBins - 1) - rd);
+      r8 -= before;
     }
-    thr_rank = prefix;                                                       // exactly need2 ranks are >= prefix
+    thr = prefix;   // exactly the wanted number of indices with low8 == d8 are <= thr
   }
   __syncthreads();
   for (uint32_t i0 = 0; i0 < n_cand; i0 += blockDim.x) {
     const uint32_t i = i0 + threadIdx.x;
     const uint64_t v = i < n_cand ? cl[i] : 0ull;
-    const uint32_t key = static_cast<uint32_t>(v >> 32);
+    const uint32_t key = static_cast<uint32_t>(v >> 32), idx = static_cast<uint32_t>(v);
     const uint32_t b2 = (key >> 8) & 0xFFF;
     bool take = i < n_cand && need1 > 0 && b2 > T2;
-    if (i < n_cand && b2 == T2) {
-      const uint64_t rank = (static_cast<uint64_t>(key & 0xFF) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(v));
-      take = need2 > 0 && (need2 >= n_eq2 || rank >= thr_rank);
-    }
-    warp_append_i32(take, static_cast<int32_t>(static_cast<uint32_t>(v)), &s_nfin, fin, static_cast<uint32_t>(k));
+    if (i < n_cand && b2 == T2 && need2 > 0)
+      take = need2 >= n_eq2 || (key & 0xFF) > d8 || ((key & 0xFF) == d8 && idx <= thr);
+    warp_append_i32(take, static_cast<int32_t>(idx), &s_nfin, fin, static_cast<uint32_t>(k));
   }
   __syncthreads();
+  // the k blocks in ascending index order (padding -1 only on inconsistent input)
+  const uint32_t nf = s_nfin < static_cast<uint32_t>(k) ? s_nfin : static_cast<uint32_t>(k);
   int P = 1;
   while (P < k) P <<= 1;
-  for (int i = threadIdx.x + k; i < P; i += blockDim.x) fin[i] = 0x7FFFFFFF;
+  for (int i = threadIdx.x + static_cast<int>(nf); i < P; i += blockDim.x) fin[i] = 0x7FFFFFFF;
   __syncthreads();
   block_sort_asc(fin, P);
-  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = fin[i];
+  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < static_cast<int>(nf) ? fin[i] : -1;
 }
 
 int launch_topk_select(const IndexArgs& a, int sel_ctas, cudaStream_t st) {

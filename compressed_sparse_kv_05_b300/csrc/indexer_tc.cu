@@ -12,13 +12,14 @@
 // weights, writes one fp32 score per block and histograms the top 12 bits of
 // the score keys for the top-k selection that follows.
 //
-// CTA roles (256 threads): warp 0 allocates tensor memory and streams key tiles
+// CTA roles (384 threads): warp 0 allocates tensor memory and streams key tiles
 // with TMA into an S-stage ring; warp 1 issues tcgen05.cp (block scales) and
 // the MMAs (one thread); warps 2-3 rearrange each tile's key scales in shared
 // memory into the 32-row x 16-byte blocks that tcgen05.cp moves to tensor
-// memory; warps 4-7 (one per 32-lane quarter of tensor memory) turn finished
-// accumulators into scores. The accumulator and the scale slots are
-// double-buffered so the MMA of tile i+1 overlaps the epilogue of tile i.
+// memory; warps 4-11 turn finished accumulators into scores, in two sets of
+// four (one warp per 32-lane quarter of tensor memory) that take alternate
+// tiles. The accumulator is double-buffered (one buffer per set) so the MMA
+// of tile i+1 overlaps the epilogue of tile i.
 //
 // Scale block layout (one per 128 rows and K=64 step): row r's four scale bytes
 // (one per 16 elements, the first in the lowest byte) form the 32-bit word at
@@ -39,7 +40,8 @@ namespace dsv4 {
 namespace {
 
 constexpr int kTile = 128;     // compressed blocks per MMA tile (M)
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kEpiThreads = 256;   // warps 4-11
 constexpr int kSfBlock = 512;  // bytes of one scale block (128 rows x 4 scales)
 
 template <int ROWB>
@@ -61,13 +63,13 @@ struct SmemTail {
   uint32_t hist[kBins];  // histogram of score-key bits 31..20 of this CTA's blocks
 };
 
-// named barrier among the four epilogue warps
-DSV4_DEV void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barrier among the eight epilogue warps
+DSV4_DEV void epilogue_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 }  // namespace
 
 template <int ROWB>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     index_scores_tc_kernel(const __grid_constant__ CUtensorMap keys, const __grid_constant__ CUtensorMap qmap,
                            IndexTcArgs a) {
   using C = TcCfg<ROWB>;
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sfbuf = qbuf + ((a.N * ROWB + 1023) & ~1023);           // S x SF_BYTES key scale blocks
   unsigned char* qsf = sfbuf + C::STAGES * C::SF_BYTES;                   // query scale blocks (N <= 128 rows)
   SmemTail* t = reinterpret_cast<SmemTail*>(qsf + C::SF_BYTES);
-  float* wsm = reinterpret_cast<float*>(t + 1);
+  float* wsm = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(t + 1) + 15) & ~uintptr_t(15));   // head weights
   pdl_trigger();
   if (threadIdx.x == 0) {
     tc::prefetch_tensormap(&keys);
@@ -243,25 +245,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 4-7)
+    // ------------------------------------------------------------ epilogue (warps 4-11)
+    // Two sets of four warps (one per 32-lane quarter of tensor memory): set s
+    // takes the tiles of parity s, whose accumulator is buffer s.
+    const int set = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                  // tensor-memory lane == tile row
+    const int et = threadIdx.x - 128;                     // 0 .. 255
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    for (int i = row; i < 4096; i += 128) t->hist[i] = 0;
+    for (int i = et; i < kBins; i += kEpiThreads) t->hist[i] = 0;
     epilogue_sync();
     float* out = a.scores + static_cast<int64_t>(b) * a.capacity;
-    for (int i = 0; i < ntile; ++i) {
-      const int ab = i & 1, ra = i >> 1;
+    for (int i = set; i < ntile; i += 2) {
+      const int ab = set, ra = i >> 1;
       if (!tc::mbar_wait(&t->acc_full[ab], ra & 1, abort)) break;
       tc::tc_fence_after();
-      float score = 0.f;
+      // sum_h w_h max(0, s_h), four partial sums
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int c = 0; c < N; c += 32) {
         uint32_t v[32];
         tc::tmem_ld32(taddr + lane_base + acc_col0 + ab * N + c, v);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) score = fmaf(wsm[c + h], fmaxf(__uint_as_float(v[h]), 0.f), score);
+        for (int h = 0; h < 32; h += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(wsm + c + h);
+          acc[0] = fmaf(w4.x, fmaxf(__uint_as_float(v[h]), 0.f), acc[0]);
+          acc[1] = fmaf(w4.y, fmaxf(__uint_as_float(v[h + 1]), 0.f), acc[1]);
+          acc[2] = fmaf(w4.z, fmaxf(__uint_as_float(v[h + 2]), 0.f), acc[2]);
+          acc[3] = fmaf(w4.w, fmaxf(__uint_as_float(v[h + 3]), 0.f), acc[3]);
+        }
       }
+      const float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t->acc_empty[ab]);
@@ -270,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_hist_add(t->hist, score_key(score) >> 20, s < n_c);
     }
     epilogue_sync();
-    uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * 4096;
-    for (int i = row; i < 4096; i += 128)
+    uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
+    for (int i = et; i < kBins; i += kEpiThreads)
       if (t->hist[i]) atomicAdd(&gh[i], t->hist[i]);
   }
 
@@ -294,19 +308,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (!t->last || n_c <= a.k) return;
   __threadfence();
+  if (threadIdx.x >= kEpiThreads) return;
   {
     // every CTA's histogram atomics are done (counter above); L2 reads, all in flight
     const uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
-    constexpr int per = kBins / kThreads;
+    constexpr int per = kBins / kEpiThreads;
     uint32_t v[per];
 #pragma unroll
-    for (int u = 0; u < per; ++u) v[u] = __ldcg(gh + threadIdx.x + u * kThreads);
+    for (int u = 0; u < per; ++u) v[u] = __ldcg(gh + threadIdx.x + u * kEpiThreads);
 #pragma unroll
-    for (int u = 0; u < per; ++u) t->hist[threadIdx.x + u * kThreads] = v[u];
+    for (int u = 0; u < per; ++u) t->hist[threadIdx.x + u * kEpiThreads] = v[u];
   }
-  __syncthreads();
+  sync_threads_of<kEpiThreads, 3>();
   uint32_t n_gt1;
-  const int T1 = block_suffix_select<kThreads>(t->hist, static_cast<uint32_t>(a.k), &n_gt1, t->scratch);
+  const int T1 = block_suffix_select<kEpiThreads, 3>(t->hist, static_cast<uint32_t>(a.k), &n_gt1, t->scratch);
   if (threadIdx.x == 0) {
     cnt[4] = static_cast<uint32_t>(T1);
     cnt[5] = n_gt1;
@@ -348,7 +363,7 @@ template <int ROWB>
 int launch_tc(const IndexTcArgs& a, const CUtensorMap& keys, const CUtensorMap& qmap, cudaStream_t st) {
   using C = TcCfg<ROWB>;
   size_t smem = 1024 + C::STAGES * (C::STAGE_BYTES + C::SF_BYTES) + ((a.N * ROWB + 1023) & ~1023) + C::SF_BYTES +
-                sizeof(SmemTail) + a.N * 4;
+                sizeof(SmemTail) + 16 + a.N * 4;
   // keep at most two CTAs per SM so that their tensor-memory allocations always fit
   const size_t floor_bytes = a.tmem_cols > 256 ? 120 * 1024 : 80 * 1024;
   if (smem < floor_bytes) smem = floor_bytes;
@@ -360,6 +375,18 @@ int launch_tc(const IndexTcArgs& a, const CUtensorMap& keys, const CUtensorMap& 
 }
 
 }  // namespace
+
+bool encode_u8_rows(CUtensorMap* map, const void* base, int64_t rows, int row_bytes, int box_bytes, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int launch_index_scores_tc(const IndexTcArgs& a, const uint8_t* key_codes, const uint8_t* q_codes, cudaStream_t st) {
   const int rowb = a.Di / 2;

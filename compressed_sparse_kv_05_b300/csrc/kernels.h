@@ -2,6 +2,7 @@
 // blocks handed to the kernels and the kernels themselves.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -77,6 +78,9 @@ struct AttnArgs {
   int B, H, D, Dv, d_nope, d_rope, ratio, window, capacity, separate_v;
   int n_sel;               // top-k width (CSA) or 0 for HCA (every entry)
   int splits, rows_per_split;
+  int tile_rows;           // tensor-core kernel: rows per tile (32, 64 or 128)
+  int tiles_per_split;     // tensor-core kernel: tiles per CTA
+  int tma;                 // tensor-core kernel: the compressed rows arrive by TMA boxes (AttnMaps valid)
   float sm_scale;
   const uint16_t* q;
   const int32_t* topk;
@@ -85,18 +89,29 @@ struct AttnArgs {
   const uint16_t *k_rope, *v_rope, *win_k, *win_v;
   const int64_t* n_tokens;
   int32_t* status;
-  float* part_o;           // [B][H][splits][Dv] fp32 (CUDA-core kernel); f16 [B][splits][hg][D][64] (tensor-core)
+  float* part_o;           // [B][H][splits][Dv] fp32 (CUDA-core kernel); f16 [B][splits][hg][D][64], granules swizzled (tensor-core)
   float* part_lse;         // [B][H][splits]
   float* out;              // [B][H][Dv]
   float* lse;              // [B][H] or null
 };
+// Tensor maps of the contiguous compressed rows (HCA) for the tensor-core
+// kernel: boxes of tile_rows rows x 128 code bytes, x the last chunk's code
+// bytes, and x all RoPE bytes of a row.
+struct AttnMaps {
+  CUtensorMap nope, nope_tail, rope;
+};
 // launches the split kernel over (splits, B, head_groups) and the merge; returns a DSV4 status
 int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st);
-// the tensor-core split kernel (tiles of 128 rows, up to 64 heads per CTA) and the merge
+// the tensor-core split kernel (tiles of up to 128 rows, up to 64 heads per CTA) and the merge
 bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v);
+// whether the tensor-core kernel can take the compressed rows of this shape by TMA boxes
+bool attention_tc_tma_shape(int d_nope, int d_rope, int separate_v);
 int launch_attention_tc(const AttnArgs& a, int head_groups, cudaStream_t st);
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st);
 // merge of the tensor-core kernel's f16 partials ([B][splits][head groups][D][64])
 int launch_attention_merge_tc(const AttnArgs& a, int head_groups, cudaStream_t st);
+// 2D tensor map over `rows` rows of `row_bytes` bytes (uint8, no swizzle), box
+// of box_bytes x box_rows; false if the driver's encoder is unavailable or refuses
+bool encode_u8_rows(CUtensorMap* map, const void* base, int64_t rows, int row_bytes, int box_bytes, int box_rows);
 
 }  // namespace dsv4

@@ -11,11 +11,19 @@ namespace dsv4 {
 
 constexpr int kBins = 4096;   // 12-bit digit histograms
 
-// Suffix search over a 4096-bin histogram h (shared memory) with NT threads:
-// the largest bin T with sum_{j >= T} h[j] >= need (need >= 1 and at most the
-// histogram's total). Returns T in every thread and writes sum_{j > T} h[j] to
-// *above. `scratch` is NT / 32 + 2 words of shared memory.
-template <int NT>
+// Barrier among threads [0, NT): the whole block (BAR = 0) or named barrier BAR.
+template <int NT, int BAR>
+DSV4_DEV void sync_threads_of() {
+  if (BAR == 0) __syncthreads();
+  else asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT) : "memory");
+}
+
+// Suffix search over a 4096-bin histogram h (shared memory) with threads
+// [0, NT): the largest bin T with sum_{j >= T} h[j] >= need (need >= 1 and at
+// most the histogram's total). Returns T in every thread and writes
+// sum_{j > T} h[j] to *above. `scratch` is NT / 32 + 2 words of shared memory.
+// BAR = 0: NT is the whole block; otherwise the named barrier BAR is used.
+template <int NT, int BAR = 0>
 DSV4_DEV int block_suffix_select(const uint32_t* h, uint32_t need, uint32_t* above, uint32_t* scratch) {
   constexpr int per = kBins / NT;
   constexpr int nw = NT / 32;
@@ -34,7 +42,7 @@ DSV4_DEV int block_suffix_select(const uint32_t* h, uint32_t need, uint32_t* abo
     if (lane + o < 32) suf += v;
   }
   if (lane == 0) scratch[w] = suf;
-  __syncthreads();
+  sync_threads_of<NT, BAR>();
   uint32_t after = 0;
   for (int ww = w + 1; ww < nw; ++ww) after += scratch[ww];
   const uint32_t incl = suf + after;   // bins >= t * per
@@ -51,10 +59,10 @@ DSV4_DEV int block_suffix_select(const uint32_t* h, uint32_t need, uint32_t* abo
       acc += c;
     }
   }
-  __syncthreads();
+  sync_threads_of<NT, BAR>();
   const int bin = static_cast<int>(scratch[nw]);
   *above = scratch[nw + 1];
-  __syncthreads();
+  sync_threads_of<NT, BAR>();
   return bin;
 }
 

@@ -239,6 +239,12 @@ def test_index_topk_full_size_planted(layer):
             assert set(g_topk[b].tolist()) == set(sorted(planted)[:layer.topk])
         else:
             assert planted <= set(g_topk[b].tolist())
+    # the attention over that selection (32-row tiles at batch 1 and 2)
+    g_out, g_lse = _decode(desc, cache, layer, dec["q"], to_dev(g_topk), layer.topk)
+    for b in range(layer.batch):
+        o_out, o_lse = _oracle_attend_planes(layer, planes[b], dec["q"][b], g_topk[b])
+        assert row_rel_err(g_out[b], o_out).max() <= TOL
+        assert np.abs(g_lse[b] - o_lse).max() <= 1e-3
 
 
 def test_topk_ties_go_to_lower_index():
@@ -307,6 +313,65 @@ def test_hca_decode_hca_128k():
     g_out, g_lse = _decode(desc, cache, layer, dec["q"])
     assert row_rel_err(g_out[0], o_out).max() <= TOL
     assert np.abs(g_lse[0] - o_lse).max() <= 1e-3
+
+
+def _oracle_attend_planes(layer, p, q, sel):
+    args = (layer.n_tokens, layer.ratio, layer.window, p["k_nope"], p["k_scale"], p["k_rope"], p["ring_k"])
+    if sel is None:
+        return O.hca_attend(q, np.float32(layer.sm_scale), *args)
+    return O.csa_attend(q, np.float32(layer.sm_scale), sel, *args)
+
+
+@pytest.mark.parametrize("n_tokens", [128 * 1000 + 77, 128 * 257, 128 * 40 + 5])
+def test_hca_decode_stack_shape(n_tokens):
+    """D = 512 (448 FP8 + 64 RoPE), 64 heads, K = V, four sequences as in the
+    decode step: compressed rows by TMA boxes over several tiles per CTA, a
+    partial last tile, the window tile; small contexts take 64- and 32-row tiles."""
+    layer = W.scaled(W.STACK_HCA, n_tokens=n_tokens)
+    planes = oracle_direct_planes(layer, "hcastack", 1, range(layer.batch))
+    desc, cache = gpu_cache_from_planes(layer, planes)
+    dec = synth.decode_inputs("hcastack", 1, layer)
+    g_out, g_lse = _decode(desc, cache, layer, dec["q"])
+    assert dsv4.dsv4_read_status(cache) == 0
+    for b in range(layer.batch):
+        o_out, o_lse = _oracle_attend_planes(layer, planes[b], dec["q"][b], None)
+        assert row_rel_err(g_out[b], o_out).max() <= TOL
+        assert np.abs(g_lse[b] - o_lse).max() <= 1e-3
+
+
+def test_hca_decode_full_size_decode_step():
+    """The decode step's HCA layer at full size (the benchmark's launch):
+    four sequences of 2^20 tokens, 8192 compressed entries each."""
+    layer = W.STACK_HCA
+    planes = oracle_direct_planes(layer, "hcafull", 1, range(layer.batch), processes=4)
+    desc, cache = gpu_cache_from_planes(layer, planes, extra=64)
+    dec = synth.decode_inputs("hcafull", 1, layer)
+    g_out, g_lse = _decode(desc, cache, layer, dec["q"])
+    assert dsv4.dsv4_read_status(cache) == 0
+    for b in range(layer.batch):
+        o_out, o_lse = _oracle_attend_planes(layer, planes[b], dec["q"][b], None)
+        assert row_rel_err(g_out[b], o_out).max() <= TOL
+        assert np.abs(g_lse[b] - o_lse).max() <= 1e-3
+
+
+@pytest.mark.parametrize("n_tokens", [4 * 3000 + 3, 4 * 400])
+def test_csa_decode_stack_shape_chained(n_tokens):
+    """D = 512 CSA with four sequences (tiles of 32 rows): index_topk ->
+    csa_decode; the selection is checked against the oracle's, the attention
+    against the oracle's attention over the same selection."""
+    layer = W.scaled(W.STACK_CSA, n_tokens=n_tokens)
+    planes = oracle_direct_planes(layer, "csastack", 0, range(layer.batch))
+    desc, cache = gpu_cache_from_planes(layer, planes)
+    dec = synth.decode_inputs("csastack", 0, layer)
+    g_topk, _ = _index(desc, cache, layer, dec, layer.topk)
+    g_out, g_lse = _decode(desc, cache, layer, dec["q"], to_dev(g_topk), layer.topk)
+    assert dsv4.dsv4_read_status(cache) == 0
+    for b in range(layer.batch):
+        o_scores = O.index_scores(planes[b]["idx_codes"], planes[b]["idx_scales"], dec["q_idx"][b], dec["w"][b])
+        check_topk(g_topk[b], o_scores, O.topk_blocks(o_scores, layer.topk), layer.topk)
+        o_out, o_lse = _oracle_attend_planes(layer, planes[b], dec["q"][b], g_topk[b])
+        assert row_rel_err(g_out[b], o_out).max() <= TOL
+        assert np.abs(g_lse[b] - o_lse).max() <= 1e-3
 
 
 @pytest.mark.parametrize("n", [0, 1, 3, 4, 5, 127, 128, 129, 700])
