@@ -227,25 +227,26 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
 // groups][D][64 heads] (normalised; in each 128-byte row of a dim d the
 // 16-byte granule of heads 8q .. 8q + 7 sits at granule q ^ (d & 7)),
 // log-sum-exps fp32 [B][H][splits].
-// grid (B * head groups, D / 8), block 512: 8 dims x 64 heads per CTA; thread
-// t takes split group t / 64 (splits s = t / 64 mod 8), dim t / 8 % 8 and
+// grid (B * head groups, D / 8), block 256: 8 dims x 64 heads per CTA; thread
+// t takes split group t / 64 (splits s = t / 64 mod 4), dim t / 8 % 8 and
 // heads 8 (t % 8) .. + 7. Per pass of up to 64 splits every thread issues its
-// partial loads while the CTA stages the log-sum-exps in shared memory (one
-// round trip); the split weights exp(lse - max) / sum are then computed once
-// per CTA in place, each thread accumulates its splits, and the eight split
-// groups are summed in shared memory. With more than 64 splits the passes
-// rescale the running result (online softmax over passes).
-__global__ void __launch_bounds__(512, 2) attn_merge_tc_kernel(AttnArgs a) {
+// partial loads and its share of the log-sum-exps at once (one round trip);
+// the split weights exp(lse - max) are computed once per CTA, each thread
+// accumulates its splits and the four split groups are summed in shared
+// memory. With more than 64 splits the passes rescale the running result.
+__global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
+  constexpr int kT = 256;
   constexpr int kS = 64;   // splits per pass
-  constexpr int kSg = 8;   // split groups
+  constexpr int kSg = 4;   // split groups
   constexpr int kU = kS / kSg;
+  constexpr int kL = 64 * kS / kT;   // log-sum-exps each thread stages per pass
   pdl_trigger();
   pdl_wait();
   const int hgs = (a.H + 63) / 64;
   const int b = blockIdx.x / hgs, hg = blockIdx.x % hgs;
   const int h0 = hg * 64;
   const int hcount = a.H - h0 < 64 ? a.H - h0 : 64;
-  __shared__ float s_w[64][kS + 1];          // log-sum-exps, then weights
+  __shared__ float s_w[64][kS + 1];             // log-sum-exps, then weights
   __shared__ float s_m[64], s_l[64], s_r[64];   // running max and sum per head, rescale of this pass
   __shared__ float s_acc[kSg][64][9];
   const int t = threadIdx.x;
@@ -267,34 +268,41 @@ __global__ void __launch_bounds__(512, 2) attn_merge_tc_kernel(AttnArgs a) {
   for (int s0 = 0; s0 < a.splits; s0 += kS) {
     const int ns = a.splits - s0 < kS ? a.splits - s0 : kS;
     uint4 v[kU];
+    float lv[kL];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int s = sg + kSg * u;
       v[u] = s < ns ? __ldcg(reinterpret_cast<const uint4*>(part + (s0 + s) * sstride)) : make_uint4(0, 0, 0, 0);
     }
-    for (int i = t; i < 64 * kS; i += blockDim.x) {
-      const int h = i >> 6, s = i & (kS - 1);
-      s_w[h][s] = h < hcount && s < ns ? lse0[static_cast<int64_t>(h) * a.splits + s0 + s] : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kL; ++u) {
+      const int i = t + u * kT, h = i >> 6, s = i & (kS - 1);
+      lv[u] = h < hcount && s < ns ? __ldcg(lse0 + static_cast<int64_t>(h) * a.splits + s0 + s) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < kL; ++u) {
+      const int i = t + u * kT;
+      s_w[i >> 6][i & (kS - 1)] = lv[u];
     }
     __syncthreads();
     {
-      // head t / 8: this pass's max and sum of exp (eight threads, eight splits each)
-      const int h = t >> 3, part8 = t & 7;
+      // head t / 4: this pass's max and sum of exp (four threads, sixteen splits each)
+      const int h = t >> 2, part4 = t & 3;
       float mx = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx = fmaxf(mx, s_w[h][part8 + 8 * u]);
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      for (int u = 0; u < 16; ++u) mx = fmaxf(mx, s_w[h][part4 + 4 * u]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float mo = s_m[h], mn = fmaxf(mo, mx);
       float sum = 0.f;
       if (mn != -INFINITY) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) sum += __expf(s_w[h][part8 + 8 * u] - mn);   // exp(-inf) = 0
+        for (int u = 0; u < 16; ++u) sum += __expf(s_w[h][part4 + 4 * u] - mn);   // exp(-inf) = 0
       }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
       __syncthreads();
-      if (part8 == 0) {
+      if (part4 == 0) {
         const float r = mo == -INFINITY ? 0.f : __expf(mo - mn);
         s_r[h] = r;
         s_l[h] = s_l[h] * r + sum;
@@ -302,9 +310,9 @@ __global__ void __launch_bounds__(512, 2) attn_merge_tc_kernel(AttnArgs a) {
       }
       // weights relative to the running max (a split without rows gets 0)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float x = s_w[h][part8 + 8 * u];
-        s_w[h][part8 + 8 * u] = x == -INFINITY ? 0.f : __expf(x - mn);
+      for (int u = 0; u < 16; ++u) {
+        const float x = s_w[h][part4 + 4 * u];
+        s_w[h][part4 + 4 * u] = x == -INFINITY ? 0.f : __expf(x - mn);
       }
     }
     __syncthreads();
@@ -329,15 +337,13 @@ __global__ void __launch_bounds__(512, 2) attn_merge_tc_kernel(AttnArgs a) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) s_acc[sg][hq + i][dl] = acc[i];
   __syncthreads();
-  {
-    const int r = t >> 3, dd = t & 7;   // head r, dim dd of the CTA's 8
+  for (int o = t; o < 64 * 8; o += kT) {
+    const int r = o >> 3, dd = o & 7;   // head r, dim dd of the CTA's 8
     if (r < hcount) {
-      float o = 0.f;
-#pragma unroll
-      for (int g = 0; g < kSg; ++g) o += s_acc[g][r][dd];
+      const float sum = (s_acc[0][r][dd] + s_acc[1][r][dd]) + (s_acc[2][r][dd] + s_acc[3][r][dd]);
       const float L = s_l[r];
       const int dg = blockIdx.y * 8 + dd;
-      if (dg < a.D) a.out[(static_cast<int64_t>(b) * a.H + h0 + r) * a.Dv + dg] = L > 0.f ? o / L : 0.f;
+      if (dg < a.D) a.out[(static_cast<int64_t>(b) * a.H + h0 + r) * a.Dv + dg] = L > 0.f ? sum / L : 0.f;
       if (blockIdx.y == 0 && dd == 0 && a.lse)
         a.lse[static_cast<int64_t>(b) * a.H + h0 + r] = L > 0.f ? s_m[r] + logf(L) : -INFINITY;
     }
@@ -379,7 +385,7 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
 }
 
 int launch_attention_merge_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
-  return launch_pdl(attn_merge_tc_kernel, dim3(a.B * head_groups, (a.D + 7) / 8), dim3(512), 0, st, a);
+  return launch_pdl(attn_merge_tc_kernel, dim3(a.B * head_groups, (a.D + 7) / 8), dim3(256), 0, st, a);
 }
 
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st) {

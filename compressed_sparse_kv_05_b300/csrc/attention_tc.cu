@@ -359,6 +359,19 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
   }
 }
 
+// One producer thread: the TMA boxes of chunk c of compressed tile tl
+// (contiguous rows) into the chunk's region, completing on xland[c].
+DSV4_DEV void issue_tma_chunk(const AttnArgs& a, const AttnMaps& maps, int b, const Tile& tl, int c,
+                              unsigned char* xk, uint64_t* xland) {
+  const int y = static_cast<int>(static_cast<int64_t>(b) * a.capacity + tl.r0);
+  const ChunkSplit cs = chunk_split(a, c);
+  unsigned char* xc = xk + c * kChunkBytes;
+  tc::mbar_arrive_expect_tx(&xland[c], static_cast<uint32_t>(a.tile_rows * (cs.nn + cs.rb)));
+  if (cs.nn == 128) tc::tma_load_2d(xc, &maps.nope, &xland[c], c * 128, y);
+  else if (cs.nn > 0) tc::tma_load_2d(xc, &maps.nope_tail, &xland[c], c * 128, y);
+  if (cs.rb > 0) tc::tma_load_2d(xc + cs.rope_off, &maps.rope, &xland[c], 0, y);
+}
+
 // In-warp reduce-scatter of 32 values per lane (one per head): afterwards v[0]
 // holds the max (or sum) over the warp's 32 lanes for head `lane`. Each step
 // keeps half of the values and takes the other half from the partner lane.
@@ -445,6 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   volatile int* abort = &t->abort;
 
   if (warp == 0) tc::tmem_alloc(&t->taddr, cols);
+  const Tile first = tile_at(a, rs, tile0);
+  const bool first_tma = !SEP && a.tma && !first.win;
   if (threadIdx.x == 32) {
     for (int c = 0; c < kMaxChunks; ++c) {
       tc::mbar_init(&t->xland[c], 1);
@@ -460,28 +475,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     tc::fence_mbar_init();
   }
   if (threadIdx.x < kHeads) t->m_used[threadIdx.x] = -INFINITY;
-  {
-    // row sources of every tile of the split (CSA: one round trip for the top-k indices)
-    int32_t sr[2];
-    float ks[2], vs[2];
+  // Row sources of every tile of the split (CSA: one round trip for the top-k
+  // indices) and their scales. The small loads the first conversions need
+  // (query, scales) go out before the tile's bulk data, so that they are not
+  // queued behind it: for contiguous rows the scale loads leave at once and
+  // the first tile's boxes after the first barrier; gathered rows leave
+  // together with their scale loads once the sources are known.
+  int32_t sr[2];
+  float ks[2] = {0.f, 0.f}, vs[2] = {0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = threadIdx.x + k * kThreads, tt = i >> 7;
-      sr[k] = tt < nt ? row_source(a, rs, b, tile_at(a, rs, tile0 + tt), i & (kRows - 1)) : -1;
-    }
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + k * kThreads, tt = i >> 7;
+    sr[k] = tt < nt ? row_source(a, rs, b, tile_at(a, rs, tile0 + tt), i & (kRows - 1)) : -1;
+    if (tt < nt) t->src[i] = sr[k];
+  }
+  if (a.n_sel == 0) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       ks[k] = sr[k] >= 0 ? __ldg(a.k_scale + sr[k]) : 0.f;
       vs[k] = SEP && sr[k] >= 0 ? __ldg(a.v_scale + sr[k]) : 0.f;
     }
+  }
+  __syncthreads();
+  if (first_tma && threadIdx.x == 32)
+    for (int c = 0; c < nch; ++c) issue_tma_chunk(a, maps, b, first, c, xk, t->xland);
+  if (!first_tma && warp >= 2) {
+    const int wtid = threadIdx.x - 64;
+    const int rc = (first.cnt + 15) & ~15;
+    for (int c = 0; c < nch; ++c) {
+      issue_chunk(a, b, first.win, t->src, c, rc, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, wtid);
+      if (SEP) issue_chunk(a, b, first.win, t->src, c, rc, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, wtid);
+      cp_async_commit();
+    }
+  }
+  if (a.n_sel > 0) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int i = threadIdx.x + k * kThreads;
-      if ((i >> 7) < nt) {
-        t->src[i] = sr[k];
-        t->sk[i] = ks[k];
-        if (SEP) t->sv[i] = vs[k];
-      }
+      ks[k] = sr[k] >= 0 ? __ldg(a.k_scale + sr[k]) : 0.f;
+      vs[k] = SEP && sr[k] >= 0 ? __ldg(a.v_scale + sr[k]) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    if ((i >> 7) < nt) {
+      t->sk[i] = ks[k];
+      if (SEP) t->sv[i] = vs[k];
     }
   }
   tc::tc_fence_before();
@@ -537,32 +576,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (!SEP && a.tma) {
       const int64_t row_base = static_cast<int64_t>(b) * a.capacity;
       if (lane == 0) {
-        int issued = 0;
-        for (int tt = 0; tt < nt; ++tt) {
+        // boxes issued per chunk (the first tile's went out before the setup)
+        int issued[kMaxChunks];
+        for (int c = 0; c < kMaxChunks; ++c) issued[c] = first_tma ? 1 : 0;
+        bool ok = true;
+        for (int tt = first_tma ? 1 : 0; ok && tt < nt; ++tt) {
           const Tile tl = tile_at(a, rs, tile0 + tt);
           if (tl.win) break;   // window tiles come last and go by cp.async
-          const int y = static_cast<int>(row_base + tl.r0);
-          bool ok = true;
           for (int c = 0; c < nch; ++c) {
-            if (tt > 0 && !(ok = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort))) break;
-            const ChunkSplit cs = chunk_split(a, c);
-            unsigned char* xc = xk + c * kChunkBytes;
-            tc::mbar_arrive_expect_tx(&t->xland[c], static_cast<uint32_t>(a.tile_rows * (cs.nn + cs.rb)));
-            if (cs.nn == 128) tc::tma_load_2d(xc, &maps.nope, &t->xland[c], c * 128, y);
-            else if (cs.nn > 0) tc::tma_load_2d(xc, &maps.nope_tail, &t->xland[c], c * 128, y);
-            if (cs.rb > 0) tc::tma_load_2d(xc + cs.rope_off, &maps.rope, &t->xland[c], 0, y);
+            if (!(ok = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort))) break;
+            issue_tma_chunk(a, maps, b, tl, c, xk, t->xland);
+            ++issued[c];
           }
-          if (!ok) break;
-          ++issued;
         }
         // every box issued must land before the CTA's shared memory goes away
-        if (issued > 0)
-          for (int c = 0; c < nch; ++c) tc::mbar_wait_drain(&t->xland[c], (issued - 1) & 1);
-      } else if (nt > 1) {
-        // later tiles' compressed rows into L2 (the first tile's boxes are on their way)
+        for (int c = 0; c < nch; ++c)
+          if (issued[c] > 0) tc::mbar_wait_drain(&t->xland[c], (issued[c] - 1) & 1);
+      } else if (nt > 1 && (lane == 1 || lane == 2)) {
+        // later tiles' compressed rows into L2 (the first tile's boxes are on
+        // their way); after the query has arrived, so that it is not queued
+        // behind them
         const Tile t1 = tile_at(a, rs, tile0 + 1);
         const Tile tl = tile_at(a, rs, tile0 + nt - 1);
-        if (!t1.win) {
+        if (!t1.win && tc::mbar_wait(&t->qready, 0, abort)) {
           const int64_t e0 = row_base + t1.r0;
           const int64_t n = (tl.win ? rs.n_main : tl.r0 + tl.cnt) - t1.r0;
           if (lane == 1) prefetch_range(a.k_nope + e0 * a.d_nope, n * a.d_nope);
@@ -582,17 +618,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const float c2 = a.sm_scale * 1.4426950408889634f;
     float mx = 0.f;
 
-    // tile 0's gathered rows: all copies in flight before the query work
-    const Tile first = tile_at(a, rs, tile0);
-    const bool first_cp = SEP || !a.tma || first.win;
-    if (first_cp) {
-      const int rc = (first.cnt + 15) & ~15;
-      for (int c = 0; c < nch; ++c) {
-        issue_chunk(a, b, first.win, src, c, rc, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, wtid);
-        if (SEP) issue_chunk(a, b, first.win, src, c, rc, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, wtid);
-        cp_async_commit();
-      }
-    }
     {
       // the query, bf16 -> f16 into the K-major operand (heads beyond H zero)
       float qmax = 0.f;

@@ -57,7 +57,10 @@ constexpr int kSelThreads = 512;
 constexpr int kMaxK = 2048;
 constexpr int kScanItems = 8;        // scores each thread loads per round trip
 constexpr int kCandCache = 4096;     // candidates the resolving CTA keeps in shared memory
-constexpr int kTopkDynSmem = kCandCache * 8;   // candidate cache
+constexpr int kRegCand = 8;         // candidates per thread kept in registers by the resolving CTA
+constexpr int kDigitPasses = 4;     // 8-bit index digits (indices < 2^32)
+constexpr int kBitmapWords = 10240; // bitmap emission of the selection: n_c <= 327680
+constexpr int kTopkDynSmem = (kCandCache * 8 > kBitmapWords * 4 ? kCandCache * 8 : kBitmapWords * 4);
 
 // Append `flag`-ed values of a warp to list[*counter ...] with one atomic per
 // warp; positions at or beyond `cap` are dropped.
@@ -166,6 +169,119 @@ DSV4_DEV void load_to_smem(T* dst, const T* src, uint32_t n) {
 
 }  // namespace
 
+// The resolving CTA's work when every candidate fits in registers (up to
+// kRegCand per thread): T2 from the second-level histogram; inside bin
+// (T1, T2) the need2 best by (low 8 key bits desc, index asc), found by
+// 8-bit digit selections over the candidates held in registers; the k blocks
+// are emitted in ascending order from a bitmap of the selection (n_c up to
+// 32 * kBitmapWords), else by a bitonic sort.
+DSV4_DEV void resolve_in_registers(int k, int64_t n_c, uint32_t n_above, uint32_t n_cand,
+                                   uint32_t need1, const uint32_t* hist2, const int32_t* above,
+                                   const uint64_t* cand, int32_t* out, uint32_t* h, int32_t* fin,
+                                   uint32_t (*h8)[256], uint32_t* scratch, uint64_t* dyn, uint32_t* s_nfin,
+                                   uint32_t* s_d, uint32_t* s_rem) {
+  const int t = threadIdx.x;
+  uint64_t cv[kRegCand];
+  uint32_t hv[kBins / kSelThreads];
+#pragma unroll
+  for (int u = 0; u < kRegCand; ++u) {
+    const uint32_t i = t + u * kSelThreads;
+    cv[u] = i < n_cand ? __ldcg(cand + i) : 0ull;
+  }
+#pragma unroll
+  for (int u = 0; u < kBins / kSelThreads; ++u) hv[u] = __ldcg(hist2 + t + u * kSelThreads);
+  for (uint32_t i = t; i < n_above; i += kSelThreads) fin[i] = __ldcg(above + i);
+#pragma unroll
+  for (int u = 0; u < kBins / kSelThreads; ++u) h[t + u * kSelThreads] = hv[u];
+  for (int i = t; i < (kDigitPasses + 1) * 256; i += kSelThreads) (&h8[0][0])[i] = 0;
+  if (t == 0) *s_nfin = n_above;
+  __syncthreads();
+  uint32_t n_gt2 = 0;
+  const uint32_t T2 = need1 ? static_cast<uint32_t>(block_suffix_select<kSelThreads>(h, need1, &n_gt2, scratch)) : 0xFFFFu;
+  const uint32_t need2 = need1 - n_gt2;
+  const uint32_t n_eq2 = T2 < static_cast<uint32_t>(kBins) ? h[T2] : 0u;
+  uint32_t d8 = 0, thr = 0;
+  if (need2 > 0 && need2 < n_eq2) {
+#pragma unroll
+    for (int u = 0; u < kRegCand; ++u) {
+      const uint32_t key = static_cast<uint32_t>(cv[u] >> 32);
+      warp_hist_add(h8[0], key & 0xFF, t + u * kSelThreads < n_cand && ((key >> 8) & 0xFFF) == T2);
+    }
+    __syncthreads();
+    if (t < 32) warp_digit_select(h8[0], need2, s_d, s_rem);
+    __syncthreads();
+    d8 = *s_d;
+    uint32_t r = need2 - *s_rem;   // lowest indices to take among the keys with low8 == d8
+    int nbits = 1;
+    while (nbits < 32 && (static_cast<int64_t>(1) << nbits) < n_c) ++nbits;
+    const int passes = (nbits + 7) / 8;
+    uint32_t prefix = 0;
+    for (int p = 0; p < passes; ++p) {
+      const int shift = 8 * (passes - 1 - p);
+#pragma unroll
+      for (int u = 0; u < kRegCand; ++u) {
+        const uint32_t key = static_cast<uint32_t>(cv[u] >> 32), idx = static_cast<uint32_t>(cv[u]);
+        const bool in = t + u * kSelThreads < n_cand && ((key >> 8) & 0xFFF) == T2 && (key & 0xFF) == d8 &&
+                        (p == 0 || (static_cast<uint64_t>(idx) >> (shift + 8)) == prefix);
+        // reversed digit: the largest reversed digit with enough keys at or above it is the smallest digit
+        warp_hist_add(h8[1 + p], 255 - ((idx >> shift) & 0xFF), in);
+      }
+      __syncthreads();
+      if (t < 32) warp_digit_select(h8[1 + p], r, s_d, s_rem);
+      __syncthreads();
+      prefix = (prefix << 8) | (255 - *s_d);
+      r -= *s_rem;
+    }
+    thr = prefix;   // exactly the wanted number of indices with low8 == d8 are <= thr
+  }
+#pragma unroll
+  for (int u = 0; u < kRegCand; ++u) {
+    const uint32_t key = static_cast<uint32_t>(cv[u] >> 32), idx = static_cast<uint32_t>(cv[u]);
+    const uint32_t b2 = (key >> 8) & 0xFFF;
+    const bool valid = t + u * kSelThreads < n_cand;
+    bool take = valid && need1 > 0 && b2 > T2;
+    if (valid && b2 == T2 && need2 > 0)
+      take = need2 >= n_eq2 || (key & 0xFF) > d8 || ((key & 0xFF) == d8 && idx <= thr);
+    warp_append_i32(take, static_cast<int32_t>(idx), s_nfin, fin, static_cast<uint32_t>(k));
+  }
+  __syncthreads();
+  const uint32_t nf = *s_nfin < static_cast<uint32_t>(k) ? *s_nfin : static_cast<uint32_t>(k);
+  const int64_t words = (n_c + 31) / 32;
+  if (words <= kBitmapWords) {
+    // the selected blocks as bits, then emitted in ascending order
+    uint32_t* bm = reinterpret_cast<uint32_t*>(dyn);
+    const int per = static_cast<int>((words + kSelThreads - 1) / kSelThreads);
+    for (int i = t; i < per * kSelThreads; i += kSelThreads) bm[i] = 0;
+    __syncthreads();
+    for (uint32_t i = t; i < nf; i += kSelThreads) {
+      const uint32_t x = static_cast<uint32_t>(fin[i]);
+      atomicOr(&bm[x >> 5], 1u << (x & 31));
+    }
+    __syncthreads();
+    uint32_t cntw = 0;
+    for (int q = 0; q < per; ++q) cntw += __popc(bm[t * per + q]);
+    uint32_t tot;
+    uint32_t pos = block_excl_scan_packed(cntw, &tot, scratch);
+    for (int q = 0; q < per; ++q) {
+      uint32_t wd = bm[t * per + q];
+      while (wd) {
+        const int bit = __ffs(wd) - 1;
+        wd &= wd - 1;
+        if (pos < static_cast<uint32_t>(k)) out[pos] = (t * per + q) * 32 + bit;
+        ++pos;
+      }
+    }
+    for (uint32_t i = tot + t; i < static_cast<uint32_t>(k); i += kSelThreads) out[i] = -1;   // inconsistent input only
+    return;
+  }
+  int P = 1;
+  while (P < k) P <<= 1;
+  for (int i = t + static_cast<int>(nf); i < P; i += kSelThreads) fin[i] = 0x7FFFFFFF;
+  __syncthreads();
+  block_sort_asc(fin, P);
+  for (int i = t; i < k; i += kSelThreads) out[i] = i < static_cast<int>(nf) ? fin[i] : -1;
+}
+
 // Top-k selection, grid (sel_ctas, B), block 512. The scoring kernel has
 // histogrammed the top 12 bits of every score key and its last CTA stored the
 // threshold bin T1 (the bin holding the k-th largest key) and the number of keys
@@ -179,9 +295,10 @@ DSV4_DEV void load_to_smem(T* dst, const T* src, uint32_t n) {
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   __shared__ uint32_t h[kBins];
   __shared__ int32_t fin[kMaxK];
+  __shared__ uint32_t h8[kDigitPasses + 1][256];   // resolution histograms of 8-bit digits
   __shared__ uint32_t scratch[kSelThreads / 32 + 2];
   __shared__ uint32_t s_nfin, s_last, s_d, s_rem, s_base[2];
-  extern __shared__ uint64_t dyn[];   // candidate cache
+  extern __shared__ uint64_t dyn[];   // candidate cache, or the bitmap of the selected blocks
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
@@ -249,12 +366,16 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   }
   for (int i = threadIdx.x; i < kBins; i += blockDim.x)
     if (h[i]) atomicAdd(&hist2[i], h[i]);
-  __threadfence();
+  // the CTA's appends and histogram atomics precede its completion count (the
+  // fence after the barrier is cumulative over the CTA's writes)
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&cnt[2], 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&cnt[2], 1u) == gridDim.x - 1;
+    if (s_last) __threadfence();
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
   // ---- the last CTA of sequence b resolves the boundary
   uint32_t n_above = __ldcg(&cnt[0]);
@@ -262,6 +383,11 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   if (n_above > static_cast<uint32_t>(k)) n_above = k;                      // only on inconsistent input
   if (n_cand > static_cast<uint32_t>(a.capacity)) n_cand = a.capacity;
   const uint32_t need1 = static_cast<uint32_t>(k) - n_above;                 // taken from cand
+  if (n_cand <= static_cast<uint32_t>(kRegCand * kSelThreads)) {
+    resolve_in_registers(k, n_c, n_above, n_cand, need1, hist2, above, cand, out, h, fin, h8, scratch, dyn,
+                         &s_nfin, &s_d, &s_rem);
+    return;
+  }
   load_to_smem(h, hist2, kBins);
   load_to_smem(fin, above, n_above);
   if (threadIdx.x == 0) s_nfin = n_above;

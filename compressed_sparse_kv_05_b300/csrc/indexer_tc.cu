@@ -304,10 +304,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     __threadfence();
     const int active = (tiles + per - 1) / per;   // CTAs of this sequence that had tiles
     t->last = atomicAdd(&cnt[3], 1u) == static_cast<uint32_t>(active - 1);
+    if (t->last) __threadfence();
   }
   __syncthreads();
   if (!t->last || n_c <= a.k) return;
-  __threadfence();
   if (threadIdx.x >= kEpiThreads) return;
   {
     // every CTA's histogram atomics are done (counter above); L2 reads, all in flight

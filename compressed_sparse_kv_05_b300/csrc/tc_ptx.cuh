@@ -49,6 +49,7 @@ DSV4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase of `bar` with parity `parity` to complete. Gives up (and
 // raises *abort) after kWaitNs, or as soon as another warp raised it.
 DSV4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;   // the common case: no clock read
   const uint64_t t0 = now_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -63,6 +64,7 @@ DSV4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
 // Wait without an abort flag (draining copies or MMAs before shared or tensor
 // memory is released); gives up after kWaitNs.
 DSV4_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = now_ns();
   while (!mbar_try_wait(bar, parity))
     if (now_ns() - t0 > kWaitNs) return false;
