@@ -261,15 +261,16 @@ DSV4_DEV void resolve_in_registers(int k, int64_t n_c, uint32_t n_above, uint32_
     uint32_t cntw = 0;
     for (int q = 0; q < per; ++q) cntw += __popc(bm[t * per + q]);
     uint32_t tot;
-    uint32_t pos = block_excl_scan_packed(cntw, &tot, scratch);
-    for (int q = 0; q < per; ++q) {
-      uint32_t wd = bm[t * per + q];
-      while (wd) {
-        const int bit = __ffs(wd) - 1;
-        wd &= wd - 1;
-        if (pos < static_cast<uint32_t>(k)) out[pos] = (t * per + q) * 32 + bit;
-        ++pos;
-      }
+    const uint32_t pos = block_excl_scan_packed(cntw, &tot, scratch);
+    h[t] = pos;   // set bits in the words of threads before t
+    __syncthreads();
+    // every selected block to its rank: set bits before it in ascending order
+    for (uint32_t i = t; i < nf; i += kSelThreads) {
+      const uint32_t x = static_cast<uint32_t>(fin[i]), w = x >> 5, owner = w / per;
+      uint32_t r = h[owner];
+      for (uint32_t v = owner * per; v < w; ++v) r += __popc(bm[v]);
+      r += __popc(bm[w] & ((1u << (x & 31)) - 1u));
+      if (r < static_cast<uint32_t>(k)) out[r] = static_cast<int32_t>(x);
     }
     for (uint32_t i = tot + t; i < static_cast<uint32_t>(k); i += kSelThreads) out[i] = -1;   // inconsistent input only
     return;
