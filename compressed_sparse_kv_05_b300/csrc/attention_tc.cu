@@ -82,8 +82,8 @@ struct TcTail {
   uint32_t taddr;
   int abort;
   int32_t src[kMaxTiles * kRows];   // row sources of every tile of the split (see row_source), 128 per tile
-  float sk[kMaxTiles * kRows];      // key (or shared entry) scale of every row, 0 for others
-  float sv[kMaxTiles * kRows];      // value scale (separate V)
+  uint32_t sk[kMaxTiles * kRows];   // key (or shared entry) scale * 2^8 of every row as f16x2, 0 for others
+  uint32_t sv[kMaxTiles * kRows];   // the same for the value scale (separate V)
   float m_used[kHeads];             // running max per head, log2 domain
   float alpha[kHeads];
   float lsum[kHeads];
@@ -282,27 +282,52 @@ DSV4_DEV void store_group(unsigned char* xc, int j, int g, uint4 h) {
 // Dequantise chunk c of a tile in place: every worker first reads the raw
 // bytes of its items (8-dim groups, see chunk_item), then, after a barrier of
 // the workers, writes them as f16 into the two 64-dim swizzle atoms of the
-// chunk. Rows without a source read nothing and become zeros (their scale is
-// 0). Tracks the largest |value| that must fit f16 (range check). The
-// conversions run without per-item branches whenever a warp's items are all
-// codes or all bf16, so the items of a thread overlap.
-DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, const float* sc, int c, int rc,
+// chunk. `s2` holds each row's scale * 2^8 as f16x2 (0 for rows without a
+// source). Rows without a source read stale bytes, which are discarded: they
+// become zeros. Each warp's items are all codes or all bf16 (the layouts of
+// the 448 + 64 entry and of window tokens), so the items of a thread run
+// without per-item branches; other layouts take the general path.
+DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, const uint32_t* s2, int c, int rc,
                             unsigned char* xc, int wtid, float& mx) {
   const ChunkSplit cs = chunk_split(a, c);
   const int nn = win ? 128 : cs.nn;   // window rows: the item layout of a full chunk
   const int n_items = rc * 16;
+  const int warp_q = wtid >> 5;       // items of a thread share the parity of i >> 5 (kWorkers is a multiple of 64)
+  const bool all_codes = !win && (cs.nn == 128 || (cs.nn == 64 && (warp_q & 1) == 0));
+  const bool all_bf16 = win || cs.nn == 0 || (cs.nn == 64 && (warp_q & 1) == 1);
   uint4 raw[kItems];
+  if (all_codes) {
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int i = wtid + it * kWorkers;
-    int j, g;
-    chunk_item(nn, i, j, g);
-    raw[it] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < n_items) {
-      const int32_t sr = src[j];
-      if (win) {
-        if (sr <= -2) raw[it] = *reinterpret_cast<const uint4*>(xc + j * 256 + 16 * g);
-      } else if (sr >= 0) {
+    for (int it = 0; it < kItems; ++it) {
+      const int i = wtid + it * kWorkers;
+      int j, g;
+      chunk_item(nn, i, j, g);
+      raw[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < n_items) {
+        const uint2 w = *reinterpret_cast<const uint2*>(xc + j * cs.nn + 8 * g);
+        raw[it].x = w.x;
+        raw[it].y = w.y;
+      }
+    }
+  } else if (all_bf16) {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int i = wtid + it * kWorkers;
+      int j, g;
+      chunk_item(nn, i, j, g);
+      raw[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < n_items)
+        raw[it] = *reinterpret_cast<const uint4*>(win ? xc + j * 256 + 16 * g
+                                                      : xc + cs.rope_off + j * cs.rb + 2 * (8 * g - cs.nn));
+    }
+  } else {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int i = wtid + it * kWorkers;
+      int j, g;
+      chunk_item(nn, i, j, g);
+      raw[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < n_items && src[j] >= 0) {
         if (8 * g < cs.nn) {
           const uint2 w = *reinterpret_cast<const uint2*>(xc + j * cs.nn + 8 * g);
           raw[it].x = w.x;
@@ -314,20 +339,17 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
     }
   }
   tc::bar_named(kBarWork, kWorkers);
-  // the kind of this thread's items: all codes, all bf16, or mixed
-  const int warp_q = wtid >> 5;   // items of a thread share the parity of i >> 5 (kWorkers is a multiple of 64)
-  const bool all_codes = !win && (cs.nn == 128 || (cs.nn == 64 && (warp_q & 1) == 0));
-  const bool all_bf16 = win || cs.nn == 0 || (cs.nn == 64 && (warp_q & 1) == 1);
   if (all_codes) {
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
       const int i = wtid + it * kWorkers;
       int j, g;
       chunk_item(nn, i, j, g);
-      const float scl = i < n_items ? sc[j] : 0.f;
-      mx = fmaxf(mx, fabsf(scl) * 448.f);
-      const uint4 h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), f16x2_of(scl * 256.f));
-      if (i < n_items) store_group(xc, j, g, h);
+      if (i < n_items) {
+        const uint32_t w2 = s2[j];
+        const uint4 h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), w2);
+        store_group(xc, j, g, w2 ? h : make_uint4(0u, 0u, 0u, 0u));
+      }
     }
   } else if (all_bf16) {
 #pragma unroll
@@ -335,8 +357,14 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
       const int i = wtid + it * kWorkers;
       int j, g;
       chunk_item(nn, i, j, g);
-      const uint4 h = bf16x8_to_f16x8(raw[it], mx);
-      if (i < n_items) store_group(xc, j, g, h);
+      if (i < n_items) {
+        const int32_t sr = src[j];
+        const bool valid = win ? sr <= -2 : sr >= 0;
+        float m = 0.f;
+        const uint4 h = bf16x8_to_f16x8(raw[it], m);
+        mx = valid ? fmaxf(mx, m) : mx;
+        store_group(xc, j, g, valid ? h : make_uint4(0u, 0u, 0u, 0u));
+      }
     }
   } else {
 #pragma unroll
@@ -345,13 +373,10 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
       if (i < n_items) {
         int j, g;
         chunk_item(nn, i, j, g);
-        uint4 h;
-        if (8 * g < cs.nn) {
-          const float scl = sc[j];
-          mx = fmaxf(mx, fabsf(scl) * 448.f);
-          h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), f16x2_of(scl * 256.f));
-        } else {
-          h = bf16x8_to_f16x8(raw[it], mx);
+        uint4 h = make_uint4(0u, 0u, 0u, 0u);
+        if (src[j] >= 0) {
+          if (8 * g < cs.nn) h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), s2[j]);
+          else h = bf16x8_to_f16x8(raw[it], mx);
         }
         store_group(xc, j, g, h);
       }
@@ -515,13 +540,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       vs[k] = SEP && sr[k] >= 0 ? __ldg(a.v_scale + sr[k]) : 0.f;
     }
   }
+  {
+    // scales as f16x2 words of scale * 2^8 (a code times 2^-8 times this word is
+    // the dequantised value); a scale whose codes can exceed f16 raises RANGE
+    float smax = 0.f;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int i = threadIdx.x + k * kThreads;
-    if ((i >> 7) < nt) {
-      t->sk[i] = ks[k];
-      if (SEP) t->sv[i] = vs[k];
+    for (int k = 0; k < 2; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      smax = fmaxf(smax, fmaxf(fabsf(ks[k]), fabsf(vs[k])));
+      if ((i >> 7) < nt) {
+        t->sk[i] = sr[k] >= 0 ? f16x2_of(ks[k] * 256.f) : 0u;
+        if (SEP) t->sv[i] = sr[k] >= 0 ? f16x2_of(vs[k] * 256.f) : 0u;
+      }
     }
+    if (smax * 448.f >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
   }
   tc::tc_fence_before();
   __syncthreads();
