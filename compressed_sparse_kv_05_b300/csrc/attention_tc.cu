@@ -223,10 +223,18 @@ DSV4_DEV ChunkSplit chunk_split(const AttnArgs& a, int c) {
 
 // Issue the cp.async copies of chunk c of a tile (row sources `src`, rc rows)
 // into the chunk region xc; rows without a source get nothing.
+DSV4_DEV void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+
 DSV4_DEV void issue_chunk(const AttnArgs& a, int b, bool win, const int32_t* src, int c, int rc, const uint8_t* nope,
-                          const uint16_t* rope, const uint16_t* wbuf, unsigned char* xc, int wtid) {
+                          const uint16_t* rope, const float* scale, const uint16_t* wbuf, unsigned char* xc,
+                          uint32_t* sk, int wtid) {
   const ChunkSplit cs = chunk_split(a, c);
   const int ng = cs.nn / 16, nr = cs.rb / 16;
+  // with the first chunk, every row's scale (raw fp32, turned into its f16x2
+  // multiplier when the chunk converts)
+  if (c == 0 && !win && wtid < rc && src[wtid] >= 0) cp_async4(sk + wtid, scale + src[wtid]);
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
     const int i = wtid + it * kWorkers;
@@ -282,14 +290,25 @@ DSV4_DEV void store_group(unsigned char* xc, int j, int g, uint4 h) {
 // Dequantise chunk c of a tile in place: every worker first reads the raw
 // bytes of its items (8-dim groups, see chunk_item), then, after a barrier of
 // the workers, writes them as f16 into the two 64-dim swizzle atoms of the
-// chunk. `s2` holds each row's scale * 2^8 as f16x2 (0 for rows without a
-// source). Rows without a source read stale bytes, which are discarded: they
+// chunk. `s2` holds each row's raw scale until chunk 0 turns it into the
+// row's multiplier scale * 2^8 as f16x2 (0 for rows without a source); the
+// barrier between the phases orders that before any use. Rows without a
+// source read stale bytes, which are discarded: they
 // become zeros. Each warp's items are all codes or all bf16 (the layouts of
 // the 448 + 64 entry and of window tokens), so the items of a thread run
 // without per-item branches; other layouts take the general path.
-DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, const uint32_t* s2, int c, int rc,
+DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, uint32_t* s2, int c, int rc,
                             unsigned char* xc, int wtid, float& mx) {
   const ChunkSplit cs = chunk_split(a, c);
+  if (c == 0 && !win && wtid < rc) {
+    // the tile's raw scales (landed with this chunk) become f16x2 multipliers
+    // scale * 2^8 (zero for rows without a source); a scale whose codes can
+    // exceed f16 raises RANGE
+    const float scl = __uint_as_float(s2[wtid]);
+    const bool ok = src[wtid] >= 0;
+    mx = ok ? fmaxf(mx, fabsf(scl) * 448.f) : mx;
+    s2[wtid] = ok ? f16x2_of(scl * 256.f) : 0u;
+  }
   const int nn = win ? 128 : cs.nn;   // window rows: the item layout of a full chunk
   const int n_items = rc * 16;
   const int warp_q = wtid >> 5;       // items of a thread share the parity of i >> 5 (kWorkers is a multiple of 64)
@@ -387,11 +406,16 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
 // One producer thread: the TMA boxes of chunk c of compressed tile tl
 // (contiguous rows) into the chunk's region, completing on xland[c].
 DSV4_DEV void issue_tma_chunk(const AttnArgs& a, const AttnMaps& maps, int b, const Tile& tl, int c,
-                              unsigned char* xk, uint64_t* xland) {
+                              unsigned char* xk, uint64_t* xland, uint32_t* sk) {
   const int y = static_cast<int>(static_cast<int64_t>(b) * a.capacity + tl.r0);
   const ChunkSplit cs = chunk_split(a, c);
   unsigned char* xc = xk + c * kChunkBytes;
-  tc::mbar_arrive_expect_tx(&xland[c], static_cast<uint32_t>(a.tile_rows * (cs.nn + cs.rb)));
+  // with the first chunk, the tile's scales (raw fp32, a whole number of
+  // 16-byte granules: the capacity is a multiple of 4 on this path, so the
+  // copy starts aligned and ends inside the sequence's rows)
+  const uint32_t sbytes = c == 0 && sk ? static_cast<uint32_t>((tl.cnt + 3) & ~3) * 4u : 0u;
+  tc::mbar_arrive_expect_tx(&xland[c], static_cast<uint32_t>(a.tile_rows * (cs.nn + cs.rb)) + sbytes);
+  if (sbytes) tc::bulk_load(sk, a.k_scale + y, sbytes, &xland[c]);
   if (cs.nn == 128) tc::tma_load_2d(xc, &maps.nope, &xland[c], c * 128, y);
   else if (cs.nn > 0) tc::tma_load_2d(xc, &maps.nope_tail, &xland[c], c * 128, y);
   if (cs.rb > 0) tc::tma_load_2d(xc + cs.rope_off, &maps.rope, &xland[c], 0, y);
@@ -501,63 +525,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   }
   if (threadIdx.x < kHeads) t->m_used[threadIdx.x] = -INFINITY;
   // Row sources of every tile of the split (CSA: one round trip for the top-k
-  // indices) and their scales. The small loads the first conversions need
-  // (query, scales) go out before the tile's bulk data, so that they are not
-  // queued behind it: for contiguous rows the scale loads leave at once and
-  // the first tile's boxes after the first barrier; gathered rows leave
-  // together with their scale loads once the sources are known.
+  // indices). Each tile's scales travel with its first chunk: a bulk copy
+  // beside the TMA boxes (contiguous rows, capacity a multiple of 4) or one
+  // 4-byte copy per gathered row; otherwise they are loaded here.
+  const bool bulk_scales = !SEP && a.tma && (a.capacity & 3) == 0;
   int32_t sr[2];
-  float ks[2] = {0.f, 0.f}, vs[2] = {0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int i = threadIdx.x + k * kThreads, tt = i >> 7;
     sr[k] = tt < nt ? row_source(a, rs, b, tile_at(a, rs, tile0 + tt), i & (kRows - 1)) : -1;
     if (tt < nt) t->src[i] = sr[k];
   }
-  if (a.n_sel == 0) {
+  if (!SEP && a.tma && !bulk_scales) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      ks[k] = sr[k] >= 0 ? __ldg(a.k_scale + sr[k]) : 0.f;
-      vs[k] = SEP && sr[k] >= 0 ? __ldg(a.v_scale + sr[k]) : 0.f;
+      const int i = threadIdx.x + k * kThreads, tt = i >> 7;
+      if (tt < nt && !tile_at(a, rs, tile0 + tt).win) t->sk[i] = __float_as_uint(sr[k] >= 0 ? __ldg(a.k_scale + sr[k]) : 0.f);
     }
-  }
-  __syncthreads();
-  if (first_tma && threadIdx.x == 32)
-    for (int c = 0; c < nch; ++c) issue_tma_chunk(a, maps, b, first, c, xk, t->xland);
-  if (!first_tma && warp >= 2) {
-    const int wtid = threadIdx.x - 64;
-    const int rc = (first.cnt + 15) & ~15;
-    for (int c = 0; c < nch; ++c) {
-      issue_chunk(a, b, first.win, t->src, c, rc, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, wtid);
-      if (SEP) issue_chunk(a, b, first.win, t->src, c, rc, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, wtid);
-      cp_async_commit();
-    }
-  }
-  if (a.n_sel > 0) {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      ks[k] = sr[k] >= 0 ? __ldg(a.k_scale + sr[k]) : 0.f;
-      vs[k] = SEP && sr[k] >= 0 ? __ldg(a.v_scale + sr[k]) : 0.f;
-    }
-  }
-  {
-    // scales as f16x2 words of scale * 2^8 (a code times 2^-8 times this word is
-    // the dequantised value); a scale whose codes can exceed f16 raises RANGE
-    float smax = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = threadIdx.x + k * kThreads;
-      smax = fmaxf(smax, fmaxf(fabsf(ks[k]), fabsf(vs[k])));
-      if ((i >> 7) < nt) {
-        t->sk[i] = sr[k] >= 0 ? f16x2_of(ks[k] * 256.f) : 0u;
-        if (SEP) t->sv[i] = sr[k] >= 0 ? f16x2_of(vs[k] * 256.f) : 0u;
-      }
-    }
-    if (smax * 448.f >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  if (first_tma && threadIdx.x == 32)
+    for (int c = 0; c < nch; ++c)
+      issue_tma_chunk(a, maps, b, first, c, xk, t->xland, bulk_scales ? t->sk : nullptr);
+  if (!first_tma && warp >= 2) {
+    const int wtid = threadIdx.x - 64;
+    const int rc = (first.cnt + 15) & ~15;
+    for (int c = 0; c < nch; ++c) {
+      issue_chunk(a, b, first.win, t->src, c, rc, a.k_nope, a.k_rope, a.k_scale, a.win_k, xk + c * kChunkBytes, t->sk, wtid);
+      if (SEP)
+        issue_chunk(a, b, first.win, t->src, c, rc, a.v_nope, a.v_rope, a.v_scale, a.win_v, xv + c * kChunkBytes, t->sv, wtid);
+      cp_async_commit();
+    }
+  }
   const uint32_t taddr = t->taddr;
   const uint32_t s_tmem = taddr, o_tmem = taddr + kHeads;
   const int32_t* src = t->src;
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           if (tl.win) break;   // window tiles come last and go by cp.async
           for (int c = 0; c < nch; ++c) {
             if (!(ok = tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort))) break;
-            issue_tma_chunk(a, maps, b, tl, c, xk, t->xland);
+            issue_tma_chunk(a, maps, b, tl, c, xk, t->xland, bulk_scales ? t->sk + tt * kRows : nullptr);
             ++issued[c];
           }
         }
@@ -683,8 +684,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         for (int c = 0; c < nch; ++c) {
           const bool w = soft_ok && tc::mbar_wait(&t->xfree[c], (tt - 1) & 1, abort);
           if (!(ok = tc::bar_and(kBarWork, kWorkers, w))) break;
-          issue_chunk(a, b, tl.win, src_t, c, rc, a.k_nope, a.k_rope, a.win_k, xk + c * kChunkBytes, wtid);
-          if (SEP) issue_chunk(a, b, tl.win, src_t, c, rc, a.v_nope, a.v_rope, a.win_v, xv + c * kChunkBytes, wtid);
+          issue_chunk(a, b, tl.win, src_t, c, rc, a.k_nope, a.k_rope, a.k_scale, a.win_k, xk + c * kChunkBytes,
+                      t->sk + tt * kRows, wtid);
+          if (SEP)
+            issue_chunk(a, b, tl.win, src_t, c, rc, a.v_nope, a.v_rope, a.v_scale, a.win_v, xv + c * kChunkBytes,
+                        t->sv + tt * kRows, wtid);
           cp_async_commit();
         }
         if (!ok) break;

@@ -322,14 +322,18 @@ def _oracle_attend_planes(layer, p, q, sel):
     return O.csa_attend(q, np.float32(layer.sm_scale), sel, *args)
 
 
-@pytest.mark.parametrize("n_tokens", [128 * 1000 + 77, 128 * 257, 128 * 40 + 5])
-def test_hca_decode_stack_shape(n_tokens):
+@pytest.mark.parametrize("n_tokens,cap_extra", [(128 * 1000 + 77, None), (128 * 257, None), (128 * 40 + 5, None),
+                                                (128 * 257 + 9, 2)])
+def test_hca_decode_stack_shape(n_tokens, cap_extra):
     """D = 512 (448 FP8 + 64 RoPE), 64 heads, K = V, four sequences as in the
     decode step: compressed rows by TMA boxes over several tiles per CTA, a
-    partial last tile, the window tile; small contexts take 64- and 32-row tiles."""
+    partial last tile, the window tile; small contexts take 64- and 32-row
+    tiles. A capacity that is not a multiple of 4 takes the scales by loads
+    instead of bulk copies."""
     layer = W.scaled(W.STACK_HCA, n_tokens=n_tokens)
     planes = oracle_direct_planes(layer, "hcastack", 1, range(layer.batch))
-    desc, cache = gpu_cache_from_planes(layer, planes)
+    cap = None if cap_extra is None else layer.n_comp + cap_extra
+    desc, cache = gpu_cache_from_planes(layer, planes, capacity=cap)
     dec = synth.decode_inputs("hcastack", 1, layer)
     g_out, g_lse = _decode(desc, cache, layer, dec["q"])
     assert dsv4.dsv4_read_status(cache) == 0
