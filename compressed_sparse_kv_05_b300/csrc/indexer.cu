@@ -171,10 +171,11 @@ DSV4_DEV void load_to_smem(T* dst, const T* src, uint32_t n) {
 
 // The resolving CTA's work when every candidate fits in registers (up to
 // kRegCand per thread): T2 from the second-level histogram; inside bin
-// (T1, T2) the need2 best by (low 8 key bits desc, index asc), found by
-// 8-bit digit selections over the candidates held in registers; the k blocks
-// are emitted in ascending order from a bitmap of the selection (n_c up to
-// 32 * kBitmapWords), else by a bitonic sort.
+// (T1, T2) the need2 best by (low 8 key bits desc, index asc): the index
+// threshold is the r-th lowest set bit of a bitmap of the tied blocks (n_c up
+// to 32 * kBitmapWords), else found by 8-bit digit selections over the
+// candidates held in registers; the k blocks are emitted in ascending order
+// from a bitmap of the selection, else by a bitonic sort.
 DSV4_DEV void resolve_in_registers(int k, int64_t n_c, uint32_t n_above, uint32_t n_cand,
                                    uint32_t need1, const uint32_t* hist2, const int32_t* above,
                                    const uint64_t* cand, int32_t* out, uint32_t* h, int32_t* fin,
@@ -212,6 +213,39 @@ DSV4_DEV void resolve_in_registers(int k, int64_t n_c, uint32_t n_above, uint32_
     __syncthreads();
     d8 = *s_d;
     uint32_t r = need2 - *s_rem;   // lowest indices to take among the keys with low8 == d8
+    const int64_t words = (n_c + 31) / 32;
+    if (words <= kBitmapWords) {
+      // the tied blocks as bits: the r-th lowest set bit is the threshold
+      uint32_t* bm = reinterpret_cast<uint32_t*>(dyn);
+      const int per = static_cast<int>((words + kSelThreads - 1) / kSelThreads);
+      for (int i = t; i < per * kSelThreads; i += kSelThreads) bm[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kRegCand; ++u) {
+        const uint32_t key = static_cast<uint32_t>(cv[u] >> 32), idx = static_cast<uint32_t>(cv[u]);
+        if (t + u * kSelThreads < n_cand && ((key >> 8) & 0xFFF) == T2 && (key & 0xFF) == d8)
+          atomicOr(&bm[idx >> 5], 1u << (idx & 31));
+      }
+      __syncthreads();
+      uint32_t cntw = 0;
+      for (int q = 0; q < per; ++q) cntw += __popc(bm[t * per + q]);
+      uint32_t tot;
+      uint32_t before = block_excl_scan_packed(cntw, &tot, scratch);
+      if (before < r && before + cntw >= r) {   // this thread's words hold the r-th bit
+        for (int q = 0; q < per; ++q) {
+          uint32_t wd = bm[t * per + q];
+          const uint32_t c = __popc(wd);
+          if (before + c >= r) {
+            for (uint32_t k2 = r - before; k2 > 1; --k2) wd &= wd - 1;   // drop the lower set bits
+            *s_d = (t * per + q) * 32 + (__ffs(wd) - 1);
+            break;
+          }
+          before += c;
+        }
+      }
+      __syncthreads();
+      thr = *s_d;
+    } else {
     int nbits = 1;
     while (nbits < 32 && (static_cast<int64_t>(1) << nbits) < n_c) ++nbits;
     const int passes = (nbits + 7) / 8;
@@ -233,6 +267,7 @@ DSV4_DEV void resolve_in_registers(int k, int64_t n_c, uint32_t n_above, uint32_
       r -= *s_rem;
     }
     thr = prefix;   // exactly the wanted number of indices with low8 == d8 are <= thr
+    }
   }
 #pragma unroll
   for (int u = 0; u < kRegCand; ++u) {
