@@ -246,8 +246,9 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
   const int b = blockIdx.x / hgs, hg = blockIdx.x % hgs;
   const int h0 = hg * 64;
   const int hcount = a.H - h0 < 64 ? a.H - h0 : 64;
-  __shared__ float s_w[64][kS + 1];             // log-sum-exps, then weights
-  __shared__ float s_m[64], s_l[64], s_r[64];   // running max and sum per head, rescale of this pass
+  __shared__ float s_lse[64][kS + 1];                   // [head][split]
+  __shared__ __align__(16) float s_w[kS][64 + 4];       // [split][head]: weights relative to the running max
+  __shared__ float s_m[64], s_l[64], s_r[64];           // running max and sum per head, rescale of this pass
   __shared__ float s_acc[kSg][64][9];
   const int t = threadIdx.x;
   const int sg = t >> 6, dl = (t >> 3) & 7, hq = (t & 7) * 8;
@@ -282,37 +283,32 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
 #pragma unroll
     for (int u = 0; u < kL; ++u) {
       const int i = t + u * kT;
-      s_w[i >> 6][i & (kS - 1)] = lv[u];
+      s_lse[i >> 6][i & (kS - 1)] = lv[u];
     }
     __syncthreads();
     {
-      // head t / 4: this pass's max and sum of exp (four threads, sixteen splits each)
+      // head t / 4: this pass's max and sum of exp (four threads, every fourth split)
       const int h = t >> 2, part4 = t & 3;
       float mx = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) mx = fmaxf(mx, s_w[h][part4 + 4 * u]);
+      for (int s = part4; s < ns; s += 4) mx = fmaxf(mx, s_lse[h][s]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float mo = s_m[h], mn = fmaxf(mo, mx);
       float sum = 0.f;
-      if (mn != -INFINITY) {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) sum += __expf(s_w[h][part4 + 4 * u] - mn);   // exp(-inf) = 0
+      for (int s = part4; s < ns; s += 4) {
+        // weight relative to the running max; a split without rows gets 0
+        const float x = s_lse[h][s];
+        const float w = x == -INFINITY ? 0.f : __expf(x - mn);
+        s_w[s][h] = w;
+        sum += w;
       }
       sum += __shfl_xor_sync(0xffffffffu, sum, 1);
       sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      __syncthreads();
       if (part4 == 0) {
         const float r = mo == -INFINITY ? 0.f : __expf(mo - mn);
         s_r[h] = r;
         s_l[h] = s_l[h] * r + sum;
         s_m[h] = mn;
-      }
-      // weights relative to the running max (a split without rows gets 0)
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float x = s_w[h][part4 + 4 * u];
-        s_w[h][part4 + 4 * u] = x == -INFINITY ? 0.f : __expf(x - mn);
       }
     }
     __syncthreads();
@@ -323,12 +319,14 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
       const int s = sg + kSg * u;
       if (s < ns) {
         const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const float4 wa = *reinterpret_cast<const float4*>(&s_w[s][hq]);
+        const float4 wb = *reinterpret_cast<const float4*>(&s_w[s][hq + 4]);
+        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float w = s_w[hq + i][s];
           const uint16_t bits = static_cast<uint16_t>((i & 1) ? w4[i >> 1] >> 16 : w4[i >> 1] & 0xFFFFu);
           // a split without rows may have left its partial unwritten
-          acc[i] = w > 0.f ? fmaf(w, __half2float(__ushort_as_half(bits)), acc[i]) : acc[i];
+          acc[i] = w[i] > 0.f ? fmaf(w[i], __half2float(__ushort_as_half(bits)), acc[i]) : acc[i];
         }
       }
     }
