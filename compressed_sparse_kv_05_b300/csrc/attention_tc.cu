@@ -78,12 +78,14 @@ constexpr float kRescale = 8.f;                // lazy-rescale threshold (log2 u
 constexpr float kF16Max = 65504.f;
 
 struct TcTail {
-  uint64_t xland[kMaxChunks], xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, pvdone, qready, drain;
+  uint64_t xland[kMaxChunks], xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, qready, drain;
   uint32_t taddr;
   int abort;
-  int32_t src[kMaxTiles * kRows];   // row sources of every tile of the split (see row_source), 128 per tile
-  uint32_t sk[kMaxTiles * kRows];   // key (or shared entry) scale * 2^8 of every row as f16x2, 0 for others
-  uint32_t sv[kMaxTiles * kRows];   // the same for the value scale (separate V)
+  // the per-row arrays are 16-byte aligned: the scales of a tile arrive by bulk copies
+  alignas(16) int32_t src[kMaxTiles * kRows];   // row sources of every tile of the split (see row_source), 128 per tile
+  alignas(16) uint32_t sk[kMaxTiles * kRows];   // key (or shared entry) scale of every row: raw fp32 until the
+                                                // tile's first chunk turns it into scale * 2^8 as f16x2 (0 for others)
+  alignas(16) uint32_t sv[kMaxTiles * kRows];   // the same for the value scale (separate V)
   float m_used[kHeads];             // running max per head, log2 domain
   float alpha[kHeads];
   float lsum[kHeads];
@@ -517,7 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     tc::mbar_init(&t->sfull, 1);
     tc::mbar_init(&t->pfull, kSoftThreads / 32);
-    tc::mbar_init(&t->pvdone, 1);
     tc::mbar_init(&t->qready, kWorkers / 32);
     tc::mbar_init(&t->drain, 1);
     t->abort = 0;
@@ -599,7 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           tc::tc_commit(&t->xfree[c]);
         }
       }
-      tc::tc_commit(&t->pvdone);
       // every MMA issued must finish before tensor memory is released
       tc::tc_commit(&t->drain);
       tc::mbar_wait_drain(&t->drain, 0);
@@ -769,11 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     if (soft) {
       // ---- epilogue: normalise O^T and store this split's f16 partial [D][64 heads]
-      ok = ok && soft_ok;
-      if (ok) ok = tc::mbar_wait(&t->pvdone, 0, abort);
-      ok = tc::bar_and(kBarSoft, kSoftThreads, ok);
+      unsigned char* stage = xk;
+      ok = tc::bar_and(kBarSoft, kSoftThreads, ok && soft_ok);
       if (ok) {
-        tc::tc_fence_after();
         t->red[qd][hb + lane] = lw;
         tc::bar_named(kBarSoft, kSoftThreads);
         if (st < kHeads) {
@@ -782,11 +780,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           t->alpha[st] = l > 0.f ? 1.f / l : 0.f;
         }
         tc::bar_named(kBarSoft, kSoftThreads);
-        // normalised O^T as f16 rows [dim][64 heads] staged in the (now free) X
+        // Normalised O^T as f16 rows [dim][64 heads] staged in the (now free) X
         // region, 16-byte granule q of row r at granule q ^ (r & 7) (no bank
-        // conflicts; the merge reads the same swizzle), then one bulk copy
-        unsigned char* stage = xk;
-        for (int c = 0; c < nch; ++c) {
+        // conflicts; the merge reads the same swizzle), then one bulk copy. Each
+        // 128-dim block is staged as soon as the last tile's P.V of that block
+        // has finished (its stage bytes lie in X chunks whose P.V is done), so
+        // the staging overlaps the remaining MMAs.
+        for (int c = 0; ok && c < nch; ++c) {
+          if (!(ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->xfree[c], (nt - 1) & 1, abort)))) break;
+          tc::tc_fence_after();
           uint32_t v[32];
           tc::tmem_ld32(o_tmem + lane_off + c * kHeads + hb, v);
           tc::tmem_wait_ld();
@@ -801,6 +803,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             *reinterpret_cast<uint4*>(stage + r * 128 + ((((hb >> 3) + q4) ^ (r & 7)) << 4)) =
                 make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
         }
+      }
+      if (ok) {
         tc::fence_proxy_async_smem();
         tc::bar_named(kBarSoft, kSoftThreads);
         if (st == 0) {
@@ -815,7 +819,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + st) * a.splits + split] =
               l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
-        if (st == 0) tc::bulk_wait();   // the stage must outlive the copy, and its writes precede the merge
+        // the stage must outlive the copy's reads; its global writes are
+        // performed by the time the grid completes, which the merge waits for
+        if (st == 0) tc::bulk_wait_read();
       }
     }
   }

@@ -338,6 +338,19 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
+  // The CTA's slice of the scores is fixed by the capacity, so the first
+  // round of score loads leaves together with the loads of T1 and n_tokens;
+  // blocks at or beyond n_c are discarded when classified.
+  const float* sc = a.scores + static_cast<int64_t>(b) * a.capacity;
+  const int64_t chunk = (static_cast<int64_t>(a.capacity) + gridDim.x - 1) / gridDim.x;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
+  const int64_t cap_end = c0 + chunk < a.capacity ? c0 + chunk : a.capacity;
+  uint32_t key0[kScanItems];
+#pragma unroll
+  for (int u = 0; u < kScanItems; ++u) {
+    const int64_t s = c0 + threadIdx.x + u * blockDim.x;
+    key0[u] = s < cap_end ? score_key(__ldg(sc + s)) : 0u;
+  }
   uint32_t* cnt = a.cnt + b * kCntWords;
   const uint32_t T1 = cnt[4];
   int64_t n_c = a.n_tokens[b] / a.ratio;
@@ -349,22 +362,19 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
       for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < n_c ? i : -1;
     return;
   }
-  const float* sc = a.scores + static_cast<int64_t>(b) * a.capacity;
   int32_t* above = a.above + static_cast<int64_t>(b) * k;
   uint64_t* cand = a.cand + static_cast<int64_t>(b) * a.capacity;
   uint32_t* hist2 = a.hist2 + static_cast<int64_t>(b) * kBins;
 
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
   __syncthreads();
-  const int64_t chunk = (n_c + gridDim.x - 1) / gridDim.x;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
-  const int64_t c1 = c0 + chunk < n_c ? c0 + chunk : n_c;
+  const int64_t c1 = cap_end < n_c ? cap_end : n_c;
   for (int64_t base = c0; base < c1; base += kScanItems * blockDim.x) {
     uint32_t key[kScanItems];
 #pragma unroll
     for (int u = 0; u < kScanItems; ++u) {
       const int64_t s = base + threadIdx.x + u * blockDim.x;
-      key[u] = s < c1 ? score_key(__ldg(sc + s)) : 0u;
+      key[u] = base == c0 ? key0[u] : (s < c1 ? score_key(__ldg(sc + s)) : 0u);
     }
     uint32_t mine = 0;   // packed counts: above T1 (low 16 bits), in T1 (high 16 bits)
 #pragma unroll

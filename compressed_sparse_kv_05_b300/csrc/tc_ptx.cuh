@@ -303,6 +303,9 @@ DSV4_DEV void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
 DSV4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk copy of this thread has completed (its writes are performed).
 DSV4_DEV void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until every committed bulk copy of this thread has read its shared-memory
+// source (the writes complete on their own; the grid's completion covers them).
+DSV4_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 DSV4_DEV void bar_named(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
 
