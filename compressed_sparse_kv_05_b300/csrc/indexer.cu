@@ -319,16 +319,15 @@ DSV4_DEV void resolve_in_registers(int k, int64_t n_c, uint32_t n_above, uint32_
 }
 
 // Top-k selection, grid (sel_ctas, B), block 512. The scoring kernel has
-// histogrammed the top 12 bits of every score key and its last CTA stored the
-// threshold bin T1 (the bin holding the k-th largest key) and the number of keys
-// above it. Each CTA scans its slice of the scores, appends every block above
+// histogrammed the top 12 bits of every score key; every CTA finds in it the
+// threshold bin T1 (the bin holding the k-th largest key). Each CTA scans its slice of the scores, appends every block above
 // T1 to `above` and every block in T1 to `cand` (key, index) with one reservation
 // per CTA, while histogramming the next 12 key bits (hist2). The last CTA of the
 // sequence to finish (a completion counter, no waiting) resolves the boundary:
 // candidates above the second-level threshold bin T2 are taken; ties in T2 are
 // settled by the low 8 key bits, then by the lower index (radix select over
 // 12-bit index digits); the k blocks are sorted into ascending index order.
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 2) topk_select_kernel(IndexArgs a) {
   __shared__ uint32_t h[kBins];
   __shared__ int32_t fin[kMaxK];
   __shared__ uint32_t h8[kDigitPasses + 1][256];   // resolution histograms of 8-bit digits
@@ -338,21 +337,13 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
-  // The CTA's slice of the scores is fixed by the capacity, so the first
-  // round of score loads leaves together with the loads of T1 and n_tokens;
-  // blocks at or beyond n_c are discarded when classified.
+  // The CTA's slice of the scores is fixed by the capacity (blocks at or
+  // beyond n_c are discarded when classified).
   const float* sc = a.scores + static_cast<int64_t>(b) * a.capacity;
   const int64_t chunk = (static_cast<int64_t>(a.capacity) + gridDim.x - 1) / gridDim.x;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
   const int64_t cap_end = c0 + chunk < a.capacity ? c0 + chunk : a.capacity;
-  uint32_t key0[kScanItems];
-#pragma unroll
-  for (int u = 0; u < kScanItems; ++u) {
-    const int64_t s = c0 + threadIdx.x + u * blockDim.x;
-    key0[u] = s < cap_end ? score_key(__ldg(sc + s)) : 0u;
-  }
   uint32_t* cnt = a.cnt + b * kCntWords;
-  const uint32_t T1 = cnt[4];
   int64_t n_c = a.n_tokens[b] / a.ratio;
   if (n_c > a.capacity) n_c = a.capacity;
   int32_t* out = a.topk + static_cast<int64_t>(b) * a.k;
@@ -364,8 +355,22 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
   }
   int32_t* above = a.above + static_cast<int64_t>(b) * k;
   uint64_t* cand = a.cand + static_cast<int64_t>(b) * a.capacity;
-  uint32_t* hist2 = a.hist2 + static_cast<int64_t>(b) * kBins;
 
+  uint32_t* hist2 = a.hist2 + static_cast<int64_t>(b) * kBins;
+  // the first-level threshold bin T1 (the bin holding the k-th largest key)
+  // from the scoring kernel's full histogram, found by every CTA
+  {
+    const uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
+    constexpr int per = kBins / kSelThreads;
+    uint32_t v[per];
+#pragma unroll
+    for (int u = 0; u < per; ++u) v[u] = __ldcg(gh + threadIdx.x + u * kSelThreads);
+#pragma unroll
+    for (int u = 0; u < per; ++u) h[threadIdx.x + u * kSelThreads] = v[u];
+  }
+  __syncthreads();
+  uint32_t n_gt1;
+  const uint32_t T1 = static_cast<uint32_t>(block_suffix_select<kSelThreads>(h, static_cast<uint32_t>(k), &n_gt1, scratch));
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const int64_t c1 = cap_end < n_c ? cap_end : n_c;
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexArgs a) {
 #pragma unroll
     for (int u = 0; u < kScanItems; ++u) {
       const int64_t s = base + threadIdx.x + u * blockDim.x;
-      key[u] = base == c0 ? key0[u] : (s < c1 ? score_key(__ldg(sc + s)) : 0u);
+      key[u] = s < c1 ? score_key(__ldg(sc + s)) : 0u;
     }
     uint32_t mine = 0;   // packed counts: above T1 (low 16 bits), in T1 (high 16 bits)
 #pragma unroll

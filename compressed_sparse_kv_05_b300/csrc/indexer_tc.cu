@@ -10,7 +10,8 @@
 // compressed blocks, with the per-16 e4m3 scales of keys and query applied by
 // the MMA itself (UE4M3 block scales). The epilogue applies ReLU and the head
 // weights, writes one fp32 score per block and histograms the top 12 bits of
-// the score keys for the top-k selection that follows.
+// the score keys for the top-k selection that follows (which finds the
+// threshold bin in the full histogram).
 //
 // CTA roles (384 threads): warp 0 allocates tensor memory and streams key tiles
 // with TMA into an S-stage ring; warp 1 issues tcgen05.cp (block scales) and
@@ -58,8 +59,6 @@ struct SmemTail {
   uint64_t full[8], empty[8], sf_full[8], acc_full[2], acc_empty[2], q_full, qsf_full, drain;
   uint32_t taddr;
   int abort;
-  uint32_t last;
-  uint32_t scratch[kThreads / 32 + 2];
   uint32_t hist[kBins];  // histogram of score-key bits 31..20 of this CTA's blocks
 };
 
@@ -296,36 +295,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::tmem_dealloc(taddr, ncols);
   }
   if (threadIdx.x == 0 && t->abort) atomicOr(a.status, DSV4_STATUS_TIMEOUT);
-
-  // The last CTA of sequence b to finish (a completion counter, no waiting)
-  // finds the first-level threshold bin of the top-k in the full histogram.
-  uint32_t* cnt = a.cnt + b * kCntWords;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int active = (tiles + per - 1) / per;   // CTAs of this sequence that had tiles
-    t->last = atomicAdd(&cnt[3], 1u) == static_cast<uint32_t>(active - 1);
-    if (t->last) __threadfence();
-  }
-  __syncthreads();
-  if (!t->last || n_c <= a.k) return;
-  if (threadIdx.x >= kEpiThreads) return;
-  {
-    // every CTA's histogram atomics are done (counter above); L2 reads, all in flight
-    const uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
-    constexpr int per = kBins / kEpiThreads;
-    uint32_t v[per];
-#pragma unroll
-    for (int u = 0; u < per; ++u) v[u] = __ldcg(gh + threadIdx.x + u * kEpiThreads);
-#pragma unroll
-    for (int u = 0; u < per; ++u) t->hist[threadIdx.x + u * kEpiThreads] = v[u];
-  }
-  sync_threads_of<kEpiThreads, 3>();
-  uint32_t n_gt1;
-  const int T1 = block_suffix_select<kEpiThreads, 3>(t->hist, static_cast<uint32_t>(a.k), &n_gt1, t->scratch);
-  if (threadIdx.x == 0) {
-    cnt[4] = static_cast<uint32_t>(T1);
-    cnt[5] = n_gt1;
-  }
 }
 
 // ------------------------------------------------------------------------------ host side

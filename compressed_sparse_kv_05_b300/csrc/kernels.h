@@ -35,8 +35,7 @@ __global__ void pool_rows_kernel(const uint16_t* x, const uint16_t* z, const flo
 
 // ---- indexer + top-k
 // Per-sequence counter words of the top-k: [0] blocks above the threshold bin,
-// [1] candidates in it, [2] finished selection CTAs, [3] finished scoring CTAs,
-// [4] first-level threshold bin T1, [5] keys in bins above T1.
+// [1] candidates in it, [2] finished selection CTAs; the rest unused.
 constexpr int kCntWords = 8;
 struct IndexArgs {
   int B, Hi, N, Di, k, capacity, ratio;
