@@ -289,28 +289,34 @@ DSV4_DEV void store_group(unsigned char* xc, int j, int g, uint4 h) {
   *reinterpret_cast<uint4*>(xc + atom * kAtomBytes + j * 128 + ((gg ^ (j & 7)) << 4)) = h;
 }
 
-// Dequantise chunk c of a tile in place: every worker first reads the raw
-// bytes of its items (8-dim groups, see chunk_item), then, after a barrier of
-// the workers, writes them as f16 into the two 64-dim swizzle atoms of the
-// chunk. `s2` holds each row's raw scale until chunk 0 turns it into the
-// row's multiplier scale * 2^8 as f16x2 (0 for rows without a source); the
-// barrier between the phases orders that before any use. Rows without a
-// source read stale bytes, which are discarded: they
-// become zeros. Each warp's items are all codes or all bf16 (the layouts of
-// the 448 + 64 entry and of window tokens), so the items of a thread run
-// without per-item branches; other layouts take the general path.
-DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, uint32_t* s2, int c, int rc,
-                            unsigned char* xc, int wtid, float& mx) {
-  const ChunkSplit cs = chunk_split(a, c);
-  if (c == 0 && !win && wtid < rc) {
-    // the tile's raw scales (landed with this chunk) become f16x2 multipliers
-    // scale * 2^8 (zero for rows without a source); a scale whose codes can
-    // exceed f16 raises RANGE
+// A compressed tile's raw row scales (landed with its first chunk) become
+// f16x2 multipliers scale * 2^8 (zero for rows without a source); a scale
+// whose codes can exceed f16 raises RANGE. Worker wtid converts row wtid's,
+// before the worker barrier that precedes the first chunk's conversion.
+DSV4_DEV void convert_scales(const int32_t* src, uint32_t* s2, int rc, int wtid, float& mx) {
+  if (wtid < rc) {
     const float scl = __uint_as_float(s2[wtid]);
     const bool ok = src[wtid] >= 0;
     mx = ok ? fmaxf(mx, fabsf(scl) * 448.f) : mx;
     s2[wtid] = ok ? f16x2_of(scl * 256.f) : 0u;
   }
+}
+
+// Dequantise chunk c of a tile in place: every worker first reads the raw
+// bytes of its items (8-dim groups, see chunk_item), then writes them as f16
+// into the two 64-dim swizzle atoms of the chunk. Between the phases stands a
+// barrier of the workers, or only of the warp where a chunk holds 128 code
+// dims: there row j's raw bytes are [128 j, 128 j + 128), read by the 16
+// items of row j (16 consecutive workers, one warp), and the only raw bytes
+// any f16 write covers are those of its own row. `s2` holds each row's
+// multiplier (convert_scales). Rows without a source read stale bytes, which
+// are discarded: they become zeros. Each warp's items are all codes or all
+// bf16 (the layouts of the 448 + 64 entry and of window tokens), so the items
+// of a thread run without per-item branches; other layouts take the general
+// path.
+DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, const uint32_t* s2, int c, int rc,
+                            unsigned char* xc, int wtid, float& mx) {
+  const ChunkSplit cs = chunk_split(a, c);
   const int nn = win ? 128 : cs.nn;   // window rows: the item layout of a full chunk
   const int n_items = rc * 16;
   const int warp_q = wtid >> 5;       // items of a thread share the parity of i >> 5 (kWorkers is a multiple of 64)
@@ -359,7 +365,8 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, uin
       }
     }
   }
-  tc::bar_named(kBarWork, kWorkers);
+  if (!win && cs.nn == 128) __syncwarp();
+  else tc::bar_named(kBarWork, kWorkers);
   if (all_codes) {
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
@@ -474,11 +481,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     tc::prefetch_tensormap(&maps.nope_tail);
     tc::prefetch_tensormap(&maps.rope);
   }
-  pdl_wait();
-
   const int split = blockIdx.x, b = blockIdx.y;
   const int h0 = blockIdx.z * kHeads;
   const int hcount = a.H - h0 < kHeads ? a.H - h0 : kHeads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // workers: the query rows of this head group (bf16), all loads in flight
+  // while the CTA waits for the previous kernel and sets up; converted into
+  // the MMA operand further down. The query is an input no kernel of this
+  // library writes, complete before the call's kernels start, so it is read
+  // before the programmatic-launch wait.
+  const int gpr = D / 8;   // 8-dim groups per head
+  // head of query group i: i / gpr = (i / 16) / (D / 128) by an exact
+  // reciprocal (exact for every i < 128 * gpr and D / 128 <= 16)
+  const uint32_t qrcp = (65536u + (D >> 7) - 1) / static_cast<uint32_t>(D >> 7);
+  uint4 qw[kQItems];
+  if (warp >= 2) {
+    const int wtid = threadIdx.x - 64;
+#pragma unroll
+    for (int u = 0; u < kQItems; ++u) {
+      const int i = wtid + u * kWorkers;
+      const int h = static_cast<int>(((static_cast<uint32_t>(i) >> 4) * qrcp) >> 16);
+      qw[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < kHeads * gpr && h < hcount)
+        qw[u] = __ldg(reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.H + h0 + h) * D) +
+                      (i - h * gpr));
+    }
+  }
+  pdl_wait();
+
   const RowSpace rs = row_space(a, b);
   const int tile0 = split * a.tiles_per_split;
   const int tiles = rs.mt + rs.wt;
@@ -489,21 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     return;
   }
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // workers: the query rows of this head group (bf16), all loads in flight
-  // while the CTA sets up; converted into the MMA operand further down
-  const int gpr = D / 8;   // 8-dim groups per head
-  uint4 qw[kQItems];
-  if (warp >= 2) {
-    const int wtid = threadIdx.x - 64;
-#pragma unroll
-    for (int u = 0; u < kQItems; ++u) {
-      const int i = wtid + u * kWorkers, h = i / gpr;
-      qw[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (i < kHeads * gpr && h < hcount)
-        qw[u] = __ldg(reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.H + h0 + h) * D) + i % gpr);
-    }
-  }
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(kHeads * (1 + nch))) cols <<= 1;
   volatile int* abort = &t->abort;
@@ -658,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int u = 0; u < kQItems; ++u) {
         const int i = wtid + u * kWorkers;
         if (i < kHeads * gpr) {
-          const int h = i / gpr, d0 = (i % gpr) * 8;
+          const int h = static_cast<int>(((static_cast<uint32_t>(i) >> 4) * qrcp) >> 16), d0 = (i - h * gpr) * 8;
           const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
           *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) =
               bf16x8_to_f16x8(qw[u], qmax);
@@ -697,6 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         bool w = soft_ok;
         if (via_tma) w = w && tc::mbar_wait(&t->xland[c], tt & 1, abort);
         else cp_async_wait(nch - 1 - c);
+        if (c == 0 && !tl.win && w) {
+          convert_scales(src_t, t->sk + tt * kRows, rc, wtid, mx);
+          if (SEP) convert_scales(src_t, t->sv + tt * kRows, rc, wtid, mx);
+        }
         // every worker's copies of chunk c have landed (or the boxes have)
         if (!(ok = tc::bar_and(kBarWork, kWorkers, w))) break;
         convert_chunk(a, tl.win, src_t, t->sk + tt * kRows, c, rc, xk + c * kChunkBytes, wtid, mx);
@@ -769,7 +788,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     if (soft) {
       // ---- epilogue: normalise O^T and store this split's f16 partial [D][64 heads]
-      unsigned char* stage = xk;
       ok = tc::bar_and(kBarSoft, kSoftThreads, ok && soft_ok);
       if (ok) {
         t->red[qd][hb + lane] = lw;
@@ -780,12 +798,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           t->alpha[st] = l > 0.f ? 1.f / l : 0.f;
         }
         tc::bar_named(kBarSoft, kSoftThreads);
-        // Normalised O^T as f16 rows [dim][64 heads] staged in the (now free) X
-        // region, 16-byte granule q of row r at granule q ^ (r & 7) (no bank
-        // conflicts; the merge reads the same swizzle), then one bulk copy. Each
-        // 128-dim block is staged as soon as the last tile's P.V of that block
-        // has finished (its stage bytes lie in X chunks whose P.V is done), so
-        // the staging overlaps the remaining MMAs.
+        if (st < hcount) {
+          const float l = t->lsum[st];
+          a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + st) * a.splits + split] =
+              l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
+        // Normalised O^T as f16 rows [dim][64 heads], 16-byte granule q of row r
+        // at granule q ^ (r & 7) (the merge reads the same swizzle), stored
+        // straight from registers: each thread writes 64 contiguous bytes of
+        // its dim's row. A 128-dim block is stored as soon as the last tile's
+        // P.V of that block has finished, overlapping the remaining MMAs.
+        const int hgs = gridDim.z;
+        unsigned char* part = reinterpret_cast<unsigned char*>(a.part_o) +
+                              ((static_cast<int64_t>(b) * a.splits + split) * hgs + blockIdx.z) * D * kHeads * 2;
         for (int c = 0; ok && c < nch; ++c) {
           if (!(ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->xfree[c], (nt - 1) & 1, abort)))) break;
           tc::tc_fence_after();
@@ -800,28 +825,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const int r = c * 128 + j;
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(stage + r * 128 + ((((hb >> 3) + q4) ^ (r & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(part + r * 128 + ((((hb >> 3) + q4) ^ (r & 7)) << 4)) =
                 make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
         }
-      }
-      if (ok) {
-        tc::fence_proxy_async_smem();
-        tc::bar_named(kBarSoft, kSoftThreads);
-        if (st == 0) {
-          const int hgs = gridDim.z;
-          uint16_t* part = reinterpret_cast<uint16_t*>(a.part_o) +
-                           ((static_cast<int64_t>(b) * a.splits + split) * hgs + blockIdx.z) * D * kHeads;
-          tc::bulk_store(part, stage, static_cast<uint32_t>(D) * kHeads * 2);
-          tc::bulk_commit();
-        }
-        if (st < hcount) {
-          const float l = t->lsum[st];
-          a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + st) * a.splits + split] =
-              l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-        }
-        // the stage must outlive the copy's reads; its global writes are
-        // performed by the time the grid completes, which the merge waits for
-        if (st == 0) tc::bulk_wait_read();
       }
     }
   }
