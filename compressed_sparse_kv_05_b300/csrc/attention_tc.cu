@@ -86,8 +86,8 @@ struct TcTail {
   alignas(16) uint32_t sk[kMaxTiles * kRows];   // key (or shared entry) scale of every row: raw fp32 until the
                                                 // tile's first chunk turns it into scale * 2^8 as f16x2 (0 for others)
   alignas(16) uint32_t sv[kMaxTiles * kRows];   // the same for the value scale (separate V)
-  float m_used[kHeads];             // running max per head, log2 domain
-  float alpha[kHeads];
+  alignas(16) float m_used[kHeads];   // running max per head, log2 domain (read as float4)
+  alignas(16) float alpha[kHeads];
   float lsum[kHeads];
   float red[4][kHeads];
 };
@@ -460,6 +460,24 @@ DSV4_DEV void load_scores32(uint32_t taddr, float c2, bool valid, float* s) {
   for (int i = 0; i < 32; ++i) s[i] = valid ? __uint_as_float(v[i]) * c2 : -INFINITY;
 }
 
+// The query rows a worker loaded (8-dim bf16 groups, item i = wtid + u *
+// workers, head i / gpr by the exact reciprocal qrcp) as f16 into the K-major
+// operand qs; a value beyond f16 raises RANGE.
+DSV4_DEV void stage_query(unsigned char* qs, const uint4* qw, int wtid, int gpr, uint32_t qrcp, int* status) {
+  float qmax = 0.f;
+#pragma unroll
+  for (int u = 0; u < kQItems; ++u) {
+    const int i = wtid + u * kWorkers;
+    if (i < kHeads * gpr) {
+      const int h = static_cast<int>(((static_cast<uint32_t>(i) >> 4) * qrcp) >> 16), d0 = (i - h * gpr) * 8;
+      const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
+      *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) =
+          bf16x8_to_f16x8(qw[u], qmax);
+    }
+  }
+  if (qmax >= kF16Max) atomicOr(status, DSV4_STATUS_RANGE);
+}
+
 }  // namespace
 
 // grid (splits, B, head groups), block 512. See the top of the file.
@@ -507,6 +525,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                       (i - h * gpr));
     }
   }
+  // CSA CTAs start long before the top-k they read is done: they stage the
+  // query in the meantime (HCA CTAs start just before the append ends, and
+  // stage it after the setup).
+  const bool q_early = a.n_sel > 0;
+  if (q_early && warp >= 2) stage_query(qs, qw, threadIdx.x - 64, gpr, qrcp, a.status);
   pdl_wait();
 
   const RowSpace rs = row_space(a, b);
@@ -668,18 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     {
       // the query, bf16 -> f16 into the K-major operand (heads beyond H zero)
-      float qmax = 0.f;
-#pragma unroll
-      for (int u = 0; u < kQItems; ++u) {
-        const int i = wtid + u * kWorkers;
-        if (i < kHeads * gpr) {
-          const int h = static_cast<int>(((static_cast<uint32_t>(i) >> 4) * qrcp) >> 16), d0 = (i - h * gpr) * 8;
-          const int atom = d0 >> 6, gg = (d0 >> 3) & 7;
-          *reinterpret_cast<uint4*>(qs + atom * kQAtomBytes + h * 128 + ((gg ^ (h & 7)) << 4)) =
-              bf16x8_to_f16x8(qw[u], qmax);
-        }
-      }
-      if (qmax >= kF16Max) atomicOr(a.status, DSV4_STATUS_RANGE);
+      if (!q_early) stage_query(qs, qw, wtid, gpr, qrcp, a.status);
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&t->qready);
@@ -737,7 +749,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       load_scores32(s_tmem + lane_off + hb, c2, valid, s);
       bool need = false;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) need |= s[i] > t->m_used[hb + i] + kRescale;
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mu = *reinterpret_cast<const float4*>(t->m_used + hb + i);
+        need |= (s[i] > mu.x + kRescale) | (s[i + 1] > mu.y + kRescale) | (s[i + 2] > mu.z + kRescale) |
+                (s[i + 3] > mu.w + kRescale);
+      }
       if (tc::bar_or(kBarSoft, kSoftThreads, need)) {
         // the running max of some head moves: reduce this tile's column max
         warp_reduce_scatter32<true>(s, lane);
@@ -768,7 +784,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
       // probabilities of this row and heads, f16, into P (row j, 16-byte chunks, swizzled)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s[i] = valid ? ex2(s[i] - t->m_used[hb + i]) : 0.f;
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mu = *reinterpret_cast<const float4*>(t->m_used + hb + i);
+        s[i] = valid ? ex2(s[i] - mu.x) : 0.f;
+        s[i + 1] = valid ? ex2(s[i + 1] - mu.y) : 0.f;
+        s[i + 2] = valid ? ex2(s[i + 2] - mu.z) : 0.f;
+        s[i + 3] = valid ? ex2(s[i + 3] - mu.w) : 0.f;
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const int i = g * 8, gc = (hb >> 3) + g;
@@ -819,9 +841,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           tc::tmem_wait_ld();
           uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = f32x2_to_f16x2(__uint_as_float(v[2 * i]) * t->alpha[hb + 2 * i],
-                                  __uint_as_float(v[2 * i + 1]) * t->alpha[hb + 2 * i + 1]);
+          for (int i = 0; i < 16; i += 2) {
+            const float4 al = *reinterpret_cast<const float4*>(t->alpha + hb + 2 * i);
+            w[i] = f32x2_to_f16x2(__uint_as_float(v[2 * i]) * al.x, __uint_as_float(v[2 * i + 1]) * al.y);
+            w[i + 1] = f32x2_to_f16x2(__uint_as_float(v[2 * i + 2]) * al.z, __uint_as_float(v[2 * i + 3]) * al.w);
+          }
           const int r = c * 128 + j;
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
