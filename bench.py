@@ -310,9 +310,11 @@ def traffic_for(call):
             rec = json.load(f).get(call)
         if not rec:
             return None
-        src = os.path.join(ROOT, rec["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return rec["bytes_per_launch"] if h == rec["source_sha"] else None
+        for src, sha in rec["sources"].items():
+            h = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+            if h != sha:
+                return None
+        return rec["bytes_per_launch"]
     except Exception:
         return None
 
