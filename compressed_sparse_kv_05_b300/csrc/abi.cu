@@ -309,7 +309,8 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   uint32_t cols = 32;
   while (cols < need) cols <<= 1;
   t.tmem_cols = cols;
-  t.n_tokens = c->n_tokens; t.idx_scales = c->idx_scales; t.q_scales = a.q_scales; t.wpad = a.wpad;
+  t.n_tokens = c->n_tokens; t.idx_codes = c->idx_codes; t.idx_scales = c->idx_scales; t.q_scales = a.q_scales;
+  t.wpad = a.wpad;
   t.scores = a.scores; t.hist1 = a.hist1; t.cnt = a.cnt; t.k = k; t.status = c->status;
   if ((e = launch_index_scores_tc(t, c->idx_codes, a.q_codes, st))) return e;
   int sel = (2 * kSms) / a.B;

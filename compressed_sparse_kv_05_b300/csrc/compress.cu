@@ -162,9 +162,25 @@ __global__ void __launch_bounds__(256) append_tail_kernel(AppendArgs a) {
 __global__ void __launch_bounds__(256) append_one_kernel(AppendArgs a) {
   extern __shared__ float smem[];
   pdl_trigger();
-  pdl_wait();
   const int b = blockIdx.x;
   const int D = a.d_nope + a.d_rope;
+  {
+    // The new token's rows are inputs no kernel of this library writes: their
+    // 128-byte lines are pulled into L1 while the previous kernel finishes, so
+    // the copies and the pooling after the wait find them there.
+    const int lk = D * 2 / 128, lu = a.idx_dim * 2 / 128;
+    const int i = threadIdx.x;
+    const char* p = nullptr;
+    if (i < lk) p = reinterpret_cast<const char*>(a.k + static_cast<int64_t>(b) * D) + i * 128;
+    else if (i < 2 * lk) p = reinterpret_cast<const char*>(a.z + static_cast<int64_t>(b) * D) + (i - lk) * 128;
+    else if (i < 3 * lk && a.separate_v) p = reinterpret_cast<const char*>(a.v + static_cast<int64_t>(b) * D) + (i - 2 * lk) * 128;
+    else if (i >= 3 * lk && i < 3 * lk + lu && a.u)
+      p = reinterpret_cast<const char*>(a.u + static_cast<int64_t>(b) * a.idx_dim) + (i - 3 * lk) * 128;
+    else if (i >= 3 * lk + lu && i < 3 * lk + 2 * lu && a.zu)
+      p = reinterpret_cast<const char*>(a.zu + static_cast<int64_t>(b) * a.idx_dim) + (i - 3 * lk - lu) * 128;
+    if (p) asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+  }
+  pdl_wait();
   const int m = a.ratio;
   const int64_t n_old = a.n_tokens[b];
   const int64_t n_new = n_old + 1;

@@ -22,25 +22,31 @@ namespace dsv4 {
 // zero codes, zero scales and zero weight.
 __global__ void quant_query_fp4_kernel(IndexArgs a) {
   pdl_trigger();
-  pdl_wait();
   const int row = blockIdx.x;               // b * N + h
   const int b = row / a.N, h = row % a.N;
   const int blk = threadIdx.x;
   const int nblk = a.Di / 16;
+  // the indexer query and head weights are inputs no kernel of this library
+  // writes: read before the wait; every write (the workspace) after it
+  const bool live = blk < nblk && h < a.Hi;
+  float v[16];
+  if (live) {
+    const uint16_t* src = a.q_idx + (static_cast<int64_t>(b) * a.Hi + h) * a.Di + blk * 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = bf16_to_f32(src[i]);
+  }
+  const float wv = blk == 0 && h < a.Hi ? a.w[b * a.Hi + h] : 0.f;
+  pdl_wait();
   if (blk >= nblk) return;
   uint8_t* codes = a.q_codes + static_cast<int64_t>(row) * (a.Di / 2) + blk * 8;
   uint8_t* scale = a.q_scales + static_cast<int64_t>(row) * nblk + blk;
-  if (h >= a.Hi) {
+  if (!live) {
     reinterpret_cast<uint2*>(codes)[0] = make_uint2(0u, 0u);
     *scale = 0;
   } else {
-    const uint16_t* src = a.q_idx + (static_cast<int64_t>(b) * a.Hi + h) * a.Di + blk * 16;
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = bf16_to_f32(src[i]);
     *scale = static_cast<uint8_t>(quant_fp4_block16(v, codes));
   }
-  if (blk == 0) a.wpad[row] = h < a.Hi ? a.w[b * a.Hi + h] : 0.f;
+  if (blk == 0) a.wpad[row] = wv;
   // zero this sequence's top-k histograms and counters (the N blocks of a sequence share the work)
   const int words = 2 * kBins + kCntWords;
   const int per = (words + a.N - 1) / a.N;

@@ -86,6 +86,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::prefetch_tensormap(&keys);
     tc::prefetch_tensormap(&qmap);
   }
+  if (threadIdx.x == 32 || threadIdx.x == 64) {
+    // While the previous kernel finishes (the memory system is otherwise idle
+    // then), this CTA's first ring's worth of key tiles is pulled into L2: a
+    // hint, with the tile range of a full cache (the real range needs
+    // n_tokens, read after the wait). Keys are only ever appended, and L2 is
+    // coherent with the append's writes.
+    const int tiles_c = static_cast<int>((static_cast<int64_t>(a.capacity) + kTile - 1) / kTile);
+    const int per_c = (tiles_c + a.ctas_per_seq - 1) / a.ctas_per_seq;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * per_c * kTile;
+    if (r0 < a.capacity) {
+      const int64_t want = static_cast<int64_t>(C::STAGES) * kTile;
+      const int64_t n = a.capacity - r0 < want ? a.capacity - r0 : want;
+      const int64_t row = static_cast<int64_t>(blockIdx.y) * a.capacity + r0;
+      if (threadIdx.x == 32) tc::prefetch_l2_bulk(a.idx_codes + row * ROWB, static_cast<uint32_t>(n * ROWB));
+      else tc::prefetch_l2_bulk(a.idx_scales + row * (ROWB / 8), static_cast<uint32_t>(n * (ROWB / 8)));
+    }
+  }
   pdl_wait();
 
   const int b = blockIdx.y;

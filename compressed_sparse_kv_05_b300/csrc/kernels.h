@@ -61,6 +61,7 @@ struct IndexTcArgs {
   int B, N, Di, capacity, ratio, ctas_per_seq, k;
   uint32_t tmem_cols;
   const int64_t* n_tokens;
+  const uint8_t* idx_codes;    // [B][capacity][Di/2] (read through the tensor map; its address for L2 prefetches)
   const uint8_t* idx_scales;   // [B][capacity][Di/16]
   const uint8_t* q_scales;     // [B][N][Di/16]
   const float* wpad;           // [B][N]
