@@ -220,7 +220,11 @@ DSV4_DEV void resolve_in_registers(int k, int64_t n_c, uint32_t n_above, uint32_
     d8 = *s_d;
     uint32_t r = need2 - *s_rem;   // lowest indices to take among the keys with low8 == d8
     const int64_t words = (n_c + 31) / 32;
-    if (words <= kBitmapWords) {
+    if (r >= h8[0][d8]) {
+      // every key equal to the boundary key is taken (no tie to break, the
+      // usual case): no index threshold
+      thr = 0xFFFFFFFFu;
+    } else if (words <= kBitmapWords) {
       // the tied blocks as bits: the r-th lowest set bit is the threshold
       uint32_t* bm = reinterpret_cast<uint32_t*>(dyn);
       const int per = static_cast<int>((words + kSelThreads - 1) / kSelThreads);
