@@ -293,20 +293,6 @@ DSV4_DEV void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* 
                : "memory");
 }
 
-// Bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16),
-// tracked by this thread's bulk-async groups.
-DSV4_DEV void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
-DSV4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk copy of this thread has completed (its writes are performed).
-DSV4_DEV void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Wait until every committed bulk copy of this thread has read its shared-memory
-// source (the writes complete on their own; the grid's completion covers them).
-DSV4_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
 DSV4_DEV void bar_named(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
 
 }  // namespace tc
