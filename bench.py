@@ -319,6 +319,21 @@ def traffic_for(call):
         return None
 
 
+def max_over_ranks(x, world, device):
+    """The largest x over the ranks (the slowest rank's time); x itself on one rank."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, batch, ms_per_step):
+    """Whole-job throughput: every rank decodes its own `batch` sequences (weak
+    scaling), one token each per step, in the slowest rank's step time."""
+    return world * batch * 1000.0 / ms_per_step
+
+
 def run_ours(args, rank, world):
     from compressed_sparse_kv_05_b300 import dsv4
     layers = WORKLOADS[args.workload]
@@ -373,13 +388,9 @@ def run_ours(args, rank, world):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, "cuda")
     ms_step = ms / K
-    value = world * B * 1000.0 / ms_step
+    value = job_tokens_per_s(world, B, ms_step)
 
     # per-call durations: K more steps through the graphs with events
     for g in ev_graphs:
@@ -427,12 +438,8 @@ def run_ours(args, rank, world):
         e1.record(stream)
     stream.synchronize()
     wall = (time.perf_counter() - w0) * 1e3
-    e2e_ms = max(e0.elapsed_time(e1), wall)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e = {"value": round(world * B * 1000.0 / (e2e_ms / K), 1), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), wall), world, "cuda")
+    e2e = {"value": round(job_tokens_per_s(world, B, e2e_ms / K), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": int(st.in_bytes), "d2h_bytes_per_step": int(st.out.numel() * 4)}
 
     line = {
