@@ -10,7 +10,14 @@ caches (2.8 GB) and every step's inputs are resident in HBM before timing. A
 step moves 393.5 MB of algorithmic bytes, more than the 126 MB L2, so no L2
 flush is needed between steps.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+The same JSON line also carries, measured in the same run: `layers`, one CSA
+and one HCA layer of the stack timed on their own (per-layer decode tokens/s),
+and `compress_1m`, the compressor streaming 2**20 tokens of 512 dims in
+4096-token chunks into a ratio-4 CSA cache (with FP4 indexer keys) and a
+ratio-128 HCA cache (cache GB/s read and written). `--workload` makes one of
+these, or the batched CSA configuration (csa_b32_128k), the headline instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 Prints one JSON line (rank 0). Under torchrun every rank runs its own four
 sequences (weak scaling, no data-path collective); `value` is the tokens/s of
@@ -46,8 +53,11 @@ WORKLOADS = {
     "stack_1m_csa": (W.STACK_CSA,),
     "stack_1m_hca": (W.STACK_HCA,),
     "csa_b32_128k": (W.CSA_B32_128K,),
+    "compress_1m": (W.COMPRESS_1M_CSA, W.COMPRESS_1M_HCA),
 }
 FALLBACK_HBM_GBS = 6400.0
+DTYPE = ("fp8-e4m3 / bf16 / fp4-e2m1 storage; attention on f16 tensor-core operands with fp32 accumulation, "
+         "indexer on block-scaled fp4 tensor-core operands with fp32 accumulation, pooling and softmax in fp32")
 
 
 def parse():
@@ -57,6 +67,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-compress", action="store_true", help="skip the compressor sub-measurement")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack_1m")
     return ap.parse_args()
 
@@ -230,10 +241,13 @@ class Stack:
                 cache.idx_codes[b, idx] = codes
                 cache.idx_scales[b, idx] = scales
 
-    def step(self, s, events=None):
-        """Launch one decode step (inputs of step slot s). events: dict call -> list of (start, end)."""
+    def step(self, s, events=None, only=None):
+        """Launch one decode step (inputs of step slot s). events: dict call -> list of (start, end).
+        only: run that one layer instead of the whole stack."""
         d = self.dsv4
         for li, L in enumerate(self.layers):
+            if only is not None and li != only:
+                continue
             desc, cache = self.descs[li], self.caches[li]
             v = lambda n: self.view(s, li, n)  # noqa: E731
             H = L.heads
@@ -262,6 +276,137 @@ class Stack:
                 timed("append", lambda: d.dsv4_compress_append(desc, cache, 1, v("k"), None, v("z"), self.bias[li],
                                                                None, None, None))
                 timed("hca_decode", lambda: d.dsv4_hca_decode(desc, cache, H, v("q"), L.sm_scale, out, lse, self.ws))
+
+
+class Compress:
+    """The compressor workload: one sequence of 2**20 tokens (512 dims, ~N(0,1))
+    streamed in 4096-token chunks into a ratio-4 CSA cache (with 128-dim FP4
+    indexer keys) and a ratio-128 HCA cache, each compressor with its own gate
+    logits ~N(0,1) and position bias ~N(0,0.1). A step appends the whole stream
+    to empty caches (n_tokens reset at its start), chunk by chunk: the CSA
+    cache's call, then the HCA cache's."""
+
+    def __init__(self, dsv4, seed):
+        self.dsv4 = dsv4
+        self.csa, self.hca = W.COMPRESS_1M_CSA, W.COMPRESS_1M_HCA
+        n, C = W.COMPRESS_1M_TOKENS, W.COMPRESS_1M_CHUNK
+        self.n, self.chunk = n, C
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed)
+
+        def bf16(shape):
+            t = torch.empty(shape, dtype=torch.int16, device="cuda")
+            for r0 in range(0, shape[0], 1 << 18):
+                r1 = min(shape[0], r0 + (1 << 18))
+                t[r0:r1].copy_(torch.randn((r1 - r0,) + shape[1:], generator=g, device="cuda")
+                               .to(torch.bfloat16).view(torch.int16))
+            return t
+
+        D, Di = self.csa.dim, self.csa.idx_dim
+        self.x = bf16((n, D))
+        self.z_csa = bf16((n, D))
+        self.z_hca = bf16((n, D))
+        self.u = bf16((n, Di))
+        self.zu = bf16((n, Di))
+        self.b_csa = 0.1 * torch.randn((self.csa.ratio, D), generator=g, device="cuda")
+        self.b_hca = 0.1 * torch.randn((self.hca.ratio, D), generator=g, device="cuda")
+        self.bu = 0.1 * torch.randn((self.csa.ratio, Di), generator=g, device="cuda")
+        self.d_csa = dsv4.layer_desc(self.csa, n // self.csa.ratio + 1)
+        self.d_hca = dsv4.layer_desc(self.hca, n // self.hca.ratio + 1)
+        self.c_csa = dsv4.Cache(self.d_csa)
+        self.c_hca = dsv4.Cache(self.d_hca)
+        torch.cuda.synchronize()
+
+    def input_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.x, self.z_csa, self.z_hca, self.u, self.zu))
+
+    def step(self):
+        d = self.dsv4
+        self.c_csa.n_tokens.zero_()
+        self.c_hca.n_tokens.zero_()
+        for t0 in range(0, self.n, self.chunk):
+            t1 = t0 + self.chunk
+            d.dsv4_compress_append(self.d_csa, self.c_csa, self.chunk, self.x[t0:t1], None, self.z_csa[t0:t1],
+                                   self.b_csa, self.u[t0:t1], self.zu[t0:t1], self.bu)
+            d.dsv4_compress_append(self.d_hca, self.c_hca, self.chunk, self.x[t0:t1], None, self.z_hca[t0:t1],
+                                   self.b_hca)
+
+
+def compress_bytes():
+    """Algorithmic bytes of one pass of the compressor workload: the token
+    stream read once (x shared by both compressors, each compressor's gate
+    logits, the indexer-key stream and its gates), the caches' entries and keys
+    written once."""
+    csa, hca = W.COMPRESS_1M_CSA, W.COMPRESS_1M_HCA
+    n = W.COMPRESS_1M_TOKENS
+    read = n * (csa.dim * 2 * 3 + csa.idx_dim * 2 * 2)
+    written = (n // csa.ratio) * (accounting.entry_bytes(csa) + accounting.idx_key_bytes(csa)) + \
+        (n // hca.ratio) * accounting.entry_bytes(hca)
+    return read, written
+
+
+def time_compress(dsv4, K, Wm, seed, peak, e2e=False):
+    """Times K passes of the compressor workload (one CUDA graph per pass) after
+    Wm warm-up passes; returns a dict of the figures (and the end-to-end pass
+    with the token stream copied from pinned host memory when e2e)."""
+    cp = Compress(dsv4, seed)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        cp.step()                                 # eager pass: kernel attributes set outside capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        cp.step()
+    probe = torch.cuda.CUDAGraph(keep_graph=True)      # captured only to count its kernel nodes
+    with torch.cuda.graph(probe, stream=stream):
+        cp.step()
+    kernels = count_kernel_nodes(probe)
+    del probe
+    for _ in range(Wm):
+        with torch.cuda.stream(stream):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        with torch.cuda.stream(stream):
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    read, written = compress_bytes()
+    gbs = (read + written) / (ms * 1e-3) / 1e9
+    out = {"workload": "compress_1m", "ms_per_pass": round(ms, 4), "tokens_per_s": round(cp.n / (ms * 1e-3), 1),
+           "GB/s": round(gbs, 1), "roofline_frac": round(gbs / peak, 4), "bytes_read": int(read),
+           "bytes_written": int(written),
+           "note": ("algorithmic bytes count the shared token stream x once; the two compressors are separate "
+                    "calls, so x is read twice (the bytes the kernels move exceed the algorithmic bytes by "
+                    f"{cp.x.numel() * 2 / 1e9:.2f} GB)"),
+           "kernel_nodes_per_pass": kernels,
+           "kernel_nodes_note": "library launches (two per append call) plus the two n_tokens resets"}
+    if e2e:
+        host = {n_: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n_, t in (("x", cp.x), ("z_csa", cp.z_csa), ("z_hca", cp.z_hca), ("u", cp.u), ("zu", cp.zu))}
+        for n_, t in host.items():
+            t.copy_(getattr(cp, n_).cpu())
+        res = torch.empty(2, dtype=torch.int64, pin_memory=True)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(K):
+                for n_, t in host.items():
+                    getattr(cp, n_).copy_(t, non_blocking=True)
+                g.replay()
+                res[0:1].copy_(cp.c_csa.n_tokens, non_blocking=True)
+                res[1:2].copy_(cp.c_hca.n_tokens, non_blocking=True)
+        stream.synchronize()
+        ms_e2e = (time.perf_counter() - w0) * 1e3 / K
+        out["e2e"] = {"value": round(cp.n / (ms_e2e * 1e-3), 1), "unit": "tokens/s", "ms_per_pass": ms_e2e,
+                      "h2d_bytes_per_step": int(cp.input_bytes()), "d2h_bytes_per_step": 16}
+    del g, cp
+    torch.cuda.synchronize()
+    return out
 
 
 def workload_config(name, layers, world, step_bytes):
@@ -343,8 +488,9 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     # input slots: [0, total) timed run, [total, total + K) per-call event run and
     # end-to-end run, then one eager warm-up step and one probe capture
-    # appends: eager warm-up, W + K timed, K per-call, K end-to-end steps
-    st = Stack(dsv4, layers, total + K + 2, seed=1234 + rank, extra_tokens=total + 2 * K + 2)
+    # appends: eager warm-up, W + K timed, K per-call, K end-to-end steps, and
+    # W + K steps of each layer timed on its own
+    st = Stack(dsv4, layers, total + K + 2, seed=1234 + rank, extra_tokens=2 * total + 2 * K + 4)
     stream = torch.cuda.Stream()
     # eager warm-up of every call (kernel attributes are set outside capture)
     with torch.cuda.stream(stream):
@@ -442,10 +588,41 @@ def run_ours(args, rank, world):
     e2e = {"value": round(job_tokens_per_s(world, B, e2e_ms / K), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": int(st.in_bytes), "d2h_bytes_per_step": int(st.out.numel() * 4)}
 
+    # per-layer decode: the first CSA and the first HCA layer of the stack, each
+    # replayed on its own (append + its attention calls), W + K graphs
+    per_layer = {}
+    if len(layers) > 1:
+        for li in (0, 1):
+            L = layers[li]
+            gs = []
+            for s in range(total):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    st.step(s, only=li)
+                gs.append(g)
+            for s in range(Wm):
+                with torch.cuda.stream(stream):
+                    gs[s].replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for s in range(Wm, total):
+                with torch.cuda.stream(stream):
+                    gs[s].replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            lms = max_over_ranks(e0.elapsed_time(e1), world, "cuda") / K
+            lbytes = accounting.decode_step_bytes(L) + accounting.call_bytes(L, "append")
+            per_layer[f"{args.workload}_{L.kind}"] = {
+                "layer": li, "kind": L.kind, "tokens_per_s": round(job_tokens_per_s(world, L.batch, lms), 1),
+                "ms_per_step": round(lms, 4), "bytes_per_step": int(lbytes),
+                "GB/s": round(lbytes / (lms * 1e-3) / 1e9, 1),
+                "roofline_frac": round(lbytes / (lms * 1e-3) / 1e9 / peak, 4)}
+            del gs
+
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8-e4m3/bf16/fp4-e2m1 storage, f32 compute", "data": "synthetic",
+        "dtype": DTYPE, "data": "synthetic",
         "config": workload_config(args.workload, layers, world, step_bytes),
         "step_bytes": int(step_bytes),
         "step_GBps": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
@@ -458,7 +635,47 @@ def run_ours(args, rank, world):
         "gpu_launches": (kernels_per_step * K) if kernels_per_step is not None else None,
         "clocks": clk,
     }
+    if per_layer:
+        line["layers"] = per_layer
+    if args.workload == "stack_1m" and not args.no_compress:
+        del graphs, ev_graphs, probe
+        line["compress_1m"] = time_compress(dsv4, min(K, 10), 3, 4321 + rank, peak)
     return line
+
+
+def run_compress(args, rank, world):
+    """The compressor workload as the headline: cache GB/s read and written."""
+    from compressed_sparse_kv_05_b300 import dsv4
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    peak, peak_kind = hbm_peak()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    r = time_compress(dsv4, args.steps, args.warmup, 4321 + rank, peak, e2e=True)
+    clk = clocks.stop()
+    ms = max_over_ranks(r["ms_per_pass"], world, "cuda")
+    read, written = compress_bytes()
+    gbs = world * (read + written) / (ms * 1e-3) / 1e9
+    e2e = r.pop("e2e")
+    e2e_ms = max_over_ranks(e2e.pop("ms_per_pass"), world, "cuda")
+    e2e["value"] = round(world * (read + written) / (e2e_ms * 1e-3) / 1e9, 1)
+    e2e["unit"] = "GB/s"
+    return {"metric": "compressor cache GB/s read + written (2^20 tokens of 512 dims in 4096-token chunks into "
+                      "a ratio-4 CSA and a ratio-128 HCA cache)",
+            "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE, "data": "synthetic",
+            "config": {"workload": "compress_1m", "tokens": W.COMPRESS_1M_TOKENS, "chunk": W.COMPRESS_1M_CHUNK,
+                       "kv_dim": "448 fp8 + 64 bf16", "csa": "ratio 4, FP4 indexer keys 128 dims",
+                       "hca": "ratio 128", "l2": f"inputs {(read / 1e9):.2f} GB per pass > 126 MB L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "compress_append", "achieved": round(gbs / world, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs / world / peak, 4), "peak_kind": peak_kind,
+                         "traffic": None, "algorithmic_bytes_per_launch": int(read + written)},
+            "detail": r, "e2e": e2e,
+            "gpu_launches": (r["kernel_nodes_per_pass"] - 2) * args.steps if r["kernel_nodes_per_pass"] else None,
+            "clocks": clk}
 
 
 # ----------------------------------------------------------------------------- the oracle on the host
@@ -511,50 +728,137 @@ def oracle_sample_step(sample):
                          p["k_nope"], p["k_scale"], p["k_rope"], p["ring"])
 
 
-def oracle_threads():
+def cpu_model():
     try:
-        from threadpoolctl import threadpool_info
-        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        return 1
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 def sample_desc(name, layers):
+    if name == "compress_1m":
+        return (f"the first {COMPRESS_SAMPLE_TOKENS} tokens of the compressor stream pooled and quantised into both "
+                f"caches per sample step; GB/s = algorithmic bytes of those tokens / sample-step time")
     kinds = sorted({L.kind.upper() for L in layers})
     return (f"one sequence x (one {' + one '.join(kinds)} layer) of {name} at the full context per sample step; "
             f"tokens/s = 1 / (sample-step time x {sample_scale(layers)})")
 
 
-def time_oracle(layers, steps, warmup):
-    sample = oracle_sample_setup(layers)
+COMPRESS_SAMPLE_TOKENS = 8192
+
+
+def oracle_compress_setup():
+    tag = "bench"
+    n = COMPRESS_SAMPLE_TOKENS
+    csa, hca = W.COMPRESS_1M_CSA, W.COMPRESS_1M_HCA
+    t = synth.token_stream(tag, 0, csa, 1, 0, n)
+    zh = synth.token_stream(tag, 1, hca, 1, 0, n)["z"]
+    return {"k": t["k"][0], "z": t["z"][0], "u": t["u"][0], "zu": t["zu"][0], "zh": zh[0],
+            "b": synth.position_bias(tag, 0, csa, "b"), "bu": synth.position_bias(tag, 0, csa, "bu"),
+            "bh": synth.position_bias(tag, 1, hca, "b")}
+
+
+def oracle_compress_step(p):
+    import oracle as O
+    csa, hca = W.COMPRESS_1M_CSA, W.COMPRESS_1M_HCA
+    O.build_cache(p["k"], p["z"], p["b"], csa.ratio, csa.d_nope, csa.window, None, p["u"], p["zu"], p["bu"])
+    O.build_cache(p["k"], p["zh"], p["bh"], hca.ratio, hca.d_nope, hca.window)
+
+
+def oracle_sample(name, layers):
+    """(sample inputs, step function) of the oracle for a workload."""
+    if name == "compress_1m":
+        return oracle_compress_setup(), oracle_compress_step
+    return oracle_sample_setup(layers), oracle_sample_step
+
+
+BLAS_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                    "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")
+
+
+def oracle_child(name, steps, warmup):
+    """Runs in a child process whose BLAS pool was sized by the environment
+    before numpy loaded: seconds per sample step of the oracle."""
+    sample, fn = oracle_sample(name, WORKLOADS[name])
     for _ in range(warmup):
-        oracle_sample_step(sample)
+        fn(sample)
     t = time.perf_counter()
     for _ in range(steps):
-        oracle_sample_step(sample)
-    return (time.perf_counter() - t) / steps
+        fn(sample)
+    return {"dt": (time.perf_counter() - t) / steps}
+
+
+def time_oracle(name, steps, warmup, threads):
+    """Seconds per sample step of the oracle with its BLAS threads pinned to
+    `threads`: timed in a child process started with every BLAS thread-count
+    variable set, so the pin holds whichever BLAS numpy carries."""
+    env = dict(os.environ)
+    for v in BLAS_THREAD_VARS:
+        env[v] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ("import json, bench; "
+            f"print('ORACLE ' + json.dumps(bench.oracle_child({name!r}, {int(steps)}, {int(warmup)})))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    for line in r.stdout.splitlines():
+        if line.startswith("ORACLE "):
+            return json.loads(line[7:])["dt"]
+    raise RuntimeError("oracle timing failed:\n" + r.stdout[-2000:] + r.stderr[-2000:])
+
+
+def oracle_rate(name, layers, dt):
+    """(value, unit) of the oracle from its sample-step time."""
+    if name == "compress_1m":
+        read, written = compress_bytes()
+        frac = COMPRESS_SAMPLE_TOKENS / W.COMPRESS_1M_TOKENS
+        return (read + written) * frac / dt / 1e9, "GB/s"
+    return 1.0 / (sample_scale(layers) * dt), "tokens/s"
 
 
 def cpu_baseline(name, layers, steps=2):
-    dt = time_oracle(layers, steps, 1)
-    return {"value": round(1.0 / (sample_scale(layers) * dt), 4), "unit": "tokens/s", "cores": oracle_threads(),
-            "kind": "oracle", "sample": sample_desc(name, layers), "s_per_sample_step": round(dt, 3)}
+    """The oracle as it stands (numpy; BLAS threads pinned explicitly) on a
+    bounded sample of the workload: with one BLAS thread per host core and with
+    one thread."""
+    n = os.cpu_count() or 1
+    dt_all = time_oracle(name, steps, 1, n)
+    dt_one = time_oracle(name, steps, 1, 1)
+    v_all, unit = oracle_rate(name, layers, dt_all)
+    v_one, _ = oracle_rate(name, layers, dt_one)
+    return {"value": round(v_all, 4), "unit": unit, "cores": n, "kind": "oracle", "sample": sample_desc(name, layers),
+            "s_per_sample_step": round(dt_all, 3), "cpu_model": cpu_model(),
+            "one_thread": {"value": round(v_one, 4), "cores": 1, "s_per_sample_step": round(dt_one, 3)}}
 
 
 def run_reference(args):
+    """The reference arm: the float64 oracle, as it stands, on the host cores,
+    on a bounded sample of the same workload (each step one sample step)."""
     layers = WORKLOADS[args.workload]
-    dt = time_oracle(layers, args.steps, args.warmup)
-    scale = sample_scale(layers)
-    value = 1.0 / (scale * dt)
+    n = os.cpu_count() or 1
+    dt = time_oracle(args.workload, args.steps, args.warmup, n)
+    value, unit = oracle_rate(args.workload, layers, dt)
     desc = sample_desc(args.workload, layers)
-    cb = {"value": round(value, 4), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle", "sample": desc}
-    config = workload_config(args.workload, layers, 1, sum(accounting.decode_step_bytes(L) for L in layers))
-    config["sample"] = desc
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * scale * 1e3, 2),
+    cb = {"value": round(value, 4), "unit": unit, "cores": n, "kind": "oracle", "sample": desc,
+          "cpu_model": cpu_model()}
+    if args.workload == "compress_1m":
+        metric = ("compressor cache GB/s read + written (2^20 tokens of 512 dims in 4096-token chunks into "
+                  "a ratio-4 CSA and a ratio-128 HCA cache)")
+        config = {"workload": "compress_1m", "tokens": W.COMPRESS_1M_TOKENS, "chunk": W.COMPRESS_1M_CHUNK}
+        projected = None
+    else:
+        metric = METRIC
+        step_bytes = sum(accounting.decode_step_bytes(L) + accounting.call_bytes(L, "append") for L in layers)
+        config = workload_config(args.workload, layers, 1, step_bytes)
+        projected = round(dt * sample_scale(layers) * layers[0].batch * 1e3, 2)
+    return {"impl": "reference", "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+            "sample_step": "each timed step is one sample step of the oracle (see cpu_baseline.sample)",
+            "projected_ms_per_full_step": projected,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config, "cpu_baseline": cb,
-            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
@@ -567,7 +871,7 @@ def main():
         return
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    line = run_ours(args, rank, world)
+    line = run_compress(args, rank, world) if args.workload == "compress_1m" else run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload, WORKLOADS[args.workload])

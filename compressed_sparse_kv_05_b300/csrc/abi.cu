@@ -12,8 +12,6 @@
 namespace dsv4 {
 namespace {
 
-constexpr int kSms = 148;                // streaming multiprocessors of a B300
-constexpr int kSplitTarget = 2 * kSms;  // CTAs the CUDA-core split-K attention aims for
 constexpr int kTcTile = 128;            // rows per tile of the tensor-core attention, at most
 constexpr int kTcMinTile = 32;          // and at least
 constexpr int kTcMaxTiles = 8;          // tiles per CTA of the tensor-core attention, at most
@@ -21,6 +19,31 @@ constexpr int kRowTile = 16;
 constexpr int kHeadGroup = 64;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Streaming multiprocessors of the current device, queried once per device
+// (148 on a B300; also the answer when no device can be queried, so that the
+// host-side plans stay defined without a GPU). Grids are sized from it.
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  constexpr int kDefault = 148;
+  static std::mutex mu;
+  static int count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return kDefault;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = kDefault;
+    }
+    count[dev] = n;
+  }
+  return count[dev];
+}
 
 int check_desc(const dsv4_layer_desc* d) {
   if (!d) return DSV4_ERR_INVALID_ARG;
@@ -69,10 +92,12 @@ struct AttnPlan {
   size_t ws_bytes;
 };
 
+// n_sel: top-k width (CSA), 0 for every entry (HCA), < 0 for none (window only).
 AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
   AttnPlan p{};
+  const int sms = sm_count();
   p.head_groups = (H + kHeadGroup - 1) / kHeadGroup;
-  const int64_t n_main = n_sel > 0 ? n_sel : d->capacity;
+  const int64_t n_main = n_sel > 0 ? n_sel : (n_sel < 0 ? 0 : d->capacity);
   const int64_t rmax = n_main + d->window;
   const size_t Dv = static_cast<size_t>(d->d_nope + d->d_rope);
   p.tc = attention_tc_supported(H, d->d_nope, d->d_rope, d->separate_v);
@@ -84,9 +109,9 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
     const int64_t units = static_cast<int64_t>(d->batch) * p.head_groups;
     auto tiles_for = [&](int64_t r) { return (n_main + r - 1) / r + (d->window + r - 1) / r; };
     int64_t tr = kTcTile;
-    while (tr > kTcMinTile && units * tiles_for(tr / 2) <= kSms) tr /= 2;
+    while (tr > kTcMinTile && units * tiles_for(tr / 2) <= sms) tr /= 2;
     const int64_t tiles = tiles_for(tr);
-    int64_t per_cta = (tiles * units + kSms - 1) / kSms;
+    int64_t per_cta = (tiles * units + sms - 1) / sms;
     if (per_cta > kTcMaxTiles) per_cta = kTcMaxTiles;   // a CTA keeps its rows' sources in shared memory
     if (per_cta < 1) per_cta = 1;
     p.tile_rows = static_cast<int>(tr);
@@ -99,7 +124,7 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
     p.ws_bytes = p.part_bytes + static_cast<size_t>(d->batch) * H * p.splits * sizeof(float) + 256;
     return p;
   }
-  const int64_t want = (kSplitTarget + d->batch * p.head_groups - 1) / (d->batch * p.head_groups);
+  const int64_t want = (2 * sms + d->batch * p.head_groups - 1) / (d->batch * p.head_groups);
   const int64_t max_splits = (rmax + kRowTile - 1) / kRowTile;
   int64_t s = want < max_splits ? want : max_splits;
   if (s < 1) s = 1;
@@ -147,8 +172,10 @@ void set_smem_once(std::once_flag& flag, F func, int bytes) {
 
 int launch_status() { return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA; }
 
+// n_sel: the top-k width (CSA), 0 for every entry (HCA), -1 for no compressed
+// entry at all (a window-only CSA call, k = 0).
 int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const uint16_t* q, float sm_scale,
-                  const int32_t* topk, int k, float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+                  const int32_t* topk, int n_sel, float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
   int e = check_desc(d);
   if (e) return e;
   if ((e = check_cache_read(d, c))) return e;
@@ -159,12 +186,12 @@ int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const ui
   DSV4_REQ(ws);
   if (lse && !aligned16(lse)) return DSV4_ERR_MISALIGNED;
   if (!(sm_scale == sm_scale)) return DSV4_ERR_INVALID_ARG;
-  const AttnPlan p = attn_plan(d, H, k);
+  const AttnPlan p = attn_plan(d, H, n_sel);
   if (ws_bytes < p.ws_bytes) return DSV4_ERR_WORKSPACE;
   AttnArgs a{};
   a.B = d->batch; a.H = H; a.D = d->d_nope + d->d_rope; a.Dv = a.D; a.d_nope = d->d_nope; a.d_rope = d->d_rope;
   a.ratio = d->ratio; a.window = d->window; a.capacity = d->capacity; a.separate_v = d->separate_v ? 1 : 0;
-  a.n_sel = k; a.splits = p.splits; a.rows_per_split = p.rows_per_split; a.sm_scale = sm_scale;
+  a.n_sel = n_sel; a.splits = p.splits; a.rows_per_split = p.rows_per_split; a.sm_scale = sm_scale;
   a.tile_rows = p.tile_rows; a.tiles_per_split = p.tiles_per_split;
   a.q = q; a.topk = topk;
   a.k_nope = c->k.nope; a.k_scale = c->k.scale; a.k_rope = c->k.rope; a.win_k = c->win_k;
@@ -302,7 +329,7 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   IndexTcArgs t{};
   t.B = a.B; t.N = N; t.Di = a.Di; t.capacity = a.capacity; t.ratio = a.ratio;
   const int tiles = (d->capacity + 127) / 128;
-  int per_seq = kSplitTarget / a.B;
+  int per_seq = 2 * sm_count() / a.B;
   if (per_seq < 1) per_seq = 1;
   t.ctas_per_seq = per_seq < tiles ? per_seq : tiles;
   uint32_t need = 2 * N + 3 * 4 * (a.Di / 64);
@@ -313,7 +340,7 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   t.wpad = a.wpad;
   t.scores = a.scores; t.hist1 = a.hist1; t.cnt = a.cnt; t.k = k; t.status = c->status;
   if ((e = launch_index_scores_tc(t, c->idx_codes, a.q_codes, st))) return e;
-  int sel = (2 * kSms) / a.B;
+  int sel = (2 * sm_count()) / a.B;
   const int sel_max = (d->capacity + 511) / 512;
   if (sel > sel_max) sel = sel_max;
   if (sel < 1) sel = 1;
@@ -323,8 +350,9 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
 int dsv4_csa_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q, float sm_scale,
                     const int32_t* topk, int32_t k, float* out, float* lse, void* ws, size_t ws_bytes,
                     void* stream) {
-  if (k < 1) return DSV4_ERR_INVALID_ARG;
+  if (k < 0) return DSV4_ERR_INVALID_ARG;
   if (k > 2048) return DSV4_ERR_UNSUPPORTED;
+  if (k == 0) return decode_common(d, c, H, q, sm_scale, nullptr, -1, out, lse, ws, ws_bytes, stream);
   if (!topk) return DSV4_ERR_INVALID_ARG;
   if (!aligned16(topk)) return DSV4_ERR_MISALIGNED;
   return decode_common(d, c, H, q, sm_scale, topk, k, out, lse, ws, ws_bytes, stream);
@@ -351,6 +379,8 @@ int dsv4_hca_decode_static(const dsv4_layer_desc* d, const dsv4_cache* c, int32_
 size_t dsv4_workspace_size(const dsv4_layer_desc* d, int32_t H, int32_t Hi, int32_t k) {
   if (check_desc(d) || H < 1 || H > 128 || Hi < 0 || Hi > 128 || k < 0 || k > 2048) return 0;
   size_t need = attn_plan(d, H, 0).ws_bytes;
+  const size_t win = attn_plan(d, H, -1).ws_bytes;
+  if (win > need) need = win;
   if (k > 0) {
     const size_t csa = attn_plan(d, H, k).ws_bytes;
     if (csa > need) need = csa;
@@ -360,6 +390,21 @@ size_t dsv4_workspace_size(const dsv4_layer_desc* d, int32_t H, int32_t Hi, int3
     if (idx > need) need = idx;
   }
   return need;
+}
+
+int dsv4_decode_plan(const dsv4_layer_desc* d, int32_t H, int32_t k, int32_t* plan) {
+  int e = check_desc(d);
+  if (e) return e;
+  if (!plan || H < 1 || k < -1) return DSV4_ERR_INVALID_ARG;
+  if (H > 128 || k > 2048) return DSV4_ERR_UNSUPPORTED;
+  const AttnPlan p = attn_plan(d, H, k > 0 ? k : (k == 0 ? -1 : 0));
+  plan[0] = p.tc ? 1 : 0;
+  plan[1] = p.splits;
+  plan[2] = p.tc ? p.tile_rows : p.rows_per_split;
+  plan[3] = p.tc ? p.tiles_per_split : 1;
+  plan[4] = p.head_groups;
+  plan[5] = sm_count();
+  return DSV4_OK;
 }
 
 int dsv4_read_status(const dsv4_cache* c, void* stream) {

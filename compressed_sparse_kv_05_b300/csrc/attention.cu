@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
   const int64_t n_tok = a.n_tokens[b];
   const int64_t n_c = n_tok / a.ratio < a.capacity ? n_tok / a.ratio : a.capacity;
   const int64_t n_win = n_tok < a.window ? n_tok : a.window;
-  const int64_t n_main = a.n_sel > 0 ? a.n_sel : n_c;
+  const int64_t n_main = a.n_sel > 0 ? a.n_sel : (a.n_sel < 0 ? 0 : n_c);
   const int64_t R = n_main + n_win;
   const int64_t r0 = static_cast<int64_t>(split) * a.rows_per_split;
   int64_t r1 = r0 + a.rows_per_split;

@@ -143,7 +143,7 @@ DSV4_DEV RowSpace row_space(const AttnArgs& a, int b) {
   s.n_tok = a.n_tokens[b];
   s.n_c = s.n_tok / a.ratio < a.capacity ? s.n_tok / a.ratio : a.capacity;
   s.n_win = s.n_tok < a.window ? s.n_tok : a.window;
-  s.n_main = a.n_sel > 0 ? a.n_sel : s.n_c;
+  s.n_main = a.n_sel > 0 ? a.n_sel : (a.n_sel < 0 ? 0 : s.n_c);
   s.mt = static_cast<int>((s.n_main + a.tile_rows - 1) / a.tile_rows);
   s.wt = static_cast<int>((s.n_win + a.tile_rows - 1) / a.tile_rows);
   return s;
@@ -183,16 +183,6 @@ DSV4_DEV int32_t row_source(const AttnArgs& a, const RowSpace& s, int b, const T
   }
   const int64_t pos = s.n_tok - s.n_win + r;
   return static_cast<int32_t>(-2 - pos % a.window);
-}
-
-// [p, p + bytes) into L2, both ends rounded down to 16 bytes (never past the range).
-DSV4_DEV void prefetch_range(const void* p, int64_t bytes) {
-  const uintptr_t lo = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
-  const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes) & ~static_cast<uintptr_t>(15);
-  for (uintptr_t x = lo; x < hi; x += (1u << 20)) {
-    const uintptr_t n = hi - x < (1u << 20) ? hi - x : (1u << 20);
-    tc::prefetch_l2_bulk(reinterpret_cast<const void*>(x), static_cast<uint32_t>(n));
-  }
 }
 
 DSV4_DEV void cp_async16(void* dst, const void* src) {
@@ -528,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   // CSA CTAs start long before the top-k they read is done: they stage the
   // query in the meantime (HCA CTAs start just before the append ends, and
   // stage it after the setup).
-  const bool q_early = a.n_sel > 0;
+  const bool q_early = a.n_sel != 0;
   if (q_early && warp >= 2) stage_query(qs, qw, threadIdx.x - 64, gpr, qrcp, a.status);
   pdl_wait();
 
@@ -672,8 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (!t1.win && tc::mbar_wait(&t->qready, 0, abort)) {
           const int64_t e0 = row_base + t1.r0;
           const int64_t n = (tl.win ? rs.n_main : tl.r0 + tl.cnt) - t1.r0;
-          if (lane == 1) prefetch_range(a.k_nope + e0 * a.d_nope, n * a.d_nope);
-          if (lane == 2 && a.d_rope) prefetch_range(a.k_rope + e0 * a.d_rope, n * a.d_rope * 2);
+          if (lane == 1) tc::prefetch_l2_range(a.k_nope + e0 * a.d_nope, n * a.d_nope);
+          if (lane == 2 && a.d_rope) tc::prefetch_l2_range(a.k_rope + e0 * a.d_rope, n * a.d_rope * 2);
         }
       }
     }

@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int64_t want = static_cast<int64_t>(C::STAGES) * kTile;
       const int64_t n = a.capacity - r0 < want ? a.capacity - r0 : want;
       const int64_t row = static_cast<int64_t>(blockIdx.y) * a.capacity + r0;
-      if (threadIdx.x == 32) tc::prefetch_l2_bulk(a.idx_codes + row * ROWB, static_cast<uint32_t>(n * ROWB));
-      else tc::prefetch_l2_bulk(a.idx_scales + row * (ROWB / 8), static_cast<uint32_t>(n * (ROWB / 8)));
+      // a sequence's slice of the scale plane starts on a 16-byte boundary only
+      // when capacity * Di / 16 is a multiple of 16: the range helper trims it
+      if (threadIdx.x == 32) tc::prefetch_l2_range(a.idx_codes + row * ROWB, n * ROWB);
+      else tc::prefetch_l2_range(a.idx_scales + row * (ROWB / 8), n * (ROWB / 8));
     }
   }
   pdl_wait();

@@ -76,7 +76,7 @@ int launch_index_scores_tc(const IndexTcArgs& a, const uint8_t* key_codes, const
 // ---- attention
 struct AttnArgs {
   int B, H, D, Dv, d_nope, d_rope, ratio, window, capacity, separate_v;
-  int n_sel;               // top-k width (CSA) or 0 for HCA (every entry)
+  int n_sel;               // top-k width (CSA), 0 for HCA (every entry), -1 for none (window only)
   int splits, rows_per_split;
   int tile_rows;           // tensor-core kernel: rows per tile (32, 64 or 128)
   int tiles_per_split;     // tensor-core kernel: tiles per CTA

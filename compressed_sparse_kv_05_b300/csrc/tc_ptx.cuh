@@ -252,6 +252,18 @@ DSV4_DEV void prefetch_l2_bulk(const void* p, uint32_t bytes) {
                : "memory");
 }
 
+// Hint: bring the 16-byte granules inside [p, p + bytes) into L2, for any p and
+// bytes (the start rounded up and the end rounded down to 16 bytes, so the bulk
+// prefetch never starts unaligned nor passes the range), in pieces of 1 MiB.
+DSV4_DEV void prefetch_l2_range(const void* p, int64_t bytes) {
+  const uintptr_t lo = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes) & ~static_cast<uintptr_t>(15);
+  for (uintptr_t x = lo; x < hi; x += (1u << 20)) {
+    const uintptr_t n = hi - x < (1u << 20) ? hi - x : (1u << 20);
+    prefetch_l2_bulk(reinterpret_cast<const void*>(x), static_cast<uint32_t>(n));
+  }
+}
+
 // Named barrier `id` over `count` threads that also ORs (resp. ANDs) a predicate
 // across them; every participating thread gets the result.
 DSV4_DEV bool bar_or(int id, int count, bool v) {

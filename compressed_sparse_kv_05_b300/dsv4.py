@@ -59,6 +59,7 @@ _SIGS = {
     "dsv4_hca_decode": ([_DESC, _CACHE, _I32, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "dsv4_hca_decode_static": ([_DESC, _CACHE, _I32, _P, ctypes.c_float, _P, _P, _P], ctypes.c_int),
     "dsv4_workspace_size": ([_DESC, _I32, _I32, _I32], ctypes.c_size_t),
+    "dsv4_decode_plan": ([_DESC, _I32, _I32, _P], ctypes.c_int),
     "dsv4_read_status": ([_CACHE, _P], ctypes.c_int),
     "dsv4_quantize_kv_rows": ([_P, _I64, _I32, _I32, _P, _P, _P, _P], ctypes.c_int),
     "dsv4_quantize_fp4_rows": ([_P, _I64, _I32, _P, _P, _P], ctypes.c_int),
@@ -171,6 +172,13 @@ def dsv4_hca_decode_static(desc, cache, H, q, sm_scale, out, lse, stream=None):
 
 def dsv4_workspace_size(desc, H, Hi, k):
     return int(lib.dsv4_workspace_size(ctypes.byref(desc), H, Hi, k))
+
+
+def dsv4_decode_plan(desc, H, k):
+    """Launch plan of a decode call (k: top-k width, 0 window-only CSA, -1 HCA) as a dict."""
+    plan = (ctypes.c_int32 * 6)()
+    _check("dsv4_decode_plan", lib.dsv4_decode_plan(ctypes.byref(desc), H, k, ctypes.cast(plan, ctypes.c_void_p)))
+    return dict(zip(("tensor_core", "splits", "tile_rows", "tiles_per_split", "head_groups", "sms"), list(plan)))
 
 
 def dsv4_read_status(cache, stream=None):

@@ -158,7 +158,9 @@ int dsv4_index_topk(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_
  *   q    : [B][H][D] bf16 query (used exactly)
  *   topk : [B][k] int32 entry indices (-1 = none); duplicates count twice
  *   out  : [B][H][D] fp32;  lse : [B][H] fp32 or NULL
- * Supported: 1 <= H <= 128, 1 <= k <= 2048. */
+ * k = 0 attends over the window alone (topk is not read and may be NULL): the
+ * standard sliding-window layer that follows the CSA / HCA stack ([HCA]).
+ * Supported: 1 <= H <= 128, 0 <= k <= 2048. */
 int dsv4_csa_decode(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_t H,
                     const uint16_t* q, float sm_scale, const int32_t* topk, int32_t k,
                     float* out, float* lse, void* ws, size_t ws_bytes, void* stream);
@@ -197,6 +199,15 @@ int dsv4_hca_decode_static(const dsv4_layer_desc* desc, const dsv4_cache* cache,
 /* Bytes of device workspace the calls above need for this layer with H query
  * heads, Hi indexer heads and top-k k (0 when the arguments are invalid). */
 size_t dsv4_workspace_size(const dsv4_layer_desc* desc, int32_t H, int32_t Hi, int32_t k);
+
+/* How a decode call of this layer splits its work (the pages describe no such
+ * call: it exposes the launch plan for tests and capacity planning). k is the
+ * top-k width of a dsv4_csa_decode call (0: its window-only form), or -1 for
+ * dsv4_hca_decode. Writes plan[0..5] = {tensor-core path (1) or CUDA-core path
+ * (0), splits per (sequence, head group), rows per tile (tensor-core path) or
+ * rows per split (CUDA-core path), tiles per split, head groups of 64,
+ * streaming multiprocessors planned for}. Host only; launches nothing. */
+int dsv4_decode_plan(const dsv4_layer_desc* desc, int32_t H, int32_t k, int32_t* plan);
 
 /* Waits for `stream`, then returns the cache's status bits (>= 0) and clears
  * them; a negative DSV4_ERR_* on failure. */

@@ -95,8 +95,10 @@ def test_csa_and_index_reject_bad_arguments_on_host(dsv4):
     d = _desc(dsv4)
     c = _cache(dsv4)
     L = dsv4.lib
-    assert L.dsv4_csa_decode(ctypes.byref(d), ctypes.byref(c), 64, FAKE, 0.1, FAKE, 0, FAKE, None, FAKE, 1 << 40,
+    assert L.dsv4_csa_decode(ctypes.byref(d), ctypes.byref(c), 64, FAKE, 0.1, FAKE, -1, FAKE, None, FAKE, 1 << 40,
                              None) == dsv4.ERR_INVALID_ARG
+    assert L.dsv4_csa_decode(ctypes.byref(d), ctypes.byref(c), 64, FAKE, 0.1, None, 0, None, None, FAKE, 1 << 40,
+                             None) == dsv4.ERR_INVALID_ARG           # window-only call: out still required
     assert L.dsv4_csa_decode(ctypes.byref(d), ctypes.byref(c), 64, FAKE, 0.1, FAKE, 4096, FAKE, None, FAKE, 1 << 40,
                              None) == dsv4.ERR_UNSUPPORTED
     assert L.dsv4_csa_decode(ctypes.byref(d), ctypes.byref(c), 64, FAKE, 0.1, FAKE + 4, 512, FAKE, None, FAKE,
@@ -137,3 +139,28 @@ def test_quantizers_and_pool_reject_bad_arguments_on_host(dsv4):
     assert L.dsv4_pool_rows(FAKE, FAKE, FAKE, 10, 0, 128, FAKE, None) == dsv4.ERR_INVALID_ARG
     assert L.dsv4_pool_rows(FAKE, FAKE, FAKE, 10, 4, 100, FAKE, None) == dsv4.ERR_UNSUPPORTED
     assert L.dsv4_read_status(None, None) == dsv4.ERR_INVALID_ARG
+
+
+def test_decode_plan_on_host(dsv4):
+    """The launch plan the decode calls take, computed on the host (148 SMs
+    when no device can be queried): the batched CSA configuration (B = 32,
+    top-512, window 128) takes 128-row tiles gathered two per CTA in three
+    splits; the four-sequence decode step takes 32-row tiles; a window-only
+    call plans the window tiles alone; D = 192 takes the CUDA-core path."""
+    sms = dsv4.dsv4_decode_plan(_desc(dsv4), 64, 512)["sms"]
+    if sms != 148:
+        pytest.skip(f"plans below are worked out for 148 SMs, this device has {sms}")
+    p = dsv4.dsv4_decode_plan(_desc(dsv4, batch=32, capacity=32768), 64, 512)
+    assert (p["tensor_core"], p["tile_rows"], p["tiles_per_split"], p["splits"]) == (1, 128, 2, 3)
+    p = dsv4.dsv4_decode_plan(_desc(dsv4, capacity=262144), 64, 512)
+    assert (p["tensor_core"], p["tile_rows"], p["tiles_per_split"], p["splits"]) == (1, 32, 1, 20)
+    p = dsv4.dsv4_decode_plan(_desc(dsv4, ratio=128, idx_dim=0, capacity=8192), 64, -1)
+    assert (p["tile_rows"], p["tiles_per_split"], p["splits"]) == (128, 2, 33)
+    p = dsv4.dsv4_decode_plan(_desc(dsv4, capacity=262144), 64, 0)
+    assert (p["tile_rows"], p["splits"]) == (32, 4)                    # 128 window rows, no entries
+    p = dsv4.dsv4_decode_plan(_desc(dsv4, d_nope=128, d_rope=64), 64, 512)
+    assert p["tensor_core"] == 0
+    p = dsv4.dsv4_decode_plan(_desc(dsv4), 128, 512)
+    assert p["head_groups"] == 2
+    with pytest.raises(dsv4.Dsv4Error):
+        dsv4.dsv4_decode_plan(_desc(dsv4), 64, -2)

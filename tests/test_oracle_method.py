@@ -93,6 +93,33 @@ def test_kv_quant_exact_on_representable_rows():
     assert np.array_equal(rope, bf16(y[:, dn:]))
 
 
+def test_dequant_kv_rows_against_library_decode():
+    """dequant_kv_rows against torch's own e4m3 and bf16 decodes, on entries
+    whose row count, code dims and RoPE dims all differ and whose per-row scales
+    all differ: each value is its code times its own row's scale, then the RoPE
+    dims follow in order (a scale broadcast along the wrong axis, a row slip or
+    a dropped RoPE block fails)."""
+    r = np.random.default_rng(31)
+    R, dn, dr = 37, 48, 16
+    codes = r.integers(0, 256, size=(R, dn)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C                                   # no NaN codes
+    s = (np.exp2(r.integers(-30, 10, R)) * r.choice([1.0, 1.25, 1.5, 1.75], R)).astype(np.float32)
+    rope = bf16(rnd(32, (R, dr)))
+    got = O.dequant_kv_rows(codes, s, rope)
+    lib_codes = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    lib_rope = torch.from_numpy(rope.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    want = np.concatenate([lib_codes * s.astype(np.float64)[:, None], lib_rope], axis=1)
+    assert got.shape == (R, dn + dr) and np.array_equal(got, want)
+    # exactly representable rows come back unchanged through quantise -> dequantise
+    codes2 = r.integers(0, 0x7F, size=(R, dn)).astype(np.uint8)
+    codes2[:, 7] = 0x7E                                                    # each row reaches 448 * s
+    s2 = np.exp2(r.integers(-24, 6, R)).astype(np.float32)
+    y = np.concatenate([(torch.from_numpy(codes2).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+                         * s2.astype(np.float64)[:, None]).astype(np.float32),
+                        O.bf16_decode(rope).astype(np.float32)], axis=1)
+    assert np.array_equal(O.dequant_kv_rows(*O.quantize_kv_rows(y, dn)), y.astype(np.float64))
+
+
 def test_kv_quant_zero_row_and_error_bound():
     y = rnd(20, (40, 80))
     y[3, :64] = 0.0

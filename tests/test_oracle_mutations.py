@@ -105,3 +105,18 @@ def test_scale_dropped_from_dequant_is_caught(monkeypatch):
     _patch(monkeypatch, "dequant_kv_rows",
            lambda nope, scale, rope: np.concatenate([F.e4m3_decode(nope), F.bf16_decode(rope)], axis=1), M)
     _fails(TM.test_csa_ratio1_all_selected_no_window_is_full_attention)
+
+
+def test_dequant_row_slip_is_caught(monkeypatch):
+    # each row takes its neighbour's scale (a row slip between the code and scale planes)
+    _patch(monkeypatch, "dequant_kv_rows",
+           lambda nope, scale, rope: np.concatenate([F.e4m3_decode(nope) * np.roll(np.asarray(scale, np.float64), 1)[:, None],
+                                                     F.bf16_decode(rope)], axis=1), M)
+    _fails(TM.test_dequant_kv_rows_against_library_decode)
+
+
+def test_dequant_rope_block_dropped_is_caught(monkeypatch):
+    _patch(monkeypatch, "dequant_kv_rows",
+           lambda nope, scale, rope: np.concatenate([F.e4m3_decode(nope) * np.asarray(scale, np.float64)[:, None],
+                                                     np.zeros(np.shape(rope))], axis=1), M)
+    _fails(TM.test_dequant_kv_rows_against_library_decode)

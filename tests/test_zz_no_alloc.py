@@ -6,7 +6,8 @@ static device array inside the library instead of a caller workspace.
 Checked through the C ABI against dsv4_hca_decode on the same cache: two calls
 in a row with different queries (the static array keeps the previous call's
 contents), on a separate-K/V layer and on a shared-entry layer that spans
-several tiles and splits; and an oversized call is refused on the host.
+several tiles and splits (there also against the float64 oracle); and an
+oversized call is refused on the host.
 
 This file is named to be collected last, so a failure here never hides the
 other GPU tests when pytest stops at the first failure."""
@@ -17,7 +18,8 @@ import torch
 from compressed_sparse_kv_05_b300 import dsv4, synth
 from compressed_sparse_kv_05_b300 import workloads as W
 
-from .gpu_util import gpu_cache_from_planes, gpu_stream_cache, oracle_direct_planes, row_rel_err, to_dev, to_host
+from .gpu_util import (gpu_cache_from_planes, gpu_stream_cache, oracle_attend_planes, oracle_direct_planes,
+                       row_rel_err, to_dev, to_host)
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
@@ -38,15 +40,20 @@ def _both(desc, cache, layer, q):
     return to_host(got), to_host(got_lse), to_host(ref), to_host(ref_lse)
 
 
-def _check_two_calls(desc, cache, layer, tag):
+def _check_two_calls(desc, cache, layer, tag, planes=None):
     need = dsv4.dsv4_workspace_size(desc, layer.heads, 0, 0)
     assert 0 < need <= dsv4.STATIC_SCRATCH_BYTES
     for call in range(2):
-        q = to_dev(synth.decode_inputs(f"{tag}{call}", 0, layer)["q"])
-        got, got_lse, ref, ref_lse = _both(desc, cache, layer, q)
+        q_host = synth.decode_inputs(f"{tag}{call}", 0, layer)["q"]
+        got, got_lse, ref, ref_lse = _both(desc, cache, layer, to_dev(q_host))
         assert np.isfinite(got).all() and np.isfinite(got_lse).all()
         assert row_rel_err(got, ref).max() <= TOL
         assert np.abs(got_lse - ref_lse).max() <= 1e-3
+        for b, p in enumerate(planes or ()):
+            # and against the float64 oracle on the same cache planes
+            o_out, o_lse = oracle_attend_planes(layer, p, q_host[b], None)
+            assert row_rel_err(got[b], o_out).max() <= TOL
+            assert np.abs(got_lse[b] - o_lse).max() <= 1e-3
     assert dsv4.dsv4_read_status(cache) == 0
 
 
@@ -60,7 +67,7 @@ def test_static_scratch_matches_workspace_shared_entry():
     layer = W.scaled(W.STACK_HCA, batch=2, n_tokens=128 * 1500)
     planes = oracle_direct_planes(layer, "static", 1, range(layer.batch))
     desc, cache = gpu_cache_from_planes(layer, planes)
-    _check_two_calls(desc, cache, layer, "static-shared")
+    _check_two_calls(desc, cache, layer, "static-shared", planes)
 
 
 def test_static_scratch_refuses_oversized_calls():
