@@ -119,9 +119,9 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
     p.rows_per_split = static_cast<int>(per_cta * tr);
     p.splits = static_cast<int>((tiles + per_cta - 1) / per_cta);
     if (p.splits < 1) p.splits = 1;
-    // f16 partials [B][splits][head groups][D][64], then fp32 log-sum-exps [B][H][splits]
+    // f16 partials [B][splits][head groups][D][64], then two fp32 log sums [B][H][splits] each
     p.part_bytes = (static_cast<size_t>(d->batch) * p.splits * p.head_groups * Dv * 64 * 2 + 255) & ~size_t(255);
-    p.ws_bytes = p.part_bytes + static_cast<size_t>(d->batch) * H * p.splits * sizeof(float) + 256;
+    p.ws_bytes = p.part_bytes + 2 * static_cast<size_t>(d->batch) * H * p.splits * sizeof(float) + 256;
     return p;
   }
   const int64_t want = (2 * sms + d->batch * p.head_groups - 1) / (d->batch * p.head_groups);
@@ -200,6 +200,7 @@ int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const ui
   char* w = static_cast<char*>(ws);
   a.part_o = reinterpret_cast<float*>(w);
   a.part_lse = reinterpret_cast<float*>(w + p.part_bytes);
+  a.part_lsev = a.part_lse + static_cast<size_t>(d->batch) * H * p.splits;
   a.out = out; a.lse = lse;
   if (p.tc) return launch_attention_tc(a, p.head_groups, static_cast<cudaStream_t>(stream));
   return launch_attention(a, p.head_groups, static_cast<cudaStream_t>(stream));

@@ -224,9 +224,11 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
 }
 
 // Merge of the tensor-core kernel's splits: partials are f16 [B][splits][head
-// groups][D][64 heads] (normalised; in each 128-byte row of a dim d the
-// 16-byte granule of heads 8q .. 8q + 7 sits at granule q ^ (d & 7)),
-// log-sum-exps fp32 [B][H][splits].
+// groups][D][64 heads] (each normalised to a convex combination of its rows;
+// in each 128-byte row of a dim d the 16-byte granule of heads 8q .. 8q + 7
+// sits at granule q ^ (d & 7)), with two fp32 log sums [B][H][splits] each:
+// lse_s, of the split's softmax weights, and lse'_s, of the scale of its
+// partial, so that out = sum_s exp(lse'_s) o_s / sum_s exp(lse_s).
 // grid (B * head groups, D / 8), block 256: 8 dims x 64 heads per CTA; thread
 // t takes split group t / 64 (splits s = t / 64 mod 4), dim t / 8 % 8 and
 // heads 8 (t % 8) .. + 7. Per pass of up to 64 splits every thread issues its
@@ -247,13 +249,14 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
   const int h0 = hg * 64;
   const int hcount = a.H - h0 < 64 ? a.H - h0 : 64;
   __shared__ float s_lse[64][kS + 1];                   // [head][split]
-  __shared__ __align__(16) float s_w[kS][64 + 4];       // [split][head]: weights relative to the running max
+  __shared__ __align__(16) float s_w[kS][64 + 4];       // [split][head]: partial weights relative to the running max
   __shared__ float s_m[64], s_l[64], s_r[64];           // running max and sum per head, rescale of this pass
   __shared__ float s_acc[kSg][64][9];
   const int t = threadIdx.x;
   const int sg = t >> 6, dl = (t >> 3) & 7, hq = (t & 7) * 8;
   const int d = blockIdx.y * 8 + dl;
   const float* lse0 = a.part_lse + (static_cast<int64_t>(b) * a.H + h0) * a.splits;
+  const float* lsev0 = a.part_lsev + (static_cast<int64_t>(b) * a.H + h0) * a.splits;
   // granule hq / 8 of dim d sits at granule (hq / 8) ^ (d & 7) of the row
   const int dd0 = d < a.D ? d : 0;
   const uint16_t* part = reinterpret_cast<const uint16_t*>(a.part_o) +
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
   for (int s0 = 0; s0 < a.splits; s0 += kS) {
     const int ns = a.splits - s0 < kS ? a.splits - s0 : kS;
     uint4 v[kU];
-    float lv[kL];
+    float lv[kL], lvv[kL];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int s = sg + kSg * u;
@@ -278,12 +281,15 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
 #pragma unroll
     for (int u = 0; u < kL; ++u) {
       const int i = t + u * kT, h = i >> 6, s = i & (kS - 1);
-      lv[u] = h < hcount && s < ns ? __ldcg(lse0 + static_cast<int64_t>(h) * a.splits + s0 + s) : -INFINITY;
+      const bool in = h < hcount && s < ns;
+      lv[u] = in ? __ldcg(lse0 + static_cast<int64_t>(h) * a.splits + s0 + s) : -INFINITY;
+      lvv[u] = in ? __ldcg(lsev0 + static_cast<int64_t>(h) * a.splits + s0 + s) : -INFINITY;
     }
 #pragma unroll
     for (int u = 0; u < kL; ++u) {
       const int i = t + u * kT;
       s_lse[i >> 6][i & (kS - 1)] = lv[u];
+      s_w[i & (kS - 1)][i >> 6] = lvv[u];     // lse', turned into the output weight below
     }
     __syncthreads();
     {
@@ -296,10 +302,12 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
       const float mo = s_m[h], mn = fmaxf(mo, mx);
       float sum = 0.f;
       for (int s = part4; s < ns; s += 4) {
-        // weight relative to the running max; a split without rows gets 0
+        // weights relative to the running max: of the normaliser (w) and of the
+        // split's partial (u); a split without rows gets 0
         const float x = s_lse[h][s];
         const float w = x == -INFINITY ? 0.f : __expf(x - mn);
-        s_w[s][h] = w;
+        const float u = x == -INFINITY ? 0.f : __expf(s_w[s][h] - mn);
+        s_w[s][h] = u;
         sum += w;
       }
       sum += __shfl_xor_sync(0xffffffffu, sum, 1);

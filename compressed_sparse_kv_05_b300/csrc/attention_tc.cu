@@ -32,22 +32,47 @@
 //               boxes (contiguous rows); the others prefetch later tiles into L2;
 //   warps 2-15  (448 workers) copy gathered rows (CSA, and every window token)
 //               with cp.async, convert the query, and dequantise every chunk in
-//               place: e4m3 codes become f16 by the hardware conversion, then
-//               two exact-range f16 multiplies (by 2^-8, then by scale * 2^8).
+//               place (see "row exponents" below).
 //               Warps 4-7 and 12-15 (two per 32-lane quarter of tensor memory)
-//               also turn S^T into P: the running max of a head only moves when
-//               a score exceeds it by more than 2^8 (then O^T and l are
-//               rescaled), so P <= 256 always fits f16. After the last tile they
+//               also turn S^T into P (see below). After the last tile they
 //               normalise O^T and store this split's partial output as f16
 //               (rows of 64 heads per dim, 16-byte granules swizzled by dim).
 // Splits are merged by attn_merge_tc_kernel (attention.cu).
 //
-// Precision: K, V and P are rounded to f16 (relative error <= 2^-11 each; a
-// row's scale is rounded to f16 once), the bf16 query converts to f16 exactly
-// for |q| in [2^-14, 65504]; products and sums are fp32; split partials are
-// stored as f16. A value that does not fit f16 (|x| >= 65504) raises
-// DSV4_STATUS_RANGE. The two e4m3 NaN codes (never written by the quantiser)
-// decode to NaN, as the format defines them.
+// Row multipliers. Every row j of a tile is held in X as a normalised f16 row
+// X_j = key_j / mu_j, with a positive fp32 multiplier mu_j per row:
+//   entry   mu_j = 256 * scale_j: the codes become code * 2^-8, exactly (the
+//           hardware e4m3 -> f16 conversion is exact, the multiply by 2^-8
+//           too), and the RoPE dims rope / mu_j (rounded once);
+//   window  mu_j = 2^L_j, L_j the binade of the row's largest |value| over all
+//           D dims (the row lands in [1, 2) at its largest element).
+// So f16 holds every row to 11 significant bits whatever the entry's scale or
+// the token's magnitude, and an entry's FP8 dims exactly. The scores take the
+// multiplier back in fp32:
+//   s_jh = (X_j . q_h) * mu_j * sm_scale * log2(e)               (log2 domain)
+// and the normaliser of head h is l_h = sum_j 2^(s_jh - m_h) with a running
+// max m_h. The value side keeps its own running max M_h of s_jh + L'_j (L'_j
+// the binade of mu'_j, the multiplier of row j's value row: mu_j itself when
+// K = V):
+//   P_jh = 2^(s_jh - M_h) mu'_j = p_jh * (mu'_j / 2^T) * 2^(T + m_h - M_h),
+//   O_h = sum_j P_jh X'_j,
+// with p_jh = 2^(s_jh - m_h), T the largest L'_j of the tile: a factor of the
+// row (< 2) and a power of two of the head. Both maxima are integers that
+// move only when a tile exceeds them by more than 2^8 (then l, resp. O^T, is
+// rescaled by an exact power of two), so p <= 256 and P < 512. The split's
+// partial output is stored normalised by l'_h = sum_j P_jh (a convex
+// combination of normalised rows, so it fits f16) with two natural-log sums:
+// lse = ln(2^m_h l_h) and lse' = ln(2^M_h l'_h); the merge weighs each
+// split's partial by exp(lse' - max lse) and divides by sum exp(lse - max lse).
+//
+// Precision: the RoPE dims and window values in X, P and the split partials
+// are rounded to f16 (relative error <= 2^-11 each); the FP8 dims are exact;
+// the bf16 query converts to f16 exactly for |q| in [2^-14, 65504]; products,
+// sums and multipliers are fp32. A query element of
+// magnitude >= 65504, or RoPE dims more than 2^15 times an entry's largest FP8
+// value, do not fit the f16 operands and raise DSV4_STATUS_RANGE. The two
+// e4m3 NaN codes (never written by the quantiser) decode to NaN, as the format
+// defines them.
 #include <mutex>
 
 #include "common.cuh"
@@ -84,13 +109,53 @@ struct TcTail {
   // the per-row arrays are 16-byte aligned: the scales of a tile arrive by bulk copies
   alignas(16) int32_t src[kMaxTiles * kRows];   // row sources of every tile of the split (see row_source), 128 per tile
   alignas(16) uint32_t sk[kMaxTiles * kRows];   // key (or shared entry) scale of every row: raw fp32 until the
-                                                // tile's first chunk turns it into scale * 2^8 as f16x2 (0 for others)
-  alignas(16) uint32_t sv[kMaxTiles * kRows];   // the same for the value scale (separate V)
-  alignas(16) float m_used[kHeads];   // running max per head, log2 domain (read as float4)
-  alignas(16) float alpha[kHeads];
+                                                // tile's first chunk turns it into f_j as f16x2 (0 for others)
+  alignas(16) uint32_t sv[kMaxTiles * kRows];   // the same for the value scale (separate V); with a shared
+                                                // entry, the row multipliers instead (see row_muls)
+  int32_t texv[kMaxTiles];            // T: the largest value-row binade of each tile (kNoExp: none yet)
+  int32_t texn[kMaxTiles];            // the smallest one (-kNoExp: none yet)
+  alignas(16) float m_used[kHeads];   // normaliser running max per head, log2 domain, an integer (read as float4)
+  alignas(16) float mv_used[kHeads];  // value-side running max per head, an integer
+  alignas(16) float alpha[kHeads];    // rescale of l (then 1 / l' in the epilogue)
+  alignas(16) float alphav[kHeads];   // rescale of O^T
+  alignas(16) float phi[2][kHeads];   // 2^(T + m - M) per head for tiles of even / odd index
   float lsum[kHeads];
+  float lvsum[kHeads];
   float red[4][kHeads];
+  float redv[4][kHeads];
 };
+
+constexpr int kNoExp = -1000;   // tile exponent before any row of the tile was seen
+
+// Reciprocal row multipliers 1 / mu_j of every row of the split (128 per
+// tile, fp32): the key rows', then (separate V) the value rows'. With a shared
+// entry they live in the unused value-scale array; with separate V they follow
+// the tail in shared memory.
+template <bool SEP>
+DSV4_DEV float* row_muls(TcTail* t) {
+  return SEP ? reinterpret_cast<float*>(t + 1) : reinterpret_cast<float*>(t->sv);
+}
+constexpr int kMulsPerSplit = kMaxTiles * kRows;
+// 2^e as fp32 for an integer e in [-126, 127] (exact).
+DSV4_DEV float pow2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// The binade of x > 0 (floor(log2 x)) clamped to [-126, hi]; 0 for x == 0.
+DSV4_DEV int binade(float x, int hi = 126) {
+  const int e = static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu) - 127;
+  return x > 0.f ? (e < -126 ? -126 : (e > hi ? hi : e)) : 0;
+}
+
+// 2^(a - b) for integer-valued a <= b (exact); 0 when a = -inf, 1 when both are -inf.
+DSV4_DEV float pow2_diff(float a, float b) {
+  if (b == -INFINITY) return 1.f;
+  if (a == -INFINITY) return 0.f;
+  const float k = a - b;
+  return k < -126.f ? 0.f : pow2i(static_cast<int>(k));
+}
+
+// 2^k for any integer k, clamped to the normal fp32 range [2^-126, 2^127]
+// (below it a product with a weight <= 256 lies far below f16's range).
+DSV4_DEV float pow2_clamped(int k) { return pow2i(k < -126 ? -126 : (k > 127 ? 127 : k)); }
 
 DSV4_DEV uint32_t f32x2_to_f16x2(float lo, float hi) {
   uint32_t r;
@@ -123,6 +188,26 @@ DSV4_DEV uint32_t bf16x2_to_f16x2(uint32_t w, float& mx) {
 DSV4_DEV uint4 bf16x8_to_f16x8(uint4 w, float& mx) {
   return make_uint4(bf16x2_to_f16x2(w.x, mx), bf16x2_to_f16x2(w.y, mx), bf16x2_to_f16x2(w.z, mx),
                     bf16x2_to_f16x2(w.w, mx));
+}
+
+// bf16 pair times a power of two (exact in fp32), then rounded to f16 once.
+DSV4_DEV uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc, float& mx) {
+  const float lo = __uint_as_float(w << 16) * sc, hi = __uint_as_float(w & 0xFFFF0000u) * sc;
+  mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+  return f32x2_to_f16x2(lo, hi);
+}
+
+DSV4_DEV uint4 bf16x8_to_f16x8_scaled(uint4 w, float sc, float& mx) {
+  return make_uint4(bf16x2_to_f16x2_scaled(w.x, sc, mx), bf16x2_to_f16x2_scaled(w.y, sc, mx),
+                    bf16x2_to_f16x2_scaled(w.z, sc, mx), bf16x2_to_f16x2_scaled(w.w, sc, mx));
+}
+
+// Largest |bf16| of 8 values, as the 15 magnitude bits of a bf16.
+DSV4_DEV uint32_t bf16x8_absmax_bits(uint4 w) {
+  const uint32_t m = 0x7FFF7FFFu;
+  const uint32_t a = __vmaxu2(__vmaxu2(w.x & m, w.y & m), __vmaxu2(w.z & m, w.w & m));
+  const uint32_t lo = a & 0xFFFFu, hi = a >> 16;
+  return lo > hi ? lo : hi;
 }
 
 DSV4_DEV float ex2(float x) {
@@ -279,16 +364,80 @@ DSV4_DEV void store_group(unsigned char* xc, int j, int g, uint4 h) {
   *reinterpret_cast<uint4*>(xc + atom * kAtomBytes + j * 128 + ((gg ^ (j & 7)) << 4)) = h;
 }
 
-// A compressed tile's raw row scales (landed with its first chunk) become
-// f16x2 multipliers scale * 2^8 (zero for rows without a source); a scale
-// whose codes can exceed f16 raises RANGE. Worker wtid converts row wtid's,
-// before the worker barrier that precedes the first chunk's conversion.
-DSV4_DEV void convert_scales(const int32_t* src, uint32_t* s2, int rc, int wtid, float& mx) {
+// The row multipliers of a compressed tile from its rows' raw scales (landed
+// with its first chunk; row wtid's by worker wtid): mu_j = 256 * scale_j, at
+// least 2^-118 (so that 1 / mu_j stays finite); 1 for a zero scale. Worker
+// wtid turns row wtid's raw scale in place into the f16x2 multiplier of its
+// codes, 256 * scale_j / mu_j (1 unless mu_j was raised), and stores 1 / mu_j
+// in rinv. With tmax, the tile's largest (smallest) binade of mu_j over rows
+// with a source is folded into *tmax (*tmin). Called by every worker (whole warps: the
+// reduction needs them), before the worker barrier that precedes the first
+// chunk's conversion.
+DSV4_DEV void scale_multipliers(const int32_t* src, uint32_t* raw, int rc, int wtid, float* rinv, int32_t* tmax,
+                                  int32_t* tmin) {
+  int e = kNoExp, f = -kNoExp;
   if (wtid < rc) {
-    const float scl = __uint_as_float(s2[wtid]);
-    const bool ok = src[wtid] >= 0;
-    mx = ok ? fmaxf(mx, fabsf(scl) * 448.f) : mx;
-    s2[wtid] = ok ? f16x2_of(scl * 256.f) : 0u;
+    const float scl = __uint_as_float(raw[wtid]);
+    const float m = scl > 0.f ? fmaxf(256.f * scl, 0x1p-118f) : 1.f;
+    const float r = __frcp_rn(m);
+    raw[wtid] = f16x2_of(256.f * scl * r);
+    rinv[wtid] = r;
+    if (src[wtid] >= 0) e = f = binade(m);
+  }
+  if (tmax) {
+    e = __reduce_max_sync(0xffffffffu, e);
+    f = __reduce_min_sync(0xffffffffu, f);
+    if ((wtid & 31) == 0 && e != kNoExp) {
+      atomicMax(tmax, e);
+      atomicMin(tmin, f);
+    }
+  }
+}
+
+// The row multipliers of a window tile whose chunks have all landed (raw
+// bf16, row j's 128 values of chunk c at chunk c's region + 256 j), stored as
+// their reciprocals in rinv: mu_j = 2^L_j with
+// L_j the binade of the row's largest |value| over the nch chunks; with tmax,
+// the tile's largest (smallest) L_j over rows that hold a token is folded
+// into *tmax (*tmin).
+// The 16 items of a row sit in 16 consecutive workers of one warp (kWorkers is
+// a multiple of 32), which combine their maxima by shuffles. Called by every
+// worker (whole warps), between the barrier that follows the last copies and
+// the one that precedes the first chunk's conversion.
+DSV4_DEV void window_multipliers(const unsigned char* x, const int32_t* src, int nch, int rc, int wtid, float* rinv,
+                                   int32_t* tmax, int32_t* tmin) {
+  int tm = kNoExp, tn = -kNoExp;
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int i = wtid + it * kWorkers;
+    const int j = i >> 4, g = i & 15;
+    uint32_t m = 0;
+    if (i < rc * 16)
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t v = bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(x + c * kChunkBytes + j * 256 + 16 * g));
+        m = v > m ? v : m;
+      }
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const uint32_t v = __shfl_xor_sync(0xffffffffu, m, o);
+      m = v > m ? v : m;
+    }
+    if (g == 0 && i < rc * 16) {
+      const int L = binade(__uint_as_float(m << 16));
+      rinv[j] = pow2i(-L);
+      if (src[j] <= -2) {
+        tm = L > tm ? L : tm;
+        tn = L < tn ? L : tn;
+      }
+    }
+  }
+  if (tmax) {
+    tm = __reduce_max_sync(0xffffffffu, tm);
+    tn = __reduce_min_sync(0xffffffffu, tn);
+    if ((wtid & 31) == 0 && tm != kNoExp) {
+      atomicMax(tmax, tm);
+      atomicMin(tmin, tn);
+    }
   }
 }
 
@@ -298,32 +447,33 @@ DSV4_DEV void convert_scales(const int32_t* src, uint32_t* s2, int rc, int wtid,
 // barrier of the workers, or only of the warp where a chunk holds 128 code
 // dims: there row j's raw bytes are [128 j, 128 j + 128), read by the 16
 // items of row j (16 consecutive workers, one warp), and the only raw bytes
-// any f16 write covers are those of its own row. `s2` holds each row's
-// multiplier (convert_scales). Rows without a source read stale bytes, which
+// any f16 write covers are those of its own row. `s2` holds each row's code
+// multiplier and `rinv` its reciprocal row multiplier (see the top of the
+// file and scale_multipliers). Rows without a source read stale bytes, which
 // are discarded: they become zeros. Each warp's items are all codes or all
 // bf16 (the layouts of the 448 + 64 entry and of window tokens), so the items
 // of a thread run without per-item branches; other layouts take the general
 // path.
-DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, const uint32_t* s2, int c, int rc,
-                            unsigned char* xc, int wtid, float& mx) {
+DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, const uint32_t* s2, const float* rinv,
+                            int c, int rc, unsigned char* xc, int wtid, float& mx) {
   const ChunkSplit cs = chunk_split(a, c);
   const int nn = win ? 128 : cs.nn;   // window rows: the item layout of a full chunk
   const int n_items = rc * 16;
   const int warp_q = wtid >> 5;       // items of a thread share the parity of i >> 5 (kWorkers is a multiple of 64)
   const bool all_codes = !win && (cs.nn == 128 || (cs.nn == 64 && (warp_q & 1) == 0));
   const bool all_bf16 = win || cs.nn == 0 || (cs.nn == 64 && (warp_q & 1) == 1);
-  uint4 raw[kItems];
+  uint4 rw[kItems];
   if (all_codes) {
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
       const int i = wtid + it * kWorkers;
       int j, g;
       chunk_item(nn, i, j, g);
-      raw[it] = make_uint4(0u, 0u, 0u, 0u);
+      rw[it] = make_uint4(0u, 0u, 0u, 0u);
       if (i < n_items) {
         const uint2 w = *reinterpret_cast<const uint2*>(xc + j * cs.nn + 8 * g);
-        raw[it].x = w.x;
-        raw[it].y = w.y;
+        rw[it].x = w.x;
+        rw[it].y = w.y;
       }
     }
   } else if (all_bf16) {
@@ -332,9 +482,9 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
       const int i = wtid + it * kWorkers;
       int j, g;
       chunk_item(nn, i, j, g);
-      raw[it] = make_uint4(0u, 0u, 0u, 0u);
+      rw[it] = make_uint4(0u, 0u, 0u, 0u);
       if (i < n_items)
-        raw[it] = *reinterpret_cast<const uint4*>(win ? xc + j * 256 + 16 * g
+        rw[it] = *reinterpret_cast<const uint4*>(win ? xc + j * 256 + 16 * g
                                                       : xc + cs.rope_off + j * cs.rb + 2 * (8 * g - cs.nn));
     }
   } else {
@@ -343,14 +493,14 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
       const int i = wtid + it * kWorkers;
       int j, g;
       chunk_item(nn, i, j, g);
-      raw[it] = make_uint4(0u, 0u, 0u, 0u);
+      rw[it] = make_uint4(0u, 0u, 0u, 0u);
       if (i < n_items && src[j] >= 0) {
         if (8 * g < cs.nn) {
           const uint2 w = *reinterpret_cast<const uint2*>(xc + j * cs.nn + 8 * g);
-          raw[it].x = w.x;
-          raw[it].y = w.y;
+          rw[it].x = w.x;
+          rw[it].y = w.y;
         } else {
-          raw[it] = *reinterpret_cast<const uint4*>(xc + cs.rope_off + j * cs.rb + 2 * (8 * g - cs.nn));
+          rw[it] = *reinterpret_cast<const uint4*>(xc + cs.rope_off + j * cs.rb + 2 * (8 * g - cs.nn));
         }
       }
     }
@@ -364,9 +514,9 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
       int j, g;
       chunk_item(nn, i, j, g);
       if (i < n_items) {
-        const uint32_t w2 = s2[j];
-        const uint4 h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), w2);
-        store_group(xc, j, g, w2 ? h : make_uint4(0u, 0u, 0u, 0u));
+        const bool valid = src[j] >= 0;
+        const uint4 h = codes8_to_f16x8(make_uint2(rw[it].x, rw[it].y), s2[j]);
+        store_group(xc, j, g, valid ? h : make_uint4(0u, 0u, 0u, 0u));
       }
     }
   } else if (all_bf16) {
@@ -379,7 +529,7 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
         const int32_t sr = src[j];
         const bool valid = win ? sr <= -2 : sr >= 0;
         float m = 0.f;
-        const uint4 h = bf16x8_to_f16x8(raw[it], m);
+        const uint4 h = bf16x8_to_f16x8_scaled(rw[it], rinv[j], m);
         mx = valid ? fmaxf(mx, m) : mx;
         store_group(xc, j, g, valid ? h : make_uint4(0u, 0u, 0u, 0u));
       }
@@ -393,8 +543,8 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
         chunk_item(nn, i, j, g);
         uint4 h = make_uint4(0u, 0u, 0u, 0u);
         if (src[j] >= 0) {
-          if (8 * g < cs.nn) h = codes8_to_f16x8(make_uint2(raw[it].x, raw[it].y), s2[j]);
-          else h = bf16x8_to_f16x8(raw[it], mx);
+          if (8 * g < cs.nn) h = codes8_to_f16x8(make_uint2(rw[it].x, rw[it].y), s2[j]);
+          else h = bf16x8_to_f16x8_scaled(rw[it], rinv[j], mx);
         }
         store_group(xc, j, g, h);
       }
@@ -527,8 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int tiles = rs.mt + rs.wt;
   const int nt = tiles - tile0 < a.tiles_per_split ? (tiles - tile0 > 0 ? tiles - tile0 : 0) : a.tiles_per_split;
   if (nt == 0) {   // uniform: nothing to attend in this split
-    for (int h = threadIdx.x; h < hcount; h += blockDim.x)
+    for (int h = threadIdx.x; h < hcount; h += blockDim.x) {
       a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + h) * a.splits + split] = -INFINITY;
+      a.part_lsev[(static_cast<int64_t>(b) * a.H + h0 + h) * a.splits + split] = -INFINITY;
+    }
     return;
   }
 
@@ -552,7 +704,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     t->abort = 0;
     tc::fence_mbar_init();
   }
-  if (threadIdx.x < kHeads) t->m_used[threadIdx.x] = -INFINITY;
+  if (threadIdx.x < kHeads) {
+    t->m_used[threadIdx.x] = -INFINITY;
+    t->mv_used[threadIdx.x] = -INFINITY;
+  }
+  if (threadIdx.x < kMaxTiles) {
+    t->texv[threadIdx.x] = kNoExp;
+    t->texn[threadIdx.x] = -kNoExp;
+  }
+  float* const rmul = row_muls<SEP>(t);
   // Row sources of every tile of the split (CSA: one round trip for the top-k
   // indices). Each tile's scales travel with its first chunk: a bulk copy
   // beside the TMA boxes (contiguous rows, capacity a multiple of 4) or one
@@ -688,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
 
     float lw = 0.f;   // softmax warps: l of head hb + lane over this warp's rows
+    float lv = 0.f;   // and l' (the sum of the value-side weights P)
     // Every worker takes part in the same sequence of worker barriers; a
     // softmax failure (a wait that gave up) reaches the others through the
     // next one, so no worker is left waiting at a named barrier.
@@ -710,20 +871,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
         if (!ok) break;
       }
+      float* const rik = rmul + tt * kRows;                        // 1 / mu of the key (or shared) rows
+      float* const riv = SEP ? rik + kMulsPerSplit : rik;          // of the value rows
       for (int c = 0; c < nch; ++c) {
         bool w = soft_ok;
         if (via_tma) w = w && tc::mbar_wait(&t->xland[c], tt & 1, abort);
-        else cp_async_wait(nch - 1 - c);
-        if (c == 0 && !tl.win && w) {
-          convert_scales(src_t, t->sk + tt * kRows, rc, wtid, mx);
-          if (SEP) convert_scales(src_t, t->sv + tt * kRows, rc, wtid, mx);
+        else cp_async_wait(tl.win ? 0 : nch - 1 - c);
+        // The rows' exponents. Every worker takes part whatever its w (the
+        // warp-wide reductions need whole warps; data read after a failed wait
+        // is garbage that the failed barrier below discards). A compressed
+        // tile's scales came with its first chunk (each row's by the worker that
+        // reads it here); a window tile needs whole rows: every worker waited
+        // for all its copies of the tile above, and after this barrier
+        // everyone's have landed, read before any chunk converts.
+        if (c == 0 && !tl.win) {
+          scale_multipliers(src_t, t->sk + tt * kRows, rc, wtid, rik, SEP ? nullptr : &t->texv[tt], &t->texn[tt]);
+          if (SEP) scale_multipliers(src_t, t->sv + tt * kRows, rc, wtid, riv, &t->texv[tt], &t->texn[tt]);
+        }
+        if (c == 0 && tl.win) {
+          tc::bar_named(kBarWork, kWorkers);
+          window_multipliers(xk, src_t, nch, rc, wtid, rik, SEP ? nullptr : &t->texv[tt], &t->texn[tt]);
+          if (SEP) window_multipliers(xv, src_t, nch, rc, wtid, riv, &t->texv[tt], &t->texn[tt]);
         }
         // every worker's copies of chunk c have landed (or the boxes have)
         if (!(ok = tc::bar_and(kBarWork, kWorkers, w))) break;
-        convert_chunk(a, tl.win, src_t, t->sk + tt * kRows, c, rc, xk + c * kChunkBytes, wtid, mx);
+        convert_chunk(a, tl.win, src_t, t->sk + tt * kRows, rik, c, rc, xk + c * kChunkBytes, wtid, mx);
         if (SEP) {
           tc::bar_named(kBarWork, kWorkers);
-          convert_chunk(a, tl.win, src_t, t->sv + tt * kRows, c, rc, xv + c * kChunkBytes, wtid, mx);
+          convert_chunk(a, tl.win, src_t, t->sv + tt * kRows, riv, c, rc, xv + c * kChunkBytes, wtid, mx);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
@@ -733,46 +908,86 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
       // ---- softmax warps: S^T -> P for this tile
       const bool valid = src_t[j] != -1;
+      const float mkj = __frcp_rn(rik[j]);          // the key row's multiplier mu_j
+      const float ck = c2 * mkj;                    // ... back on its scores
+      const float mvj = SEP ? __frcp_rn(riv[j]) : mkj;   // the value row's multiplier mu'_j
+      const float fv = static_cast<float>(binade(mvj));          // L'_j
+      const int tv = t->texv[tt] == kNoExp ? 0 : t->texv[tt];   // T, the tile's largest L'
+      const float rj = valid ? mvj * pow2i(-tv) : 0.f;          // mu'_j / 2^T < 2
+      float* const phi = t->phi[tt & 1];
+      // The head's power of two 2^(T + m - M) for this tile (recomputed below
+      // when a max moves). Tile tt - 2 used the same slot; every softmax thread
+      // finished with it before the barrier of tile tt - 1, which this thread
+      // has passed.
+      if (st < kHeads) {
+        const float mo = t->m_used[st], vo = t->mv_used[st];
+        phi[st] = (mo == -INFINITY || vo == -INFINITY) ? 0.f : pow2_clamped(tv + static_cast<int>(mo - vo));
+      }
       if (!(soft_ok = tc::bar_and(kBarSoft, kSoftThreads, tc::mbar_wait(&t->sfull, tt & 1, abort)))) continue;
       tc::tc_fence_after();
       float s[32];
-      load_scores32(s_tmem + lane_off + hb, c2, valid, s);
-      bool need = false;
+      load_scores32(s_tmem + lane_off + hb, ck, valid, s);
+      // A max moves when s > m + 2^8 or s + L' > M + 2^8; on a CTA's first
+      // tile they always do (both start at -inf).
+      bool need = tt == 0;
+      if (tt > 0) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 mu = *reinterpret_cast<const float4*>(t->m_used + hb + i);
-        need |= (s[i] > mu.x + kRescale) | (s[i + 1] > mu.y + kRescale) | (s[i + 2] > mu.z + kRescale) |
-                (s[i + 3] > mu.w + kRescale);
+        for (int i = 0; i < 32; i += 4) {
+          const float4 mu = *reinterpret_cast<const float4*>(t->m_used + hb + i);
+          const float4 mv = *reinterpret_cast<const float4*>(t->mv_used + hb + i);
+          need |= (s[i] > fminf(mu.x, mv.x - fv) + kRescale) | (s[i + 1] > fminf(mu.y, mv.y - fv) + kRescale) |
+                  (s[i + 2] > fminf(mu.z, mv.z - fv) + kRescale) | (s[i + 3] > fminf(mu.w, mv.w - fv) + kRescale);
+        }
       }
       if (tc::bar_or(kBarSoft, kSoftThreads, need)) {
-        // the running max of some head moves: reduce this tile's column max
+        // a running max of some head moves: reduce this tile's column max of s,
+        // and of s + L' unless the tile's L' lie within 2^8 of each other: then
+        // max(s) + T bounds it closely enough (the largest P of the tile stays
+        // >= 2^-9); the maxima kept are integers, so every rescale is an exact
+        // power of two
+        const bool exact_v = t->texv[tt] - t->texn[tt] > static_cast<int>(kRescale);
+        float v[32];
+        if (exact_v) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = s[i] + fv;
+          warp_reduce_scatter32<true>(v, lane);
+          t->redv[qd][hb + lane] = v[0];
+        }
         warp_reduce_scatter32<true>(s, lane);
         t->red[qd][hb + lane] = s[0];
         tc::bar_named(kBarSoft, kSoftThreads);
         if (st < kHeads) {
           const float tm = fmaxf(fmaxf(t->red[0][st], t->red[1][st]), fmaxf(t->red[2][st], t->red[3][st]));
-          const float mo = t->m_used[st];
-          const float mn = fmaxf(mo, tm);
-          t->alpha[st] = mn == -INFINITY ? 1.f : ex2(mo - mn);
+          const float tvm = exact_v ? fmaxf(fmaxf(t->redv[0][st], t->redv[1][st]), fmaxf(t->redv[2][st], t->redv[3][st]))
+                                    : tm + static_cast<float>(tv);
+          const float mo = t->m_used[st], mn = fmaxf(mo, ceilf(tm));
+          const float vo = t->mv_used[st], vn = fmaxf(vo, ceilf(tvm));
+          t->alpha[st] = pow2_diff(mo, mn);
+          t->alphav[st] = pow2_diff(vo, vn);
           t->m_used[st] = mn;
+          t->mv_used[st] = vn;
+          phi[st] = (mn == -INFINITY || vn == -INFINITY) ? 0.f : pow2_clamped(tv + static_cast<int>(mn - vn));
         }
         tc::bar_named(kBarSoft, kSoftThreads);
         lw *= t->alpha[hb + lane];
+        lv *= t->alphav[hb + lane];
         if (tt > 0) {
           for (int c = 0; c < nch; ++c) {
-            uint32_t v[32];
+            uint32_t o[32];
             const uint32_t addr = o_tmem + lane_off + c * kHeads + hb;
-            tc::tmem_ld32(addr, v);
+            tc::tmem_ld32(addr, o);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * t->alpha[hb + i]);
-            tc::tmem_st32(addr, v);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * t->alphav[hb + i]);
+            tc::tmem_st32(addr, o);
           }
           tc::tmem_wait_st();
         }
-        load_scores32(s_tmem + lane_off + hb, c2, valid, s);   // the reduction consumed s
+        load_scores32(s_tmem + lane_off + hb, ck, valid, s);   // the reduction consumed s
       }
-      // probabilities of this row and heads, f16, into P (row j, 16-byte chunks, swizzled)
+      // p = 2^(s - m) (for l) and the value-side weight P = p * mu' / 2^T *
+      // 2^(T + m - M), as f16 into P (row j, 16-byte chunks, swizzled)
+      float pr[32];
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         const float4 mu = *reinterpret_cast<const float4*>(t->m_used + hb + i);
@@ -780,16 +995,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         s[i + 1] = valid ? ex2(s[i + 1] - mu.y) : 0.f;
         s[i + 2] = valid ? ex2(s[i + 2] - mu.z) : 0.f;
         s[i + 3] = valid ? ex2(s[i + 3] - mu.w) : 0.f;
+        pr[i] = s[i] * rj;
+        pr[i + 1] = s[i + 1] * rj;
+        pr[i + 2] = s[i + 2] * rj;
+        pr[i + 3] = s[i + 3] * rj;
       }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const int i = g * 8, gc = (hb >> 3) + g;
-        *reinterpret_cast<uint4*>(pb + j * 128 + ((gc ^ (j & 7)) << 4)) =
-            make_uint4(f32x2_to_f16x2(s[i], s[i + 1]), f32x2_to_f16x2(s[i + 2], s[i + 3]),
-                       f32x2_to_f16x2(s[i + 4], s[i + 5]), f32x2_to_f16x2(s[i + 6], s[i + 7]));
+        const float4 fa = *reinterpret_cast<const float4*>(phi + hb + i);
+        const float4 fb = *reinterpret_cast<const float4*>(phi + hb + i + 4);
+        *reinterpret_cast<uint4*>(pb + j * 128 + ((gc ^ (j & 7)) << 4)) = make_uint4(
+            f32x2_to_f16x2(pr[i] * fa.x, pr[i + 1] * fa.y), f32x2_to_f16x2(pr[i + 2] * fa.z, pr[i + 3] * fa.w),
+            f32x2_to_f16x2(pr[i + 4] * fb.x, pr[i + 5] * fb.y), f32x2_to_f16x2(pr[i + 6] * fb.z, pr[i + 7] * fb.w));
       }
       warp_reduce_scatter32<false>(s, lane);
+      warp_reduce_scatter32<false>(pr, lane);
       lw += s[0];
+      lv += pr[0] * phi[hb + lane];   // l' of head hb + lane
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
@@ -803,19 +1026,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       ok = tc::bar_and(kBarSoft, kSoftThreads, ok && soft_ok);
       if (ok) {
         t->red[qd][hb + lane] = lw;
+        t->redv[qd][hb + lane] = lv;
         tc::bar_named(kBarSoft, kSoftThreads);
         if (st < kHeads) {
           const float l = (t->red[0][st] + t->red[1][st]) + (t->red[2][st] + t->red[3][st]);
+          const float lvs = (t->redv[0][st] + t->redv[1][st]) + (t->redv[2][st] + t->redv[3][st]);
           t->lsum[st] = l;
-          t->alpha[st] = l > 0.f ? 1.f / l : 0.f;
+          t->lvsum[st] = lvs;
+          t->alpha[st] = lvs > 0.f ? 1.f / lvs : 0.f;
         }
         tc::bar_named(kBarSoft, kSoftThreads);
         if (st < hcount) {
-          const float l = t->lsum[st];
-          a.part_lse[(static_cast<int64_t>(b) * a.H + h0 + st) * a.splits + split] =
-              l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+          const float l = t->lsum[st], lvs = t->lvsum[st];
+          const int64_t o = (static_cast<int64_t>(b) * a.H + h0 + st) * a.splits + split;
+          a.part_lse[o] = l > 0.f ? (t->m_used[st] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+          a.part_lsev[o] = lvs > 0.f && l > 0.f ? (t->mv_used[st] + __log2f(lvs)) * 0.6931471805599453f : -INFINITY;
         }
-        // Normalised O^T as f16 rows [dim][64 heads], 16-byte granule q of row r
+        // O^T / l' as f16 rows [dim][64 heads], 16-byte granule q of row r
         // at granule q ^ (r & 7) (the merge reads the same swizzle), stored
         // straight from registers: each thread writes 64 contiguous bytes of
         // its dim's row. A 128-dim block is stored as soon as the last tile's
@@ -859,7 +1086,7 @@ namespace {
 
 size_t tc_smem_bytes(int D, bool sep) {
   return 1024 + static_cast<size_t>(D) * 128 + kPBytes + (sep ? 2 : 1) * static_cast<size_t>(D / 128) * kChunkBytes +
-         sizeof(TcTail);
+         sizeof(TcTail) + (sep ? 2 * kMulsPerSplit * sizeof(float) : 0);
 }
 
 template <bool SEP>

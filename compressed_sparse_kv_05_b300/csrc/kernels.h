@@ -90,7 +90,8 @@ struct AttnArgs {
   const int64_t* n_tokens;
   int32_t* status;
   float* part_o;           // [B][H][splits][Dv] fp32 (CUDA-core kernel); f16 [B][splits][hg][D][64], granules swizzled (tensor-core)
-  float* part_lse;         // [B][H][splits]
+  float* part_lse;         // [B][H][splits] natural-log sum of each split's softmax weights
+  float* part_lsev;        // [B][H][splits] tensor-core kernel: natural log of the scale of its normalised partial
   float* out;              // [B][H][Dv]
   float* lse;              // [B][H] or null
 };

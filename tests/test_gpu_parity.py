@@ -117,20 +117,20 @@ def test_append_builds_oracle_cache(layer, n):
     oc = oracle_stream_cache(layer, "append", 0, n, 0)
     n_c = n // layer.ratio
     assert to_host(cache.n_tokens)[0] == n
-    dk = pooling_error_bound(oc["tokens"]["k"], layer.ratio)
+    dk = pooling_error_bound(oc, "k")
     compare_fp8_entries(to_host(cache.k_nope)[0, :n_c], to_host(cache.k_scale)[0, :n_c], oc["k_nope"], oc["k_scale"],
                         oc["pooled_k"], layer.d_nope, dk)
     compare_bf16(to_host(cache.k_rope, np.uint16)[0, :n_c], oc["k_rope"], oc["pooled_k"][:, layer.d_nope:],
                  dk[:, layer.d_nope:])
     if layer.separate_v:
-        dv = pooling_error_bound(oc["tokens"]["v"], layer.ratio)
+        dv = pooling_error_bound(oc, "v")
         compare_fp8_entries(to_host(cache.v_nope)[0, :n_c], to_host(cache.v_scale)[0, :n_c], oc["v_nope"],
                             oc["v_scale"], oc["pooled_v"], layer.d_nope, dv)
         compare_bf16(to_host(cache.v_rope, np.uint16)[0, :n_c], oc["v_rope"], oc["pooled_v"][:, layer.d_nope:],
                      dv[:, layer.d_nope:])
     if layer.idx_dim:
         compare_fp4_rows(to_host(cache.idx_codes)[0, :n_c], to_host(cache.idx_scales)[0, :n_c], oc["idx_codes"],
-                         oc["idx_scales"], oc["pooled_u"], pooling_error_bound(oc["tokens"]["u"], layer.ratio))
+                         oc["idx_scales"], oc["pooled_u"], pooling_error_bound(oc, "u"))
     ring = to_host(cache.win_k, np.uint16)[0]
     for slot, tok in oc["ring_slots"].items():
         assert np.array_equal(ring[slot], oc["tokens"]["k"][tok])

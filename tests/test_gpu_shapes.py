@@ -128,14 +128,14 @@ def _check_stream_cache(layer, cache, n, tag):
     assert (to_host(cache.n_tokens) == n).all()
     for b in range(layer.batch):
         oc = oracle_stream_cache(layer, tag, 0, n, b)
-        dk = pooling_error_bound(oc["tokens"]["k"], layer.ratio)
+        dk = pooling_error_bound(oc, "k")
         compare_fp8_entries(to_host(cache.k_nope)[b, :n_c], to_host(cache.k_scale)[b, :n_c], oc["k_nope"],
                             oc["k_scale"], oc["pooled_k"], layer.d_nope, dk)
         compare_bf16(to_host(cache.k_rope, np.uint16)[b, :n_c], oc["k_rope"], oc["pooled_k"][:, layer.d_nope:],
                      dk[:, layer.d_nope:])
         if layer.idx_dim:
             compare_fp4_rows(to_host(cache.idx_codes)[b, :n_c], to_host(cache.idx_scales)[b, :n_c], oc["idx_codes"],
-                             oc["idx_scales"], oc["pooled_u"], pooling_error_bound(oc["tokens"]["u"], layer.ratio))
+                             oc["idx_scales"], oc["pooled_u"], pooling_error_bound(oc, "u"))
         ring = to_host(cache.win_k, np.uint16)[b]
         for slot, tok in oc["ring_slots"].items():
             assert np.array_equal(ring[slot], oc["tokens"]["k"][tok])
@@ -264,7 +264,17 @@ def test_attention_far_from_unit_magnitude(kind):
     for b in range(layer.batch):
         o_out, o_lse = oracle_attend_planes(layer, planes[b], q[b], sels[b])
         assert row_rel_err(g_out[b], o_out).max() <= TOL, (b, row_rel_err(g_out[b], o_out).max())
-        assert np.abs(g_lse[b] - o_lse).max() <= 1e-3
+        # The log-sum-exp inherits the scores' rounding: the f16 key operands carry
+        # 11 significant bits, so a score moves by about 2^-11 of the size of its
+        # terms (sm_scale * ||q (.) k||, large here: keys of 2^10 give scores near
+        # 3000); 1e-3 absolute where the scores are of order one.
+        p = planes[b]
+        K = O.dequant_kv_rows(p["k_nope"], p["k_scale"], p["k_rope"])
+        sel = np.arange(layer.n_comp) if sels[b] is None else sels[b]
+        Kall = np.concatenate([K[sel], O.bf16_decode(p["ring_k"])], axis=0)
+        qd = O.bf16_decode(q[b])
+        size = layer.sm_scale * np.sqrt((qd ** 2) @ (Kall ** 2).T).max(axis=1)
+        assert (np.abs(g_lse[b] - o_lse) <= 1e-3 + 2.0 ** -8 * size).all()
 
 
 # ----------------------------------------------------------------------------- layer variants
@@ -334,5 +344,5 @@ def test_cache_round_trip_through_host():
     oc = oracle_stream_cache(layer, "trip", 0, n1 + n2, 1)
     n_c = (n1 + n2) // layer.ratio
     compare_fp8_entries(to_host(restored.k_nope)[1, :n_c], to_host(restored.k_scale)[1, :n_c], oc["k_nope"],
-                        oc["k_scale"], oc["pooled_k"], layer.d_nope, pooling_error_bound(oc["tokens"]["k"], 4))
+                        oc["k_scale"], oc["pooled_k"], layer.d_nope, pooling_error_bound(oc, "k"))
     check_pending(restored, oc, layer, 1)
