@@ -281,11 +281,34 @@ int dsv4_compress_append(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t 
   a.pend_u = c->pend_u; a.pend_zu = c->pend_zu; a.n_tokens = c->n_tokens; a.status = c->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int D = d->d_nope + d->d_rope;
-  const size_t smem = (2 * D + d->idx_dim + 32) * sizeof(float);
-  if (T == 1) return launch_pdl(append_one_kernel, dim3(d->batch), dim3(256), smem, st, a);
+  const PoolShape pk = pool_shape(d->ratio, D);
+  const PoolShape pu = pool_shape(d->ratio, d->idx_dim ? d->idx_dim : 8);
+  const int team_k = pk.G * pk.cg, team_u = d->idx_dim ? pu.G * pu.cg : 0;
+  const int part_k = pool_part_floats(pk, d->separate_v != 0), part_u = d->idx_dim ? pool_part_floats(pu, false) : 0;
+  if (T == 1) {
+    // one CTA per sequence, as large as the largest pooling team
+    int threads = team_k > team_u ? team_k : team_u;
+    threads = threads < 256 ? 256 : (threads + 31) / 32 * 32;
+    const size_t smem = (4 + (part_k > part_u ? part_k : part_u)) * sizeof(float);
+    return launch_pdl(append_one_kernel, dim3(d->batch), dim3(threads), smem, st, a);
+  }
   const int blocks = (d->ratio - 1 + T) / d->ratio;
-  if (blocks > 0) {
-    if ((e = launch_pdl(pool_append_kernel, dim3(blocks, d->batch), dim3(256), smem, st, a))) return e;
+  const int win_rows = T < d->window ? T : d->window;
+  const int ctas_w = (win_rows + kWinRowsPerCta - 1) / kWinRowsPerCta;
+  {
+    // teams of up to 512 threads, about 256 threads a CTA (several blocks a CTA for small teams)
+    a.bpc_k = team_k >= 256 ? 1 : 256 / team_k;
+    a.bpc_u = team_u == 0 ? 1 : (team_u >= 256 ? 1 : 256 / team_u);
+    const int thr_k = a.bpc_k * team_k, thr_u = a.bpc_u * team_u;
+    const int threads = ((thr_k > thr_u ? thr_k : thr_u) + 31) / 32 * 32;
+    a.ctas_k = (blocks + a.bpc_k - 1) / a.bpc_k;
+    a.ctas_u = d->idx_dim ? (blocks + a.bpc_u - 1) / a.bpc_u : 0;
+    const size_t sk = static_cast<size_t>(a.bpc_k) * (part_k + 2), su = static_cast<size_t>(a.bpc_u) * (part_u + 2);
+    const size_t smem = (sk > su ? sk : su) * sizeof(float);
+    static std::once_flag once;
+    set_smem_once(once, pool_chunk_kernel, 160 * 1024);
+    const int ctas = a.ctas_k + a.ctas_u + ctas_w;
+    if (ctas > 0 && (e = launch_pdl(pool_chunk_kernel, dim3(ctas, d->batch), dim3(threads), smem, st, a))) return e;
   }
   return launch_pdl(append_tail_kernel, dim3(d->batch), dim3(256), 0, st, a);
 }
@@ -453,13 +476,16 @@ int dsv4_quantize_fp4_rows(const float* y, int64_t rows, int32_t cols, uint8_t* 
 int dsv4_pool_rows(const uint16_t* x, const uint16_t* z, const float* b, int64_t blocks, int32_t ratio, int32_t dim,
                    float* y, void* stream) {
   if (blocks < 0 || ratio < 1 || dim < 1) return DSV4_ERR_INVALID_ARG;
-  if (ratio > 256 || dim % 8 || blocks > 0x7FFFFFFF) return DSV4_ERR_UNSUPPORTED;
+  if (ratio > 256 || dim % 8 || dim > 4096 || blocks > 0x7FFFFFFF) return DSV4_ERR_UNSUPPORTED;
   if (blocks == 0) return DSV4_OK;
   DSV4_REQ(x);
   DSV4_REQ(z);
   DSV4_REQ(b);
   DSV4_REQ(y);
-  pool_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(x, z, b, ratio, dim, y);
+  const PoolShape ps = pool_shape(ratio, dim);
+  const int threads = (ps.G * ps.cg + 31) / 32 * 32;
+  pool_rows_kernel<<<static_cast<unsigned>(blocks), threads, pool_part_floats(ps, false) * sizeof(float),
+                     static_cast<cudaStream_t>(stream)>>>(x, z, b, ratio, dim, y);
   return launch_status();
 }
 

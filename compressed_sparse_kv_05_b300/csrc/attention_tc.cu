@@ -590,6 +590,27 @@ DSV4_DEV void warp_reduce_scatter32(float* v, int lane) {
   }
 }
 
+// Two in-warp reduce-scatter sums at once (independent shuffle chains):
+// afterwards a[0] and b[0] hold the sums over the warp's 32 lanes for head
+// `lane` of each array.
+DSV4_DEV void warp_reduce_scatter32_sum2(float* a, float* b, int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int o = 16 >> step;
+    const int half = 16 >> step;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float sa = up ? a[i] : a[i + half], ka = up ? a[i + half] : a[i];
+      const float sb = up ? b[i] : b[i + half], kb = up ? b[i + half] : b[i];
+      const float ra = __shfl_xor_sync(0xffffffffu, sa, o);
+      const float rb = __shfl_xor_sync(0xffffffffu, sb, o);
+      a[i] = ka + ra;
+      b[i] = kb + rb;
+    }
+  }
+}
+
 // 32 scores (heads [col, col + 32)) of this thread's row, scaled to the log2
 // domain; -inf for a row that does not exist.
 DSV4_DEV void load_scores32(uint32_t taddr, float c2, bool valid, float* s) {
@@ -1009,8 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             f32x2_to_f16x2(pr[i] * fa.x, pr[i + 1] * fa.y), f32x2_to_f16x2(pr[i + 2] * fa.z, pr[i + 3] * fa.w),
             f32x2_to_f16x2(pr[i + 4] * fb.x, pr[i + 5] * fb.y), f32x2_to_f16x2(pr[i + 6] * fb.z, pr[i + 7] * fb.w));
       }
-      warp_reduce_scatter32<false>(s, lane);
-      warp_reduce_scatter32<false>(pr, lane);
+      warp_reduce_scatter32_sum2(s, pr, lane);
       lw += s[0];
       lv += pr[0] * phi[hb + lane];   // l' of head hb + lane
       tc::fence_proxy_async_smem();

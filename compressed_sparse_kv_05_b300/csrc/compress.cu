@@ -10,12 +10,14 @@
 // sliding window is a ring of window_size tokens overwritten cyclically.
 //
 // Per block j and channel c: y[c] = sum_i e_i x_i / sum_i e_i with
-// e_i = exp(z_i + b_i - max_i(z_i + b_i)), in fp32. An append is two kernels
-// on the caller's stream: pool_append_kernel reads the old pending tokens and
-// the new tokens of every block this call completes and writes its entry;
-// append_tail_kernel then writes the window ring and the new pending tokens and
-// advances n_tokens. Splitting them keeps the pending reads of the first
-// kernel ahead of the pending writes of the second.
+// e_i = exp(z_i + b_i - max_i(z_i + b_i)), in fp32, shared out among a team of
+// threads the same way in every kernel (see pool_team). An append of T > 1
+// tokens is two kernels on the caller's stream: pool_chunk_kernel reads the
+// old pending tokens and the new tokens of every block this call completes and
+// writes its entry; append_tail_kernel then writes the window ring and the new
+// pending tokens and advances n_tokens. Splitting them keeps the pending reads
+// of the first kernel ahead of the pending writes of the second. A single
+// token is one kernel (append_one_kernel).
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -24,59 +26,255 @@ namespace dsv4 {
 
 namespace {
 
-// Source row of token t of sequence b: the pending plane while t < n_old,
-// else the new input.
-DSV4_DEV const uint16_t* token_row(const uint16_t* pend, const uint16_t* in, int b, int64_t t,
-                                   int64_t n_old, int T, int ratio, int dim) {
-  if (t < n_old) return pend + (static_cast<int64_t>(b) * ratio + (t % ratio)) * dim;
-  return in + (static_cast<int64_t>(b) * T + (t - n_old)) * dim;
+DSV4_DEV uint4 ld16(const uint16_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+DSV4_DEV void bf16x8(uint4 w, float* f) {
+  f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(w.z << 16); f[5] = __uint_as_float(w.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(w.w << 16); f[7] = __uint_as_float(w.w & 0xFFFF0000u);
 }
 
-// Pool channels [0, dim) of one block into y (shared memory).
-// x2 (optional) is a second stream gated by the same logits.
-DSV4_DEV void pool_block(const AppendArgs& a, int b, int64_t j, int64_t n_old, const uint16_t* pend_x,
-                         const uint16_t* in_x, const uint16_t* pend_x2, const uint16_t* in_x2,
-                         const uint16_t* pend_z, const uint16_t* in_z, const float* bias, int dim,
-                         float* y, float* y2) {
-  const int m = a.ratio;
-  for (int c = threadIdx.x; c < dim; c += blockDim.x) {
-    float mx = -INFINITY;
-    for (int i = 0; i < m; ++i) {
-      const int64_t t = j * m + i;
-      const float l = bf16_to_f32(token_row(pend_z, in_z, b, t, n_old, a.T, m, dim)[c]) + bias[i * dim + c];
-      mx = fmaxf(mx, l);
+// Token rows of one compressed block j of sequence b: token i (0 <= i < m) is
+// position t0 + i; positions before n_old come from the pending planes (slot
+// t % m), the others from this call's inputs.
+struct BlockSrc {
+  const uint16_t *pend_x, *in_x, *pend_x2, *in_x2, *pend_z, *in_z;
+  const float* bias;   // [m][C]
+  int64_t t0, n_old;
+  int b, T, m, C;
+  DSV4_DEV const uint16_t* row(const uint16_t* pend, const uint16_t* in, int i) const {
+    const int64_t t = t0 + i;
+    return t < n_old ? pend + (static_cast<int64_t>(b) * m + (t % m)) * C
+                     : in + (static_cast<int64_t>(b) * T + (t - n_old)) * C;
+  }
+};
+
+// Raw loads of token i's gate logits (bf16) and position bias (fp32) for the
+// channels [c0, c0 + 8).
+struct GateLoad {
+  uint4 z;
+  float4 b0, b1;
+};
+DSV4_DEV GateLoad load_gate(const BlockSrc& s, int i, int c0) {
+  GateLoad g;
+  g.z = ld16(s.row(s.pend_z, s.in_z, i) + c0);
+  const float4* bp = reinterpret_cast<const float4*>(s.bias + static_cast<int64_t>(i) * s.C + c0);
+  g.b0 = __ldg(bp);
+  g.b1 = __ldg(bp + 1);
+  return g;
+}
+// the 8 logits z + b of a GateLoad
+DSV4_DEV void logits8(const GateLoad& g, float* l) {
+  bf16x8(g.z, l);
+  l[0] += g.b0.x; l[1] += g.b0.y; l[2] += g.b0.z; l[3] += g.b0.w;
+  l[4] += g.b1.x; l[5] += g.b1.y; l[6] += g.b1.z; l[7] += g.b1.w;
+}
+
+// Softmax-gated pooling of one block by a team (see PoolShape): team thread t
+// takes channels [8 c8, 8 c8 + 8) and tokens [g tpg, g tpg + tpg) of the
+// block, c8 = t % cg, g = t / cg. For every channel c, in fp32:
+//   M = max_i (z_i + b_i)                       (exact in any order)
+//   S = sum_i e_i, A = sum_i e_i x_i,  e_i = exp(z_i + b_i - M)
+// each group summing its tokens in order, the groups' sums then added in
+// group order; y = A / S (IEEE division). Threads of group 0 return y (and
+// y2, the second stream gated by the same logits). `part` is shared memory of
+// pool_part_floats() floats for this team. Every thread of the CTA calls it
+// (it holds CTA barriers when G > 1); `active` marks a thread with work.
+template <bool TWO>
+DSV4_DEV void pool_team_t(const BlockSrc& s, PoolShape ps, int t, bool active, float* part, float* y, float* y2) {
+  constexpr int kTokBatch = TWO ? 2 : 4;   // tokens whose loads a thread issues together
+  constexpr bool two = TWO;
+  const int c8 = t % ps.cg, g = t / ps.cg;
+  const int c0 = 8 * c8;
+  const int i0 = g * ps.tpg, i1 = i0 + ps.tpg < s.m ? i0 + ps.tpg : s.m;
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+  if (active)
+    for (int i = i0; i < i1; i += kTokBatch) {
+      // a batch of tokens: every load in flight, then the maxima in token order
+      GateLoad gl[kTokBatch];
+#pragma unroll
+      for (int u = 0; u < kTokBatch; ++u)
+        if (i + u < i1) gl[u] = load_gate(s, i + u, c0);
+#pragma unroll
+      for (int u = 0; u < kTokBatch; ++u)
+        if (i + u < i1) {
+          float l[8];
+          logits8(gl[u], l);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], l[k]);
+        }
     }
-    float sum = 0.f, acc = 0.f, acc2 = 0.f;
-    for (int i = 0; i < m; ++i) {
-      const int64_t t = j * m + i;
-      const float l = bf16_to_f32(token_row(pend_z, in_z, b, t, n_old, a.T, m, dim)[c]) + bias[i * dim + c];
-      const float e = expf(l - mx);
-      sum += e;
-      acc = fmaf(e, bf16_to_f32(token_row(pend_x, in_x, b, t, n_old, a.T, m, dim)[c]), acc);
-      if (y2) acc2 = fmaf(e, bf16_to_f32(token_row(pend_x2, in_x2, b, t, n_old, a.T, m, dim)[c]), acc2);
+  if (ps.G > 1) {
+    float* pm = part + (g * ps.cg + c8) * 8;
+    if (active)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = mx[k];
+    __syncthreads();
+    if (active)
+      for (int h = 0; h < ps.G; ++h) {
+        const float* q = part + (h * ps.cg + c8) * 8;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], q[k]);
+      }
+    __syncthreads();
+  }
+  float sum[8], acc[8], acc2[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sum[k] = acc[k] = acc2[k] = 0.f;
+  if (active)
+    for (int i = i0; i < i1; i += kTokBatch) {
+      // a batch of tokens: every load in flight, then the sums in token order
+      GateLoad gl[kTokBatch];
+      uint4 xw[kTokBatch], x2w[kTokBatch];
+#pragma unroll
+      for (int u = 0; u < kTokBatch; ++u)
+        if (i + u < i1) {
+          gl[u] = load_gate(s, i + u, c0);
+          xw[u] = ld16(s.row(s.pend_x, s.in_x, i + u) + c0);
+          if (two) x2w[u] = ld16(s.row(s.pend_x2, s.in_x2, i + u) + c0);
+        }
+#pragma unroll
+      for (int u = 0; u < kTokBatch; ++u)
+        if (i + u < i1) {
+          float l[8], x[8], x2[8];
+          logits8(gl[u], l);
+          bf16x8(xw[u], x);
+          if (two) bf16x8(x2w[u], x2);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float e = expf(l[k] - mx[k]);
+            sum[k] += e;
+            acc[k] = fmaf(e, x[k], acc[k]);
+            if (two) acc2[k] = fmaf(e, x2[k], acc2[k]);
+          }
+        }
     }
-    y[c] = __fdiv_rn(acc, sum);
-    if (y2) y2[c] = __fdiv_rn(acc2, sum);
+  if (ps.G > 1) {
+    float* pp = part + (g * ps.cg + c8) * (two ? 24 : 16);
+    if (active)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        pp[k] = sum[k];
+        pp[8 + k] = acc[k];
+        if (two) pp[16 + k] = acc2[k];
+      }
+    __syncthreads();
+    if (active && g == 0)
+      for (int h = 1; h < ps.G; ++h) {
+        const float* q = part + (h * ps.cg + c8) * (two ? 24 : 16);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          sum[k] += q[k];
+          acc[k] += q[8 + k];
+          if (two) acc2[k] += q[16 + k];
+        }
+      }
+    __syncthreads();   // `part` is reused by the next team call
+  }
+  if (active && g == 0)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      y[k] = __fdiv_rn(acc[k], sum[k]);
+      if (two) y2[k] = __fdiv_rn(acc2[k], sum[k]);
+    }
+}
+
+DSV4_DEV void pool_team(const BlockSrc& s, PoolShape ps, int t, bool active, float* part, float* y, float* y2) {
+  if (s.in_x2) pool_team_t<true>(s, ps, t, active, part, y, y2);
+  else pool_team_t<false>(s, ps, t, active, part, y, y2);
+}
+
+// The FP8 + BF16 entry of a pooled row held by a team's group-0 threads (8
+// channels each, `has` when the thread holds some): scale = amax/448 over the
+// d_nope FP8 dims (amax combined through the shared word *amax, zeroed by the
+// caller before a barrier), codes = e4m3(y / scale), the RoPE dims bf16. Every
+// thread of the CTA calls it (one CTA barrier).
+DSV4_DEV void store_entry(const float* y, bool has, int c8, int d_nope, uint32_t* amax, uint8_t* nope, float* scale,
+                          uint16_t* rope) {
+  const int c0 = 8 * c8;
+  const bool code_dims = has && c0 < d_nope;
+  if (code_dims) {
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[k]));
+    atomicMax(amax, __float_as_uint(m));
+  }
+  __syncthreads();
+  if (code_dims) {
+    const float s = __fdiv_rn(__uint_as_float(*amax), 448.f);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (s > 0.f)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[k] = f32x2_to_e4m3x2(__fdiv_rn(y[2 * k], s), __fdiv_rn(y[2 * k + 1], s));
+    *reinterpret_cast<uint2*>(nope + c0) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    if (c8 == 0) *scale = s;
+  } else if (has) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = static_cast<uint32_t>(f32_to_bf16(y[2 * k])) | (static_cast<uint32_t>(f32_to_bf16(y[2 * k + 1])) << 16);
+    *reinterpret_cast<uint4*>(rope + (c0 - d_nope)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-// Write one pooled KV row (shared memory) as an FP8 + BF16 entry.
-DSV4_DEV void store_kv_entry(const float* y, int d_nope, int d_rope, uint8_t* nope, float* scale,
-                             uint16_t* rope, float* red) {
-  const float s = block_quant_fp8_row(y, d_nope, nope, red);
-  if (threadIdx.x == 0) *scale = s;
-  for (int c = threadIdx.x; c < d_rope; c += blockDim.x) rope[c] = f32_to_bf16(y[d_nope + c]);
-}
-
-DSV4_DEV void store_fp4_row(const float* y, int cols, uint8_t* codes, uint8_t* scales) {
-  for (int blk = threadIdx.x; blk < cols / 16; blk += blockDim.x)
-    scales[blk] = static_cast<uint8_t>(quant_fp4_block16(y + blk * 16, codes + blk * 8));
+// The FP4 row of a pooled indexer key held by a team's group-0 threads: per
+// 16 channels (a pair of threads, c8 even and odd, neighbours in a warp)
+// scale = e4m3(amax/6), codes = e2m1(y / scale). Every thread of the CTA calls
+// it (one full-warp shuffle; a pair never spans two teams since cg is even).
+DSV4_DEV void store_fp4(const float* y, bool has, int c8, uint8_t* codes, uint8_t* scales) {
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[k]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  if (!has) return;
+  const uint32_t sc = f32_to_e4m3(__fdiv_rn(m, 6.f));
+  const float s = e4m3_to_f32(sc);
+  float q[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) q[k] = s > 0.f ? __fdiv_rn(y[k], s) : 0.f;
+  *reinterpret_cast<uint32_t*>(codes + 4 * c8) = s > 0.f ? f32x8_to_e2m1x8(q) : 0u;
+  if ((c8 & 1) == 0) scales[c8 >> 1] = static_cast<uint8_t>(sc);
 }
 
 }  // namespace
 
-// grid (max blocks one call can complete, B); dynamic smem: (2*D + Di) floats + 32
-__global__ void __launch_bounds__(256) pool_append_kernel(AppendArgs a) {
+namespace {
+// Copy rows of bf16 values (dim a multiple of 8, rows 16-byte aligned) with the
+// whole CTA: row r of `rows` goes from src + src_row(r) * dim to dst +
+// dst_row(r) * dim; every 16-byte piece is an independent item, loaded in
+// groups of four before they are stored.
+template <typename SrcRow, typename DstRow>
+DSV4_DEV void copy_rows(uint16_t* dst, const uint16_t* src, int rows, int dim, SrcRow src_row, DstRow dst_row) {
+  const int per = dim / 8;
+  const int n = rows * per;
+  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) v[u] = __ldg(reinterpret_cast<const uint4*>(src + src_row(i / per) * dim) + i % per);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) reinterpret_cast<uint4*>(dst + dst_row(i / per) * dim)[i % per] = v[u];
+    }
+  }
+}
+}  // namespace
+
+// Pooling of every block an append of T > 1 tokens completes, and the window
+// ring, grid (CTAs, B): CTAs [0, ctas_k) pool the key (and value) stream,
+// bpc_k blocks per CTA (a team per block, see PoolShape), and store FP8
+// entries; the next ctas_u pool the indexer-key stream, bpc_u blocks per CTA,
+// and store FP4 keys; the rest write the call's last min(W, T) tokens into the
+// window ring, kWinRowsPerCta rows each (no kernel reads the ring during an
+// append). Dynamic shared memory: the teams' combine buffers, then one amax
+// word per block.
+__global__ void __launch_bounds__(512) pool_chunk_kernel(AppendArgs a) {
   extern __shared__ float smem[];
   pdl_trigger();
   pdl_wait();
@@ -89,22 +287,54 @@ __global__ void __launch_bounds__(256) pool_append_kernel(AppendArgs a) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, DSV4_STATUS_CAPACITY);
     return;
   }
-  const int64_t j = n_old / m + blockIdx.x;
-  if ((j + 1) * m > n_new) return;
-  float* yk = smem;
-  float* yv = smem + D;
-  float* yu = smem + 2 * D;
-  float* red = yu + a.idx_dim;
-  pool_block(a, b, j, n_old, a.pend_k, a.k, a.pend_v, a.v, a.pend_z, a.z, a.bias, D, yk,
-             a.separate_v ? yv : nullptr);
-  if (a.idx_dim) pool_block(a, b, j, n_old, a.pend_u, a.u, nullptr, nullptr, a.pend_zu, a.zu, a.bias_u,
-                            a.idx_dim, yu, nullptr);
-  __syncthreads();
+  if (static_cast<int>(blockIdx.x) >= a.ctas_k + a.ctas_u) {
+    // window rows: tokens [n_new - cnt, n_new), cnt = min(W, T)
+    const int cnt = a.T < a.window ? a.T : a.window;
+    const int r0 = (blockIdx.x - a.ctas_k - a.ctas_u) * kWinRowsPerCta;
+    const int rows = cnt - r0 < kWinRowsPerCta ? cnt - r0 : kWinRowsPerCta;
+    if (rows <= 0) return;
+    const int64_t t0 = n_new - cnt + r0;   // position of the CTA's first row
+    auto src_row = [&](int r) { return static_cast<int64_t>(b) * a.T + (t0 + r - n_old); };
+    auto dst_row = [&](int r) { return static_cast<int64_t>(b) * a.window + (t0 + r) % a.window; };
+    copy_rows(a.win_k, a.k, rows, D, src_row, dst_row);
+    if (a.separate_v) copy_rows(a.win_v, a.v, rows, D, src_row, dst_row);
+    return;
+  }
+  const int64_t j0 = n_old / m, j1 = n_new / m;   // blocks [j0, j1) complete in this call
+  const bool key_stream = static_cast<int>(blockIdx.x) < a.ctas_k;
+  const int C = key_stream ? D : a.idx_dim;
+  const int bpc = key_stream ? a.bpc_k : a.bpc_u;
+  const PoolShape ps = pool_shape(m, C);
+  const int team = ps.G * ps.cg;
+  const int slot = threadIdx.x / team, t = threadIdx.x % team;
+  const int64_t j = j0 + static_cast<int64_t>(key_stream ? blockIdx.x : blockIdx.x - a.ctas_k) * bpc + slot;
+  const bool active = slot < bpc && j < j1;
+  const bool two = key_stream && a.separate_v;
+  float* part = smem + slot * pool_part_floats(ps, two);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(smem + bpc * pool_part_floats(ps, two)) + 2 * slot;
+  if (t < 2 && slot < bpc) amax[t] = 0u;
+  BlockSrc src;
+  src.t0 = j * m; src.n_old = n_old; src.b = b; src.T = a.T; src.m = m; src.C = C;
+  if (key_stream) {
+    src.pend_x = a.pend_k; src.in_x = a.k; src.pend_x2 = a.pend_v; src.in_x2 = two ? a.v : nullptr;
+    src.pend_z = a.pend_z; src.in_z = a.z; src.bias = a.bias;
+  } else {
+    src.pend_x = a.pend_u; src.in_x = a.u; src.pend_x2 = nullptr; src.in_x2 = nullptr;
+    src.pend_z = a.pend_zu; src.in_z = a.zu; src.bias = a.bias_u;
+  }
+  float y[8] = {}, y2[8] = {};
+  pool_team(src, ps, t, active, part, y, y2);
+  __syncthreads();   // the amax words are zeroed
+  const bool has = active && t < ps.cg;
   const int64_t e = static_cast<int64_t>(b) * a.capacity + j;
-  store_kv_entry(yk, a.d_nope, a.d_rope, a.k_nope + e * a.d_nope, a.k_scale + e, a.k_rope + e * a.d_rope, red);
-  if (a.separate_v)
-    store_kv_entry(yv, a.d_nope, a.d_rope, a.v_nope + e * a.d_nope, a.v_scale + e, a.v_rope + e * a.d_rope, red);
-  if (a.idx_dim) store_fp4_row(yu, a.idx_dim, a.idx_codes + e * (a.idx_dim / 2), a.idx_scales + e * (a.idx_dim / 16));
+  if (key_stream) {
+    store_entry(y, has, t, a.d_nope, amax, a.k_nope + e * a.d_nope, a.k_scale + e, a.k_rope + e * a.d_rope);
+    if (two)
+      store_entry(y2, has, t, a.d_nope, amax + 1, a.v_nope + e * a.d_nope, a.v_scale + e, a.v_rope + e * a.d_rope);
+  } else {
+    // every thread (whole warps: the pair shuffle; a pair never spans two teams)
+    store_fp4(y, has, t, a.idx_codes + e * (a.idx_dim / 2), a.idx_scales + e * (a.idx_dim / 16));
+  }
 }
 
 namespace {
@@ -116,7 +346,8 @@ DSV4_DEV void copy_row(uint16_t* dst, const uint16_t* src, int dim) {
 }
 }  // namespace
 
-// grid (B); writes the window ring and the pending tokens, then advances n_tokens.
+// grid (B); after pool_chunk_kernel: writes the tokens of the block left open
+// into the pending planes, then advances n_tokens.
 __global__ void __launch_bounds__(256) append_tail_kernel(AppendArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -126,40 +357,32 @@ __global__ void __launch_bounds__(256) append_tail_kernel(AppendArgs a) {
   const int64_t n_old = a.n_tokens[b];
   const int64_t n_new = n_old + a.T;
   if (n_new / m > a.capacity) return;
-  if (a.window > 0) {
-    const int64_t t0 = n_new - a.window > n_old ? n_new - a.window : n_old;
-    for (int64_t t = t0; t < n_new; ++t) {
-      const int64_t src = static_cast<int64_t>(b) * a.T + (t - n_old);
-      const int64_t dst = static_cast<int64_t>(b) * a.window + t % a.window;
-      copy_row(a.win_k + dst * D, a.k + src * D, D);
-      if (a.separate_v) copy_row(a.win_v + dst * D, a.v + src * D, D);
-    }
-  }
   if (m > 1) {
     const int64_t open = (n_new / m) * m;
-    const int64_t t0 = open > n_old ? open : n_old;
-    for (int64_t t = t0; t < n_new; ++t) {
-      const int64_t src = static_cast<int64_t>(b) * a.T + (t - n_old);
-      const int64_t dst = static_cast<int64_t>(b) * m + t % m;
-      copy_row(a.pend_k + dst * D, a.k + src * D, D);
-      copy_row(a.pend_z + dst * D, a.z + src * D, D);
-      if (a.separate_v) copy_row(a.pend_v + dst * D, a.v + src * D, D);
-      if (a.idx_dim) {
-        copy_row(a.pend_u + dst * a.idx_dim, a.u + src * a.idx_dim, a.idx_dim);
-        copy_row(a.pend_zu + dst * a.idx_dim, a.zu + src * a.idx_dim, a.idx_dim);
-      }
+    const int64_t t0 = open > n_old ? open : n_old;   // tokens [t0, n_new) stay open
+    const int rows = static_cast<int>(n_new - t0);
+    auto src_row = [&](int r) { return static_cast<int64_t>(b) * a.T + (t0 + r - n_old); };
+    auto dst_row = [&](int r) { return static_cast<int64_t>(b) * m + (t0 + r) % m; };
+    copy_rows(a.pend_k, a.k, rows, D, src_row, dst_row);
+    copy_rows(a.pend_z, a.z, rows, D, src_row, dst_row);
+    if (a.separate_v) copy_rows(a.pend_v, a.v, rows, D, src_row, dst_row);
+    if (a.idx_dim) {
+      copy_rows(a.pend_u, a.u, rows, a.idx_dim, src_row, dst_row);
+      copy_rows(a.pend_zu, a.zu, rows, a.idx_dim, src_row, dst_row);
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) a.n_tokens[b] = n_new;
 }
 
-// Single-token append (T = 1), grid (B), one CTA per sequence: if the token
-// completes a block, pool it (old pending tokens + the new one) and store the
-// entry; then write the token into the window ring and, while its block stays
-// open, into the pending planes; then advance n_tokens. One CTA does all of a
-// sequence's work in this order, so the pending reads precede the writes.
-__global__ void __launch_bounds__(256) append_one_kernel(AppendArgs a) {
+// Single-token append (T = 1), grid (B), one CTA per sequence (at least as
+// many threads as the largest pooling team of the layer): if the token
+// completes a block, pool it (old pending tokens + the new one) with the same
+// teams as pool_chunk_kernel and store the entry; then write the token into
+// the window ring and, while its block stays open, into the pending planes;
+// then advance n_tokens. One CTA does all of a sequence's work in this order,
+// so the pending reads precede the writes.
+__global__ void __launch_bounds__(512) append_one_kernel(AppendArgs a) {
   extern __shared__ float smem[];
   pdl_trigger();
   const int b = blockIdx.x;
@@ -188,23 +411,35 @@ __global__ void __launch_bounds__(256) append_one_kernel(AppendArgs a) {
     if (threadIdx.x == 0) atomicOr(a.status, DSV4_STATUS_CAPACITY);
     return;
   }
-  if (n_new % m == 0) {
+  if (n_new % m == 0) {   // uniform: the token completes block j
     const int64_t j = n_old / m;
-    float* yk = smem;
-    float* yv = smem + D;
-    float* yu = smem + 2 * D;
-    float* red = yu + a.idx_dim;
-    pool_block(a, b, j, n_old, a.pend_k, a.k, a.pend_v, a.v, a.pend_z, a.z, a.bias, D, yk,
-               a.separate_v ? yv : nullptr);
-    if (a.idx_dim) pool_block(a, b, j, n_old, a.pend_u, a.u, nullptr, nullptr, a.pend_zu, a.zu, a.bias_u,
-                              a.idx_dim, yu, nullptr);
-    __syncthreads();
     const int64_t e = static_cast<int64_t>(b) * a.capacity + j;
-    store_kv_entry(yk, a.d_nope, a.d_rope, a.k_nope + e * a.d_nope, a.k_scale + e, a.k_rope + e * a.d_rope, red);
+    uint32_t* amax = reinterpret_cast<uint32_t*>(smem);
+    float* part = smem + 4;
+    if (threadIdx.x < 2) amax[threadIdx.x] = 0u;
+    BlockSrc src;
+    src.t0 = j * m; src.n_old = n_old; src.b = b; src.T = 1; src.m = m; src.C = D;
+    src.pend_x = a.pend_k; src.in_x = a.k; src.pend_x2 = a.pend_v; src.in_x2 = a.separate_v ? a.v : nullptr;
+    src.pend_z = a.pend_z; src.in_z = a.z; src.bias = a.bias;
+    const PoolShape pk = pool_shape(m, D);
+    const int t = threadIdx.x;
+    const bool act_k = t < pk.G * pk.cg;
+    float y[8] = {}, y2[8] = {};
+    pool_team(src, pk, t, act_k, part, y, y2);
+    __syncthreads();
+    const bool has = act_k && t < pk.cg;
+    store_entry(y, has, t, a.d_nope, amax, a.k_nope + e * a.d_nope, a.k_scale + e, a.k_rope + e * a.d_rope);
     if (a.separate_v)
-      store_kv_entry(yv, a.d_nope, a.d_rope, a.v_nope + e * a.d_nope, a.v_scale + e, a.v_rope + e * a.d_rope, red);
-    if (a.idx_dim)
-      store_fp4_row(yu, a.idx_dim, a.idx_codes + e * (a.idx_dim / 2), a.idx_scales + e * (a.idx_dim / 16));
+      store_entry(y2, has, t, a.d_nope, amax + 1, a.v_nope + e * a.d_nope, a.v_scale + e, a.v_rope + e * a.d_rope);
+    if (a.idx_dim) {
+      src.C = a.idx_dim;
+      src.pend_x = a.pend_u; src.in_x = a.u; src.pend_x2 = nullptr; src.in_x2 = nullptr;
+      src.pend_z = a.pend_zu; src.in_z = a.zu; src.bias = a.bias_u;
+      const PoolShape pu = pool_shape(m, a.idx_dim);
+      const bool act_u = t < pu.G * pu.cg;
+      pool_team(src, pu, t, act_u, part, y, y2);
+      store_fp4(y, act_u && t < pu.cg, t, a.idx_codes + e * (a.idx_dim / 2), a.idx_scales + e * (a.idx_dim / 16));
+    }
     __syncthreads();
   }
   const int64_t src = b;   // row b of the [B][1][.] inputs
@@ -266,20 +501,24 @@ __global__ void __launch_bounds__(256) quant_fp4_rows_kernel(const float* y, int
   scales[r * per_row + blk] = static_cast<uint8_t>(quant_fp4_block16(v, codes + r * (cols / 2) + blk * 8));
 }
 
-// pooling of complete blocks: grid (blocks), block 256
-__global__ void __launch_bounds__(256) pool_rows_kernel(const uint16_t* x, const uint16_t* z, const float* bias,
+// pooling of complete blocks with the teams of the append kernels: grid
+// (blocks), one team per CTA (dynamic shared memory: its combine buffer)
+__global__ void __launch_bounds__(512) pool_rows_kernel(const uint16_t* x, const uint16_t* z, const float* bias,
                                                        int ratio, int dim, float* y) {
+  extern __shared__ float smem[];
   const int64_t j = blockIdx.x;
-  for (int c = threadIdx.x; c < dim; c += blockDim.x) {
-    float mx = -INFINITY;
-    for (int i = 0; i < ratio; ++i) mx = fmaxf(mx, bf16_to_f32(z[(j * ratio + i) * dim + c]) + bias[i * dim + c]);
-    float sum = 0.f, acc = 0.f;
-    for (int i = 0; i < ratio; ++i) {
-      const float e = expf(bf16_to_f32(z[(j * ratio + i) * dim + c]) + bias[i * dim + c] - mx);
-      sum += e;
-      acc = fmaf(e, bf16_to_f32(x[(j * ratio + i) * dim + c]), acc);
-    }
-    y[j * dim + c] = __fdiv_rn(acc, sum);
+  BlockSrc src;
+  src.t0 = j * ratio; src.n_old = 0; src.b = 0; src.T = 0; src.m = ratio; src.C = dim;
+  src.pend_x = nullptr; src.in_x = x; src.pend_x2 = nullptr; src.in_x2 = nullptr; src.pend_z = nullptr; src.in_z = z;
+  src.bias = bias;
+  const PoolShape ps = pool_shape(ratio, dim);
+  const int t = threadIdx.x;
+  float v[8] = {}, v2[8] = {};
+  pool_team(src, ps, t, t < ps.G * ps.cg, smem, v, v2);
+  if (t < ps.cg) {
+    float4* out = reinterpret_cast<float4*>(y + j * dim + 8 * t);
+    out[0] = make_float4(v[0], v[1], v[2], v[3]);
+    out[1] = make_float4(v[4], v[5], v[6], v[7]);
   }
 }
 

@@ -10,6 +10,9 @@ namespace dsv4 {
 
 struct AppendArgs {
   int T, ratio, window, capacity, d_nope, d_rope, idx_dim, separate_v;
+  int ctas_k;              // pool_chunk_kernel: CTAs of the key (and value) stream, then
+  int ctas_u;              //   CTAs of the indexer-key stream, then CTAs copying window rows (kWinRowsPerCta each)
+  int bpc_k, bpc_u;        // blocks per CTA of each stream
   const uint16_t *k, *v, *z, *u, *zu;
   const float *bias, *bias_u;
   uint8_t* k_nope;
@@ -24,7 +27,32 @@ struct AppendArgs {
   int32_t* status;
 };
 
-__global__ void pool_append_kernel(AppendArgs a);
+// How one compressed block's pooling is shared out, the same in every kernel
+// that pools (so a block's pooled bits never depend on how its tokens
+// arrived): a team of G * cg threads, cg = C / 8 groups of 8 channels, G
+// groups of tpg consecutive tokens (the last may be shorter), at most 512
+// threads.
+struct PoolShape {
+  int cg, G, tpg;
+};
+__host__ __device__ inline PoolShape pool_shape(int m, int C) {
+  PoolShape p;
+  p.cg = C / 8;
+  int G = (m + 7) / 8;
+  const int gmax = p.cg <= 512 ? 512 / p.cg : 1;
+  if (G > gmax) G = gmax;
+  if (G < 1) G = 1;
+  p.G = G;
+  p.tpg = (m + G - 1) / G;
+  return p;
+}
+// shared-memory floats a team needs to combine its token groups (0 when G == 1)
+__host__ __device__ inline int pool_part_floats(PoolShape p, bool two) {
+  return p.G > 1 ? p.G * p.cg * (two ? 24 : 16) : 0;
+}
+
+constexpr int kWinRowsPerCta = 16;
+__global__ void pool_chunk_kernel(AppendArgs a);
 __global__ void append_tail_kernel(AppendArgs a);
 __global__ void append_one_kernel(AppendArgs a);
 __global__ void quant_kv_rows_kernel(const float* y, int64_t rows, int d_nope, int d_rope, uint8_t* nope,

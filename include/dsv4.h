@@ -228,7 +228,8 @@ int dsv4_quantize_fp4_rows(const float* y, int64_t rows, int32_t cols, uint8_t* 
                            uint8_t* scales, void* stream);
 
 /* The pooling step of an append on complete blocks [HYB]:
- * x, z [blocks * ratio][dim] bf16, b [ratio][dim] fp32 -> y [blocks][dim] fp32. */
+ * x, z [blocks * ratio][dim] bf16, b [ratio][dim] fp32 -> y [blocks][dim] fp32,
+ * with the arithmetic of dsv4_compress_append. dim a multiple of 8, at most 4096. */
 int dsv4_pool_rows(const uint16_t* x, const uint16_t* z, const float* b, int64_t blocks,
                    int32_t ratio, int32_t dim, float* y, void* stream);
 
