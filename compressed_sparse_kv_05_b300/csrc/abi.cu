@@ -93,9 +93,11 @@ struct AttnPlan {
 };
 
 // n_sel: top-k width (CSA), 0 for every entry (HCA), < 0 for none (window only).
-AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
+// T: queries per sequence (the call attends for batch * T virtual sequences).
+AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel, int T = 1) {
   AttnPlan p{};
   const int sms = sm_count();
+  const int64_t nb = static_cast<int64_t>(d->batch) * T;
   p.head_groups = (H + kHeadGroup - 1) / kHeadGroup;
   const int64_t n_main = n_sel > 0 ? n_sel : (n_sel < 0 ? 0 : d->capacity);
   const int64_t rmax = n_main + d->window;
@@ -106,7 +108,7 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
     // largest R in {128, 64, 32} whose halving would still fit one wave of
     // CTAs is halved, so short row sets spread over more SMs; then runs of
     // consecutive tiles are spread evenly over one wave (one CTA per SM).
-    const int64_t units = static_cast<int64_t>(d->batch) * p.head_groups;
+    const int64_t units = nb * p.head_groups;
     auto tiles_for = [&](int64_t r) { return (n_main + r - 1) / r + (d->window + r - 1) / r; };
     int64_t tr = kTcTile;
     while (tr > kTcMinTile && units * tiles_for(tr / 2) <= sms) tr /= 2;
@@ -120,11 +122,11 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
     p.splits = static_cast<int>((tiles + per_cta - 1) / per_cta);
     if (p.splits < 1) p.splits = 1;
     // f16 partials [B][splits][head groups][D][64], then two fp32 log sums [B][H][splits] each
-    p.part_bytes = (static_cast<size_t>(d->batch) * p.splits * p.head_groups * Dv * 64 * 2 + 255) & ~size_t(255);
-    p.ws_bytes = p.part_bytes + 2 * static_cast<size_t>(d->batch) * H * p.splits * sizeof(float) + 256;
+    p.part_bytes = (static_cast<size_t>(nb) * p.splits * p.head_groups * Dv * 64 * 2 + 255) & ~size_t(255);
+    p.ws_bytes = p.part_bytes + 2 * static_cast<size_t>(nb) * H * p.splits * sizeof(float) + 256;
     return p;
   }
-  const int64_t want = (2 * sms + d->batch * p.head_groups - 1) / (d->batch * p.head_groups);
+  const int64_t want = (2 * sms + nb * p.head_groups - 1) / (nb * p.head_groups);
   const int64_t max_splits = (rmax + kRowTile - 1) / kRowTile;
   int64_t s = want < max_splits ? want : max_splits;
   if (s < 1) s = 1;
@@ -134,8 +136,8 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel) {
   if (s < 1) s = 1;
   p.splits = static_cast<int>(s);
   p.rows_per_split = static_cast<int>(rps);
-  p.part_bytes = (static_cast<size_t>(d->batch) * H * p.splits * Dv * sizeof(float) + 255) & ~size_t(255);
-  p.ws_bytes = static_cast<size_t>(d->batch) * H * p.splits * (Dv + 1) * sizeof(float) + 256;
+  p.part_bytes = (static_cast<size_t>(nb) * H * p.splits * Dv * sizeof(float) + 255) & ~size_t(255);
+  p.ws_bytes = static_cast<size_t>(nb) * H * p.splits * (Dv + 1) * sizeof(float) + 256;
   return p;
 }
 
@@ -145,10 +147,12 @@ struct IndexWs {
   size_t q_codes, q_scales, wpad, scores, hist1, hist2, cnt, above, cand, total;
 };
 
-IndexWs index_ws(const dsv4_layer_desc* d, int Hi, int k) {
+// T: queries per sequence (batch * T virtual sequences, each with its own
+// query, scores and selection).
+IndexWs index_ws(const dsv4_layer_desc* d, int Hi, int k, int T = 1) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t N = index_heads_padded(Hi);
-  const size_t B = d->batch, cap = d->capacity;
+  const size_t B = static_cast<size_t>(d->batch) * T, cap = d->capacity;
   IndexWs w{};
   w.q_codes = 0;
   w.q_scales = up(w.q_codes + B * N * (d->idx_dim / 2));
@@ -163,7 +167,7 @@ IndexWs index_ws(const dsv4_layer_desc* d, int Hi, int k) {
   return w;
 }
 
-size_t index_ws_bytes(const dsv4_layer_desc* d, int Hi, int k) { return index_ws(d, Hi, k).total; }
+size_t index_ws_bytes(const dsv4_layer_desc* d, int Hi, int k, int T = 1) { return index_ws(d, Hi, k, T).total; }
 
 template <typename F>
 void set_smem_once(std::once_flag& flag, F func, int bytes) {
@@ -173,34 +177,44 @@ void set_smem_once(std::once_flag& flag, F func, int bytes) {
 int launch_status() { return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA; }
 
 // n_sel: the top-k width (CSA), 0 for every entry (HCA), -1 for no compressed
-// entry at all (a window-only CSA call, k = 0).
+// entry at all (a window-only CSA call, k = 0). T queries per sequence; with
+// span_k the window tokens come from that span of the last T + W - 1 raw
+// tokens of each sequence instead of the cache's ring.
 int decode_common(const dsv4_layer_desc* d, const dsv4_cache* c, int H, const uint16_t* q, float sm_scale,
-                  const int32_t* topk, int n_sel, float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+                  const int32_t* topk, int n_sel, float* out, float* lse, void* ws, size_t ws_bytes, void* stream,
+                  int T = 1, const uint16_t* span_k = nullptr, const uint16_t* span_v = nullptr) {
   int e = check_desc(d);
   if (e) return e;
   if ((e = check_cache_read(d, c))) return e;
-  if (H < 1) return DSV4_ERR_INVALID_ARG;
+  if (H < 1 || T < 1) return DSV4_ERR_INVALID_ARG;
   if (H > 128) return DSV4_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->batch) * T > 65535) return DSV4_ERR_UNSUPPORTED;   // the grid's y extent
   DSV4_REQ(q);
   DSV4_REQ(out);
   DSV4_REQ(ws);
   if (lse && !aligned16(lse)) return DSV4_ERR_MISALIGNED;
   if (!(sm_scale == sm_scale)) return DSV4_ERR_INVALID_ARG;
-  const AttnPlan p = attn_plan(d, H, n_sel);
+  const bool span = T > 1 || span_k;
+  if (span && d->window) {
+    DSV4_REQ(span_k);
+    if (d->separate_v) DSV4_REQ(span_v);
+  }
+  const AttnPlan p = attn_plan(d, H, n_sel, T);
   if (ws_bytes < p.ws_bytes) return DSV4_ERR_WORKSPACE;
   AttnArgs a{};
-  a.B = d->batch; a.H = H; a.D = d->d_nope + d->d_rope; a.Dv = a.D; a.d_nope = d->d_nope; a.d_rope = d->d_rope;
+  a.B = d->batch * T; a.T = T; a.span = span ? T + d->window - 1 : 0;
+  a.H = H; a.D = d->d_nope + d->d_rope; a.Dv = a.D; a.d_nope = d->d_nope; a.d_rope = d->d_rope;
   a.ratio = d->ratio; a.window = d->window; a.capacity = d->capacity; a.separate_v = d->separate_v ? 1 : 0;
   a.n_sel = n_sel; a.splits = p.splits; a.rows_per_split = p.rows_per_split; a.sm_scale = sm_scale;
   a.tile_rows = p.tile_rows; a.tiles_per_split = p.tiles_per_split;
   a.q = q; a.topk = topk;
-  a.k_nope = c->k.nope; a.k_scale = c->k.scale; a.k_rope = c->k.rope; a.win_k = c->win_k;
-  a.v_nope = c->v.nope; a.v_scale = c->v.scale; a.v_rope = c->v.rope; a.win_v = c->win_v;
+  a.k_nope = c->k.nope; a.k_scale = c->k.scale; a.k_rope = c->k.rope; a.win_k = span ? span_k : c->win_k;
+  a.v_nope = c->v.nope; a.v_scale = c->v.scale; a.v_rope = c->v.rope; a.win_v = span ? span_v : c->win_v;
   a.n_tokens = c->n_tokens; a.status = c->status;
   char* w = static_cast<char*>(ws);
   a.part_o = reinterpret_cast<float*>(w);
   a.part_lse = reinterpret_cast<float*>(w + p.part_bytes);
-  a.part_lsev = a.part_lse + static_cast<size_t>(d->batch) * H * p.splits;
+  a.part_lsev = a.part_lse + static_cast<size_t>(a.B) * H * p.splits;
   a.out = out; a.lse = lse;
   if (p.tc) return launch_attention_tc(a, p.head_groups, static_cast<cudaStream_t>(stream));
   return launch_attention(a, p.head_groups, static_cast<cudaStream_t>(stream));
@@ -225,6 +239,10 @@ void* static_scratch() {
   }
   return addr[dev];
 }
+
+int index_topk_common(const dsv4_layer_desc* d, const dsv4_cache* c, int T, int32_t Hi, const uint16_t* q_idx,
+                      const float* w, int32_t k, int32_t* topk, float* scores, void* ws, size_t ws_bytes,
+                      void* stream);
 
 }  // namespace
 }  // namespace dsv4
@@ -316,12 +334,28 @@ int dsv4_compress_append(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t 
 int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, const uint16_t* q_idx,
                     const float* w, int32_t k, int32_t* topk, float* scores, void* ws, size_t ws_bytes,
                     void* stream) {
+  return index_topk_common(d, c, 1, Hi, q_idx, w, k, topk, scores, ws, ws_bytes, stream);
+}
+
+int dsv4_index_topk_multi(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t T, int32_t Hi,
+                          const uint16_t* q_idx, const float* w, int32_t k, int32_t* topk, float* scores, void* ws,
+                          size_t ws_bytes, void* stream) {
+  return index_topk_common(d, c, T, Hi, q_idx, w, k, topk, scores, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace dsv4 {
+namespace {
+int index_topk_common(const dsv4_layer_desc* d, const dsv4_cache* c, int T, int32_t Hi, const uint16_t* q_idx,
+                      const float* w, int32_t k, int32_t* topk, float* scores, void* ws, size_t ws_bytes,
+                      void* stream) {
   int e = check_desc(d);
   if (e) return e;
   if (!c) return DSV4_ERR_INVALID_ARG;
   if (d->idx_dim == 0) return DSV4_ERR_INVALID_ARG;
-  if (Hi < 1 || k < 1) return DSV4_ERR_INVALID_ARG;
-  if (Hi > 128 || k > 2048) return DSV4_ERR_UNSUPPORTED;
+  if (Hi < 1 || k < 1 || T < 1) return DSV4_ERR_INVALID_ARG;
+  if (Hi > 128 || k > 2048 || static_cast<int64_t>(d->batch) * T > 65535) return DSV4_ERR_UNSUPPORTED;
   DSV4_REQ(c->idx_codes);
   DSV4_REQ(c->idx_scales);
   DSV4_REQ(c->n_tokens);
@@ -331,12 +365,13 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   DSV4_REQ(topk);
   DSV4_REQ(ws);
   if (scores && !aligned16(scores)) return DSV4_ERR_MISALIGNED;
-  if (ws_bytes < index_ws_bytes(d, Hi, k)) return DSV4_ERR_WORKSPACE;
+  if (ws_bytes < index_ws_bytes(d, Hi, k, T)) return DSV4_ERR_WORKSPACE;
   const int N = index_heads_padded(Hi);
-  const IndexWs wl = index_ws(d, Hi, k);
+  const IndexWs wl = index_ws(d, Hi, k, T);
   char* wp = static_cast<char*>(ws);
   IndexArgs a{};
-  a.B = d->batch; a.Hi = Hi; a.N = N; a.Di = d->idx_dim; a.k = k; a.capacity = d->capacity; a.ratio = d->ratio;
+  a.B = d->batch * T; a.T = T;
+  a.Hi = Hi; a.N = N; a.Di = d->idx_dim; a.k = k; a.capacity = d->capacity; a.ratio = d->ratio;
   a.q_idx = q_idx; a.w = w; a.n_tokens = c->n_tokens;
   a.q_codes = reinterpret_cast<uint8_t*>(wp + wl.q_codes);
   a.q_scales = reinterpret_cast<uint8_t*>(wp + wl.q_scales);
@@ -351,7 +386,7 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((e = launch_pdl(quant_query_fp4_kernel, dim3(a.B * N), dim3(32), 0, st, a))) return e;
   IndexTcArgs t{};
-  t.B = a.B; t.N = N; t.Di = a.Di; t.capacity = a.capacity; t.ratio = a.ratio;
+  t.B = a.B; t.T = T; t.N = N; t.Di = a.Di; t.capacity = a.capacity; t.ratio = a.ratio;
   const int tiles = (d->capacity + 127) / 128;
   int per_seq = 2 * sm_count() / a.B;
   if (per_seq < 1) per_seq = 1;
@@ -370,6 +405,10 @@ int dsv4_index_topk(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t Hi, c
   if (sel < 1) sel = 1;
   return launch_topk_select(a, sel, st);
 }
+}  // namespace
+}  // namespace dsv4
+
+extern "C" {
 
 int dsv4_csa_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q, float sm_scale,
                     const int32_t* topk, int32_t k, float* out, float* lse, void* ws, size_t ws_bytes,
@@ -385,6 +424,42 @@ int dsv4_csa_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, co
 int dsv4_hca_decode(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q, float sm_scale,
                     float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
   return decode_common(d, c, H, q, sm_scale, nullptr, 0, out, lse, ws, ws_bytes, stream);
+}
+
+int dsv4_csa_decode_multi(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t T, int32_t H, const uint16_t* q,
+                          float sm_scale, const int32_t* topk, int32_t k, const uint16_t* span_k,
+                          const uint16_t* span_v, float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (k < 0) return DSV4_ERR_INVALID_ARG;
+  if (k > 2048) return DSV4_ERR_UNSUPPORTED;
+  if (k == 0)
+    return decode_common(d, c, H, q, sm_scale, nullptr, -1, out, lse, ws, ws_bytes, stream, T, span_k, span_v);
+  if (!topk) return DSV4_ERR_INVALID_ARG;
+  if (!aligned16(topk)) return DSV4_ERR_MISALIGNED;
+  return decode_common(d, c, H, q, sm_scale, topk, k, out, lse, ws, ws_bytes, stream, T, span_k, span_v);
+}
+
+int dsv4_hca_decode_multi(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t T, int32_t H, const uint16_t* q,
+                          float sm_scale, const uint16_t* span_k, const uint16_t* span_v, float* out, float* lse,
+                          void* ws, size_t ws_bytes, void* stream) {
+  return decode_common(d, c, H, q, sm_scale, nullptr, 0, out, lse, ws, ws_bytes, stream, T, span_k, span_v);
+}
+
+size_t dsv4_workspace_size_multi(const dsv4_layer_desc* d, int32_t T, int32_t H, int32_t Hi, int32_t k) {
+  if (check_desc(d) || T < 1 || static_cast<int64_t>(d->batch) * T > 65535 || H < 1 || H > 128 || Hi < 0 ||
+      Hi > 128 || k < 0 || k > 2048)
+    return 0;
+  size_t need = attn_plan(d, H, 0, T).ws_bytes;
+  const size_t win = attn_plan(d, H, -1, T).ws_bytes;
+  if (win > need) need = win;
+  if (k > 0) {
+    const size_t csa = attn_plan(d, H, k, T).ws_bytes;
+    if (csa > need) need = csa;
+  }
+  if (d->idx_dim && Hi > 0) {
+    const size_t idx = index_ws_bytes(d, Hi, k > 0 ? k : 1, T);
+    if (idx > need) need = idx;
+  }
+  return need;
 }
 
 int dsv4_hca_decode_static(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t H, const uint16_t* q,

@@ -50,13 +50,14 @@ __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
   float* kT = reinterpret_cast<float*>(smraw + ((HP * D * 2 + 15) & ~15));
   float* vs = kT + D * RT;
   float* ss = vs + RT * Dv;
-  int64_t* rowid = reinterpret_cast<int64_t*>(ss + HP * RT);   // >= 0: entry, < 0: -(window slot) - 1
+  int64_t* rowid = reinterpret_cast<int64_t*>(ss + HP * RT);   // >= 0: entry, < 0: -(window source row) - 1
 
   const int split = blockIdx.x, b = blockIdx.y;
   const int h0 = blockIdx.z * HG;
   const int tid = threadIdx.x;
 
-  const int64_t n_tok = a.n_tokens[b];
+  const int64_t n_tok = vseq_tokens(a.n_tokens, b, a.T);
+  const int64_t bs = b / a.T;   // the sequence whose cache planes this (virtual) sequence reads
   const int64_t n_c = n_tok / a.ratio < a.capacity ? n_tok / a.ratio : a.capacity;
   const int64_t n_win = n_tok < a.window ? n_tok : a.window;
   const int64_t n_main = a.n_sel > 0 ? a.n_sel : (a.n_sel < 0 ? 0 : n_c);
@@ -94,7 +95,8 @@ __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
           if (e >= 0) id = e;
         } else {
           const int64_t pos = n_tok - n_win + (r - n_main);
-          id = -(pos % a.window) - 1;
+          id = a.span == 0 ? -(bs * a.window + pos % a.window) - 1
+                           : -(bs * a.span + pos - (a.n_tokens[bs] - a.span)) - 1;
         }
       }
       rowid[tid] = id;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
       const int64_t id = rowid[r];
       float kval = 0.f, vval = 0.f;
       if (id >= 0) {
-        const int64_t e = static_cast<int64_t>(b) * a.capacity + id;
+        const int64_t e = bs * a.capacity + id;
         if (d < a.d_nope) {
           kval = e4m3_to_f32(K.nope[e * a.d_nope + d]) * K.scale[e];
           vval = a.separate_v ? e4m3_to_f32(V.nope[e * a.d_nope + d]) * V.scale[e] : kval;
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(NT) attn_split_kernel(AttnArgs a) {
           vval = a.separate_v ? bf16_to_f32(V.rope[e * a.d_rope + (d - a.d_nope)]) : kval;
         }
       } else if (id != INT64_MIN) {
-        const int64_t slot = static_cast<int64_t>(b) * a.window + (-id - 1);
+        const int64_t slot = -id - 1;
         kval = bf16_to_f32(K.win[slot * D + d]);
         vval = a.separate_v ? bf16_to_f32(V.win[slot * D + d]) : kval;
       }

@@ -225,7 +225,7 @@ struct RowSpace {
 
 DSV4_DEV RowSpace row_space(const AttnArgs& a, int b) {
   RowSpace s;
-  s.n_tok = a.n_tokens[b];
+  s.n_tok = vseq_tokens(a.n_tokens, b, a.T);
   s.n_c = s.n_tok / a.ratio < a.capacity ? s.n_tok / a.ratio : a.capacity;
   s.n_win = s.n_tok < a.window ? s.n_tok : a.window;
   s.n_main = a.n_sel > 0 ? a.n_sel : (a.n_sel < 0 ? 0 : s.n_c);
@@ -251,12 +251,15 @@ DSV4_DEV Tile tile_at(const AttnArgs& a, const RowSpace& s, int i) {
   return t;
 }
 
-// Source of row j of tile t: >= 0 entry index into the planes (b * capacity +
-// e), -1 no row (past the tile, a -1 top-k slot or an invalid index), <= -2
-// window ring slot (-2 - slot).
+// Source of row j of tile t of virtual sequence b: >= 0 entry index into the
+// planes (b_seq * capacity + e), -1 no row (past the tile, a -1 top-k slot or
+// an invalid index), <= -2 a row of the window source (-2 - row): of the ring
+// (b_seq * W + position % W) or of the span (b_seq * span + position - the
+// span's first position).
 DSV4_DEV int32_t row_source(const AttnArgs& a, const RowSpace& s, int b, const Tile& t, int j) {
   if (j >= t.cnt) return -1;
   const int64_t r = t.r0 + j;
+  const int64_t bs = b / a.T;
   if (!t.win) {
     const int64_t e = a.n_sel > 0 ? static_cast<int64_t>(a.topk[static_cast<int64_t>(b) * a.n_sel + r]) : r;
     if (e < -1 || e >= s.n_c) {
@@ -264,10 +267,11 @@ DSV4_DEV int32_t row_source(const AttnArgs& a, const RowSpace& s, int b, const T
       return -1;
     }
     if (e < 0) return -1;
-    return static_cast<int32_t>(static_cast<int64_t>(b) * a.capacity + e);
+    return static_cast<int32_t>(bs * a.capacity + e);
   }
   const int64_t pos = s.n_tok - s.n_win + r;
-  return static_cast<int32_t>(-2 - pos % a.window);
+  if (a.span == 0) return static_cast<int32_t>(-2 - (bs * a.window + pos % a.window));
+  return static_cast<int32_t>(-2 - (bs * a.span + pos - (a.n_tokens[bs] - a.span)));
 }
 
 DSV4_DEV void cp_async16(void* dst, const void* src) {
@@ -325,7 +329,7 @@ DSV4_DEV void issue_chunk(const AttnArgs& a, int b, bool win, const int32_t* src
           cp_async16(xc + cs.rope_off + j * cs.rb + 16 * (g - ng),
                      rope + static_cast<int64_t>(sr) * a.d_rope + cs.e0 + 8 * (g - ng));
       } else if (win && sr <= -2) {
-        cp_async16(xc + j * 256 + 16 * g, wbuf + (static_cast<int64_t>(b) * a.window + (-2 - sr)) * a.D + c * 128 + 8 * g);
+        cp_async16(xc + j * 256 + 16 * g, wbuf + static_cast<int64_t>(-2 - sr) * a.D + c * 128 + 8 * g);
       }
     }
   }
@@ -556,7 +560,7 @@ DSV4_DEV void convert_chunk(const AttnArgs& a, bool win, const int32_t* src, con
 // (contiguous rows) into the chunk's region, completing on xland[c].
 DSV4_DEV void issue_tma_chunk(const AttnArgs& a, const AttnMaps& maps, int b, const Tile& tl, int c,
                               unsigned char* xk, uint64_t* xland, uint32_t* sk) {
-  const int y = static_cast<int>(static_cast<int64_t>(b) * a.capacity + tl.r0);
+  const int y = static_cast<int>(static_cast<int64_t>(b / a.T) * a.capacity + tl.r0);
   const ChunkSplit cs = chunk_split(a, c);
   unsigned char* xc = xk + c * kChunkBytes;
   // with the first chunk, the tile's scales (raw fp32, a whole number of
@@ -816,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ TMA producer (HCA compressed rows)
     if (!SEP && a.tma) {
-      const int64_t row_base = static_cast<int64_t>(b) * a.capacity;
+      const int64_t row_base = static_cast<int64_t>(b / a.T) * a.capacity;
       if (lane == 0) {
         // boxes issued per chunk (the first tile's went out before the setup)
         int issued[kMaxChunks];
@@ -1140,7 +1144,7 @@ int launch_attention_tc(const AttnArgs& a0, int head_groups, cudaStream_t st) {
   memset(&maps, 0, sizeof(maps));
   a.tma = 0;
   if (a.n_sel == 0 && attention_tc_tma_shape(a.d_nope, a.d_rope, a.separate_v)) {
-    const int64_t rows = static_cast<int64_t>(a.B) * a.capacity;
+    const int64_t rows = static_cast<int64_t>(a.B / a.T) * a.capacity;
     const int tail = a.d_nope % 128;
     bool ok = a.d_nope < 128 || encode_u8_rows(&maps.nope, a.k_nope, rows, a.d_nope, 128, a.tile_rows);
     if (ok && tail) ok = encode_u8_rows(&maps.nope_tail, a.k_nope, rows, a.d_nope, tail, a.tile_rows);

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) topk_select_kernel(IndexArgs a
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
   const int64_t cap_end = c0 + chunk < a.capacity ? c0 + chunk : a.capacity;
   uint32_t* cnt = a.cnt + b * kCntWords;
-  int64_t n_c = a.n_tokens[b] / a.ratio;
+  int64_t n_c = vseq_tokens(a.n_tokens, b, a.T) / a.ratio;
   if (n_c > a.capacity) n_c = a.capacity;
   int32_t* out = a.topk + static_cast<int64_t>(b) * a.k;
   const int k = a.k;

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (r0 < a.capacity) {
       const int64_t want = static_cast<int64_t>(C::STAGES) * kTile;
       const int64_t n = a.capacity - r0 < want ? a.capacity - r0 : want;
-      const int64_t row = static_cast<int64_t>(blockIdx.y) * a.capacity + r0;
+      const int64_t row = static_cast<int64_t>(blockIdx.y / a.T) * a.capacity + r0;
       // a sequence's slice of the scale plane starts on a 16-byte boundary only
       // when capacity * Di / 16 is a multiple of 16: the range helper trims it
       if (threadIdx.x == 32) tc::prefetch_l2_range(a.idx_codes + row * ROWB, n * ROWB);
@@ -107,8 +107,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   pdl_wait();
 
-  const int b = blockIdx.y;
-  int64_t n_c = a.n_tokens[b] / a.ratio;
+  const int b = blockIdx.y;              // virtual sequence (query)
+  const int64_t bs = b / a.T;            // whose keys it scores
+  int64_t n_c = vseq_tokens(a.n_tokens, b, a.T) / a.ratio;
   if (n_c > a.capacity) n_c = a.capacity;
   const int tiles = static_cast<int>((n_c + kTile - 1) / kTile);
   const int per = (tiles + a.ctas_per_seq - 1) / a.ctas_per_seq;
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!tc::mbar_wait(&t->empty[stage], (round & 1) ^ 1, abort)) break;
         tc::mbar_arrive_expect_tx(&t->full[stage], C::STAGE_BYTES);
         tc::tma_load_2d(stages + stage * C::STAGE_BYTES, &keys, &t->full[stage], 0,
-                        static_cast<int>(static_cast<int64_t>(b) * a.capacity + static_cast<int64_t>(t0 + i) * kTile));
+                        static_cast<int>(bs * a.capacity + static_cast<int64_t>(t0 + i) * kTile));
         ++issued;
       }
       // every copy issued must land before the CTA's shared memory goes away
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int rr = 0; rr < 2; ++rr) {
         const int64_t s = static_cast<int64_t>(t0 + i) * kTile + tid + rr * 64;
         const uint32_t* src =
-            reinterpret_cast<const uint32_t*>(a.idx_scales + (static_cast<int64_t>(b) * a.capacity + s) * nblk);
+            reinterpret_cast<const uint32_t*>(a.idx_scales + (bs * a.capacity + s) * nblk);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) w[rr][kk] = (i < ntile && s < n_c) ? __ldg(src + kk) : 0u;
       }
@@ -379,7 +380,7 @@ bool encode_u8_rows(CUtensorMap* map, const void* base, int64_t rows, int row_by
 int launch_index_scores_tc(const IndexTcArgs& a, const uint8_t* key_codes, const uint8_t* q_codes, cudaStream_t st) {
   const int rowb = a.Di / 2;
   CUtensorMap keys, qmap;
-  if (!encode_rows(&keys, key_codes, rowb, static_cast<int64_t>(a.B) * a.capacity, kTile)) return DSV4_ERR_CUDA;
+  if (!encode_rows(&keys, key_codes, rowb, static_cast<int64_t>(a.B / a.T) * a.capacity, kTile)) return DSV4_ERR_CUDA;
   if (!encode_rows(&qmap, q_codes, rowb, static_cast<int64_t>(a.B) * a.N, a.N)) return DSV4_ERR_CUDA;
   switch (rowb) {
     case 32: return launch_tc<32>(a, keys, qmap, st);

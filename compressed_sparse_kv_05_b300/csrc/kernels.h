@@ -8,6 +8,15 @@
 
 namespace dsv4 {
 
+// Several queries per sequence (multi-token decode): virtual sequence v = b * T
+// + t is query t of sequence b, at position n_tokens[b] - T + t; it reads
+// sequence b's cache planes and sees the tokens up to its own position.
+// T = 1 is single-token decode (v = b).
+__device__ __forceinline__ int64_t vseq_tokens(const int64_t* n_tokens, int v, int T) {
+  const int64_t n = n_tokens[v / T] - (T - 1 - v % T);
+  return n > 0 ? n : 0;
+}
+
 struct AppendArgs {
   int T, ratio, window, capacity, d_nope, d_rope, idx_dim, separate_v;
   int ctas_k;              // pool_chunk_kernel: CTAs of the key (and value) stream, then
@@ -67,6 +76,7 @@ __global__ void pool_rows_kernel(const uint16_t* x, const uint16_t* z, const flo
 constexpr int kCntWords = 8;
 struct IndexArgs {
   int B, Hi, N, Di, k, capacity, ratio;
+  int T;                   // queries per sequence: B counts B_seq * T virtual sequences (see vseq_tokens)
   const uint16_t* q_idx;   // [B][Hi][Di] bf16
   const float* w;          // [B][Hi]
   const int64_t* n_tokens;
@@ -87,6 +97,7 @@ int launch_topk_select(const IndexArgs& a, int sel_ctas, cudaStream_t st);
 
 struct IndexTcArgs {
   int B, N, Di, capacity, ratio, ctas_per_seq, k;
+  int T;                       // queries per sequence (B counts virtual sequences)
   uint32_t tmem_cols;
   const int64_t* n_tokens;
   const uint8_t* idx_codes;    // [B][capacity][Di/2] (read through the tensor map; its address for L2 prefetches)
@@ -104,6 +115,10 @@ int launch_index_scores_tc(const IndexTcArgs& a, const uint8_t* key_codes, const
 // ---- attention
 struct AttnArgs {
   int B, H, D, Dv, d_nope, d_rope, ratio, window, capacity, separate_v;
+  int T;                   // queries per sequence: B counts B_seq * T virtual sequences (see vseq_tokens)
+  int span;                // 0: window tokens from the cache's ring (win_k: [B_seq][W][D]); else rows per
+                           // sequence of a span of recent raw tokens (win_k: [B_seq][span][D], the tokens at
+                           // positions [n - span, n) of a sequence holding n tokens)
   int n_sel;               // top-k width (CSA), 0 for HCA (every entry), -1 for none (window only)
   int splits, rows_per_split;
   int tile_rows;           // tensor-core kernel: rows per tile (32, 64 or 128)

@@ -58,6 +58,13 @@ _SIGS = {
                         ctypes.c_int),
     "dsv4_hca_decode": ([_DESC, _CACHE, _I32, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "dsv4_hca_decode_static": ([_DESC, _CACHE, _I32, _P, ctypes.c_float, _P, _P, _P], ctypes.c_int),
+    "dsv4_index_topk_multi": ([_DESC, _CACHE, _I32, _I32, _P, _P, _I32, _P, _P, _P, ctypes.c_size_t, _P],
+                              ctypes.c_int),
+    "dsv4_csa_decode_multi": ([_DESC, _CACHE, _I32, _I32, _P, ctypes.c_float, _P, _I32, _P, _P, _P, _P, _P,
+                               ctypes.c_size_t, _P], ctypes.c_int),
+    "dsv4_hca_decode_multi": ([_DESC, _CACHE, _I32, _I32, _P, ctypes.c_float, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                               _P], ctypes.c_int),
+    "dsv4_workspace_size_multi": ([_DESC, _I32, _I32, _I32, _I32], ctypes.c_size_t),
     "dsv4_workspace_size": ([_DESC, _I32, _I32, _I32], ctypes.c_size_t),
     "dsv4_decode_plan": ([_DESC, _I32, _I32, _P], ctypes.c_int),
     "dsv4_read_status": ([_CACHE, _P], ctypes.c_int),
@@ -168,6 +175,36 @@ def dsv4_hca_decode_static(desc, cache, H, q, sm_scale, out, lse, stream=None):
     return _check("dsv4_hca_decode_static", lib.dsv4_hca_decode_static(
         ctypes.byref(desc), ctypes.byref(cache.struct), H, _ptr(q), float(sm_scale), _ptr(out), _ptr(lse),
         _stream(stream)))
+
+
+def dsv4_index_topk_multi(desc, cache, T, Hi, q_idx, w, k, topk, scores, ws, stream=None):
+    return _check("dsv4_index_topk_multi", lib.dsv4_index_topk_multi(
+        ctypes.byref(desc), ctypes.byref(cache.struct), T, Hi, _ptr(q_idx), _ptr(w), k, _ptr(topk), _ptr(scores),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dsv4_csa_decode_multi(desc, cache, T, H, q, sm_scale, topk, k, span_k, span_v, out, lse, ws, stream=None):
+    return _check("dsv4_csa_decode_multi", lib.dsv4_csa_decode_multi(
+        ctypes.byref(desc), ctypes.byref(cache.struct), T, H, _ptr(q), float(sm_scale), _ptr(topk), k, _ptr(span_k),
+        _ptr(span_v), _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dsv4_hca_decode_multi(desc, cache, T, H, q, sm_scale, span_k, span_v, out, lse, ws, stream=None):
+    return _check("dsv4_hca_decode_multi", lib.dsv4_hca_decode_multi(
+        ctypes.byref(desc), ctypes.byref(cache.struct), T, H, _ptr(q), float(sm_scale), _ptr(span_k), _ptr(span_v),
+        _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dsv4_workspace_size_multi(desc, T, H, Hi, k):
+    return int(lib.dsv4_workspace_size_multi(ctypes.byref(desc), T, H, Hi, k))
+
+
+def workspace_multi(desc, T, H, Hi=0, k=0, device="cuda"):
+    """Device workspace for T queries per sequence (dsv4_workspace_size_multi bytes)."""
+    n = dsv4_workspace_size_multi(desc, T, H, Hi, k)
+    if n == 0:
+        raise Dsv4Error("dsv4_workspace_size_multi", ERR_INVALID_ARG)
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def dsv4_workspace_size(desc, H, Hi, k):

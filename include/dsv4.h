@@ -171,6 +171,35 @@ int dsv4_hca_decode(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_
                     const uint16_t* q, float sm_scale, float* out, float* lse,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* Multi-token decode (chunked prefill, speculative decoding) [CSA]: the
+ * compressor outputs entries for T new tokens per step, and all T queries of a
+ * sequence are served in one call, after their tokens were appended. Query t
+ * of sequence b sits at position p = n_tokens[b] - T + t and sees the tokens
+ * up to p only: the compressed entries complete by then, n_c(t) = (p + 1) /
+ * ratio (its indexer scores and top-k cover those alone: a causal selection),
+ * and the window of the min(W, p + 1) raw tokens ending at p. The cache's ring
+ * holds only the last W tokens, so the window tokens come from a span of raw
+ * rows the caller passes:
+ *   span_k, span_v : [B][T + W - 1][D] bf16 keys (values) of the positions
+ *                    [n_tokens[b] - T - W + 1, n_tokens[b]); rows of negative
+ *                    positions are not read; span_v only when separate_v.
+ * Layouts: q_idx [B][T][Hi][Di], w [B][T][Hi], topk [B][T][k] (index_topk
+ * output, csa input), scores [B][T][capacity] or NULL; q [B][T][H][D],
+ * out [B][T][H][D], lse [B][T][H] or NULL. Same argument rules as the
+ * single-token calls, and batch * T <= 65535; workspace:
+ * dsv4_workspace_size_multi(). T = 1 with a span of the last W tokens computes
+ * what the single-token calls compute. */
+int dsv4_index_topk_multi(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_t T, int32_t Hi,
+                          const uint16_t* q_idx, const float* w, int32_t k, int32_t* topk, float* scores,
+                          void* ws, size_t ws_bytes, void* stream);
+int dsv4_csa_decode_multi(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_t T, int32_t H,
+                          const uint16_t* q, float sm_scale, const int32_t* topk, int32_t k, const uint16_t* span_k,
+                          const uint16_t* span_v, float* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+int dsv4_hca_decode_multi(const dsv4_layer_desc* desc, const dsv4_cache* cache, int32_t T, int32_t H,
+                          const uint16_t* q, float sm_scale, const uint16_t* span_k, const uint16_t* span_v,
+                          float* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+size_t dsv4_workspace_size_multi(const dsv4_layer_desc* desc, int32_t T, int32_t H, int32_t Hi, int32_t k);
+
 /* dsv4_hca_decode for callers that cannot allocate device memory.
  * The pages describe no such call; it exists for library users. Some callers
  * cannot call cudaMalloc at all: code that runs while a CUDA graph is being

@@ -15,6 +15,7 @@ on tiny inputs, and the invariants listed in ``tests/test_oracle_*.py``.
 from .formats import (E2M1_MAX, E4M3_MAX, bf16_decode, bf16_encode, e2m1_decode,
                       e2m1_encode, e4m3_decode, e4m3_encode)
 from .method import (attend, build_cache, csa_attend, dequant_fp4_rows,
-                     dequant_kv_rows, hca_attend, index_scores, lse_merge,
-                     pool_blocks, quantize_fp4_rows, quantize_kv_rows,
-                     topk_blocks, topk_boundary_gap, window_tokens)
+                     dequant_kv_rows, hca_attend, index_scores, index_scores_causal,
+                     lse_merge, multi_attend, pool_blocks, quantize_fp4_rows,
+                     quantize_kv_rows, query_positions, topk_blocks, topk_boundary_gap,
+                     window_tokens)

@@ -290,3 +290,60 @@ def hca_attend(q_bits, sm_scale, n_tokens, ratio, window,
     all_idx = np.arange(n_c, dtype=np.int32)
     return csa_attend(q_bits, sm_scale, all_idx, n_tokens, ratio, window,
                       k_nope, k_scale, k_rope, win_k, v_nope, v_scale, v_rope, win_v)
+
+
+# ----------------------------------------------------------------------------- several queries per step
+
+
+def query_positions(n_tokens, T):
+    """Positions of the T queries of a multi-token step taken after their T
+    tokens were appended to a sequence of n_tokens tokens: n - T + t [CSA]."""
+    return np.arange(n_tokens - T, n_tokens)
+
+
+def index_scores_causal(idx_codes, idx_scales, q_idx_bits, w, n_tokens, ratio):
+    """Lightning-indexer scores of T queries [HYB], [CSA], each over the
+    compressed blocks complete at its own position (a causal selection): query
+    t at position p scores blocks j < (p + 1) // ratio, with its own indexer
+    query q_idx_bits[t] (bf16 [Hi][Di]) and head weights w[t].
+    Returns a list of T float64 arrays (scores of blocks 0 .. n_c(t) - 1)."""
+    T = q_idx_bits.shape[0]
+    out = []
+    for t, p in enumerate(query_positions(n_tokens, T)):
+        n_c = (p + 1) // ratio
+        out.append(index_scores(idx_codes[:n_c], idx_scales[:n_c], q_idx_bits[t], w[t]))
+    return out
+
+
+def multi_attend(q_bits, sm_scale, sel, n_tokens, ratio, window, k_nope, k_scale, k_rope, span_k,
+                 v_nope=None, v_scale=None, v_rope=None, span_v=None):
+    """Attention of T queries of one sequence [HYB], [CSA], [HCA]: query t at
+    position p = n - T + t attends, under one softmax, to the compressed
+    entries sel[t] (indices < (p + 1) // ratio; -1 is padding), or to every
+    entry complete by p when sel is None, together with the raw tokens of the
+    positions max(0, p - W + 1) .. p. span_k (span_v) holds the raw rows of the
+    positions n - T - W + 1 .. n - 1, row r for position n - T - W + 1 + r.
+    Returns (out [T][H][Dv], lse [T][H])."""
+    T = q_bits.shape[0]
+    first = n_tokens - T - window + 1          # position of span row 0
+    outs, lses = [], []
+    for t, p in enumerate(query_positions(n_tokens, T)):
+        n_c = (p + 1) // ratio
+        idx = np.arange(n_c) if sel is None else np.asarray([i for i in np.asarray(sel[t]).tolist() if i >= 0])
+        if np.any(idx >= n_c):
+            raise ValueError("a selected entry is not complete at the query's position")
+        idx = idx.astype(np.int64)
+        pos = np.arange(max(0, p - window + 1), p + 1)
+        K = np.concatenate([dequant_kv_rows(k_nope[idx], k_scale[idx], k_rope[idx]),
+                            bf16_decode(span_k[pos - first]) if pos.size else
+                            np.zeros((0, k_nope.shape[1] + k_rope.shape[1]))], axis=0)
+        if v_nope is None:
+            V = K
+        else:
+            V = np.concatenate([dequant_kv_rows(v_nope[idx], v_scale[idx], v_rope[idx]),
+                                bf16_decode(span_v[pos - first]) if pos.size else
+                                np.zeros((0, v_nope.shape[1] + v_rope.shape[1]))], axis=0)
+        o, l = attend(q_bits[t], K, V, sm_scale)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)

@@ -365,3 +365,85 @@ def test_decode_step_bytes():
     assert accounting.decode_step_bytes(W.STACK_CSA) == 4 * (262144 * 72 + 64 * 128 * 2 + 64 * 4 + 512 * 580
                                                               + 128 * 512 * 2 + 64 * 512 * 2 + 64 * 512 * 4)
     assert accounting.decode_step_bytes(W.STACK_HCA) == 4 * (8192 * 580 + 128 * 512 * 2 + 64 * 512 * 6)
+
+
+# ----------------------------------------------------------------------------- several queries per step
+
+def _span(rows_bits, n, T, W):
+    """Raw rows of the positions n - T - W + 1 .. n - 1 (zeros for negative positions)."""
+    first = n - T - W + 1
+    out = np.zeros((T + W - 1, rows_bits.shape[1]), np.uint16)
+    for r in range(T + W - 1):
+        if first + r >= 0:
+            out[r] = rows_bits[first + r]
+    return out
+
+
+def _ring(cache, key, W, D):
+    ring = np.zeros((W, D), np.uint16)
+    for slot, tok in cache[key].items():
+        ring[slot] = tok
+    return ring
+
+
+@pytest.mark.parametrize("n,T", [(90, 7), (9, 9), (41, 1), (130, 33)])
+def test_multi_token_step_equals_single_token_decode_on_each_prefix(n, T):
+    """Query t of a T-query step (position p = n - T + t) equals a single-token
+    decode on the cache of its own prefix of p + 1 tokens, built and attended
+    by the single-token functions: the same indexer scores, the same selection
+    and the same attention (CSA and HCA); some queries see fewer blocks than
+    the top-k, the first ones fewer tokens than the window."""
+    W, ratio, dn, dr, Di, H, Hi, kk = 8, 4, 32, 16, 32, 3, 2, 5
+    D = dn + dr
+    k, z, v = bf16(rnd(90, (n, D))), bf16(rnd(91, (n, D))), bf16(rnd(92, (n, D)))
+    u, zu = bf16(rnd(93, (n, Di))), bf16(rnd(94, (n, Di)))
+    b, bu = rnd(95, (ratio, D), 0.1), rnd(96, (ratio, Di), 0.1)
+    full = O.build_cache(k, z, b, ratio, dn, W, v, u, zu, bu)
+    q, qi = bf16(rnd(97, (T, H, D))), bf16(rnd(98, (T, Hi, Di)))
+    w = np.random.default_rng(99).uniform(0, 1, (T, Hi)).astype(np.float32)
+    sm = np.float32(1 / np.sqrt(D))
+    scores = O.index_scores_causal(full["idx_codes"], full["idx_scales"], qi, w, n, ratio)
+    sel = np.stack([O.topk_blocks(sc, kk) for sc in scores])
+    planes = (full["k_nope"], full["k_scale"], full["k_rope"], _span(k, n, T, W),
+              full["v_nope"], full["v_scale"], full["v_rope"], _span(v, n, T, W))
+    out, lse = O.multi_attend(q, sm, sel, n, ratio, W, *planes)
+    outh, lseh = O.multi_attend(q, sm, None, n, ratio, W, *planes)
+    assert out.shape == (T, H, D) and lse.shape == (T, H)
+    for t, p in enumerate(O.query_positions(n, T)):
+        pre = O.build_cache(k[:p + 1], z[:p + 1], b, ratio, dn, W, v[:p + 1], u[:p + 1], zu[:p + 1], bu)
+        args = (p + 1, ratio, W, pre["k_nope"], pre["k_scale"], pre["k_rope"], _ring(pre, "win_k", W, D),
+                pre["v_nope"], pre["v_scale"], pre["v_rope"], _ring(pre, "win_v", W, D))
+        sc1 = O.index_scores(pre["idx_codes"], pre["idx_scales"], qi[t], w[t])
+        assert np.array_equal(sc1, scores[t])
+        assert np.array_equal(O.topk_blocks(sc1, kk), sel[t])
+        o1, l1 = O.csa_attend(q[t], sm, sel[t], *args)
+        assert np.allclose(o1, out[t], rtol=1e-12, atol=1e-14) and np.allclose(l1, lse[t], rtol=1e-13, atol=1e-13)
+        oh, lh = O.hca_attend(q[t], sm, *args)
+        assert np.allclose(oh, outh[t], rtol=1e-12, atol=1e-14) and np.allclose(lh, lseh[t], rtol=1e-13, atol=1e-13)
+
+
+def test_multi_token_step_is_causal():
+    """A query does not see the tokens after its own position: changing them
+    (their raw rows and the blocks they complete) leaves its output unchanged,
+    while changing a token inside its window changes it."""
+    n, T, W, ratio, dn, dr = 64, 12, 6, 4, 32, 16
+    D = dn + dr
+    k, z = bf16(rnd(110, (n, D))), bf16(rnd(111, (n, D)))
+    b = rnd(112, (ratio, D), 0.1)
+    q = bf16(rnd(113, (T, 4, D)))
+    t = 5
+    p = n - T + t
+
+    def run(kk):
+        c = O.build_cache(kk, z, b, ratio, dn, W)
+        return O.multi_attend(q, 0.2, None, n, ratio, W, c["k_nope"], c["k_scale"], c["k_rope"], _span(kk, n, T, W))
+
+    base, _ = run(k)
+    later = k.copy()
+    later[p + 1:] = bf16(rnd(114, (n - p - 1, D)))
+    after, _ = run(later)
+    assert np.array_equal(after[:t + 1], base[:t + 1]) and not np.allclose(after[t + 1:], base[t + 1:])
+    inside = k.copy()
+    inside[p - 1] = bf16(rnd(115, (1, D)))
+    changed, _ = run(inside)
+    assert not np.allclose(changed[t], base[t]) and np.array_equal(changed[:t - 1], base[:t - 1])

@@ -120,3 +120,24 @@ def test_dequant_rope_block_dropped_is_caught(monkeypatch):
            lambda nope, scale, rope: np.concatenate([F.e4m3_decode(nope) * np.asarray(scale, np.float64)[:, None],
                                                      np.zeros(np.shape(rope))], axis=1), M)
     _fails(TM.test_dequant_kv_rows_against_library_decode)
+
+
+def test_multi_token_window_one_token_long_is_caught(monkeypatch):
+    # each query's window reaching one token further back than W
+    orig = M.multi_attend
+
+    def bad(q, sm, sel, n, ratio, W, *planes):
+        return orig(q, sm, sel, n, ratio, W + 1, *planes[:3], np.concatenate([planes[3][:1], planes[3]]),
+                    *planes[4:7], *([np.concatenate([planes[7][:1], planes[7]])] if len(planes) > 7 else []))
+    _patch(monkeypatch, "multi_attend", bad, M)
+    _fails(TM.test_multi_token_step_equals_single_token_decode_on_each_prefix, 90, 7)
+
+
+def test_multi_token_selection_not_causal_is_caught(monkeypatch):
+    # every query scoring all blocks of the sequence instead of those complete at its position
+    def bad(codes, scales, q, w, n, ratio):
+        return [M.index_scores(codes[: n // ratio], scales[: n // ratio], q[t], w[t]) for t in range(q.shape[0])]
+    _patch(monkeypatch, "index_scores_causal", bad, M)
+    # caught by the pin's comparison, or by the attention refusing a block not yet complete
+    with pytest.raises((AssertionError, ValueError)):
+        TM.test_multi_token_step_equals_single_token_decode_on_each_prefix(90, 7)
