@@ -506,6 +506,8 @@ int dsv4_decode_plan(const dsv4_layer_desc* d, int32_t H, int32_t k, int32_t* pl
   return DSV4_OK;
 }
 
+int dsv4_debug_force_timeout(int32_t on) { return attention_force_timeout(on); }
+
 int dsv4_read_status(const dsv4_cache* c, void* stream) {
   if (!c || !c->status) return DSV4_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

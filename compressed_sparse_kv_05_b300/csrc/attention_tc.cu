@@ -102,8 +102,16 @@ constexpr int kBarWork = 1, kBarSoft = 2;      // named barriers (0 is __syncthr
 constexpr float kRescale = 8.f;                // lazy-rescale threshold (log2 units)
 constexpr float kF16Max = 65504.f;
 
+// Test hook (dsv4_debug_force_timeout): when set, the MMA thread of every
+// attention CTA first waits on a barrier that nothing arrives on, so that its
+// bounded wait runs out after kForcedWaitNs and the kernel takes its timeout
+// path (abort flag, every role leaves its loop, copies and MMAs drained,
+// DSV4_STATUS_TIMEOUT raised). Never set outside tests.
+__device__ int g_force_timeout = 0;
+constexpr uint64_t kForcedWaitNs = 50000000ull;   // 50 ms
+
 struct TcTail {
-  uint64_t xland[kMaxChunks], xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, qready, drain;
+  uint64_t xland[kMaxChunks], xfull[kMaxChunks], xfree[kMaxChunks], sfull, pfull, qready, drain, never;
   uint32_t taddr;
   int abort;
   // the per-row arrays are 16-byte aligned: the scales of a tile arrive by bulk copies
@@ -726,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     tc::mbar_init(&t->pfull, kSoftThreads / 32);
     tc::mbar_init(&t->qready, kWorkers / 32);
     tc::mbar_init(&t->drain, 1);
+    tc::mbar_init(&t->never, 1);
     t->abort = 0;
     tc::fence_mbar_init();
   }
@@ -784,7 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const uint32_t id_pv = tc::idesc_f16_f32(kRows, kHeads, 1, 1);
       const uint32_t q_sa = tc::smem_u32(qs), p_sa = tc::smem_u32(pb);
       const uint32_t xk_sa = tc::smem_u32(xk), xv_sa = tc::smem_u32(xv);
-      bool ok = tc::mbar_wait(&t->qready, 0, abort);
+      bool ok = true;
+      if (g_force_timeout) ok = tc::mbar_wait_for(&t->never, 0, abort, kForcedWaitNs);   // test hook: runs out
+      ok = ok && tc::mbar_wait(&t->qready, 0, abort);
       for (int tt = 0; ok && tt < nt; ++tt) {
         const int kk_pv = (tile_at(a, rs, tile0 + tt).cnt + 15) >> 4;   // 16-row steps holding rows
         for (int c = 0; c < nch; ++c) {
@@ -1124,6 +1135,11 @@ int launch_tc(const AttnMaps& maps, const AttnArgs& a, int head_groups, cudaStre
 }
 
 }  // namespace
+
+int attention_force_timeout(int on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(g_force_timeout, &v, sizeof(v)) == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
 
 bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v) {
   const int D = d_nope + d_rope;

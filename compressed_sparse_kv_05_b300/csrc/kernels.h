@@ -148,6 +148,8 @@ struct AttnMaps {
 int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st);
 // the tensor-core split kernel (tiles of up to 128 rows, up to 64 heads per CTA) and the merge
 bool attention_tc_supported(int H, int d_nope, int d_rope, int separate_v);
+// test hook of the tensor-core attention: its MMA thread's first wait runs out (see attention_tc.cu)
+int attention_force_timeout(int on);
 // whether the tensor-core kernel can take the compressed rows of this shape by TMA boxes
 bool attention_tc_tma_shape(int d_nope, int d_rope, int separate_v);
 int launch_attention_tc(const AttnArgs& a, int head_groups, cudaStream_t st);

@@ -61,6 +61,20 @@ DSV4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   }
 }
 
+// As mbar_wait with an explicit limit in ns.
+DSV4_DEV bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (now_ns() - t0 > limit_ns) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Wait without an abort flag (draining copies or MMAs before shared or tensor
 // memory is released); gives up after kWaitNs.
 DSV4_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {

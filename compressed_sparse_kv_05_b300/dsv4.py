@@ -68,6 +68,7 @@ _SIGS = {
     "dsv4_workspace_size": ([_DESC, _I32, _I32, _I32], ctypes.c_size_t),
     "dsv4_decode_plan": ([_DESC, _I32, _I32, _P], ctypes.c_int),
     "dsv4_read_status": ([_CACHE, _P], ctypes.c_int),
+    "dsv4_debug_force_timeout": ([_I32], ctypes.c_int),
     "dsv4_quantize_kv_rows": ([_P, _I64, _I32, _I32, _P, _P, _P, _P], ctypes.c_int),
     "dsv4_quantize_fp4_rows": ([_P, _I64, _I32, _P, _P, _P], ctypes.c_int),
     "dsv4_pool_rows": ([_P, _P, _P, _I64, _I32, _I32, _P, _P], ctypes.c_int),
@@ -216,6 +217,10 @@ def dsv4_decode_plan(desc, H, k):
     plan = (ctypes.c_int32 * 6)()
     _check("dsv4_decode_plan", lib.dsv4_decode_plan(ctypes.byref(desc), H, k, ctypes.cast(plan, ctypes.c_void_p)))
     return dict(zip(("tensor_core", "splits", "tile_rows", "tiles_per_split", "head_groups", "sms"), list(plan)))
+
+
+def dsv4_debug_force_timeout(on):
+    return _check("dsv4_debug_force_timeout", lib.dsv4_debug_force_timeout(1 if on else 0))
 
 
 def dsv4_read_status(cache, stream=None):

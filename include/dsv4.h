@@ -33,8 +33,9 @@
  *     dsv4_compress_append. They must be complete when the call is enqueued in
  *     stream order, i.e. written by work that is not a kernel of this library
  *     still running in the same stream (a projection GEMM or a copy enqueued
- *     before the call qualifies; the `out` of a call enqueued just before does
- *     not).
+ *     before the call qualifies, unless it triggers programmatic launch of
+ *     its dependents before those writes; the `out` of a call enqueued just
+ *     before does not).
  *   - Return value: DSV4_OK, or a negative DSV4_ERR_* code. A call that
  *     returns an error found on the host launches nothing and changes nothing.
  *     Conditions only the device can see (capacity, bad indices) set bits of
@@ -237,6 +238,15 @@ size_t dsv4_workspace_size(const dsv4_layer_desc* desc, int32_t H, int32_t Hi, i
  * rows per split (CUDA-core path), tiles per split, head groups of 64,
  * streaming multiprocessors planned for}. Host only; launches nothing. */
 int dsv4_decode_plan(const dsv4_layer_desc* desc, int32_t H, int32_t k, int32_t* plan);
+
+/* Test hook of the failure path (the pages describe no such call). While on
+ * != 0, every tensor-core attention kernel launched by the decode calls makes
+ * its MMA-issuing thread first wait on a barrier that nothing arrives on: the
+ * bounded wait runs out after 50 ms, every role of the kernel leaves its loop
+ * (copies and MMAs in flight drained), the call's output is not computed, and
+ * DSV4_STATUS_TIMEOUT is raised in the cache's status word. Affects the current
+ * device only; call with 0 to restore normal operation. For tests. */
+int dsv4_debug_force_timeout(int32_t on);
 
 /* Waits for `stream`, then returns the cache's status bits (>= 0) and clears
  * them; a negative DSV4_ERR_* on failure. */
