@@ -383,6 +383,7 @@ int index_topk_common(const dsv4_layer_desc* d, const dsv4_cache* c, int T, int3
   a.cnt = reinterpret_cast<uint32_t*>(wp + wl.cnt);
   a.above = reinterpret_cast<int32_t*>(wp + wl.above);
   a.cand = reinterpret_cast<uint64_t*>(wp + wl.cand);
+  a.status = c->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((e = launch_pdl(quant_query_fp4_kernel, dim3(a.B * N), dim3(32), 0, st, a))) return e;
   IndexTcArgs t{};
@@ -403,7 +404,7 @@ int index_topk_common(const dsv4_layer_desc* d, const dsv4_cache* c, int T, int3
   const int sel_max = (d->capacity + 511) / 512;
   if (sel > sel_max) sel = sel_max;
   if (sel < 1) sel = 1;
-  return launch_topk_select(a, sel, st);
+  return launch_topk_select(a, sel, sm_count(), st);
 }
 }  // namespace
 }  // namespace dsv4

@@ -14,6 +14,7 @@
 #include "kernels.h"
 #include "launch.cuh"
 #include "select.cuh"
+#include "tc_ptx.cuh"
 
 namespace dsv4 {
 
@@ -534,7 +535,675 @@ __global__ void __launch_bounds__(kSelThreads, 2) topk_select_kernel(IndexArgs a
   for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < static_cast<int>(nf) ? fin[i] : -1;
 }
 
-int launch_topk_select(const IndexArgs& a, int sel_ctas, cudaStream_t st) {
+// ------------------------------------------------------------------------------ cluster top-k
+//
+// The same selection (the k largest score keys, ties to the lower index, in
+// ascending index order) by one thread-block cluster of up to 16 CTAs per
+// sequence, without global atomics or a resolving CTA. CTA r of the cluster
+// copies scores [r S, (r + 1) S) of the sequence into shared memory (one bulk
+// copy) while it finds T1, the top-12-bit bin holding the k-th largest key,
+// in the scoring kernel's histogram; it then keeps the keys at or above bin
+// T1 (a few hundred in a sequence, typically) as a list of (key, position).
+// The boundary key is found digit by digit from histograms of the next 12 and
+// the low 8 bits that every CTA adds into every CTA's shared memory
+// (distributed shared memory), so that each finds the digit itself; a level
+// is skipped when its boundary bin is taken whole. Every CTA then counts its keys above the boundary and equal to
+// it; from the cluster's counts (ascending index ranges) it knows how many of
+// its boundary keys it takes (the lowest indices) and where its selection
+// starts in the output, and writes its selection in index order (each
+// selected key's rank by counting the CTA's smaller positions). A CTA whose
+// list would overflow works on all of its keys instead (positions in index
+// order from warp ballots and block-wide prefix sums).
+
+namespace {
+
+constexpr int kClThreads = 512;
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClMaxCtas = 16;
+constexpr int kClList = kBins / 2;   // list entries (uint2) in the first-level histogram's place
+constexpr int kClRecv = 4096;        // keys of the boundary bin the first CTA receives (uint2)
+
+DSV4_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+DSV4_DEV uint32_t cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// address of shared variable p in the shared memory of cluster CTA `rank`
+DSV4_DEV uint32_t peer_addr(const void* p, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(rank));
+  return out;
+}
+DSV4_DEV void peer_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+DSV4_DEV void peer_store(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+DSV4_DEV uint32_t peer_fetch_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+DSV4_DEV void peer_store2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+// cluster-wide barrier (every thread of every CTA), split into its two halves
+DSV4_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+DSV4_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+DSV4_DEV void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// Add 1 to bin `bin` of the histogram `hist` (shared memory) of every CTA of
+// the cluster, for every lane with `active`: per distinct bin of the warp,
+// lanes 0..cs-1 each add the bin's count into one CTA. All 32 lanes call it.
+DSV4_DEV void warp_hist_add_all(uint32_t* hist, uint32_t cs, uint32_t bin, bool active) {
+  unsigned todo = __ballot_sync(0xffffffffu, active);
+  const int lane = threadIdx.x & 31;
+  const unsigned mine = __match_any_sync(0xffffffffu, active ? bin : 0xFFFFFFFFu);
+  while (todo) {
+    const int src = __ffs(todo) - 1;
+    const unsigned grp = __shfl_sync(0xffffffffu, mine, src);   // the lanes sharing src's bin
+    const uint32_t b = __shfl_sync(0xffffffffu, bin, src);
+    if (lane < static_cast<int>(cs)) peer_add(peer_addr(hist + b, lane), static_cast<uint32_t>(__popc(grp & todo)));
+    todo &= ~grp;
+  }
+}
+
+// In-place exclusive prefix sum of n <= 4 * kClThreads words of shared memory.
+DSV4_DEV void block_excl_scan_words(uint32_t* v, int n, uint32_t* scratch) {
+  const int per = (n + kClThreads - 1) / kClThreads;
+  const int i0 = threadIdx.x * per;
+  uint32_t mine = 0;
+  for (int i = 0; i < per; ++i)
+    if (i0 + i < n) mine += v[i0 + i];
+  uint32_t tot;
+  uint32_t run = block_excl_scan_packed(mine, &tot, scratch);
+  for (int i = 0; i < per; ++i)
+    if (i0 + i < n) {
+      const uint32_t c = v[i0 + i];
+      v[i0 + i] = run;
+      run += c;
+    }
+  __syncthreads();
+}
+
+template <int J>
+constexpr size_t cluster_smem_bytes() {
+  return static_cast<size_t>(J) * kClThreads * 4 + 2 * kBins * 4 + 2 * static_cast<size_t>(J / 4) * kClWarps * 4 +
+         static_cast<size_t>(kClRecv) * 8;
+}
+
+}  // namespace
+
+template <int J>
+__global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(IndexArgs a) {
+  constexpr int G = J / 4;                                 // groups of 4 * 512 scores
+  extern __shared__ __align__(16) uint32_t dsm[];
+  float* sv = reinterpret_cast<float*>(dsm);               // [G][512][4]: the CTA's scores; list mode: scratch
+  uint32_t* h1 = dsm + J * kClThreads;                     // first-level histogram, then the candidate list
+  uint2* list = reinterpret_cast<uint2*>(h1);              // (key, position) of the keys >= bin T1
+  uint32_t* h2 = h1 + kBins;                               // the cluster's next-12-bit histogram
+  uint32_t* pos_a = h2 + kBins;                            // full mode: per (group, warp) counts, then prefixes
+  uint32_t* pos_b = pos_a + G * kClWarps;
+  uint2* recv = reinterpret_cast<uint2*>(pos_b + G * kClWarps);   // first CTA: the cluster's keys of bin T1
+  __shared__ uint32_t h8[256];                             // the cluster's low-8-bit histogram
+  __shared__ uint32_t scratch[kClWarps + 2];
+  __shared__ uint32_t all_cnt[2 * kClMaxCtas];             // every CTA's keys above / at the boundary
+  __shared__ uint32_t s_d, s_above, s_list, s_nsel, s_neq;
+  __shared__ uint32_t s_recv, s_ovf, s_slot;               // first CTA: keys received, overflow
+  __shared__ uint32_t above_cnt[kClMaxCtas], sel_cnt[kClMaxCtas];
+  __shared__ uint32_t res[5];                              // from the first CTA: overflow, Kx, tie, pthr, base
+  __shared__ uint64_t landed[G];                           // bulk copy of group g
+  __shared__ int abort_flag;
+  pdl_trigger();
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  for (int i = t; i < kBins; i += kClThreads) h2[i] = 0;
+  if (t < 256) h8[t] = 0;
+  if (t == 0) {
+    for (int g = 0; g < G; ++g) tc::mbar_init(&landed[g], 1);
+    abort_flag = 0;
+    s_list = 0;
+    s_recv = 0;
+    s_ovf = 0;
+    s_nsel = 0;
+    s_neq = 0;
+    tc::fence_mbar_init();
+  }
+  cluster_arrive();   // phase 0: every CTA's histograms are zeroed before anyone adds into them
+  pdl_wait();
+  const int b = blockIdx.y;
+  const uint32_t r = cluster_rank(), cs = cluster_ctas();
+  int64_t n_c = vseq_tokens(a.n_tokens, b, a.T) / a.ratio;
+  if (n_c > a.capacity) n_c = a.capacity;
+  const int k = a.k;
+  int32_t* out = a.topk + static_cast<int64_t>(b) * k;
+  if (n_c <= k) {   // uniform across the cluster
+    if (r == 0)
+      for (int i = t; i < k; i += kClThreads) out[i] = i < n_c ? i : -1;
+    cluster_wait();
+    return;
+  }
+  // CTA r: scores [lo, lo + nl), S a multiple of 4 so that a slice starts on
+  // a 16-byte boundary whenever a sequence's row does (the host keeps S <= 512 J)
+  const int64_t S = (((n_c + cs - 1) / cs) + 3) & ~int64_t(3);
+  const int64_t lo = static_cast<int64_t>(r) * S;
+  const int nl = static_cast<int>(n_c - lo < S ? (n_c - lo > 0 ? n_c - lo : 0) : S);
+  const float* sc = a.scores + static_cast<int64_t>(b) * a.capacity + lo;
+  // the slice into shared memory: one bulk copy per group of its whole 16-byte
+  // granules when aligned, the rest (or everything) by plain loads
+  const bool bulk = (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
+  const int nbulk = bulk ? (nl & ~3) : 0;
+  __syncthreads();
+  if (t == 0)
+    for (int g = 0; g < G && g * 2048 < nbulk; ++g) {
+      const int n = nbulk - g * 2048 < 2048 ? nbulk - g * 2048 : 2048;
+      tc::mbar_arrive_expect_tx(&landed[g], static_cast<uint32_t>(n) * 4u);
+      tc::bulk_load(sv + g * 2048, sc + g * 2048, static_cast<uint32_t>(n) * 4u, &landed[g]);
+    }
+  for (int e = nbulk + t; e < nl; e += kClThreads) sv[e] = __ldcg(sc + e);
+  {
+    const uint32_t* gh = a.hist1 + static_cast<int64_t>(b) * kBins;
+    constexpr int per = kBins / kClThreads;
+    uint32_t v[per];
+#pragma unroll
+    for (int u = 0; u < per; ++u) v[u] = __ldcg(gh + t + u * kClThreads);
+#pragma unroll
+    for (int u = 0; u < per; ++u) h1[t + u * kClThreads] = v[u];
+  }
+  __syncthreads();
+  uint32_t n_gt1;
+  const uint32_t T1 = static_cast<uint32_t>(block_suffix_select<kClThreads>(h1, static_cast<uint32_t>(k), &n_gt1, scratch));
+  const uint32_t need1 = static_cast<uint32_t>(k) - n_gt1;
+  const uint32_t cnt1 = h1[T1];
+  __syncthreads();   // h1 is read; it becomes the candidate list
+  // Keys at or above bin T1 into the list (one shared-memory slot each, in no
+  // particular order). A float test that admits every such score (and NaN)
+  // comes first; the key decides.
+  const uint32_t kmin = T1 << 20;
+  float fthr;
+  {
+    const uint32_t u = (kmin & 0x80000000u) ? (kmin & 0x7FFFFFFFu) : ~kmin;
+    fthr = __uint_as_float(u);
+    if (fthr != fthr) fthr = (kmin & 0x80000000u) ? INFINITY : -INFINITY;
+  }
+  for (int g = 0; g < G; ++g) {
+    if (g * 2048 < nbulk && !tc::mbar_wait(&landed[g], 0, &abort_flag)) atomicOr(a.status, DSV4_STATUS_TIMEOUT);
+    const int p = g * 2048 + 4 * t;
+    if (p >= nl) continue;
+    float4 f;
+    if (p + 3 < nl) {
+      f = *reinterpret_cast<const float4*>(sv + p);
+    } else {
+      f.x = sv[p];
+      f.y = p + 1 < nl ? sv[p + 1] : -INFINITY;
+      f.z = p + 2 < nl ? sv[p + 2] : -INFINITY;
+      f.w = -INFINITY;
+    }
+    if (!(f.x < fthr) || !(f.y < fthr) || !(f.z < fthr) || !(f.w < fthr)) {
+      const float fs[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t key = score_key(fs[i]);
+        if (p + i < nl && key >= kmin) {
+          const uint32_t slot = atomicAdd(&s_list, 1u);
+          if (slot < static_cast<uint32_t>(kClList)) list[slot] = make_uint2(key, static_cast<uint32_t>(p + i));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t L = s_list;
+  const bool full = L > static_cast<uint32_t>(kClList);   // uniform within the CTA
+  cluster_wait();
+
+  // ---- Usual case: the first CTA resolves the boundary among the keys of bin
+  // T1 (cnt1 of them), which every CTA sends it as (key, r << 16 | position),
+  // with its count of keys above bin T1; it returns to each CTA the boundary
+  // key, whether it ties, the CTA's last boundary position taken and where its
+  // selection starts.
+  {
+    const uint32_t leader = 0;
+    uint32_t n_in = 0, n_up = 0;   // this thread's list entries in bin T1 / above it
+    if (!full)
+      for (uint32_t i = t; i < L; i += kClThreads) {
+        const uint32_t bin = list[i].x >> 20;
+        n_in += bin == T1 ? 1u : 0u;
+        n_up += bin > T1 ? 1u : 0u;
+      }
+    uint32_t tot;
+    const uint32_t off = block_excl_scan_packed(n_in | (n_up << 16), &tot, scratch);
+    if (t == 0) {
+      if (full) {
+        peer_store(peer_addr(&s_ovf, leader), 1u);
+      } else {
+        s_slot = (tot & 0xFFFFu) ? peer_fetch_add(peer_addr(&s_recv, leader), tot & 0xFFFFu) : 0u;
+        peer_store(peer_addr(&above_cnt[r], leader), tot >> 16);
+      }
+    }
+    __syncthreads();
+    if (!full && n_in) {
+      uint32_t slot = s_slot + (off & 0xFFFFu);
+      for (uint32_t i = t; i < L; i += kClThreads) {
+        const uint2 en = list[i];
+        if ((en.x >> 20) == T1) {
+          if (slot < static_cast<uint32_t>(kClRecv)) peer_store2(peer_addr(&recv[slot], leader), make_uint2(en.x, (r << 16) | en.y));
+          ++slot;
+        }
+      }
+    }
+  }
+  cluster_sync();   // phase 1: the first CTA holds the cluster's keys of bin T1
+  if (r == 0) {
+    const uint32_t R = s_recv;
+    const bool ovf = s_ovf != 0 || R > static_cast<uint32_t>(kClRecv) || R != cnt1;
+    uint32_t Kr = kmin, tie_r = 0, qthr = 0;
+    if (!ovf) {
+      if (t < kClMaxCtas) sel_cnt[t] = 0;
+      if (need1 < cnt1) {
+        for (uint32_t i = t; i < R; i += kClThreads) atomicAdd(&h2[(recv[i].x >> 8) & 0xFFFu], 1u);
+        __syncthreads();
+        uint32_t n_gt2;
+        const uint32_t T2 = static_cast<uint32_t>(block_suffix_select<kClThreads>(h2, need1, &n_gt2, scratch));
+        const uint32_t need2 = need1 - n_gt2, cnt2 = h2[T2];
+        const uint32_t p24 = (T1 << 12) | T2;
+        Kr = p24 << 8;
+        if (need2 < cnt2) {
+          for (uint32_t i = t; i < R; i += kClThreads)
+            if ((recv[i].x >> 8) == p24) atomicAdd(&h8[recv[i].x & 0xFFu], 1u);
+          __syncthreads();
+          if (w == 0) warp_digit_select(h8, need2, &s_d, &s_above);
+          __syncthreads();
+          const uint32_t d8 = s_d, need3 = need2 - s_above, cnt3 = h8[d8];
+          Kr = (p24 << 8) | d8;
+          if (need3 < cnt3) {
+            // the need3 lowest cluster positions q among the keys == Kr: a
+            // radix select over q's 20 bits (digits 8, 8, 4), smallest first
+            tie_r = 1;
+            uint32_t rneed = need3, prefix = 0;
+            const int shifts[3] = {12, 4, 0};
+            const int widths[3] = {8, 8, 4};
+            for (int ps = 0; ps < 3; ++ps) {
+              __syncthreads();
+              if (t < 256) h8[t] = 0;
+              __syncthreads();
+              const int sh = shifts[ps];
+              for (uint32_t i = t; i < R; i += kClThreads) {
+                const uint2 en = recv[i];
+                if (en.x == Kr && (ps == 0 || (en.y >> (sh + widths[ps])) == prefix))
+                  atomicAdd(&h8[255u - ((en.y >> sh) & ((1u << widths[ps]) - 1u))], 1u);
+              }
+              __syncthreads();
+              if (w == 0) warp_digit_select(h8, rneed, &s_d, &s_above);
+              __syncthreads();
+              prefix = (prefix << widths[ps]) | (255u - s_d);
+              rneed -= s_above;
+            }
+            qthr = prefix;   // exactly need3 keys == Kr have q <= qthr
+          }
+        }
+      }
+      __syncthreads();
+      for (uint32_t i = t; i < R; i += kClThreads) {
+        const uint2 en = recv[i];
+        const bool sel = en.x > Kr || (en.x == Kr && (!tie_r || en.y <= qthr));
+        if (sel) atomicAdd(&sel_cnt[en.y >> 16], 1u);
+      }
+      __syncthreads();
+    }
+    if (t < static_cast<int>(cs)) {
+      uint32_t base_t = 0;
+      for (int q = 0; q < t; ++q) base_t += above_cnt[q] + sel_cnt[q];
+      int32_t pthr = -1;
+      if (tie_r) {
+        const int qr = static_cast<int>(qthr >> 16);
+        pthr = t < qr ? 0xFFFF : t == qr ? static_cast<int32_t>(qthr & 0xFFFFu) : -1;
+      }
+      peer_store(peer_addr(&res[0], t), ovf ? 1u : 0u);
+      peer_store(peer_addr(&res[1], t), Kr);
+      peer_store(peer_addr(&res[2], t), tie_r);
+      peer_store(peer_addr(&res[3], t), static_cast<uint32_t>(pthr));
+      peer_store(peer_addr(&res[4], t), base_t);
+    }
+  }
+  cluster_sync();   // phase 2: every CTA holds the first CTA's answer
+  if (res[0] == 0) {
+    // this CTA's selection (its list: no CTA is in full mode here), each
+    // entry's rank among them by counting smaller positions
+    const uint32_t Kr = res[1], base_r = res[4];
+    const bool tie_r = res[2] != 0;
+    const int32_t pthr = static_cast<int32_t>(res[3]);
+    uint32_t* selp = reinterpret_cast<uint32_t*>(sv);   // free: every key of interest is in the list
+    for (uint32_t i0 = 0; i0 < L; i0 += kClThreads) {
+      const uint32_t i = i0 + t;
+      bool sel = false;
+      uint32_t p = 0;
+      if (i < L) {
+        const uint2 en = list[i];
+        p = en.y;
+        sel = en.x > Kr || (en.x == Kr && (!tie_r || static_cast<int32_t>(p) <= pthr));
+      }
+      warp_append_i32(sel, static_cast<int32_t>(p), &s_nsel, reinterpret_cast<int32_t*>(selp), static_cast<uint32_t>(k));
+    }
+    __syncthreads();
+    const uint32_t ns = s_nsel < static_cast<uint32_t>(k) ? s_nsel : static_cast<uint32_t>(k);
+    for (uint32_t i = t; i < ns; i += kClThreads) {
+      const uint32_t p = selp[i];
+      uint32_t rank = 0;
+      for (uint32_t q = 0; q < ns; ++q) rank += selp[q] < p ? 1u : 0u;
+      if (base_r + rank < static_cast<uint32_t>(k)) out[base_r + rank] = static_cast<int32_t>(lo + p);
+    }
+    return;
+  }
+  // ---- Otherwise (a CTA with too many keys at or above bin T1, or too many
+  // keys in bin T1 for the first CTA, which then left its histograms at zero):
+  // digit by digit across the cluster.
+
+  // The boundary: with tie == false every key >= Kx is taken; with tie ==
+  // true every key > Kx and the `need` lowest-index keys == Kx. Every key not
+  // in a CTA's list is below bin T1, so below Kx.
+  uint32_t Kx = kmin, need = 0;
+  bool tie = false;
+  // calls f(key, valid) for every key of the CTA at or above bin T1 (the list,
+  // or all keys), with whole warps
+  auto for_each_candidate = [&](auto&& f) {
+    if (!full) {
+      for (uint32_t i0 = 0; i0 < L; i0 += kClThreads) {
+        const uint32_t i = i0 + t;
+        const uint2 e = i < L ? list[i] : make_uint2(0u, 0u);
+        f(e.x, i < L);
+      }
+    } else {
+      for (int g = 0; g < G; ++g) {
+        const int p = g * 2048 + 4 * t;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f(p + i < nl ? score_key(sv[p + i]) : 0u, p + i < nl);
+      }
+    }
+  };
+  // adds 1 at bin(key) of histogram `hist` in every CTA for every key of this
+  // CTA at or above bin T1 with in(key): list mode, one remote add per
+  // (entry, CTA) pair spread over the threads; else warp-aggregated
+  auto add_all = [&](uint32_t* hist, auto&& in, auto&& bin) {
+    if (!full) {
+      for (uint32_t i = t; i < L * cs; i += kClThreads) {
+        const uint32_t key = list[i / cs].x;
+        if (in(key)) peer_add(peer_addr(hist + bin(key), i % cs), 1u);
+      }
+    } else {
+      for_each_candidate([&](uint32_t key, bool v) { warp_hist_add_all(hist, cs, bin(key), v && in(key)); });
+    }
+  };
+  if (need1 < cnt1) {
+    add_all(h2, [&](uint32_t key) { return (key >> 20) == T1; }, [](uint32_t key) { return (key >> 8) & 0xFFFu; });
+    cluster_sync();   // phase 1: every CTA holds the cluster's next-12-bit histogram
+    uint32_t n_gt2;
+    const uint32_t T2 = static_cast<uint32_t>(block_suffix_select<kClThreads>(h2, need1, &n_gt2, scratch));
+    const uint32_t need2 = need1 - n_gt2, cnt2 = h2[T2];
+    const uint32_t p24 = (T1 << 12) | T2;
+    Kx = p24 << 8;
+    if (need2 < cnt2) {
+      add_all(h8, [&](uint32_t key) { return (key >> 8) == p24; }, [](uint32_t key) { return key & 0xFFu; });
+      cluster_sync();   // phase 2: every CTA holds the cluster's low-8-bit histogram
+      if (w == 0) warp_digit_select(h8, need2, &s_d, &s_above);
+      __syncthreads();
+      const uint32_t d8 = s_d, need3 = need2 - s_above, cnt3 = h8[d8];
+      Kx = (p24 << 8) | d8;
+      if (need3 < cnt3) {
+        tie = true;
+        need = need3;
+      }
+    }
+  }
+
+  // this CTA's keys above the boundary (>= Kx without a tie) and at it
+  uint32_t g = 0, e = 0;
+  for_each_candidate([&](uint32_t key, bool v) {
+    g += (v && (tie ? key > Kx : key >= Kx)) ? 1u : 0u;
+    e += (v && tie && key == Kx) ? 1u : 0u;
+  });
+  {
+    uint32_t ge;   // both counts in one sum (each below 2^16: a CTA holds at most 512 J keys)
+    block_excl_scan_packed(g | (e << 16), &ge, scratch);
+    g = ge & 0xFFFFu;
+    e = ge >> 16;
+  }
+  if (t < static_cast<int>(cs)) {
+    peer_store(peer_addr(&all_cnt[2 * r], t), g);
+    peer_store(peer_addr(&all_cnt[2 * r + 1], t), e);
+  }
+  cluster_sync();   // phase 3: every CTA holds every CTA's counts; no shared memory is touched remotely after this
+  // the boundary keys this CTA takes and where its selection starts
+  uint32_t base = 0, eq_before = 0, take = 0;
+  for (uint32_t q = 0; q < cs; ++q) {
+    const uint32_t cq = all_cnt[2 * q + 1];
+    const uint32_t tq = tie ? (need > eq_before ? (need - eq_before < cq ? need - eq_before : cq) : 0u) : 0u;
+    if (q < r) base += all_cnt[2 * q] + tq;
+    if (q == r) take = tq;
+    eq_before += cq;
+  }
+  const bool split = tie && take > 0 && take < e;   // uniform within the CTA
+  const unsigned below = (1u << lane) - 1u;
+
+  if (!full) {
+    // positions of the boundary keys (split only), then of the selected keys,
+    // gathered in list order; each one's rank is the count of smaller positions
+    uint32_t* eqp = h2;                               // free again: no CTA adds into it after phase 1
+    uint32_t* selp = reinterpret_cast<uint32_t*>(sv);  // free: every key of interest is in the list
+    if (split) {
+      for (uint32_t i0 = 0; i0 < L; i0 += kClThreads) {
+        const uint32_t i = i0 + t;
+        const bool at_b = i < L && list[i].x == Kx;
+        warp_append_i32(at_b, static_cast<int32_t>(i < L ? list[i].y : 0u), &s_neq, reinterpret_cast<int32_t*>(eqp),
+                        static_cast<uint32_t>(kBins));
+      }
+      __syncthreads();
+    }
+    for (uint32_t i0 = 0; i0 < L; i0 += kClThreads) {
+      const uint32_t i = i0 + t;
+      bool sel = false;
+      uint32_t p = 0;
+      if (i < L) {
+        const uint2 en = list[i];
+        p = en.y;
+        sel = tie ? en.x > Kx : en.x >= Kx;
+        if (tie && en.x == Kx) {
+          if (!split) {
+            sel = take > 0;
+          } else {
+            uint32_t rank = 0;
+            for (uint32_t q = 0; q < e; ++q) rank += eqp[q] < p ? 1u : 0u;
+            sel = rank < take;
+          }
+        }
+      }
+      warp_append_i32(sel, static_cast<int32_t>(p), &s_nsel, reinterpret_cast<int32_t*>(selp), static_cast<uint32_t>(k));
+    }
+    __syncthreads();
+    const uint32_t ns = s_nsel < static_cast<uint32_t>(k) ? s_nsel : static_cast<uint32_t>(k);
+    for (uint32_t i = t; i < ns; i += kClThreads) {
+      const uint32_t p = selp[i];
+      uint32_t rank = 0;
+      for (uint32_t q = 0; q < ns; ++q) rank += selp[q] < p ? 1u : 0u;
+      if (base + rank < static_cast<uint32_t>(k)) out[base + rank] = static_cast<int32_t>(lo + p);
+    }
+  } else {
+    // every key of the CTA, in index order: group g, warp w covers positions
+    // g 2048 + 128 w ..., lane by lane, 4 per lane; a (group, warp) count from
+    // four ballots, block-wide prefix sums over (group, warp)
+    auto key_at = [&](int p) { return p < nl ? score_key(sv[p]) : 0u; };
+    if (split) {
+      for (int gg = 0; gg < G; ++gg) {
+        const int p = gg * 2048 + 4 * t;
+        uint32_t c = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c += __popc(__ballot_sync(0xffffffffu, p + i < nl && key_at(p + i) == Kx));
+        if (lane == 0) pos_a[gg * kClWarps + w] = c;
+      }
+      __syncthreads();
+      block_excl_scan_words(pos_a, G * kClWarps, scratch);
+    }
+    // selection flags of this thread's 4 keys of group gg, and the count of
+    // selected keys before them within the (group, warp)
+    auto select4 = [&](int gg, bool* sel, uint32_t* before) {
+      const int p = gg * 2048 + 4 * t;
+      bool at[4];
+      uint32_t eq_rank = split ? pos_a[gg * kClWarps + w] : 0u;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t key = key_at(p + i);
+        const bool v = p + i < nl;
+        sel[i] = v && (tie ? key > Kx : key >= Kx);
+        at[i] = v && tie && key == Kx;
+      }
+      if (split) {
+        uint32_t lower = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lower += __popc(__ballot_sync(0xffffffffu, at[i]) & below);
+        eq_rank += lower;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sel[i] |= at[i] && eq_rank < take;
+          eq_rank += at[i] ? 1u : 0u;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sel[i] |= at[i] && take > 0;
+      }
+      uint32_t lower = 0, cnt = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const unsigned m = __ballot_sync(0xffffffffu, sel[i]);
+        lower += __popc(m & below);
+        cnt += __popc(m);
+      }
+      *before = lower;
+      return cnt;
+    };
+    for (int gg = 0; gg < G; ++gg) {
+      bool sel[4];
+      uint32_t before;
+      const uint32_t c = select4(gg, sel, &before);
+      if (lane == 0) pos_b[gg * kClWarps + w] = c;
+    }
+    __syncthreads();
+    block_excl_scan_words(pos_b, G * kClWarps, scratch);
+    for (int gg = 0; gg < G; ++gg) {
+      bool sel[4];
+      uint32_t before;
+      select4(gg, sel, &before);
+      uint32_t pos = base + pos_b[gg * kClWarps + w] + before;
+      const int p = gg * 2048 + 4 * t;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (sel[i]) {
+          if (pos < static_cast<uint32_t>(k)) out[pos] = static_cast<int32_t>(lo + p + i);
+          ++pos;
+        }
+    }
+  }
+}
+
+namespace {
+constexpr int kClJ[3] = {16, 36, 72};   // scores per thread of the instantiated cluster kernels
+
+template <int J>
+void cluster_setup() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(topk_cluster_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(cluster_smem_bytes<J>()));
+    cudaFuncSetAttribute(topk_cluster_kernel<J>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+}
+
+template <int J>
+cudaLaunchConfig_t cluster_config(int cs, int B, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, B);
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = cluster_smem_bytes<J>();
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cs;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+// whether clusters of cs CTAs of topk_cluster_kernel<J> can be resident on this device
+template <int J>
+bool cluster_fits(int cs) {
+  cluster_setup<J>();
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cluster_config<J>(cs, 1, nullptr, attr);
+  cfg.attrs = attr + 1;   // the cluster shape alone
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<J>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return n > 0;
+}
+
+bool cluster_fits_j(int J, int cs) {
+  static int memo[3][5] = {};   // 0 unknown, 1 fits, 2 does not (per J, cs = 1 << i)
+  int ji = J == kClJ[0] ? 0 : J == kClJ[1] ? 1 : 2, ci = 0;
+  while ((1 << ci) < cs) ++ci;
+  int& m = memo[ji][ci];
+  if (!m) {
+    const bool ok = ji == 0 ? cluster_fits<kClJ[0]>(cs) : ji == 1 ? cluster_fits<kClJ[1]>(cs) : cluster_fits<kClJ[2]>(cs);
+    m = ok ? 1 : 2;
+  }
+  return m == 1;
+}
+
+template <int J>
+int launch_topk_cluster(const IndexArgs& a, int cs, cudaStream_t st) {
+  cluster_setup<J>();
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cluster_config<J>(cs, a.B, st, attr);
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<J>, a) == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+}  // namespace
+
+int topk_plan(int B, int capacity, int sms, int* cluster_ctas, int* per_thread) {
+  for (int cs = kClMaxCtas; cs >= 1; cs >>= 1) {
+    if (cs > 1 && B * cs > sms) continue;
+    const int64_t per_cta = (((static_cast<int64_t>(capacity) + cs - 1) / cs) + 3) & ~int64_t(3);
+    const int64_t need = (per_cta + kClThreads - 1) / kClThreads;
+    for (int J : kClJ)
+      if (need <= J && cluster_fits_j(J, cs)) {
+        *cluster_ctas = cs;
+        *per_thread = J;
+        return 1;
+      }
+  }
+  *cluster_ctas = 0;
+  *per_thread = 0;
+  return 0;
+}
+
+int launch_topk_select(const IndexArgs& a, int sel_ctas, int sms, cudaStream_t st) {
+  int cs, J;
+  if (topk_plan(a.B, a.capacity, sms, &cs, &J)) {
+    if (J == kClJ[0]) return launch_topk_cluster<kClJ[0]>(a, cs, st);
+    if (J == kClJ[1]) return launch_topk_cluster<kClJ[1]>(a, cs, st);
+    return launch_topk_cluster<kClJ[2]>(a, cs, st);
+  }
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkDynSmem);

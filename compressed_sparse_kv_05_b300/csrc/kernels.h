@@ -90,10 +90,15 @@ struct IndexArgs {
   uint32_t* cnt;           // [B][kCntWords] (see kCntWords)
   int32_t* above;          // [B][k] blocks above the threshold bin
   uint64_t* cand;          // [B][capacity] (key << 32 | index) of the blocks in the threshold bin
+  int32_t* status;         // the cache's status word
 };
 __global__ void quant_query_fp4_kernel(IndexArgs a);
 __global__ void topk_select_kernel(IndexArgs a);
-int launch_topk_select(const IndexArgs& a, int sel_ctas, cudaStream_t st);
+// Top-k launch: the cluster kernel (topk_cluster_kernel) when topk_plan finds
+// a cluster size and per-thread score count for the capacity, else the
+// global-atomic kernel with sel_ctas CTAs per sequence.
+int topk_plan(int B, int capacity, int sms, int* cluster_ctas, int* per_thread);
+int launch_topk_select(const IndexArgs& a, int sel_ctas, int sms, cudaStream_t st);
 
 struct IndexTcArgs {
   int B, N, Di, capacity, ratio, ctas_per_seq, k;

@@ -247,9 +247,11 @@ def test_index_topk_full_size_planted(layer):
         assert np.abs(g_lse[b] - o_lse).max() <= 1e-3
 
 
-def test_topk_ties_go_to_lower_index():
-    """All keys identical: every score ties, so the selection is the lowest k indices."""
-    layer = W.scaled(W.CSA_B32_128K, batch=1, n_tokens=4 * 5000, topk=512)
+@pytest.mark.parametrize("n_c", [5000, 70000])
+def test_topk_ties_go_to_lower_index(n_c):
+    """All keys identical: every score ties, so the selection is the lowest k
+    indices (at 70000 blocks more tied keys than a selecting CTA lists)."""
+    layer = W.scaled(W.CSA_B32_128K, batch=1, n_tokens=4 * n_c, topk=512)
     desc = dsv4.layer_desc(layer, layer.capacity())
     cache = dsv4.Cache(desc)
     cache.idx_codes.fill_(0x23)

@@ -314,6 +314,24 @@ def test_ratio1_selection_on_raw_tokens():
     _check_chain(layer, planes, desc, cache, dec, g_topk)
 
 
+def test_topk_beyond_one_cluster():
+    """More blocks than one cluster of CTAs holds (ratio 1 over 600000 raw
+    tokens, above 16 x 72 x 512): the selection takes the global-atomic kernel;
+    with identical planted keys competing for the k slots, the lowest indices win."""
+    n = 600000
+    layer = W.Layer("csa", 1, n, 16, 64, 64, True, 1, 128, idx_heads=4, idx_dim=64, topk=512, planted_frac=0.002)
+    planes = oracle_direct_planes(layer, "idxbig", 0, range(layer.batch))
+    desc, cache = gpu_cache_from_planes(layer, planes)
+    dec = synth.decode_inputs("idxbig", 0, layer)
+    g_topk, g_scores = _index(desc, cache, layer, dec, layer.topk)
+    o_scores = O.index_scores(planes[0]["idx_codes"], planes[0]["idx_scales"], dec["q_idx"][0], dec["w"][0])
+    assert np.abs(g_scores[0, :n] - o_scores).max() / np.abs(o_scores).max() <= 1e-5
+    o_sel = O.topk_blocks(o_scores, layer.topk)
+    check_topk(g_topk[0], o_scores, o_sel, layer.topk)
+    planted = sorted(planes[0]["planted"].tolist())
+    assert len(planted) >= layer.topk and set(g_topk[0].tolist()) == set(planted[:layer.topk])
+
+
 # ----------------------------------------------------------------------------- cache state round trip
 
 
