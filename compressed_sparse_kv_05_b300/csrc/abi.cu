@@ -144,7 +144,7 @@ AttnPlan attn_plan(const dsv4_layer_desc* d, int H, int n_sel, int T = 1) {
 int index_heads_padded(int Hi) { return Hi <= 64 ? 64 : 128; }
 
 struct IndexWs {
-  size_t q_codes, q_scales, wpad, scores, hist1, hist2, cnt, above, cand, total;
+  size_t q_codes, q_scales, scores, hist1, hist2, cnt, above, cand, total;
 };
 
 // T: queries per sequence (batch * T virtual sequences, each with its own
@@ -156,8 +156,7 @@ IndexWs index_ws(const dsv4_layer_desc* d, int Hi, int k, int T = 1) {
   IndexWs w{};
   w.q_codes = 0;
   w.q_scales = up(w.q_codes + B * N * (d->idx_dim / 2));
-  w.wpad = up(w.q_scales + B * N * (d->idx_dim / 16));
-  w.scores = up(w.wpad + B * N * sizeof(float));
+  w.scores = up(w.q_scales + B * N * (d->idx_dim / 16));
   w.hist1 = up(w.scores + B * cap * sizeof(float));
   w.hist2 = up(w.hist1 + B * 4096 * sizeof(uint32_t));
   w.cnt = up(w.hist2 + B * 4096 * sizeof(uint32_t));
@@ -375,7 +374,6 @@ int index_topk_common(const dsv4_layer_desc* d, const dsv4_cache* c, int T, int3
   a.q_idx = q_idx; a.w = w; a.n_tokens = c->n_tokens;
   a.q_codes = reinterpret_cast<uint8_t*>(wp + wl.q_codes);
   a.q_scales = reinterpret_cast<uint8_t*>(wp + wl.q_scales);
-  a.wpad = reinterpret_cast<float*>(wp + wl.wpad);
   a.scores = scores ? scores : reinterpret_cast<float*>(wp + wl.scores);
   a.topk = topk;
   a.hist1 = reinterpret_cast<uint32_t*>(wp + wl.hist1);
@@ -397,7 +395,7 @@ int index_topk_common(const dsv4_layer_desc* d, const dsv4_cache* c, int T, int3
   while (cols < need) cols <<= 1;
   t.tmem_cols = cols;
   t.n_tokens = c->n_tokens; t.idx_codes = c->idx_codes; t.idx_scales = c->idx_scales; t.q_scales = a.q_scales;
-  t.wpad = a.wpad;
+  t.w = w; t.Hi = Hi;
   t.scores = a.scores; t.hist1 = a.hist1; t.cnt = a.cnt; t.k = k; t.status = c->status;
   if ((e = launch_index_scores_tc(t, c->idx_codes, a.q_codes, st))) return e;
   int sel = (2 * sm_count()) / a.B;

@@ -20,7 +20,7 @@ namespace dsv4 {
 
 // grid (B * N), block Di/16: quantise one query head to FP4 (the same rule as the
 // keys) into the operand layout of the scoring MMA; padding heads (h >= Hi) get
-// zero codes, zero scales and zero weight.
+// zero codes and zero scales.
 __global__ void quant_query_fp4_kernel(IndexArgs a) {
   pdl_trigger();
   const int row = blockIdx.x;               // b * N + h
@@ -36,7 +36,6 @@ __global__ void quant_query_fp4_kernel(IndexArgs a) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = bf16_to_f32(src[i]);
   }
-  const float wv = blk == 0 && h < a.Hi ? a.w[b * a.Hi + h] : 0.f;
   pdl_wait();
   if (blk >= nblk) return;
   uint8_t* codes = a.q_codes + static_cast<int64_t>(row) * (a.Di / 2) + blk * 8;
@@ -47,7 +46,6 @@ __global__ void quant_query_fp4_kernel(IndexArgs a) {
   } else {
     *scale = static_cast<uint8_t>(quant_fp4_block16(v, codes));
   }
-  if (blk == 0) a.wpad[row] = wv;
   // zero this sequence's top-k histograms and counters (the N blocks of a sequence share the work)
   const int words = 2 * kBins + kCntWords;
   const int per = (words + a.N - 1) / a.N;

@@ -105,6 +105,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       else tc::prefetch_l2_range(a.idx_scales + row * (ROWB / 8), n * (ROWB / 8));
     }
   }
+  // head weights: the caller's input, which no kernel of this library writes
+  // (heads beyond Hi weigh zero)
+  for (int i = threadIdx.x; i < a.N; i += blockDim.x) wsm[i] = i < a.Hi ? a.w[static_cast<int64_t>(blockIdx.y) * a.Hi + i] : 0.f;
   pdl_wait();
 
   const int b = blockIdx.y;              // virtual sequence (query)
@@ -142,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     t->abort = 0;
     tc::fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < N; i += blockDim.x) wsm[i] = a.wpad[static_cast<int64_t>(b) * N + i];
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();

@@ -82,7 +82,6 @@ struct IndexArgs {
   const int64_t* n_tokens;
   uint8_t* q_codes;        // [B][N][Di/2] FP4 query, heads padded to N with zeros (workspace)
   uint8_t* q_scales;       // [B][N][Di/16]
-  float* wpad;             // [B][N] head weights, zero for padding heads
   float* scores;           // [B][capacity]
   int32_t* topk;           // [B][k]
   uint32_t* hist1;         // [B][4096] histogram of score-key bits 31..20 (filled while scoring)
@@ -108,7 +107,8 @@ struct IndexTcArgs {
   const uint8_t* idx_codes;    // [B][capacity][Di/2] (read through the tensor map; its address for L2 prefetches)
   const uint8_t* idx_scales;   // [B][capacity][Di/16]
   const uint8_t* q_scales;     // [B][N][Di/16]
-  const float* wpad;           // [B][N]
+  const float* w;              // [B][Hi] head weights (the caller's input)
+  int Hi;
   float* scores;               // [B][capacity]
   uint32_t* hist1;             // [B][4096]
   uint32_t* cnt;               // [B][kCntWords]

@@ -18,16 +18,18 @@ DSV4_DEV void sync_threads_of() {
   else asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT) : "memory");
 }
 
-// Suffix search over a 4096-bin histogram h (shared memory) with threads
-// [0, NT): the largest bin T with sum_{j >= T} h[j] >= need (need >= 1 and at
-// most the histogram's total). Returns T in every thread and writes
-// sum_{j > T} h[j] to *above. `scratch` is NT / 32 + 2 words of shared memory.
-// BAR = 0: NT is the whole block; otherwise the named barrier BAR is used.
+// Suffix search over a 4096-bin histogram h (shared memory) by NT threads,
+// thread number tid in [0, NT) (threadIdx.x by default): the largest bin T
+// with sum_{j >= T} h[j] >= need (need >= 1 and at most the histogram's
+// total). Returns T in every thread and writes sum_{j > T} h[j] to *above.
+// `scratch` is NT / 32 + 2 words of shared memory. BAR = 0: NT is the whole
+// block; otherwise the named barrier BAR of those NT threads is used.
 template <int NT, int BAR = 0>
-DSV4_DEV int block_suffix_select(const uint32_t* h, uint32_t need, uint32_t* above, uint32_t* scratch) {
+DSV4_DEV int block_suffix_select(const uint32_t* h, uint32_t need, uint32_t* above, uint32_t* scratch,
+                                 int tid = -1) {
   constexpr int per = kBins / NT;
   constexpr int nw = NT / 32;
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int t = tid < 0 ? static_cast<int>(threadIdx.x) : tid, lane = t & 31, w = t >> 5;
   if (t == 0) {
     scratch[nw] = 0;
     scratch[nw + 1] = 0;
