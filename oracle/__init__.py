@@ -16,6 +16,6 @@ from .formats import (E2M1_MAX, E4M3_MAX, bf16_decode, bf16_encode, e2m1_decode,
                       e2m1_encode, e4m3_decode, e4m3_encode)
 from .method import (attend, build_cache, csa_attend, dequant_fp4_rows,
                      dequant_kv_rows, hca_attend, index_scores, index_scores_causal,
-                     lse_merge, multi_attend, pool_blocks, quantize_fp4_rows,
-                     quantize_kv_rows, query_positions, topk_blocks, topk_boundary_gap,
+                     lse_merge, multi_attend, pool_blocks, project_streams, quantize_fp4_rows,
+                     quantize_kv_rows, query_positions, rope_rotate, topk_blocks, topk_boundary_gap,
                      window_tokens)

@@ -18,6 +18,10 @@ What the pages fix, and where (titles and sections of the source pages):
         compressor whose outputs are filtered to the top-k by an index.
   [HCA] same page, section 2.2 "HCA：重度压缩注意力": 128:1 compression,
         alternating with CSA across layers.
+  [ROPE] devpress.csdn.net, "DeepSeek-V4：百万Token上下文，这次智能体真的能用了",
+        section "二、DeepSeek-V4的核心架构创新", part "位置编码的长度泛化优化":
+        positions enter through RoPE, extended to long contexts by training
+        (no inference-time change to the rotation is described).
 
 Readings taken where the pages leave a step open (the plainest one the rest
 supports):
@@ -36,7 +40,14 @@ supports):
   * attention is one softmax over (selected compressed entries) U (window
     tokens); the window holds the last min(W, n) raw bf16 tokens and is not
     masked against the compressed blocks it overlaps; the query is used
-    exactly as given (bf16); V = K for a shared entry.
+    exactly as given (bf16); V = K for a shared entry;
+  * the streams the compressor pools (token keys x, gate logits z, indexer keys
+    u and their gates zu) are linear projections of the hidden state ([HYB]:
+    the pooling is learned); RoPE is the standard rotation: pairs (2i, 2i + 1)
+    of the rotated dims turn by pos * base^(-2i/d), applied to the trailing
+    d_rope dims of x and the trailing min(d_rope, Di) dims of u at each
+    token's absolute position, before pooling and before the window ring; each
+    projected stream is rounded once to bf16 (the compressor's input format).
 """
 import numpy as np
 
@@ -347,3 +358,45 @@ def multi_attend(q_bits, sm_scale, sel, n_tokens, ratio, window, k_nope, k_scale
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)
+
+
+def rope_rotate(x, pos, base):
+    """RoPE [ROPE] of the rows of x (float64, d even columns) at positions pos
+    (one per row): pair (2i, 2i + 1) turns by the angle pos * base^(-2i/d),
+    (a, b) -> (a cos - b sin, a sin + b cos)."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    theta = float(base) ** (-2.0 * np.arange(d // 2) / d)
+    ang = np.asarray(pos, np.float64).reshape(-1, 1) * theta[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def project_streams(h_bits, w_bits, d_nope, d_rope, idx_dim, pos, base):
+    """The compressor's input streams of T tokens from their hidden states
+    ([HYB] learned pooling, [ROPE]): y = h . W^T over the bf16 operands in
+    float64, W's rows being x (D = d_nope + d_rope), z (D), u (idx_dim), zu
+    (idx_dim) in that order; RoPE at the tokens' positions on the trailing
+    d_rope dims of x and the trailing min(d_rope, idx_dim) dims of u; each
+    stream rounded once to bf16. Returns the bf16 bit patterns (x, z, u, zu),
+    u and zu with idx_dim columns (zero columns when idx_dim is 0)."""
+    h = bf16_decode(h_bits)
+    w = bf16_decode(w_bits)
+    D = d_nope + d_rope
+    if w.shape[0] != 2 * D + 2 * idx_dim or w.shape[1] != h.shape[1]:
+        raise ValueError("weight rows must be 2 (d_nope + d_rope) + 2 idx_dim, columns the hidden size")
+    y = h @ w.T
+    x = y[:, :D].copy()
+    z = y[:, D:2 * D]
+    u = y[:, 2 * D:2 * D + idx_dim].copy()
+    zu = y[:, 2 * D + idx_dim:]
+    if d_rope:
+        x[:, d_nope:] = rope_rotate(x[:, d_nope:], pos, base)
+    ur = min(d_rope, idx_dim)
+    if ur:
+        u[:, idx_dim - ur:] = rope_rotate(u[:, idx_dim - ur:], pos, base)
+    return tuple(bf16_encode(a) for a in (x, z, u, zu))

@@ -447,3 +447,88 @@ def test_multi_token_step_is_causal():
     inside[p - 1] = bf16(rnd(115, (1, D)))
     changed, _ = run(inside)
     assert not np.allclose(changed[t], base[t]) and np.array_equal(changed[:t - 1], base[:t - 1])
+
+
+# ----------------------------------------------------------------------------- projections and RoPE
+
+
+def test_rope_position_zero_is_identity():
+    x = rnd(120, (5, 64))
+    assert np.array_equal(O.rope_rotate(x, np.zeros(5), 10000.0), x)
+
+
+def test_rope_keeps_every_pair_norm():
+    x = rnd(121, (7, 32)).astype(np.float64)
+    y = O.rope_rotate(x, np.arange(7) * 977 + 3, 10000.0)
+    nx = x[:, 0::2] ** 2 + x[:, 1::2] ** 2
+    ny = y[:, 0::2] ** 2 + y[:, 1::2] ** 2
+    assert np.allclose(nx, ny, rtol=1e-12, atol=0)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """<rope(q, m), rope(k, n)> = <rope(q, m - n), k>: the rotation composes by
+    angle, so a score sees only the distance (and pins the sign convention: a
+    rotation by -angle for one operand would break it)."""
+    q, k = rnd(122, (1, 64)).astype(np.float64), rnd(123, (1, 64)).astype(np.float64)
+    for m, n in [(5, 2), (1000, 37), (1 << 20, (1 << 20) - 129)]:
+        lhs = (O.rope_rotate(q, [m], 500.0) * O.rope_rotate(k, [n], 500.0)).sum()
+        rhs = (O.rope_rotate(q, [m - n], 500.0) * k).sum()
+        assert abs(lhs - rhs) <= 1e-9 * (np.abs(q).sum() * np.abs(k).max())
+
+
+def test_rope_pairs_are_adjacent_dims_with_geometric_frequencies():
+    """A one-hot at dim 2i stays in dims (2i, 2i + 1) and turns by pos * base^(-2i/d):
+    the first pair by pos radians, the middle pair (i = d/4) by pos / sqrt(base)."""
+    d, base = 64, 10000.0
+    for i, pos, ang in [(0, 1, 1.0), (0, 3, 3.0), (d // 4, 200, 200 / math.sqrt(base))]:
+        e = np.zeros((1, d))
+        e[0, 2 * i] = 1.0
+        y = O.rope_rotate(e, [pos], base)[0]
+        others = np.delete(y, [2 * i, 2 * i + 1])
+        assert np.all(others == 0)
+        assert abs(y[2 * i] - math.cos(ang)) < 1e-12 and abs(y[2 * i + 1] - math.sin(ang)) < 1e-12
+
+
+def test_project_streams_one_hot_hidden_rows_pick_weight_columns():
+    """Hidden rows with a single 1.0 select one weight column: the unrotated
+    dims of x, all of z and zu, and the unrotated dims of u are that column's
+    bf16 weights exactly; the rotated dims are its rotation at the token's position."""
+    dn, dr, di, hdim = 8, 8, 16, 24
+    D = dn + dr
+    w = bf16(rnd(124, (2 * D + 2 * di, hdim)))
+    cols = [0, 5, 23]
+    h = np.zeros((3, hdim))
+    for r, c in enumerate(cols):
+        h[r, c] = 1.0
+    pos = np.array([0, 7, 1 << 19])
+    x, z, u, zu = O.project_streams(bf16(h), w, dn, dr, di, pos, 10000.0)
+    wf = O.bf16_decode(w)
+    for r, c in enumerate(cols):
+        col = wf[:, c]
+        assert np.array_equal(O.bf16_decode(x[r, :dn]), col[:dn])
+        assert np.array_equal(O.bf16_decode(z[r]), col[D:2 * D])
+        assert np.array_equal(O.bf16_decode(u[r, :di - dr]), col[2 * D:2 * D + di - dr])
+        assert np.array_equal(O.bf16_decode(zu[r]), col[2 * D + di:])
+        rx = O.rope_rotate(col[None, dn:D], [pos[r]], 10000.0)[0]
+        ru = O.rope_rotate(col[None, 2 * D + di - dr:2 * D + di], [pos[r]], 10000.0)[0]
+        assert np.array_equal(x[r, dn:], O.bf16_encode(rx))
+        assert np.array_equal(u[r, di - dr:], O.bf16_encode(ru))
+
+
+def test_project_streams_small_integers_are_exact_dot_products():
+    """Integer hidden states and weights small enough that every dot product is
+    an integer of magnitude < 256 (exact in bf16): the unrotated streams equal
+    the dot products summed in Python integers."""
+    dn, dr, di, hdim = 4, 4, 8, 6
+    D = dn + dr
+    rng = np.random.default_rng(125)
+    h = rng.integers(-3, 4, (5, hdim))
+    w = rng.integers(-3, 4, (2 * D + 2 * di, hdim))
+    x, z, u, zu = O.project_streams(bf16(h.astype(np.float64)), bf16(w.astype(np.float64)), dn, dr, di,
+                                    np.arange(5), 10000.0)
+    for t in range(5):
+        exact = [sum(int(h[t, c]) * int(w[n, c]) for c in range(hdim)) for n in range(w.shape[0])]
+        assert O.bf16_decode(z[t]).tolist() == exact[D:2 * D]
+        assert O.bf16_decode(x[t, :dn]).tolist() == exact[:dn]
+        assert O.bf16_decode(zu[t]).tolist() == exact[2 * D + di:]
+        assert O.bf16_decode(u[t, :di - dr]).tolist() == exact[2 * D:2 * D + di - dr]

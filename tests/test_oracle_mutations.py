@@ -141,3 +141,61 @@ def test_multi_token_selection_not_causal_is_caught(monkeypatch):
     # caught by the pin's comparison, or by the attention refusing a block not yet complete
     with pytest.raises((AssertionError, ValueError)):
         TM.test_multi_token_step_equals_single_token_decode_on_each_prefix(90, 7)
+
+
+def test_rope_sin_sign_flipped_is_caught(monkeypatch):
+    orig = M.rope_rotate
+    _patch(monkeypatch, "rope_rotate", lambda x, pos, base: orig(x, -np.asarray(pos, np.float64), base), M)
+    _fails(TM.test_rope_pairs_are_adjacent_dims_with_geometric_frequencies)
+
+
+def test_rope_half_split_pairs_are_caught(monkeypatch):
+    orig = M.rope_rotate
+
+    def bad(x, pos, base):
+        x = np.asarray(x, np.float64)
+        d = x.shape[-1]
+        perm = np.concatenate([np.arange(0, d, 2), np.arange(1, d, 2)])   # (i, i + d/2) pairs
+        inv = np.argsort(perm)
+        return orig(x[..., inv], pos, base)[..., perm]
+    _patch(monkeypatch, "rope_rotate", bad, M)
+    _fails(TM.test_rope_pairs_are_adjacent_dims_with_geometric_frequencies)
+
+
+def test_rope_wrong_frequency_exponent_is_caught(monkeypatch):
+    def bad(x, pos, base):
+        x = np.asarray(x, np.float64)
+        d = x.shape[-1]
+        theta = float(base) ** (-np.arange(d // 2) / d)            # -i/d instead of -2i/d
+        ang = np.asarray(pos, np.float64).reshape(-1, 1) * theta[None, :]
+        out = np.empty_like(x)
+        out[..., 0::2] = x[..., 0::2] * np.cos(ang) - x[..., 1::2] * np.sin(ang)
+        out[..., 1::2] = x[..., 0::2] * np.sin(ang) + x[..., 1::2] * np.cos(ang)
+        return out
+    _patch(monkeypatch, "rope_rotate", bad, M)
+    _fails(TM.test_rope_pairs_are_adjacent_dims_with_geometric_frequencies)
+
+
+def test_projection_rope_on_leading_dims_is_caught(monkeypatch):
+    orig = M.project_streams
+
+    def bad(h_bits, w_bits, d_nope, d_rope, idx_dim, pos, base):
+        h, w = O.bf16_decode(h_bits), O.bf16_decode(w_bits)
+        D = d_nope + d_rope
+        y = h @ w.T
+        x = y[:, :D].copy()
+        x[:, :d_rope] = M.rope_rotate(x[:, :d_rope], pos, base)   # the leading dims rotated
+        u = y[:, 2 * D:2 * D + idx_dim].copy()
+        return tuple(O.bf16_encode(a) for a in (x, y[:, D:2 * D], u, y[:, 2 * D + idx_dim:]))
+    _patch(monkeypatch, "project_streams", bad, M)
+    _fails(TM.test_project_streams_one_hot_hidden_rows_pick_weight_columns)
+
+
+def test_projection_streams_swapped_is_caught(monkeypatch):
+    orig = M.project_streams
+
+    def bad(*a):
+        x, z, u, zu = orig(*a)
+        return x, z, zu, u
+    _patch(monkeypatch, "project_streams", bad, M)
+    _fails(TM.test_project_streams_small_integers_are_exact_dot_products)
