@@ -505,6 +505,41 @@ int dsv4_decode_plan(const dsv4_layer_desc* d, int32_t H, int32_t k, int32_t* pl
   return DSV4_OK;
 }
 
+int dsv4_project_streams(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t T, int32_t d_model,
+                         const uint16_t* hidden, const uint16_t* weight, float rope_base, uint16_t* x, uint16_t* z,
+                         uint16_t* u, uint16_t* zu, void* stream) {
+  int e = check_desc(d);
+  if (e) return e;
+  if (!c || T < 0 || d_model <= 0 || !(rope_base > 1.f)) return DSV4_ERR_INVALID_ARG;
+  if (d->separate_v) return DSV4_ERR_UNSUPPORTED;
+  const int D = d->d_nope + d->d_rope;
+  if (d_model % 64 || d->d_nope % 32 || D % 32 || d->idx_dim % 32 || d->d_rope > 64) return DSV4_ERR_UNSUPPORTED;
+  DSV4_REQ(c->n_tokens);
+  DSV4_REQ(c->status);
+  if (T == 0) return DSV4_OK;
+  DSV4_REQ(hidden);
+  DSV4_REQ(weight);
+  DSV4_REQ(x);
+  DSV4_REQ(z);
+  if (d->idx_dim) {
+    DSV4_REQ(u);
+    DSV4_REQ(zu);
+  }
+  ProjArgs a{};
+  a.M = d->batch * T;
+  a.N = 2 * D + 2 * d->idx_dim;
+  a.K = d_model;
+  a.T = T;
+  a.d_nope = d->d_nope;
+  a.d_rope = d->d_rope;
+  a.Di = d->idx_dim;
+  a.ur = d->d_rope < d->idx_dim ? d->d_rope : d->idx_dim;
+  a.n_tokens = c->n_tokens;
+  a.x = x; a.z = z; a.u = u; a.zu = zu;
+  a.status = c->status;
+  return launch_project(a, hidden, weight, static_cast<double>(rope_base), sm_count(), static_cast<cudaStream_t>(stream));
+}
+
 int dsv4_debug_force_timeout(int32_t on) { return attention_force_timeout(on); }
 
 int dsv4_read_status(const dsv4_cache* c, void* stream) {

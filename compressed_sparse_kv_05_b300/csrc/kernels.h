@@ -93,6 +93,20 @@ struct IndexArgs {
 };
 __global__ void quant_query_fp4_kernel(IndexArgs a);
 __global__ void topk_select_kernel(IndexArgs a);
+// Projection of the compressor's streams from hidden states with RoPE (project.cu).
+struct ProjArgs {
+  int M, N, K;                 // token rows (B * T), output columns (2 D + 2 Di), hidden size
+  int T;                       // tokens per sequence: row r is token r % T of sequence r / T
+  int d_nope, d_rope, Di, ur;  // ur = min(d_rope, Di) rotated dims of u
+  int tiles_n, tiles;          // set by launch_project
+  const int64_t* n_tokens;     // [B] tokens before this call: positions n_tokens[b] + t
+  uint16_t *x, *z, *u, *zu;    // [M][D], [M][D], [M][Di], [M][Di] bf16
+  int32_t* status;
+  float rx_hi[32], rx_lo[32];  // theta_i / pi of x's rotated dims as float pairs (set by launch_project)
+  float ru_hi[32], ru_lo[32];  // and of u's
+};
+int launch_project(ProjArgs a, const void* hidden, const void* weight, double rope_base, int sms, cudaStream_t st);
+
 // Top-k launch: the cluster kernel (topk_cluster_kernel) when topk_plan finds
 // a cluster size and per-thread score count for the capacity, else the
 // global-atomic kernel with sel_ctas CTAs per sequence.

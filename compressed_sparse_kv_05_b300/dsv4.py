@@ -69,6 +69,7 @@ _SIGS = {
     "dsv4_decode_plan": ([_DESC, _I32, _I32, _P], ctypes.c_int),
     "dsv4_read_status": ([_CACHE, _P], ctypes.c_int),
     "dsv4_debug_force_timeout": ([_I32], ctypes.c_int),
+    "dsv4_project_streams": ([_DESC, _CACHE, _I32, _I32, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P], ctypes.c_int),
     "dsv4_quantize_kv_rows": ([_P, _I64, _I32, _I32, _P, _P, _P, _P], ctypes.c_int),
     "dsv4_quantize_fp4_rows": ([_P, _I64, _I32, _P, _P, _P], ctypes.c_int),
     "dsv4_pool_rows": ([_P, _P, _P, _I64, _I32, _I32, _P, _P], ctypes.c_int),
@@ -217,6 +218,12 @@ def dsv4_decode_plan(desc, H, k):
     plan = (ctypes.c_int32 * 6)()
     _check("dsv4_decode_plan", lib.dsv4_decode_plan(ctypes.byref(desc), H, k, ctypes.cast(plan, ctypes.c_void_p)))
     return dict(zip(("tensor_core", "splits", "tile_rows", "tiles_per_split", "head_groups", "sms"), list(plan)))
+
+
+def dsv4_project_streams(desc, cache, T, d_model, hidden, weight, rope_base, x, z, u, zu, stream=None):
+    return _check("dsv4_project_streams", lib.dsv4_project_streams(
+        ctypes.byref(desc), ctypes.byref(cache.struct), T, d_model, _ptr(hidden), _ptr(weight), float(rope_base),
+        _ptr(x), _ptr(z), _ptr(u), _ptr(zu), _stream(stream)))
 
 
 def dsv4_debug_force_timeout(on):

@@ -16,6 +16,9 @@
  *         window_size entries overwritten cyclically, and a compressor whose
  *         outputs are filtered to the top-k by an index.
  *   [HCA] same page, section 2.2 "HCA：重度压缩注意力".
+ *   [ROPE] devpress.csdn.net, "DeepSeek-V4：百万Token上下文，这次智能体真的能用了",
+ *         section "二、DeepSeek-V4的核心架构创新", part "位置编码的长度泛化优化":
+ *         positions enter through RoPE.
  *
  * Conventions shared by every call
  *   - Data pointers are DEVICE pointers owned by the caller (the library never
@@ -238,6 +241,27 @@ size_t dsv4_workspace_size(const dsv4_layer_desc* desc, int32_t H, int32_t Hi, i
  * rows per split (CUDA-core path), tiles per split, head groups of 64,
  * streaming multiprocessors planned for}. Host only; launches nothing. */
 int dsv4_decode_plan(const dsv4_layer_desc* desc, int32_t H, int32_t k, int32_t* plan);
+
+/* The streams dsv4_compress_append pools, projected from hidden states with
+ * RoPE, on the tensor cores [HYB] (the pooling is learned: its inputs are
+ * projections of the token's hidden state), [ROPE] (positions enter through
+ * RoPE).
+ *   hidden  [B][T][d_model] bf16: T new tokens of every sequence;
+ *   weight  [2 D + 2 Di][d_model] bf16: the rows of the x, z, u and zu
+ *           projections in that order (D = d_nope + d_rope, Di = idx_dim);
+ *   x, z    [B][T][D] bf16 outputs; u, zu [B][T][Di] bf16 (NULL when Di = 0).
+ * Per token at position p = n_tokens[b] + t (the cache's count before the
+ * append of these tokens, so call this first): y = W . h in fp32 (bf16
+ * products, fp32 accumulation), then RoPE on the trailing d_rope dims of x
+ * and the trailing min(d_rope, Di) dims of u: pair (2i, 2i + 1) of those dims
+ * turns by p * rope_base^(-2i/d) (d the number of rotated dims), and every
+ * value is rounded once to bf16. Positions are exact below 2^24.
+ * Requirements: shared K = V (separate_v = 0), d_model a multiple of 64,
+ * d_nope, D and Di multiples of 32, d_rope <= 64, rope_base > 1
+ * (DSV4_ERR_UNSUPPORTED / DSV4_ERR_INVALID_ARG otherwise). T may be 0. */
+int dsv4_project_streams(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t T, int32_t d_model,
+                         const uint16_t* hidden, const uint16_t* weight, float rope_base, uint16_t* x, uint16_t* z,
+                         uint16_t* u, uint16_t* zu, void* stream);
 
 /* Test hook of the failure path (the pages describe no such call). While on
  * != 0, every tensor-core attention kernel launched by the decode calls makes
