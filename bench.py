@@ -56,6 +56,7 @@ WORKLOADS = {
     "compress_1m": (W.COMPRESS_1M_CSA, W.COMPRESS_1M_HCA),
 }
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1400.0
 DTYPE = ("fp8-e4m3 / bf16 / fp4-e2m1 storage; attention on f16 tensor-core operands with fp32 accumulation, "
          "indexer on block-scaled fp4 tensor-core operands with fp32 accumulation, pooling and softmax in fp32")
 
@@ -72,7 +73,36 @@ def parse():
     return ap.parse_args()
 
 
+# ----------------------------------------------------------------------------- graphs
+
+
+def upload_graphs(graphs, stream):
+    """Uploads each instantiated graph to the device ahead of its first launch
+    (otherwise the first launch does it, inside whatever is being timed)."""
+    try:
+        from cuda.bindings import runtime as rt
+        st = rt.cudaStream_t(init_value=stream.cuda_stream)
+        for g in graphs:
+            err, = rt.cudaGraphUpload(rt.cudaGraphExec_t(init_value=g.raw_cuda_graph_exec()), st)
+            if err != rt.cudaError_t.cudaSuccess:
+                return False
+        stream.synchronize()
+        return True
+    except Exception:
+        return False
+
+
 # ----------------------------------------------------------------------------- peaks, clocks
+
+
+def tensor_peak():
+    """The measured sustained dense bf16 peak (a kernel timed inside a long loop), TFLOP/s."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback (sustained)"
 
 
 def hbm_peak():
@@ -345,6 +375,66 @@ def compress_bytes():
     return read, written
 
 
+def time_project(dsv4, K, Wm, seed):
+    """Times K passes of the projection workload: the x, z, u and zu streams of
+    a ratio-4 layer with 128-dim indexer keys (1280 output columns) projected
+    from 2^20 hidden states of 4096 dims (~N(0,1) bf16, weights ~N(0, 1/4096))
+    in 4096-token calls, RoPE on the rotated dims; one CUDA graph per pass.
+    Tensor-core bound: FLOPs = 2 x tokens x 4096 x 1280."""
+    L = W.COMPRESS_1M_CSA
+    n, C, dm = W.COMPRESS_1M_TOKENS, W.COMPRESS_1M_CHUNK, W.PROJECT_D_MODEL
+    D, Di = L.dim, L.idx_dim
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    hidden = torch.empty((n, dm), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, n, 1 << 16):
+        hidden[r0:r0 + (1 << 16)] = torch.randn((min(1 << 16, n - r0), dm), generator=g, device="cuda")
+    weight = (torch.randn((2 * D + 2 * Di, dm), generator=g, device="cuda") / dm ** 0.5).to(torch.bfloat16)
+    desc = dsv4.layer_desc(L, 64)
+    cache = dsv4.Cache(desc)
+    x = torch.empty((C, D), dtype=torch.bfloat16, device="cuda")
+    z = torch.empty_like(x)
+    u = torch.empty((C, Di), dtype=torch.bfloat16, device="cuda")
+    zu = torch.empty_like(u)
+    stream = torch.cuda.Stream()
+
+    def one_pass():
+        for c0 in range(0, n, C):
+            dsv4.dsv4_project_streams(desc, cache, C, dm, hidden[c0:c0 + C], weight, 10000.0, x, z, u, zu,
+                                      stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        one_pass()
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        one_pass()
+    for _ in range(Wm):
+        with torch.cuda.stream(stream):
+            gr.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        with torch.cuda.stream(stream):
+            gr.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    flops = 2.0 * n * dm * (2 * D + 2 * Di)
+    tf = flops / (ms * 1e-3) / 1e12
+    peak, kind = tensor_peak()
+    out = {"workload": "project_1m", "ms_per_pass": round(ms, 4), "tokens_per_s": round(n / (ms * 1e-3), 1),
+           "TFLOP/s": round(tf, 1),
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(tf / peak, 4), "peak_kind": kind},
+           "shape": f"{n} tokens x {dm} hidden -> {2 * D + 2 * Di} columns (x, z, u, zu), {C}-token calls",
+           "launches_per_pass": n // C}
+    del gr, hidden
+    return out
+
+
 def time_compress(dsv4, K, Wm, seed, peak, e2e=False):
     """Times K passes of the compressor workload (one CUDA graph per pass) after
     Wm warm-up passes; returns a dict of the figures (and the end-to-end pass
@@ -516,6 +606,7 @@ def run_ours(args, rank, world):
     with torch.cuda.graph(probe, stream=stream):
         st.step(total + K + 1)
     kernels_per_step = count_kernel_nodes(probe)
+    uploaded = upload_graphs(graphs + ev_graphs, stream)
     for s in range(Wm):
         graphs[s].replay()
     torch.cuda.synchronize()
@@ -600,6 +691,7 @@ def run_ours(args, rank, world):
                 with torch.cuda.graph(g, stream=stream):
                     st.step(s, only=li)
                 gs.append(g)
+            upload_graphs(gs, stream)
             for s in range(Wm):
                 with torch.cuda.stream(stream):
                     gs[s].replay()
@@ -635,11 +727,13 @@ def run_ours(args, rank, world):
         "gpu_launches": (kernels_per_step * K) if kernels_per_step is not None else None,
         "clocks": clk,
     }
+    line["config"]["graphs_uploaded_before_timing"] = uploaded
     if per_layer:
         line["layers"] = per_layer
     if args.workload == "stack_1m" and not args.no_compress:
         del graphs, ev_graphs, probe
         line["compress_1m"] = time_compress(dsv4, min(K, 10), 3, 4321 + rank, peak)
+        line["project_1m"] = time_project(dsv4, min(K, 5), 2, 8765 + rank)
     return line
 
 

@@ -74,6 +74,7 @@ STACK_1M = tuple(STACK_CSA if l % 2 == 0 else STACK_HCA for l in range(8))
 # compress_1m: the same token stream into both caches
 COMPRESS_1M_TOKENS = 1 << 20
 COMPRESS_1M_CHUNK = 4096
+PROJECT_D_MODEL = 4096   # hidden size of the projection workload (the pages give none)
 COMPRESS_1M_CSA = Layer("csa", 1, 0, 0, 448, 64, False, 4, 128, idx_dim=128)
 COMPRESS_1M_HCA = Layer("hca", 1, 0, 0, 448, 64, False, 128, 128)
 
