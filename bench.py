@@ -54,7 +54,10 @@ WORKLOADS = {
     "stack_1m_hca": (W.STACK_HCA,),
     "csa_b32_128k": (W.CSA_B32_128K,),
     "compress_1m": (W.COMPRESS_1M_CSA, W.COMPRESS_1M_HCA),
+    "project_1m": (W.COMPRESS_1M_CSA,),
 }
+PROJECT_METRIC = ("projection TFLOP/s (2^20 hidden states of 4096 dims to the x, z, u, zu streams of a ratio-4 "
+                  "layer with 128-dim indexer keys, RoPE on the rotated dims, 4096-token calls)")
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1400.0
 DTYPE = ("fp8-e4m3 / bf16 / fp4-e2m1 storage; attention on f16 tensor-core operands with fp32 accumulation, "
@@ -375,7 +378,7 @@ def compress_bytes():
     return read, written
 
 
-def time_project(dsv4, K, Wm, seed):
+def time_project(dsv4, K, Wm, seed, e2e=False):
     """Times K passes of the projection workload: the x, z, u and zu streams of
     a ratio-4 layer with 128-dim indexer keys (1280 output columns) projected
     from 2^20 hidden states of 4096 dims (~N(0,1) bf16, weights ~N(0, 1/4096))
@@ -431,6 +434,24 @@ def time_project(dsv4, K, Wm, seed):
                         "frac": round(tf / peak, 4), "peak_kind": kind},
            "shape": f"{n} tokens x {dm} hidden -> {2 * D + 2 * Di} columns (x, z, u, zu), {C}-token calls",
            "launches_per_pass": n // C}
+    if e2e:
+        # end to end: every pass copies the hidden states from pinned host
+        # memory and reads the last chunk's streams back
+        host = torch.empty(hidden.shape, dtype=hidden.dtype, pin_memory=True)
+        host.copy_(hidden.cpu())
+        back = torch.empty((C, D), dtype=torch.bfloat16, pin_memory=True)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(K):
+                hidden.copy_(host, non_blocking=True)
+                gr.replay()
+                back.copy_(x, non_blocking=True)
+        stream.synchronize()
+        ms_e2e = (time.perf_counter() - w0) * 1e3 / K
+        out["e2e"] = {"unit": "TFLOP/s", "ms_per_pass": ms_e2e, "h2d_bytes_per_step": int(hidden.numel() * 2),
+                      "d2h_bytes_per_step": int(back.numel() * 2)}
+        del host
     del gr, hidden
     return out
 
@@ -737,6 +758,40 @@ def run_ours(args, rank, world):
     return line
 
 
+def project_config(world):
+    L = W.COMPRESS_1M_CSA
+    return {"workload": "project_1m", "tokens": W.COMPRESS_1M_TOKENS, "chunk": W.COMPRESS_1M_CHUNK,
+            "d_model": W.PROJECT_D_MODEL, "columns": 2 * L.dim + 2 * L.idx_dim,
+            "streams": "x 448+64 (RoPE on the last 64), z 512, u 128 (RoPE on the last 64), zu 128",
+            "l2": "hidden states 8.6 GB per pass > 126 MB L2 (no flush)", "parallelism": f"replicas x{world}"}
+
+
+def run_project(args, rank, world):
+    """The projection workload as the headline: TFLOP/s on the tensor cores."""
+    from compressed_sparse_kv_05_b300 import dsv4
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    r = time_project(dsv4, args.steps, args.warmup, 8765 + rank, e2e=True)
+    clk = clocks.stop()
+    ms = max_over_ranks(r["ms_per_pass"], world, "cuda")
+    flops = project_flops(W.COMPRESS_1M_TOKENS)
+    tf = world * flops / (ms * 1e-3) / 1e12
+    e2e = r.pop("e2e")
+    e2e_ms = max_over_ranks(e2e.pop("ms_per_pass"), world, "cuda")
+    e2e["value"] = round(world * flops / (e2e_ms * 1e-3) / 1e12, 1)
+    roof = dict(r["roofline"])
+    roof.update({"achieved": round(tf / world, 1), "frac": round(tf / world / roof["peak"], 4), "kernel": "project",
+                 "traffic": None, "algorithmic_flops_per_launch": project_flops(W.COMPRESS_1M_CHUNK)})
+    return {"metric": PROJECT_METRIC, "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 operands, fp32 accumulate, bf16 out",
+            "data": "synthetic", "config": project_config(world), "roofline": roof, "detail": r, "e2e": e2e,
+            "gpu_launches": r["launches_per_pass"] * args.steps, "clocks": clk}
+
+
 def run_compress(args, rank, world):
     """The compressor workload as the headline: cache GB/s read and written."""
     from compressed_sparse_kv_05_b300 import dsv4
@@ -834,6 +889,9 @@ def cpu_model():
 
 
 def sample_desc(name, layers):
+    if name == "project_1m":
+        return (f"{PROJECT_SAMPLE_TOKENS} tokens of the projection (float64 matmul and RoPE) per sample step; "
+                f"TFLOP/s = the sample's FLOPs / sample-step time")
     if name == "compress_1m":
         return (f"the first {COMPRESS_SAMPLE_TOKENS} tokens of the compressor stream pooled and quantised into both "
                 f"caches per sample step; GB/s = algorithmic bytes of those tokens / sample-step time")
@@ -863,10 +921,34 @@ def oracle_compress_step(p):
     O.build_cache(p["k"], p["zh"], p["bh"], hca.ratio, hca.d_nope, hca.window)
 
 
+PROJECT_SAMPLE_TOKENS = 256
+
+
+def oracle_project_setup():
+    L = W.COMPRESS_1M_CSA
+    D, Di, dm = L.dim, L.idx_dim, W.PROJECT_D_MODEL
+    h = synth.bf16_bits(synth.normal(("bench", "project", "h"), (PROJECT_SAMPLE_TOKENS, dm)))
+    w = synth.bf16_bits(synth.normal(("bench", "project", "w"), (2 * D + 2 * Di, dm)) / np.sqrt(dm))
+    return {"h": h, "w": w}
+
+
+def oracle_project_step(p):
+    import oracle as O
+    L = W.COMPRESS_1M_CSA
+    O.project_streams(p["h"], p["w"], L.d_nope, L.d_rope, L.idx_dim, np.arange(PROJECT_SAMPLE_TOKENS), 10000.0)
+
+
+def project_flops(tokens):
+    L = W.COMPRESS_1M_CSA
+    return 2.0 * tokens * W.PROJECT_D_MODEL * (2 * L.dim + 2 * L.idx_dim)
+
+
 def oracle_sample(name, layers):
     """(sample inputs, step function) of the oracle for a workload."""
     if name == "compress_1m":
         return oracle_compress_setup(), oracle_compress_step
+    if name == "project_1m":
+        return oracle_project_setup(), oracle_project_step
     return oracle_sample_setup(layers), oracle_sample_step
 
 
@@ -905,6 +987,8 @@ def time_oracle(name, steps, warmup, threads):
 
 def oracle_rate(name, layers, dt):
     """(value, unit) of the oracle from its sample-step time."""
+    if name == "project_1m":
+        return project_flops(PROJECT_SAMPLE_TOKENS) / dt / 1e12, "TFLOP/s"
     if name == "compress_1m":
         read, written = compress_bytes()
         frac = COMPRESS_SAMPLE_TOKENS / W.COMPRESS_1M_TOKENS
@@ -941,6 +1025,10 @@ def run_reference(args):
                   "a ratio-4 CSA and a ratio-128 HCA cache)")
         config = {"workload": "compress_1m", "tokens": W.COMPRESS_1M_TOKENS, "chunk": W.COMPRESS_1M_CHUNK}
         projected = None
+    elif args.workload == "project_1m":
+        metric = PROJECT_METRIC
+        config = project_config(1)
+        projected = None
     else:
         metric = METRIC
         step_bytes = sum(accounting.decode_step_bytes(L) + accounting.call_bytes(L, "append") for L in layers)
@@ -965,7 +1053,12 @@ def main():
         return
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    line = run_compress(args, rank, world) if args.workload == "compress_1m" else run_ours(args, rank, world)
+    if args.workload == "compress_1m":
+        line = run_compress(args, rank, world)
+    elif args.workload == "project_1m":
+        line = run_project(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload, WORKLOADS[args.workload])

@@ -98,7 +98,7 @@ struct ProjArgs {
   int M, N, K;                 // token rows (B * T), output columns (2 D + 2 Di), hidden size
   int T;                       // tokens per sequence: row r is token r % T of sequence r / T
   int d_nope, d_rope, Di, ur;  // ur = min(d_rope, Di) rotated dims of u
-  int tiles_n, tiles;          // set by launch_project
+  int bn, tiles_n, tiles;      // tile width and tile counts, set by launch_project
   const int64_t* n_tokens;     // [B] tokens before this call: positions n_tokens[b] + t
   uint16_t *x, *z, *u, *zu;    // [M][D], [M][D], [M][Di], [M][Di] bf16
   int32_t* status;

@@ -14,8 +14,9 @@
 //
 // C[M][N] = H[M][K] . W[N][K]^T with M = B * T token rows, K the hidden size
 // and N = 2 D + 2 Di output columns (W's rows: x, z, u, zu). Tiles of 128 rows
-// x 256 columns; K in steps of 64 (128-byte rows, 128-byte swizzle) through a
-// 4-stage TMA ring; one thread issues 4 MMAs (M = 128, N = 256, K = 16) per
+// x bn columns (bn of 128 .. 256 chosen per call so that the tiles fill the
+// SMs' waves); K in steps of 64 (128-byte rows, 128-byte swizzle) through a
+// 4-stage TMA ring; one thread issues 4 MMAs (M = 128, N = bn, K = 16) per
 // step into one of two accumulators (256 tensor-memory columns each), so the
 // epilogue of one tile overlaps the MMAs of the next. Persistent CTAs take
 // tiles column-block first, so the CTAs working at one time share their
@@ -61,7 +62,7 @@ struct ProjTail {
 
 // bf16 with both operands K-major, fp32 accumulator (the f16 descriptor with
 // the A and B formats set to bf16)
-constexpr uint32_t kIdescBf16 = tc::idesc_f16_f32(kPM, kPN, 0, 0) | (1u << 7) | (1u << 10);
+DSV4_DEV uint32_t idesc_bf16(uint32_t N) { return tc::idesc_f16_f32(kPM, N, 0, 0) | (1u << 7) | (1u << 10); }
 
 // the row's position (n_tokens of its sequence before this call, plus its token index)
 DSV4_DEV float row_position(const ProjArgs& a, int row) {
@@ -136,9 +137,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const int s = g % kPStages, round = g / kPStages;
           if (!(ok = tc::mbar_wait(&t->empty[s], (round & 1) ^ 1, abort))) break;
           unsigned char* st = stages + s * kPStageBytes;
-          tc::mbar_arrive_expect_tx(&t->full[s], kPStageBytes);
+          tc::mbar_arrive_expect_tx(&t->full[s], kPABytes + a.bn * kPK * 2);
           tc::tma_load_2d(st, &hmap, &t->full[s], ks * kPK, mt * kPM);
-          tc::tma_load_2d(st + kPABytes, &wmap, &t->full[s], ks * kPK, nt * kPN);
+          tc::tma_load_2d(st + kPABytes, &wmap, &t->full[s], ks * kPK, nt * a.bn);
         }
       }
       // every copy issued must land before the CTA's shared memory goes away
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       int g = 0, j = 0;
       bool ok = true;
+      const uint32_t idesc = idesc_bf16(static_cast<uint32_t>(a.bn));
       for (int tile = blockIdx.x; ok && tile < a.tiles; tile += gridDim.x, ++j) {
         const int buf = j & 1, use = j >> 1;
         if (!(ok = tc::mbar_wait(&t->acc_empty[buf], (use & 1) ^ 1, abort))) break;
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int kk = 0; kk < kPK / 16; ++kk) {
             const uint64_t ad = tc::smem_desc(a_sa + kk * 32, 1024, tc::kSwizzle128B);
             const uint64_t bd = tc::smem_desc(b_sa + kk * 32, 1024, tc::kSwizzle128B);
-            tc::mma_f16(acc, ad, bd, kIdescBf16, (ks | kk) ? 1u : 0u);
+            tc::mma_f16(acc, ad, bd, idesc, (ks | kk) ? 1u : 0u);
           }
           tc::tc_commit(&t->empty[s]);
         }
@@ -190,11 +192,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int row = mt * kPM + q * 32 + lane;
       const bool live = row < a.M;
       const float pos = live ? row_position(a, live ? row : 0) : 0.f;
-      for (int c = 0; c < kPN / 32; ++c) {
+      for (int c = 0; c < a.bn / 32; ++c) {
         uint32_t raw[32];
         tc::tmem_ld32(taddr + lane_off + buf * kPN + c * 32, raw);
         tc::tmem_wait_ld();
-        const int n0 = nt * kPN + c * 32;                    // first output column of the chunk
+        const int n0 = nt * a.bn + c * 32;                   // first output column of the chunk
         if (!live || n0 >= a.N) continue;
         float v[32];
 #pragma unroll
@@ -277,13 +279,30 @@ void rope_table(double base, int d, float* hi, float* lo) {
 size_t project_smem_bytes() { return 1024 + static_cast<size_t>(kPStages) * kPStageBytes + sizeof(ProjTail); }
 
 int launch_project(ProjArgs a, const void* hidden, const void* weight, double rope_base, int sms, cudaStream_t st) {
+  // Tile width: the one of 256, 224, 192, 160, 128 columns with the least
+  // time over all waves of tiles (tiles of one wave run side by side), so that
+  // the last wave is not left nearly empty. A tile takes time in proportion to
+  // bn + 218: its own columns plus a fixed part (the 128 hidden rows it loads,
+  // the MMA issue, the epilogue) measured worth about 218 columns.
+  const int tiles_m = (a.M + kPM - 1) / kPM;
+  int best = kPN;
+  int64_t best_cost = -1;
+  for (int bn = kPN; bn >= 128; bn -= 32) {
+    const int64_t tiles = static_cast<int64_t>(tiles_m) * ((a.N + bn - 1) / bn);
+    const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 218);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  a.bn = best;
   CUtensorMap hmap, wmap;
-  if (!encode_bf16_rows(&hmap, hidden, a.M, a.K, kPM) || !encode_bf16_rows(&wmap, weight, a.N, a.K, kPN))
+  if (!encode_bf16_rows(&hmap, hidden, a.M, a.K, kPM) || !encode_bf16_rows(&wmap, weight, a.N, a.K, a.bn))
     return DSV4_ERR_CUDA;
   rope_table(rope_base, a.d_rope, a.rx_hi, a.rx_lo);
   rope_table(rope_base, a.ur, a.ru_hi, a.ru_lo);
-  a.tiles_n = (a.N + kPN - 1) / kPN;
-  a.tiles = ((a.M + kPM - 1) / kPM) * a.tiles_n;
+  a.tiles_n = (a.N + a.bn - 1) / a.bn;
+  a.tiles = tiles_m * a.tiles_n;
   const int grid = a.tiles < sms ? a.tiles : sms;
   const size_t smem = project_smem_bytes();
   static std::once_flag once;

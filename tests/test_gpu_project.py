@@ -97,3 +97,11 @@ def test_project_streams_zero_tokens_and_unsupported_shapes():
     for d_model in (100, 0):
         with pytest.raises(RuntimeError):
             dsv4.dsv4_project_streams(desc, cache, 1, d_model, x, x, BASE, x, x, x, x)
+
+
+def test_project_streams_chunk_shape_and_full_width_tiles():
+    """The tile width follows the call's shape (it fills the SMs' waves): a
+    4096-token call of the decode step's layer (1280 columns) takes 160-column
+    tiles on 148 SMs; 18944 tokens of a 256-column layer take 256-column tiles."""
+    _check(W.scaled(W.STACK_CSA, batch=1), 4096, 256, (100000,), ("proj_chunk",))
+    _check(W.Layer("hca", 1, 0, 8, 64, 64, False, 128, 128), 18944, 128, (3,), ("proj_wide",))
