@@ -164,3 +164,24 @@ def test_decode_plan_on_host(dsv4):
     assert p["head_groups"] == 2
     with pytest.raises(dsv4.Dsv4Error):
         dsv4.dsv4_decode_plan(_desc(dsv4), 64, -2)
+
+
+def test_projection_rejects_bad_arguments_on_host(dsv4):
+    d = _desc(dsv4)
+    L = dsv4.lib
+    c = _cache(dsv4)
+
+    def proj(desc, cache, T=4, d_model=512, hidden=FAKE, weight=FAKE, base=10000.0, x=FAKE, u=FAKE):
+        return L.dsv4_project_streams(ctypes.byref(desc), ctypes.byref(cache), T, d_model, hidden, weight,
+                                      ctypes.c_float(base), x, FAKE, u, FAKE, None)
+
+    assert proj(d, c, T=-1) == dsv4.ERR_INVALID_ARG
+    assert proj(d, c, d_model=0) == dsv4.ERR_INVALID_ARG
+    assert proj(d, c, base=1.0) == dsv4.ERR_INVALID_ARG
+    assert proj(d, c, d_model=100) == dsv4.ERR_UNSUPPORTED                   # not a multiple of 64
+    assert proj(_desc(dsv4, separate_v=1), c) == dsv4.ERR_UNSUPPORTED        # shared K = V only
+    assert proj(_desc(dsv4, d_nope=40), c) == dsv4.ERR_UNSUPPORTED           # d_nope not a multiple of 32
+    assert proj(d, c, hidden=FAKE + 2) == dsv4.ERR_MISALIGNED
+    assert proj(d, c, u=None) == dsv4.ERR_INVALID_ARG                        # indexer streams missing
+    assert proj(d, _cache(dsv4, n_tokens=0)) == dsv4.ERR_INVALID_ARG
+    assert proj(d, c, T=0, hidden=None, weight=None, x=None, u=None) == dsv4.OK   # nothing to do
