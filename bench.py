@@ -223,8 +223,10 @@ class Stack:
         H_max = max(L.heads for L in layers)
         D_max = max(L.dim for L in layers)
         B = layers[0].batch
-        self.out = torch.zeros((len(layers), B, H_max, D_max), dtype=torch.float32, device="cuda")
-        self.lse = torch.zeros((len(layers), B, H_max), dtype=torch.float32, device="cuda")
+        # one output slot per step slot, so that a step's read-back can overlap the next step
+        slots = self.inbuf.shape[0]
+        self.out = torch.zeros((slots, len(layers), B, H_max, D_max), dtype=torch.float32, device="cuda")
+        self.lse = torch.zeros((slots, len(layers), B, H_max), dtype=torch.float32, device="cuda")
         torch.cuda.synchronize()
 
     def view(self, step, li, name):
@@ -284,8 +286,8 @@ class Stack:
             desc, cache = self.descs[li], self.caches[li]
             v = lambda n: self.view(s, li, n)  # noqa: E731
             H = L.heads
-            out = self.out[li, :, :H, :L.dim]
-            lse = self.lse[li, :, :H]
+            out = self.out[s, li, :, :H, :L.dim]
+            lse = self.lse[s, li, :, :H]
 
             def timed(call, fn):
                 if events is None:
@@ -676,29 +678,46 @@ def run_ours(args, rank, world):
     step_bytes = sum(accounting.decode_step_bytes(L) + accounting.call_bytes(L, "append") for L in layers)
 
     # end to end: per step, H2D of that step's inputs from pinned host memory,
-    # the step, and a D2H read of every layer's output
+    # the step, and a D2H read of every layer's output; the copies run on their
+    # own streams, so step i's read-back and step i + 1's inputs overlap the
+    # steps around them (each step waits for its inputs, each read-back for its step)
     in_host = torch.empty((K, st.in_bytes), dtype=torch.uint8, pin_memory=True)
     in_host.copy_(st.inbuf[Wm:total].cpu())
-    out_host = torch.empty((K,) + tuple(st.out.shape), dtype=torch.float32, pin_memory=True)
+    out_host = torch.empty((K,) + tuple(st.out.shape[1:]), dtype=torch.float32, pin_memory=True)
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    inputs_in = [torch.cuda.Event() for _ in range(K)]
+    step_done = [torch.cuda.Event() for _ in range(K)]
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     w0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(K):
-            s = Wm + i
-            st.inbuf[s].copy_(in_host[i], non_blocking=True)
+    e0.record(stream)
+    h2d.wait_event(e0)
+    for i in range(K):
+        with torch.cuda.stream(h2d):
+            st.inbuf[Wm + i].copy_(in_host[i], non_blocking=True)
+            inputs_in[i].record(h2d)
+    for i in range(K):
+        s = Wm + i
+        stream.wait_event(inputs_in[i])
+        with torch.cuda.stream(stream):
             graphs[s].replay()
-            out_host[i].copy_(st.out, non_blocking=True)
-        e1.record(stream)
+            step_done[i].record(stream)
+        d2h.wait_event(step_done[i])
+        with torch.cuda.stream(d2h):
+            out_host[i].copy_(st.out[s], non_blocking=True)
+    reads_done = torch.cuda.Event()
+    reads_done.record(d2h)
+    stream.wait_event(reads_done)
+    e1.record(stream)
     stream.synchronize()
     wall = (time.perf_counter() - w0) * 1e3
     e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), wall), world, "cuda")
     e2e = {"value": round(job_tokens_per_s(world, B, e2e_ms / K), 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": int(st.in_bytes), "d2h_bytes_per_step": int(st.out.numel() * 4)}
+           "h2d_bytes_per_step": int(st.in_bytes), "d2h_bytes_per_step": int(st.out[0].numel() * 4),
+           "copies": "own streams, overlapping the neighbouring steps"}
 
     # per-layer decode: the first CSA and the first HCA layer of the stack, each
     # replayed on its own (append + its attention calls), W + K graphs
