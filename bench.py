@@ -380,6 +380,117 @@ def compress_bytes():
     return read, written
 
 
+def _graph_time(fn, K, Wm, stream):
+    """ms per call of fn() captured in one CUDA graph, K timed replays after Wm."""
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    upload_graphs([g], stream)
+    for _ in range(Wm):
+        with torch.cuda.stream(stream):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        with torch.cuda.stream(stream):
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / K
+
+
+def time_next_rows(dsv4, st, K, Wm, seed):
+    """The decode-side rows beyond single-token decode, on the stack's first CSA
+    and HCA layers (their caches as the stack step left them):
+      multi_token  T = 4 queries per sequence after their tokens were appended
+                   (speculative or chunked decode): causal top-k, CSA and HCA
+                   attention with the window rows from a span of the last
+                   T + W - 1 raw tokens; tokens/s = B * T / (time of one CSA and
+                   one HCA layer's calls);
+      window_only  the window-only layer (k = 0) at the CSA layer's shape;
+      ratio1       selection over the raw tokens (ratio 1) at a 128K context:
+                   index_topk then csa_decode, B = 4, the stack's dims."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    stream = torch.cuda.Stream()
+    Lc, Lh = st.layers[0], st.layers[1]
+    dc, cc, dh, ch = st.descs[0], st.caches[0], st.descs[1], st.caches[1]
+    B, H, D, Hi, Di, k = Lc.batch, Lc.heads, Lc.dim, Lc.idx_heads, Lc.idx_dim, Lc.topk
+
+    def bf16(shape):
+        return torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
+
+    out = {}
+    T = 4
+    q, qh = bf16((B, T, H, D)), bf16((B, T, Lh.heads, Lh.dim))
+    qi = bf16((B, T, Hi, Di))
+    w = torch.rand((B, T, Hi), generator=g, device="cuda")
+    span_c, span_h = bf16((B, T + Lc.window - 1, D)), bf16((B, T + Lh.window - 1, Lh.dim))
+    ws_c = dsv4.workspace_multi(dc, T, H, Hi, k)
+    ws_h = dsv4.workspace_multi(dh, T, Lh.heads)
+    topk = torch.zeros((B, T, k), dtype=torch.int32, device="cuda")
+    o_c = torch.empty((B, T, H, D), device="cuda")
+    l_c = torch.empty((B, T, H), device="cuda")
+    o_h = torch.empty((B, T, Lh.heads, Lh.dim), device="cuda")
+    l_h = torch.empty((B, T, Lh.heads), device="cuda")
+
+    def multi():
+        dsv4.dsv4_index_topk_multi(dc, cc, T, Hi, qi, w, k, topk, None, ws_c)
+        dsv4.dsv4_csa_decode_multi(dc, cc, T, H, q, Lc.sm_scale, topk, k, span_c, None, o_c, l_c, ws_c)
+        dsv4.dsv4_hca_decode_multi(dh, ch, T, Lh.heads, qh, Lh.sm_scale, span_h, None, o_h, l_h, ws_h)
+
+    ms = _graph_time(multi, K, Wm, stream)
+    out["multi_token"] = {"queries_per_sequence": T, "ms_per_step": round(ms, 4),
+                          "tokens_per_s": round(B * T / (ms * 1e-3), 1),
+                          "layers": "one CSA + one HCA layer of stack_1m (appends not included)"}
+    del ws_c, ws_h
+
+    ws = dsv4.workspace(dc, H, Hi, k)
+    q1 = bf16((B, H, D))
+    o1 = torch.empty((B, H, D), device="cuda")
+    l1 = torch.empty((B, H), device="cuda")
+    ms = _graph_time(lambda: dsv4.dsv4_csa_decode(dc, cc, H, q1, Lc.sm_scale, None, 0, o1, l1, ws), K, Wm, stream)
+    out["window_only"] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+                          "layer": f"window {Lc.window}, {H} heads, {Lc.d_nope}+{Lc.d_rope} dims, B = {B}"}
+    del ws
+
+    # ratio 1 at a 128K context: a cache of raw tokens (entries and FP4 keys drawn directly)
+    n = 1 << 17
+    L1 = W.scaled(Lc, ratio=1, n_tokens=n, planted_frac=0.0)
+    d1 = dsv4.layer_desc(L1, n + 64)
+    c1 = dsv4.Cache(d1)
+    for b in range(B):
+        for r0 in range(0, n, 1 << 16):
+            r1 = min(n, r0 + (1 << 16))
+            y = torch.randn((r1 - r0, D), generator=g, device="cuda")
+            dsv4.dsv4_quantize_kv_rows(y, r1 - r0, L1.d_nope, L1.d_rope, c1.k_nope[b, r0:r1], c1.k_scale[b, r0:r1],
+                                       c1.k_rope[b, r0:r1])
+            yi = torch.randn((r1 - r0, Di), generator=g, device="cuda")
+            dsv4.dsv4_quantize_fp4_rows(yi, r1 - r0, Di, c1.idx_codes[b, r0:r1], c1.idx_scales[b, r0:r1])
+        c1.win_k[b].copy_(bf16((L1.window, D)).view(torch.int16))
+    c1.n_tokens.fill_(n)
+    ws = dsv4.workspace(d1, H, Hi, k)
+    qi1 = bf16((B, Hi, Di))
+    w1 = torch.rand((B, Hi), generator=g, device="cuda")
+    tk = torch.zeros((B, k), dtype=torch.int32, device="cuda")
+
+    def ratio1():
+        dsv4.dsv4_index_topk(d1, c1, Hi, qi1, w1, k, tk, None, ws)
+        dsv4.dsv4_csa_decode(d1, c1, H, q1, L1.sm_scale, tk, k, o1, l1, ws)
+
+    ms = _graph_time(ratio1, K, Wm, stream)
+    out["ratio1"] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+                     "layer": f"ratio 1 over {n} raw tokens, top-{k}, window {L1.window}, B = {B}"}
+    del c1, ws
+    return out
+
+
 def time_project(dsv4, K, Wm, seed, e2e=False):
     """Times K passes of the projection workload: the x, z, u and zu streams of
     a ratio-4 layer with 128-dim indexer keys (1280 output columns) projected
@@ -770,6 +881,8 @@ def run_ours(args, rank, world):
     line["config"]["graphs_uploaded_before_timing"] = uploaded
     if per_layer:
         line["layers"] = per_layer
+    if args.workload == "stack_1m":
+        line["next_rows"] = time_next_rows(dsv4, st, min(K, 10), 3, 2468 + rank)
     if args.workload == "stack_1m" and not args.no_compress:
         del graphs, ev_graphs, probe
         line["compress_1m"] = time_compress(dsv4, min(K, 10), 3, 4321 + rank, peak)
