@@ -231,19 +231,25 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
 // sits at granule q ^ (d & 7)), with two fp32 log sums [B][H][splits] each:
 // lse_s, of the split's softmax weights, and lse'_s, of the scale of its
 // partial, so that out = sum_s exp(lse'_s) o_s / sum_s exp(lse_s).
-// grid (B * head groups, D / 8), block 256: 8 dims x 64 heads per CTA; thread
-// t takes split group t / 64 (splits s = t / 64 mod 4), dim t / 8 % 8 and
-// heads 8 (t % 8) .. + 7. Per pass of up to 64 splits every thread issues its
-// partial loads and its share of the log-sum-exps at once (one round trip);
-// the split weights exp(lse - max) are computed once per CTA, each thread
-// accumulates its splits and the four split groups are summed in shared
-// memory. With more than 64 splits the passes rescale the running result.
-__global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
+// grid (B * head groups, D / KD), block 256: KD dims x 64 heads per CTA;
+// thread t takes split group t / (8 KD) (splits s = group mod KSG), dim
+// t / 8 % KD and heads 8 (t % 8) .. + 7. Per pass of up to KS splits every
+// thread issues its partial loads and its share of the log-sum-exps at once
+// (one round trip); the split weights exp(lse - max) are computed once per
+// CTA, each thread accumulates its splits and the split groups are summed in
+// shared memory. With more than KS splits the passes rescale the running result.
+// KS splits per pass in KSG groups of threads; each CTA merges KD dims of one
+// sequence and head group (KSG * KD * 8 = 256 threads: split group, dim, 8 heads).
+// Many splits: (64, 4, 8); a few (at most 8, the batched CSA plan): (8, 1, 32),
+// so that the CTAs are fewer, lighter and all resident at once.
+template <int KS, int KSG, int KD>
+__global__ void __launch_bounds__(256, KS <= 8 ? 4 : 2) attn_merge_tc_kernel(AttnArgs a) {
   constexpr int kT = 256;
-  constexpr int kS = 64;   // splits per pass
-  constexpr int kSg = 4;   // split groups
+  constexpr int kS = KS;   // splits per pass
+  constexpr int kSg = KSG; // split groups
   constexpr int kU = kS / kSg;
   constexpr int kL = 64 * kS / kT;   // log-sum-exps each thread stages per pass
+  static_assert(KSG * KD * 8 == kT, "one thread per (split group, dim, 8 heads)");
   pdl_trigger();
   pdl_wait();
   const int hgs = (a.H + 63) / 64;
@@ -253,10 +259,10 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
   __shared__ float s_lse[64][kS + 1];                   // [head][split]
   __shared__ __align__(16) float s_w[kS][64 + 4];       // [split][head]: partial weights relative to the running max
   __shared__ float s_m[64], s_l[64], s_r[64];           // running max and sum per head, rescale of this pass
-  __shared__ float s_acc[kSg][64][9];
+  __shared__ float s_acc[kSg][64][KD + 1];
   const int t = threadIdx.x;
-  const int sg = t >> 6, dl = (t >> 3) & 7, hq = (t & 7) * 8;
-  const int d = blockIdx.y * 8 + dl;
+  const int sg = t / (8 * KD), dl = (t >> 3) % KD, hq = (t & 7) * 8;
+  const int d = blockIdx.y * KD + dl;
   const float* lse0 = a.part_lse + (static_cast<int64_t>(b) * a.H + h0) * a.splits;
   const float* lsev0 = a.part_lsev + (static_cast<int64_t>(b) * a.H + h0) * a.splits;
   // granule hq / 8 of dim d sits at granule (hq / 8) ^ (d & 7) of the row
@@ -282,7 +288,7 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < kL; ++u) {
-      const int i = t + u * kT, h = i >> 6, s = i & (kS - 1);
+      const int i = t + u * kT, h = i / kS, s = i % kS;
       const bool in = h < hcount && s < ns;
       lv[u] = in ? __ldcg(lse0 + static_cast<int64_t>(h) * a.splits + s0 + s) : -INFINITY;
       lvv[u] = in ? __ldcg(lsev0 + static_cast<int64_t>(h) * a.splits + s0 + s) : -INFINITY;
@@ -290,8 +296,8 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
 #pragma unroll
     for (int u = 0; u < kL; ++u) {
       const int i = t + u * kT;
-      s_lse[i >> 6][i & (kS - 1)] = lv[u];
-      s_w[i & (kS - 1)][i >> 6] = lvv[u];     // lse', turned into the output weight below
+      s_lse[i / kS][i % kS] = lv[u];
+      s_w[i % kS][i / kS] = lvv[u];     // lse', turned into the output weight below
     }
     __syncthreads();
     {
@@ -345,12 +351,14 @@ __global__ void __launch_bounds__(256, 2) attn_merge_tc_kernel(AttnArgs a) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) s_acc[sg][hq + i][dl] = acc[i];
   __syncthreads();
-  for (int o = t; o < 64 * 8; o += kT) {
-    const int r = o >> 3, dd = o & 7;   // head r, dim dd of the CTA's 8
+  for (int o = t; o < 64 * KD; o += kT) {
+    const int r = o / KD, dd = o % KD;   // head r, dim dd of the CTA's KD
     if (r < hcount) {
-      const float sum = (s_acc[0][r][dd] + s_acc[1][r][dd]) + (s_acc[2][r][dd] + s_acc[3][r][dd]);
+      float sum;
+      if (KSG == 4) sum = (s_acc[0][r][dd] + s_acc[1][r][dd]) + (s_acc[2][r][dd] + s_acc[3][r][dd]);
+      else sum = s_acc[0][r][dd];
       const float L = s_l[r];
-      const int dg = blockIdx.y * 8 + dd;
+      const int dg = blockIdx.y * KD + dd;
       if (dg < a.D) a.out[(static_cast<int64_t>(b) * a.H + h0 + r) * a.Dv + dg] = L > 0.f ? sum / L : 0.f;
       if (blockIdx.y == 0 && dd == 0 && a.lse)
         a.lse[static_cast<int64_t>(b) * a.H + h0 + r] = L > 0.f ? s_m[r] + logf(L) : -INFINITY;
@@ -393,7 +401,9 @@ int launch_attention(const AttnArgs& a, int head_groups, cudaStream_t st) {
 }
 
 int launch_attention_merge_tc(const AttnArgs& a, int head_groups, cudaStream_t st) {
-  return launch_pdl(attn_merge_tc_kernel, dim3(a.B * head_groups, (a.D + 7) / 8), dim3(256), 0, st, a);
+  if (a.splits <= 8)
+    return launch_pdl(attn_merge_tc_kernel<8, 1, 32>, dim3(a.B * head_groups, (a.D + 31) / 32), dim3(256), 0, st, a);
+  return launch_pdl(attn_merge_tc_kernel<64, 4, 8>, dim3(a.B * head_groups, (a.D + 7) / 8), dim3(256), 0, st, a);
 }
 
 int launch_attention_merge(const AttnArgs& a, cudaStream_t st) {
