@@ -318,8 +318,10 @@ class Compress:
     streamed in 4096-token chunks into a ratio-4 CSA cache (with 128-dim FP4
     indexer keys) and a ratio-128 HCA cache, each compressor with its own gate
     logits ~N(0,1) and position bias ~N(0,0.1). A step appends the whole stream
-    to empty caches (n_tokens reset at its start), chunk by chunk: the CSA
-    cache's call, then the HCA cache's."""
+    to empty caches (n_tokens reset at its start), chunk by chunk. The two
+    caches are independent, so their calls run on two streams (the CSA cache's
+    on the caller's stream, the HCA cache's on a second stream forked from it
+    and joined at the end of the step); each cache's chunks stay in order."""
 
     def __init__(self, dsv4, seed):
         self.dsv4 = dsv4
@@ -350,6 +352,7 @@ class Compress:
         self.d_hca = dsv4.layer_desc(self.hca, n // self.hca.ratio + 1)
         self.c_csa = dsv4.Cache(self.d_csa)
         self.c_hca = dsv4.Cache(self.d_hca)
+        self.side = torch.cuda.Stream()
         torch.cuda.synchronize()
 
     def input_bytes(self):
@@ -357,14 +360,18 @@ class Compress:
 
     def step(self):
         d = self.dsv4
+        main, side = torch.cuda.current_stream(), self.side
+        side.wait_stream(main)
         self.c_csa.n_tokens.zero_()
-        self.c_hca.n_tokens.zero_()
+        with torch.cuda.stream(side):
+            self.c_hca.n_tokens.zero_()
         for t0 in range(0, self.n, self.chunk):
             t1 = t0 + self.chunk
             d.dsv4_compress_append(self.d_csa, self.c_csa, self.chunk, self.x[t0:t1], None, self.z_csa[t0:t1],
-                                   self.b_csa, self.u[t0:t1], self.zu[t0:t1], self.bu)
+                                   self.b_csa, self.u[t0:t1], self.zu[t0:t1], self.bu, stream=main)
             d.dsv4_compress_append(self.d_hca, self.c_hca, self.chunk, self.x[t0:t1], None, self.z_hca[t0:t1],
-                                   self.b_hca)
+                                   self.b_hca, stream=side)
+        main.wait_stream(side)
 
 
 def compress_bytes():

@@ -312,7 +312,22 @@ int dsv4_compress_append(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t 
   const int blocks = (d->ratio - 1 + T) / d->ratio;
   const int win_rows = T < d->window ? T : d->window;
   const int ctas_w = (win_rows + kWinRowsPerCta - 1) / kWinRowsPerCta;
-  {
+  if (d->ratio > 8 && !d->idx_dim && D % 64 == 0 && D <= 512) {
+    // long blocks: each block's channels split over a cluster of D / 64 CTAs
+    const int cs = D / 64;
+    a.ctas_k = blocks * cs;
+    a.ctas_u = 0;
+    PoolShape slice = pk;
+    slice.cg = 8;
+    int threads = 8 * pk.G;
+    threads = threads < 64 ? 64 : (threads + 31) / 32 * 32;
+    const size_t smem = static_cast<size_t>(d->ratio) * 64 * (4 + 2 * (d->separate_v ? 3 : 2)) +
+                        pool_part_floats(slice, d->separate_v != 0) * sizeof(float) + 4 * sizeof(uint32_t);
+    static std::once_flag once;
+    set_smem_once(once, pool_cluster_kernel, 200 * 1024);
+    const int ctas = a.ctas_k + (ctas_w + cs - 1) / cs * cs;
+    if ((e = launch_pdl_cluster(pool_cluster_kernel, dim3(ctas, d->batch), dim3(threads), smem, cs, st, a))) return e;
+  } else {
     // teams of up to 512 threads, about 256 threads a CTA (several blocks a CTA for small teams)
     a.bpc_k = team_k >= 256 ? 1 : 256 / team_k;
     a.bpc_u = team_u == 0 ? 1 : (team_u >= 256 ? 1 : 256 / team_u);

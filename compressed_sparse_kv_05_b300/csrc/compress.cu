@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
+#include "tc_ptx.cuh"
 
 namespace dsv4 {
 
@@ -35,9 +36,22 @@ DSV4_DEV void bf16x8(uint4 w, float* f) {
   f[6] = __uint_as_float(w.w << 16); f[7] = __uint_as_float(w.w & 0xFFFF0000u);
 }
 
-// Token rows of one compressed block j of sequence b: token i (0 <= i < m) is
-// position t0 + i; positions before n_old come from the pending planes (slot
-// t % m), the others from this call's inputs.
+// Raw loads of token i's gate logits (bf16) and position bias (fp32) for the
+// channels [c0, c0 + 8).
+struct GateLoad {
+  uint4 z;
+  float4 b0, b1;
+};
+// the 8 logits z + b of a GateLoad
+DSV4_DEV void logits8(const GateLoad& g, float* l) {
+  bf16x8(g.z, l);
+  l[0] += g.b0.x; l[1] += g.b0.y; l[2] += g.b0.z; l[3] += g.b0.w;
+  l[4] += g.b1.x; l[5] += g.b1.y; l[6] += g.b1.z; l[7] += g.b1.w;
+}
+
+// Token rows of one compressed block j of sequence b in global memory: token
+// i (0 <= i < m) is position t0 + i; positions before n_old come from the
+// pending planes (slot t % m), the others from this call's inputs.
 struct BlockSrc {
   const uint16_t *pend_x, *in_x, *pend_x2, *in_x2, *pend_z, *in_z;
   const float* bias;   // [m][C]
@@ -48,28 +62,38 @@ struct BlockSrc {
     return t < n_old ? pend + (static_cast<int64_t>(b) * m + (t % m)) * C
                      : in + (static_cast<int64_t>(b) * T + (t - n_old)) * C;
   }
+  DSV4_DEV bool two() const { return in_x2 != nullptr; }
+  DSV4_DEV GateLoad gate(int i, int c0) const {
+    GateLoad g;
+    g.z = ld16(row(pend_z, in_z, i) + c0);
+    const float4* bp = reinterpret_cast<const float4*>(bias + static_cast<int64_t>(i) * C + c0);
+    g.b0 = __ldg(bp);
+    g.b1 = __ldg(bp + 1);
+    return g;
+  }
+  DSV4_DEV uint4 x(int i, int c0) const { return ld16(row(pend_x, in_x, i) + c0); }
+  DSV4_DEV uint4 x2(int i, int c0) const { return ld16(row(pend_x2, in_x2, i) + c0); }
 };
 
-// Raw loads of token i's gate logits (bf16) and position bias (fp32) for the
-// channels [c0, c0 + 8).
-struct GateLoad {
-  uint4 z;
-  float4 b0, b1;
+// The same rows of one slice of cc channels, copied into shared memory: x, x2
+// (or null), z as [m][cc] bf16 and the position bias as [m][cc] fp32; c0 counts
+// from the slice's first channel.
+struct SmemRows {
+  const uint16_t *xs, *x2s, *zs;
+  const float* bs;
+  int cc;
+  DSV4_DEV bool two() const { return x2s != nullptr; }
+  DSV4_DEV GateLoad gate(int i, int c0) const {
+    GateLoad g;
+    g.z = *reinterpret_cast<const uint4*>(zs + i * cc + c0);
+    const float4* bp = reinterpret_cast<const float4*>(bs + i * cc + c0);
+    g.b0 = bp[0];
+    g.b1 = bp[1];
+    return g;
+  }
+  DSV4_DEV uint4 x(int i, int c0) const { return *reinterpret_cast<const uint4*>(xs + i * cc + c0); }
+  DSV4_DEV uint4 x2(int i, int c0) const { return *reinterpret_cast<const uint4*>(x2s + i * cc + c0); }
 };
-DSV4_DEV GateLoad load_gate(const BlockSrc& s, int i, int c0) {
-  GateLoad g;
-  g.z = ld16(s.row(s.pend_z, s.in_z, i) + c0);
-  const float4* bp = reinterpret_cast<const float4*>(s.bias + static_cast<int64_t>(i) * s.C + c0);
-  g.b0 = __ldg(bp);
-  g.b1 = __ldg(bp + 1);
-  return g;
-}
-// the 8 logits z + b of a GateLoad
-DSV4_DEV void logits8(const GateLoad& g, float* l) {
-  bf16x8(g.z, l);
-  l[0] += g.b0.x; l[1] += g.b0.y; l[2] += g.b0.z; l[3] += g.b0.w;
-  l[4] += g.b1.x; l[5] += g.b1.y; l[6] += g.b1.z; l[7] += g.b1.w;
-}
 
 // Softmax-gated pooling of one block by a team (see PoolShape): team thread t
 // takes channels [8 c8, 8 c8 + 8) and tokens [g tpg, g tpg + tpg) of the
@@ -81,32 +105,58 @@ DSV4_DEV void logits8(const GateLoad& g, float* l) {
 // y2, the second stream gated by the same logits). `part` is shared memory of
 // pool_part_floats() floats for this team. Every thread of the CTA calls it
 // (it holds CTA barriers when G > 1); `active` marks a thread with work.
-template <bool TWO>
-DSV4_DEV void pool_team_t(const BlockSrc& s, PoolShape ps, int t, bool active, float* part, float* y, float* y2) {
+// ONE: a group's tokens fit one batch of loads (tpg <= 4), which are then all
+// issued in the first pass and kept in registers for the second. The
+// arithmetic, and so every result bit, is the same whatever the source and
+// batching.
+template <bool TWO, bool ONE, typename Src>
+DSV4_DEV void pool_team_t(const Src& s, PoolShape ps, int m, int t, bool active, float* part, float* y, float* y2) {
   constexpr int kTokBatch = TWO ? 2 : 4;   // tokens whose loads a thread issues together
   constexpr bool two = TWO;
   const int c8 = t % ps.cg, g = t / ps.cg;
   const int c0 = 8 * c8;
-  const int i0 = g * ps.tpg, i1 = i0 + ps.tpg < s.m ? i0 + ps.tpg : s.m;
+  const int i0 = g * ps.tpg, i1 = i0 + ps.tpg < m ? i0 + ps.tpg : m;
   float mx[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-  if (active)
-    for (int i = i0; i < i1; i += kTokBatch) {
-      // a batch of tokens: every load in flight, then the maxima in token order
-      GateLoad gl[kTokBatch];
+  GateLoad g1[ONE ? kTokBatch : 1];
+  uint4 x1[ONE ? kTokBatch : 1], x21[ONE ? kTokBatch : 1];
+  if (active) {
+    if constexpr (ONE) {
+      // the group's only batch: the gates and the values, all in flight
 #pragma unroll
       for (int u = 0; u < kTokBatch; ++u)
-        if (i + u < i1) gl[u] = load_gate(s, i + u, c0);
+        if (i0 + u < i1) {
+          g1[u] = s.gate(i0 + u, c0);
+          x1[u] = s.x(i0 + u, c0);
+          if (two) x21[u] = s.x2(i0 + u, c0);
+        }
 #pragma unroll
       for (int u = 0; u < kTokBatch; ++u)
-        if (i + u < i1) {
+        if (i0 + u < i1) {
           float l[8];
-          logits8(gl[u], l);
+          logits8(g1[u], l);
 #pragma unroll
           for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], l[k]);
         }
+    } else {
+      for (int i = i0; i < i1; i += kTokBatch) {
+        // a batch of tokens: every load in flight, then the maxima in token order
+        GateLoad gl[kTokBatch];
+#pragma unroll
+        for (int u = 0; u < kTokBatch; ++u)
+          if (i + u < i1) gl[u] = s.gate(i + u, c0);
+#pragma unroll
+        for (int u = 0; u < kTokBatch; ++u)
+          if (i + u < i1) {
+            float l[8];
+            logits8(gl[u], l);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], l[k]);
+          }
+      }
     }
+  }
   if (ps.G > 1) {
     float* pm = part + (g * ps.cg + c8) * 8;
     if (active)
@@ -132,9 +182,15 @@ DSV4_DEV void pool_team_t(const BlockSrc& s, PoolShape ps, int t, bool active, f
 #pragma unroll
       for (int u = 0; u < kTokBatch; ++u)
         if (i + u < i1) {
-          gl[u] = load_gate(s, i + u, c0);
-          xw[u] = ld16(s.row(s.pend_x, s.in_x, i + u) + c0);
-          if (two) x2w[u] = ld16(s.row(s.pend_x2, s.in_x2, i + u) + c0);
+          if constexpr (ONE) {
+            gl[u] = g1[u];
+            xw[u] = x1[u];
+            if (two) x2w[u] = x21[u];
+          } else {
+            gl[u] = s.gate(i + u, c0);
+            xw[u] = s.x(i + u, c0);
+            if (two) x2w[u] = s.x2(i + u, c0);
+          }
         }
 #pragma unroll
       for (int u = 0; u < kTokBatch; ++u)
@@ -182,29 +238,33 @@ DSV4_DEV void pool_team_t(const BlockSrc& s, PoolShape ps, int t, bool active, f
     }
 }
 
-DSV4_DEV void pool_team(const BlockSrc& s, PoolShape ps, int t, bool active, float* part, float* y, float* y2) {
-  if (s.in_x2) pool_team_t<true>(s, ps, t, active, part, y, y2);
-  else pool_team_t<false>(s, ps, t, active, part, y, y2);
+// (the one-batch form for a single stream only, and where the kernel allows
+// it: with two streams, or in a kernel with other work, it holds too many
+// registers)
+template <bool ALLOW_ONE = true, typename Src>
+DSV4_DEV void pool_team(const Src& s, PoolShape ps, int m, int t, bool active, float* part, float* y, float* y2) {
+  if (s.two()) pool_team_t<true, false>(s, ps, m, t, active, part, y, y2);
+  else if (ALLOW_ONE && ps.tpg <= 4) pool_team_t<false, true>(s, ps, m, t, active, part, y, y2);   // uniform
+  else pool_team_t<false, false>(s, ps, m, t, active, part, y, y2);
 }
 
 // The FP8 + BF16 entry of a pooled row held by a team's group-0 threads (8
 // channels each, `has` when the thread holds some): scale = amax/448 over the
-// d_nope FP8 dims (amax combined through the shared word *amax, zeroed by the
-// caller before a barrier), codes = e4m3(y / scale), the RoPE dims bf16. Every
-// thread of the CTA calls it (one CTA barrier).
-DSV4_DEV void store_entry(const float* y, bool has, int c8, int d_nope, uint32_t* amax, uint8_t* nope, float* scale,
-                          uint16_t* rope) {
-  const int c0 = 8 * c8;
-  const bool code_dims = has && c0 < d_nope;
-  if (code_dims) {
-    float m = 0.f;
+// d_nope FP8 dims, codes = e4m3(y / scale), the RoPE dims bf16.
+// entry_amax: this thread's share of amax (0 when it holds no FP8 dims).
+DSV4_DEV float entry_amax(const float* y, bool has, int c8, int d_nope) {
+  float m = 0.f;
+  if (has && 8 * c8 < d_nope)
 #pragma unroll
     for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[k]));
-    atomicMax(amax, __float_as_uint(m));
-  }
-  __syncthreads();
-  if (code_dims) {
-    const float s = __fdiv_rn(__uint_as_float(*amax), 448.f);
+  return m;
+}
+// entry_write: this thread's dims of the entry, given the row's amax.
+DSV4_DEV void entry_write(const float* y, bool has, int c8, int d_nope, float amax, uint8_t* nope, float* scale,
+                          uint16_t* rope) {
+  const int c0 = 8 * c8;
+  if (has && c0 < d_nope) {
+    const float s = __fdiv_rn(amax, 448.f);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (s > 0.f)
 #pragma unroll
@@ -218,6 +278,15 @@ DSV4_DEV void store_entry(const float* y, bool has, int c8, int d_nope, uint32_t
       w[k] = static_cast<uint32_t>(f32_to_bf16(y[2 * k])) | (static_cast<uint32_t>(f32_to_bf16(y[2 * k + 1])) << 16);
     *reinterpret_cast<uint4*>(rope + (c0 - d_nope)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+// The whole entry by one CTA: amax combined through the shared word *amax
+// (zeroed by the caller before a barrier). Every thread of the CTA calls it
+// (one CTA barrier).
+DSV4_DEV void store_entry(const float* y, bool has, int c8, int d_nope, uint32_t* amax, uint8_t* nope, float* scale,
+                          uint16_t* rope) {
+  if (has && 8 * c8 < d_nope) atomicMax(amax, __float_as_uint(entry_amax(y, has, c8, d_nope)));
+  __syncthreads();
+  entry_write(y, has, c8, d_nope, __uint_as_float(*amax), nope, scale, rope);
 }
 
 // The FP4 row of a pooled indexer key held by a team's group-0 threads: per
@@ -277,10 +346,30 @@ DSV4_DEV void copy_rows(uint16_t* dst, const uint16_t* src, int rows, int dim, S
 __global__ void __launch_bounds__(512) pool_chunk_kernel(AppendArgs a) {
   extern __shared__ float smem[];
   pdl_trigger();
-  pdl_wait();
   const int b = blockIdx.y;
   const int D = a.d_nope + a.d_rope;
   const int m = a.ratio;
+  if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < a.ctas_k + a.ctas_u) {
+    // While the previous kernel finishes: the input rows this CTA pools when
+    // the call starts on a block boundary (the usual case) are pulled into L2.
+    // A hint only, and L2 is coherent with whatever that kernel still writes.
+    const bool key_stream = static_cast<int>(blockIdx.x) < a.ctas_k;
+    const int bpc = key_stream ? a.bpc_k : a.bpc_u;
+    const int64_t r0 = static_cast<int64_t>(key_stream ? blockIdx.x : blockIdx.x - a.ctas_k) * bpc * m;
+    const int64_t r1 = r0 + static_cast<int64_t>(bpc) * m < a.T ? r0 + static_cast<int64_t>(bpc) * m : a.T;
+    if (r0 < r1) {
+      const int64_t row = static_cast<int64_t>(b) * a.T + r0;
+      if (key_stream) {
+        tc::prefetch_l2_range(a.k + row * D, (r1 - r0) * D * 2);
+        tc::prefetch_l2_range(a.z + row * D, (r1 - r0) * D * 2);
+        if (a.separate_v) tc::prefetch_l2_range(a.v + row * D, (r1 - r0) * D * 2);
+      } else {
+        tc::prefetch_l2_range(a.u + row * a.idx_dim, (r1 - r0) * a.idx_dim * 2);
+        tc::prefetch_l2_range(a.zu + row * a.idx_dim, (r1 - r0) * a.idx_dim * 2);
+      }
+    }
+  }
+  pdl_wait();
   const int64_t n_old = a.n_tokens[b];
   const int64_t n_new = n_old + a.T;
   if (n_new / m > a.capacity) {
@@ -323,7 +412,7 @@ __global__ void __launch_bounds__(512) pool_chunk_kernel(AppendArgs a) {
     src.pend_z = a.pend_zu; src.in_z = a.zu; src.bias = a.bias_u;
   }
   float y[8] = {}, y2[8] = {};
-  pool_team(src, ps, t, active, part, y, y2);
+  pool_team(src, ps, m, t, active, part, y, y2);
   __syncthreads();   // the amax words are zeroed
   const bool has = active && t < ps.cg;
   const int64_t e = static_cast<int64_t>(b) * a.capacity + j;
@@ -335,6 +424,126 @@ __global__ void __launch_bounds__(512) pool_chunk_kernel(AppendArgs a) {
     // every thread (whole warps: the pair shuffle; a pair never spans two teams)
     store_fp4(y, has, t, a.idx_codes + e * (a.idx_dim / 2), a.idx_scales + e * (a.idx_dim / 16));
   }
+}
+
+// Pooling of the key (and value) stream of an append of T > 1 tokens for a
+// layer with blocks of more than 8 tokens, D = d_nope + d_rope a multiple of 64
+// up to 512, and no indexer. Grid (ctas_k + window CTAs, B) in clusters of
+// cs = D / 64 CTAs: cluster q pools block j0 + q, its CTA r the channels
+// [64 r, 64 r + 64). A CTA copies the block's rows of its slice (pending
+// tokens or this call's), gate logits and position bias into shared memory
+// (cp.async, one round trip), pools them with the team arithmetic of every
+// other pooling kernel (8 channel groups x G token groups: the same bits), and
+// the cluster combines the FP8 scale's amax in distributed shared memory
+// before each CTA writes its dims of the entry. CTAs past ctas_k (whole
+// clusters) write the window ring as pool_chunk_kernel does. Dynamic shared
+// memory: bias [m][64] fp32, z, x (, v) [m][64] bf16, the team's combine
+// buffer, four words (the cluster's amax of K and V, which the peers raise;
+// this CTA's).
+__global__ void __launch_bounds__(256, 1) pool_cluster_kernel(AppendArgs a) {
+  extern __shared__ __align__(16) unsigned char csm[];
+  const int D = a.d_nope + a.d_rope;
+  const int m = a.ratio;
+  const bool two = a.separate_v != 0;
+  const PoolShape pk = pool_shape(m, D);
+  PoolShape ps;   // the team of one 64-channel slice
+  ps.cg = 8; ps.G = pk.G; ps.tpg = pk.tpg;
+  float* bias_s = reinterpret_cast<float*>(csm);
+  uint16_t* z_s = reinterpret_cast<uint16_t*>(bias_s + m * 64);
+  uint16_t* x_s = z_s + m * 64;
+  uint16_t* x2_s = x_s + m * 64;
+  float* part = reinterpret_cast<float*>(x_s + (two ? 2 : 1) * m * 64);
+  uint32_t* words = reinterpret_cast<uint32_t*>(part + pool_part_floats(ps, two));
+  pdl_trigger();
+  const int b = blockIdx.y;
+  const uint32_t r = tc::cluster_rank(), cs = tc::cluster_ctas();
+  const int cbase = 64 * static_cast<int>(r);
+  const bool pool = static_cast<int>(blockIdx.x) < a.ctas_k;
+  if (pool) {
+    // the slice's position bias: a caller input that no kernel of this library writes
+    for (int i = threadIdx.x; i < m * 16; i += blockDim.x)
+      tc::cp_async16(bias_s + (i >> 4) * 64 + (i & 15) * 4, a.bias + static_cast<int64_t>(i >> 4) * D + cbase + (i & 15) * 4);
+    tc::cp_async_commit();
+    // the input rows of the cluster's block when the call starts on a block
+    // boundary (the usual case), this CTA's share of them, into L2: a hint
+    // only, and L2 is coherent with whatever the previous kernel still writes
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x / cs) * m;
+    const int64_t i1 = i0 + m < a.T ? i0 + m : a.T;
+    const int64_t share = (i1 - i0 + cs - 1) / cs;
+    const int64_t r0 = i0 + r * share, r1 = r0 + share < i1 ? r0 + share : i1;
+    if (threadIdx.x == 0 && r0 < r1) {
+      const int64_t row = static_cast<int64_t>(b) * a.T + r0;
+      tc::prefetch_l2_range(a.z + row * D, (r1 - r0) * D * 2);
+      tc::prefetch_l2_range(a.k + row * D, (r1 - r0) * D * 2);
+      if (two) tc::prefetch_l2_range(a.v + row * D, (r1 - r0) * D * 2);
+    }
+  }
+  if (threadIdx.x < 4) words[threadIdx.x] = 0u;
+  tc::cluster_arrive();   // the amax words are zeroed before any peer raises them
+  pdl_wait();
+  const int64_t n_old = a.n_tokens[b];
+  const int64_t n_new = n_old + a.T;
+  const int64_t j = n_old / m + static_cast<int64_t>(blockIdx.x / cs);   // the cluster's block
+  bool work = pool && j < n_new / m;                                   // uniform across a cluster
+  if (n_new / m > a.capacity) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, DSV4_STATUS_CAPACITY);
+    work = false;
+  } else if (!pool) {
+    // window rows: tokens [n_new - cnt, n_new), cnt = min(W, T)
+    const int cnt = a.T < a.window ? a.T : a.window;
+    const int r0 = (blockIdx.x - a.ctas_k) * kWinRowsPerCta;
+    const int rows = cnt - r0 < kWinRowsPerCta ? cnt - r0 : kWinRowsPerCta;
+    if (rows > 0) {
+      const int64_t t0 = n_new - cnt + r0;
+      auto src_row = [&](int q) { return static_cast<int64_t>(b) * a.T + (t0 + q - n_old); };
+      auto dst_row = [&](int q) { return static_cast<int64_t>(b) * a.window + (t0 + q) % a.window; };
+      copy_rows(a.win_k, a.k, rows, D, src_row, dst_row);
+      if (two) copy_rows(a.win_v, a.v, rows, D, src_row, dst_row);
+    }
+  }
+  if (!work) {
+    tc::cp_async_wait_all();   // no copy may land after the CTA has gone
+    tc::cluster_wait();
+    return;
+  }
+  BlockSrc src;
+  src.t0 = j * m; src.n_old = n_old; src.b = b; src.T = a.T; src.m = m; src.C = D;
+  src.pend_x = a.pend_k; src.in_x = a.k; src.pend_x2 = a.pend_v; src.in_x2 = two ? a.v : nullptr;
+  src.pend_z = a.pend_z; src.in_z = a.z; src.bias = a.bias;
+  for (int i = threadIdx.x; i < m * 8; i += blockDim.x) {
+    const int row = i >> 3, q = (i & 7) * 8;
+    tc::cp_async16(z_s + row * 64 + q, src.row(src.pend_z, src.in_z, row) + cbase + q);
+    tc::cp_async16(x_s + row * 64 + q, src.row(src.pend_x, src.in_x, row) + cbase + q);
+    if (two) tc::cp_async16(x2_s + row * 64 + q, src.row(src.pend_x2, src.in_x2, row) + cbase + q);
+  }
+  tc::cp_async_commit();
+  tc::cp_async_wait_all();
+  __syncthreads();
+  SmemRows rows;
+  rows.xs = x_s; rows.x2s = two ? x2_s : nullptr; rows.zs = z_s; rows.bs = bias_s; rows.cc = 64;
+  const int t = threadIdx.x;
+  const bool active = t < 8 * ps.G;
+  float y[8] = {}, y2[8] = {};
+  pool_team(rows, ps, m, t, active, part, y, y2);
+  const bool has = active && t < 8;
+  const int c8 = cbase / 8 + t;   // the thread's channel group in the row
+  if (has && 8 * c8 < a.d_nope) {
+    atomicMax(&words[2], __float_as_uint(entry_amax(y, has, c8, a.d_nope)));
+    if (two) atomicMax(&words[3], __float_as_uint(entry_amax(y2, has, c8, a.d_nope)));
+  }
+  __syncthreads();
+  tc::cluster_wait();   // every CTA of the cluster has zeroed its amax words
+  if (threadIdx.x < cs) {
+    tc::peer_max(tc::peer_addr(&words[0], threadIdx.x), words[2]);
+    if (two) tc::peer_max(tc::peer_addr(&words[1], threadIdx.x), words[3]);
+  }
+  tc::cluster_sync();   // every CTA holds the row's amax; no peer touches this CTA's memory after it
+  const int64_t e = static_cast<int64_t>(b) * a.capacity + j;
+  entry_write(y, has, c8, a.d_nope, __uint_as_float(words[0]), a.k_nope + e * a.d_nope, a.k_scale + e,
+              a.k_rope + e * a.d_rope);
+  if (two)
+    entry_write(y2, has, c8, a.d_nope, __uint_as_float(words[1]), a.v_nope + e * a.d_nope, a.v_scale + e,
+                a.v_rope + e * a.d_rope);
 }
 
 namespace {
@@ -388,9 +597,11 @@ __global__ void __launch_bounds__(512) append_one_kernel(AppendArgs a) {
   const int b = blockIdx.x;
   const int D = a.d_nope + a.d_rope;
   {
-    // The new token's rows are inputs no kernel of this library writes: their
-    // 128-byte lines are pulled into L1 while the previous kernel finishes, so
-    // the copies and the pooling after the wait find them there.
+    // The new token's 128-byte lines are pulled into L2 while the previous
+    // kernel finishes, so the copies and the pooling after the wait find them
+    // there. Only L2, which every SM sees coherently: the rows may be written
+    // by that kernel (dsv4_project_streams), and a line held in this SM's L1
+    // from before its writes would be stale.
     const int lk = D * 2 / 128, lu = a.idx_dim * 2 / 128;
     const int i = threadIdx.x;
     const char* p = nullptr;
@@ -401,7 +612,7 @@ __global__ void __launch_bounds__(512) append_one_kernel(AppendArgs a) {
       p = reinterpret_cast<const char*>(a.u + static_cast<int64_t>(b) * a.idx_dim) + (i - 3 * lk) * 128;
     else if (i >= 3 * lk + lu && i < 3 * lk + 2 * lu && a.zu)
       p = reinterpret_cast<const char*>(a.zu + static_cast<int64_t>(b) * a.idx_dim) + (i - 3 * lk - lu) * 128;
-    if (p) asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+    if (p) asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
   }
   pdl_wait();
   const int m = a.ratio;
@@ -425,7 +636,7 @@ __global__ void __launch_bounds__(512) append_one_kernel(AppendArgs a) {
     const int t = threadIdx.x;
     const bool act_k = t < pk.G * pk.cg;
     float y[8] = {}, y2[8] = {};
-    pool_team(src, pk, t, act_k, part, y, y2);
+    pool_team<false>(src, pk, m, t, act_k, part, y, y2);
     __syncthreads();
     const bool has = act_k && t < pk.cg;
     store_entry(y, has, t, a.d_nope, amax, a.k_nope + e * a.d_nope, a.k_scale + e, a.k_rope + e * a.d_rope);
@@ -437,7 +648,7 @@ __global__ void __launch_bounds__(512) append_one_kernel(AppendArgs a) {
       src.pend_z = a.pend_zu; src.in_z = a.zu; src.bias = a.bias_u;
       const PoolShape pu = pool_shape(m, a.idx_dim);
       const bool act_u = t < pu.G * pu.cg;
-      pool_team(src, pu, t, act_u, part, y, y2);
+      pool_team<false>(src, pu, m, t, act_u, part, y, y2);
       store_fp4(y, act_u && t < pu.cg, t, a.idx_codes + e * (a.idx_dim / 2), a.idx_scales + e * (a.idx_dim / 16));
     }
     __syncthreads();
@@ -514,7 +725,7 @@ __global__ void __launch_bounds__(512) pool_rows_kernel(const uint16_t* x, const
   const PoolShape ps = pool_shape(ratio, dim);
   const int t = threadIdx.x;
   float v[8] = {}, v2[8] = {};
-  pool_team(src, ps, t, t < ps.G * ps.cg, smem, v, v2);
+  pool_team(src, ps, ratio, t, t < ps.G * ps.cg, smem, v, v2);
   if (t < ps.cg) {
     float4* out = reinterpret_cast<float4*>(y + j * dim + 8 * t);
     out[0] = make_float4(v[0], v[1], v[2], v[3]);

@@ -62,6 +62,7 @@ __host__ __device__ inline int pool_part_floats(PoolShape p, bool two) {
 
 constexpr int kWinRowsPerCta = 16;
 __global__ void pool_chunk_kernel(AppendArgs a);
+__global__ void pool_cluster_kernel(AppendArgs a);
 __global__ void append_tail_kernel(AppendArgs a);
 __global__ void append_one_kernel(AppendArgs a);
 __global__ void quant_kv_rows_kernel(const float* y, int64_t rows, int d_nope, int d_rope, uint8_t* nope,

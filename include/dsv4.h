@@ -30,15 +30,15 @@
  *   - Kernels are launched as programmatic dependent launches: each may start
  *     while the kernel before it in the stream finishes, and waits for that
  *     kernel before it reads anything it may have written. A few inputs are
- *     read before that wait: the attention query `q` of dsv4_csa_decode and
- *     dsv4_hca_decode(_static), the indexer query `q_idx` and weights `w` of
- *     dsv4_index_topk, and the token rows x, v, z, u, zu of a single-token
- *     dsv4_compress_append. They must be complete when the call is enqueued in
- *     stream order, i.e. written by work that is not a kernel of this library
- *     still running in the same stream (a projection GEMM or a copy enqueued
- *     before the call qualifies, unless it triggers programmatic launch of
- *     its dependents before those writes; the `out` of a call enqueued just
- *     before does not).
+ *     read before that wait: the attention query `q` of dsv4_csa_decode(_multi)
+ *     and dsv4_hca_decode(_static), the indexer query `q_idx` and weights `w`
+ *     of dsv4_index_topk(_multi). They must be complete when the call is
+ *     enqueued in stream order, i.e. written by work that is not a kernel of
+ *     this library still running in the same stream (a projection GEMM or a
+ *     copy enqueued before the call qualifies, unless it triggers
+ *     programmatic launch of its dependents before those writes; the `out` of
+ *     a call enqueued just before does not). The streams dsv4_project_streams
+ *     writes are read by dsv4_compress_append after its wait.
  *   - Return value: DSV4_OK, or a negative DSV4_ERR_* code. A call that
  *     returns an error found on the host launches nothing and changes nothing.
  *     Conditions only the device can see (capacity, bad indices) set bits of

@@ -105,3 +105,37 @@ def test_project_streams_chunk_shape_and_full_width_tiles():
     tiles on 148 SMs; 18944 tokens of a 256-column layer take 256-column tiles."""
     _check(W.scaled(W.STACK_CSA, batch=1), 4096, 256, (100000,), ("proj_chunk",))
     _check(W.Layer("hca", 1, 0, 8, 64, 64, False, 128, 128), 18944, 128, (3,), ("proj_wide",))
+
+
+def test_projection_feeds_single_token_appends_in_stream():
+    """The streams the projection writes are what the compressor reads: one
+    token at a time, projection then append, back to back on one stream with
+    no synchronisation (each kernel may start while the one before it
+    finishes) gives the same cache bytes as the same calls each followed by a
+    device synchronisation."""
+    layer = W.scaled(W.STACK_CSA, batch=2)
+    B, D, Di, d_model, steps = layer.batch, layer.dim, layer.idx_dim, 512, 48
+    h = to_dev(synth.bf16_bits(synth.normal(("chain", "h"), (steps, B, 1, d_model))))
+    w = to_dev(synth.bf16_bits(synth.normal(("chain", "w"), (2 * D + 2 * Di, d_model)) / np.sqrt(d_model)))
+    b = to_dev(synth.position_bias("chain", 0, layer, "b"))
+    bu = to_dev(synth.position_bias("chain", 0, layer, "bu"))
+    desc = dsv4.layer_desc(layer, 64)
+    caches = []
+    for sync in (False, True):
+        cache = dsv4.Cache(desc)
+        x, z = (torch.zeros((B, 1, D), dtype=torch.int16, device="cuda") for _ in range(2))
+        u, zu = (torch.zeros((B, 1, Di), dtype=torch.int16, device="cuda") for _ in range(2))
+        for s in range(steps):
+            dsv4.dsv4_project_streams(desc, cache, 1, d_model, h[s], w, BASE, x, z, u, zu)
+            if sync:
+                torch.cuda.synchronize()
+            dsv4.dsv4_compress_append(desc, cache, 1, x, None, z, b, u, zu, bu)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert dsv4.dsv4_read_status(cache) == 0
+        caches.append(cache)
+    assert int(caches[0].n_tokens[0]) == steps
+    for name, t in vars(caches[1]).items():
+        if isinstance(t, torch.Tensor):
+            assert torch.equal(getattr(caches[0], name), t), name

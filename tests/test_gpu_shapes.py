@@ -166,6 +166,28 @@ def test_append_d512_single_tokens(base):
     _check_stream_cache(layer, cache, n, "app512t1")
 
 
+@pytest.mark.parametrize("base", [W.HCA_128K, W.STACK_HCA], ids=["d128_sep_v", "d512"])
+def test_long_block_chunk_invariance_bytes(base):
+    """Ratio-128 layers pool a chunk's blocks with each block's channels split
+    over a cluster of CTAs, single tokens with one CTA: the caches are
+    byte-identical whatever the chunking (blocks straddling two calls
+    included), for a separate-V 128-dim layer (clusters of 2) and the 448 + 64
+    layer (clusters of 8)."""
+    n = 128 * 9 + 37
+    layer = W.scaled(base, batch=2, n_tokens=n, cache_source="stream")
+    ref = gpu_stream_cache(layer, "lbchunks", 0, n, (4096,))[1]
+    open_slots = n % layer.ratio
+    for chunks in ((1,), (300, 7), (5, 128, 2), (200,)):
+        c = gpu_stream_cache(layer, "lbchunks", 0, n, chunks)[1]
+        assert dsv4.dsv4_read_status(c) == 0
+        for name in ("k_nope", "k_scale", "k_rope", "v_nope", "v_scale", "v_rope", "win_k", "win_v", "n_tokens"):
+            if getattr(ref, name) is not None:
+                assert torch.equal(getattr(ref, name), getattr(c, name)), (chunks, name)
+        for name in ("pend_k", "pend_z", "pend_v"):
+            if getattr(ref, name) is not None:
+                assert torch.equal(getattr(ref, name)[:, :open_slots], getattr(c, name)[:, :open_slots]), (chunks, name)
+
+
 # ----------------------------------------------------------------------------- other declared shapes
 
 
