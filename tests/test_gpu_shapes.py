@@ -173,7 +173,7 @@ def test_long_block_chunk_invariance_bytes(base):
     byte-identical whatever the chunking (blocks straddling two calls
     included), for a separate-V 128-dim layer (clusters of 2) and the 448 + 64
     layer (clusters of 8)."""
-    n = 128 * 9 + 37
+    n = 128 * 5 + 37
     layer = W.scaled(base, batch=2, n_tokens=n, cache_source="stream")
     ref = gpu_stream_cache(layer, "lbchunks", 0, n, (4096,))[1]
     open_slots = n % layer.ratio
