@@ -282,8 +282,10 @@ DSV4_DEV int32_t row_source(const AttnArgs& a, const RowSpace& s, int b, const T
   return static_cast<int32_t>(-2 - (bs * a.span + pos - (a.n_tokens[bs] - a.span)));
 }
 
-using tc::cp_async16;
-using tc::cp_async_commit;
+DSV4_DEV void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+DSV4_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // wait until at most n of this thread's committed groups are pending (n < 4)
 DSV4_DEV void cp_async_wait(int n) {
   switch (n) {

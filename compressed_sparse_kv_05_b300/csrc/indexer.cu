@@ -561,12 +561,23 @@ constexpr int kClMaxCtas = 16;
 constexpr int kClList = kBins / 2;   // list entries (uint2) in the first-level histogram's place
 constexpr int kClRecv = 4096;        // keys of the boundary bin the first CTA receives (uint2)
 
-using tc::cluster_arrive;
-using tc::cluster_ctas;
-using tc::cluster_rank;
-using tc::cluster_sync;
-using tc::cluster_wait;
-using tc::peer_addr;
+DSV4_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+DSV4_DEV uint32_t cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// address of shared variable p in the shared memory of cluster CTA `rank`
+DSV4_DEV uint32_t peer_addr(const void* p, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(rank));
+  return out;
+}
 DSV4_DEV void peer_add(uint32_t addr, uint32_t v) {
   asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -580,6 +591,13 @@ DSV4_DEV uint32_t peer_fetch_add(uint32_t addr, uint32_t v) {
 }
 DSV4_DEV void peer_store2(uint32_t addr, uint2 v) {
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+// cluster-wide barrier (every thread of every CTA), split into its two halves
+DSV4_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+DSV4_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+DSV4_DEV void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
 }
 
 // Add 1 to bin `bin` of the histogram `hist` (shared memory) of every CTA of
