@@ -73,7 +73,15 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compress", action="store_true", help="skip the compressor sub-measurement")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack_1m")
-    return ap.parse_args()
+    ap.add_argument("--compress-tokens", type=int, default=None,
+                    help="tokens of the compressor workload (a multiple of 4096; default 2^20): smaller cases "
+                         "for profiling, named in the line's config")
+    args = ap.parse_args()
+    if args.compress_tokens:
+        if args.compress_tokens % W.COMPRESS_1M_CHUNK:
+            ap.error("--compress-tokens must be a multiple of the 4096-token chunk")
+        W.COMPRESS_1M_TOKENS = args.compress_tokens
+    return args
 
 
 # ----------------------------------------------------------------------------- graphs
