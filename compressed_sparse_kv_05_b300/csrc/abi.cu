@@ -319,10 +319,10 @@ int dsv4_compress_append(const dsv4_layer_desc* d, const dsv4_cache* c, int32_t 
     a.ctas_u = 0;
     PoolShape slice = pk;
     slice.cg = 8;
-    int threads = 8 * pk.G;
-    threads = threads < 64 ? 64 : (threads + 31) / 32 * 32;
+    const int threads = 64 * pk.G / slice_cpt(pk.G);   // 64 to 256
     const size_t smem = static_cast<size_t>(d->ratio) * 64 * (4 + 2 * (d->separate_v ? 3 : 2)) +
-                        pool_part_floats(slice, d->separate_v != 0) * sizeof(float) + 4 * sizeof(uint32_t);
+                        pool_part_floats(slice, d->separate_v != 0) * sizeof(float) + 4 * sizeof(uint32_t) +
+                        128 * sizeof(float);
     static std::once_flag once;
     set_smem_once(once, pool_cluster_kernel, 200 * 1024);
     const int ctas = a.ctas_k + (ctas_w + cs - 1) / cs * cs;

@@ -75,24 +75,11 @@ struct BlockSrc {
   DSV4_DEV uint4 x2(int i, int c0) const { return ld16(row(pend_x2, in_x2, i) + c0); }
 };
 
-// The same rows of one slice of cc channels, copied into shared memory: x, x2
-// (or null), z as [m][cc] bf16 and the position bias as [m][cc] fp32; c0 counts
-// from the slice's first channel.
+// The same rows of one 64-channel slice, copied into shared memory: x, x2 (or
+// null), z as [m][64] bf16 and the position bias as [m][64] fp32.
 struct SmemRows {
   const uint16_t *xs, *x2s, *zs;
   const float* bs;
-  int cc;
-  DSV4_DEV bool two() const { return x2s != nullptr; }
-  DSV4_DEV GateLoad gate(int i, int c0) const {
-    GateLoad g;
-    g.z = *reinterpret_cast<const uint4*>(zs + i * cc + c0);
-    const float4* bp = reinterpret_cast<const float4*>(bs + i * cc + c0);
-    g.b0 = bp[0];
-    g.b1 = bp[1];
-    return g;
-  }
-  DSV4_DEV uint4 x(int i, int c0) const { return *reinterpret_cast<const uint4*>(xs + i * cc + c0); }
-  DSV4_DEV uint4 x2(int i, int c0) const { return *reinterpret_cast<const uint4*>(x2s + i * cc + c0); }
 };
 
 // Softmax-gated pooling of one block by a team (see PoolShape): team thread t
@@ -107,10 +94,10 @@ struct SmemRows {
 // (it holds CTA barriers when G > 1); `active` marks a thread with work.
 // ONE: a group's tokens fit one batch of loads (tpg <= 4), which are then all
 // issued in the first pass and kept in registers for the second. The
-// arithmetic, and so every result bit, is the same whatever the source and
-// batching.
-template <bool TWO, bool ONE, typename Src>
-DSV4_DEV void pool_team_t(const Src& s, PoolShape ps, int m, int t, bool active, float* part, float* y, float* y2) {
+// arithmetic, and so every result bit, is the same whatever the batching.
+template <bool TWO, bool ONE>
+DSV4_DEV void pool_team_t(const BlockSrc& s, PoolShape ps, int m, int t, bool active, float* part, float* y,
+                          float* y2) {
   constexpr int kTokBatch = TWO ? 2 : 4;   // tokens whose loads a thread issues together
   constexpr bool two = TWO;
   const int c8 = t % ps.cg, g = t / ps.cg;
@@ -241,12 +228,112 @@ DSV4_DEV void pool_team_t(const Src& s, PoolShape ps, int m, int t, bool active,
 // (the one-batch form for a single stream only, and where the kernel allows
 // it: with two streams, or in a kernel with other work, it holds too many
 // registers)
-template <bool ALLOW_ONE = true, typename Src>
-DSV4_DEV void pool_team(const Src& s, PoolShape ps, int m, int t, bool active, float* part, float* y, float* y2) {
+template <bool ALLOW_ONE = true>
+DSV4_DEV void pool_team(const BlockSrc& s, PoolShape ps, int m, int t, bool active, float* part, float* y,
+                        float* y2) {
   if (s.two()) pool_team_t<true, false>(s, ps, m, t, active, part, y, y2);
   else if (ALLOW_ONE && ps.tpg <= 4) pool_team_t<false, true>(s, ps, m, t, active, part, y, y2);   // uniform
   else pool_team_t<false, false>(s, ps, m, t, active, part, y, y2);
 }
+
+// n consecutive bf16 (n = 2, 4, 8; 4n-byte aligned) from shared memory as floats
+template <int N>
+DSV4_DEV void lds_bf16(const uint16_t* p, float* f) {
+  if constexpr (N == 2) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    f[0] = __uint_as_float(w << 16); f[1] = __uint_as_float(w & 0xFFFF0000u);
+  } else if constexpr (N == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  } else {
+    bf16x8(*reinterpret_cast<const uint4*>(p), f);
+  }
+}
+
+// Pooling of one block's 64-channel slice from shared memory with the team
+// arithmetic of pool_team_t (G token groups of tpg tokens), the channels dealt
+// CPT to a thread instead of 8, so that more threads share the same work:
+// thread t takes channels [CPT q, CPT q + CPT) and tokens [g tpg, g tpg + tpg),
+// q = t % (64 / CPT), g = t / (64 / CPT). Every operation on a channel is the
+// one pool_team_t performs, in the same order: the same bits. Group 0's
+// threads leave y (and y2) in ys[64] (ys2). `part` holds G * 64 * 3 floats.
+// Every thread of the CTA calls it (CTA barriers when G > 1).
+template <int CPT, bool TWO>
+DSV4_DEV void pool_slice(const SmemRows& s, int G, int tpg, int m, int t, float* part, float* ys, float* ys2) {
+  constexpr int NQ = 64 / CPT;
+  constexpr int S = TWO ? 3 : 2;   // combined sums per channel
+  const int q = t % NQ, g = t / NQ;
+  const bool active = g < G;
+  const int c0 = q * CPT;
+  const int i0 = g * tpg, i1 = i0 + tpg < m ? i0 + tpg : m;
+  float mx[CPT];
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) mx[k] = -INFINITY;
+  if (active)
+    for (int i = i0; i < i1; ++i) {
+      float l[CPT];
+      lds_bf16<CPT>(s.zs + i * 64 + c0, l);
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) mx[k] = fmaxf(mx[k], l[k] + s.bs[i * 64 + c0 + k]);
+    }
+  if (G > 1) {
+    if (active)
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) part[g * 64 + c0 + k] = mx[k];
+    __syncthreads();
+    if (active)
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) mx[k] = fmaxf(mx[k], part[h * 64 + c0 + k]);
+    __syncthreads();
+  }
+  float sum[CPT], acc[CPT], acc2[CPT];
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) sum[k] = acc[k] = acc2[k] = 0.f;
+  if (active)
+    for (int i = i0; i < i1; ++i) {
+      float l[CPT], x[CPT], x2[CPT];
+      lds_bf16<CPT>(s.zs + i * 64 + c0, l);
+      lds_bf16<CPT>(s.xs + i * 64 + c0, x);
+      if (TWO) lds_bf16<CPT>(s.x2s + i * 64 + c0, x2);
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        const float e = expf((l[k] + s.bs[i * 64 + c0 + k]) - mx[k]);
+        sum[k] += e;
+        acc[k] = fmaf(e, x[k], acc[k]);
+        if (TWO) acc2[k] = fmaf(e, x2[k], acc2[k]);
+      }
+    }
+  if (G > 1) {
+    if (active)
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        float* pp = part + (g * 64 + c0 + k) * S;
+        pp[0] = sum[k];
+        pp[1] = acc[k];
+        if (TWO) pp[2] = acc2[k];
+      }
+    __syncthreads();
+    if (active && g == 0)
+      for (int h = 1; h < G; ++h)
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+          const float* pq = part + (h * 64 + c0 + k) * S;
+          sum[k] += pq[0];
+          acc[k] += pq[1];
+          if (TWO) acc2[k] += pq[2];
+        }
+    __syncthreads();
+  }
+  if (active && g == 0)
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      ys[c0 + k] = __fdiv_rn(acc[k], sum[k]);
+      if (TWO) ys2[c0 + k] = __fdiv_rn(acc2[k], sum[k]);
+    }
+}
+
 
 // The FP8 + BF16 entry of a pooled row held by a team's group-0 threads (8
 // channels each, `has` when the thread holds some): scale = amax/448 over the
@@ -433,13 +520,13 @@ __global__ void __launch_bounds__(512) pool_chunk_kernel(AppendArgs a) {
 // [64 r, 64 r + 64). A CTA copies the block's rows of its slice (pending
 // tokens or this call's), gate logits and position bias into shared memory
 // (cp.async, one round trip), pools them with the team arithmetic of every
-// other pooling kernel (8 channel groups x G token groups: the same bits), and
-// the cluster combines the FP8 scale's amax in distributed shared memory
-// before each CTA writes its dims of the entry. CTAs past ctas_k (whole
-// clusters) write the window ring as pool_chunk_kernel does. Dynamic shared
-// memory: bias [m][64] fp32, z, x (, v) [m][64] bf16, the team's combine
-// buffer, four words (the cluster's amax of K and V, which the peers raise;
-// this CTA's).
+// other pooling kernel (G token groups; 64 / CPT x G threads, CPT channels a
+// thread: pool_slice, the same bits), and the cluster combines the FP8
+// scale's amax in distributed shared memory before each CTA writes its dims
+// of the entry. CTAs past ctas_k (whole clusters) write the window ring as
+// pool_chunk_kernel does. Dynamic shared memory: bias [m][64] fp32, z, x (, v)
+// [m][64] bf16, the combine buffer, four words (the cluster's amax of K and V,
+// which the peers raise; this CTA's), the pooled slice (K, V) [2][64] fp32.
 __global__ void __launch_bounds__(256, 1) pool_cluster_kernel(AppendArgs a) {
   extern __shared__ __align__(16) unsigned char csm[];
   const int D = a.d_nope + a.d_rope;
@@ -520,12 +607,27 @@ __global__ void __launch_bounds__(256, 1) pool_cluster_kernel(AppendArgs a) {
   tc::cp_async_wait_all();
   __syncthreads();
   SmemRows rows;
-  rows.xs = x_s; rows.x2s = two ? x2_s : nullptr; rows.zs = z_s; rows.bs = bias_s; rows.cc = 64;
+  rows.xs = x_s; rows.x2s = two ? x2_s : nullptr; rows.zs = z_s; rows.bs = bias_s;
   const int t = threadIdx.x;
-  const bool active = t < 8 * ps.G;
+  float* ys = reinterpret_cast<float*>(words + 4);   // the pooled slice [64] (and V's [64])
+  switch (slice_cpt(ps.G) * (two ? -1 : 1)) {       // uniform across the CTA
+    case 2: pool_slice<2, false>(rows, ps.G, ps.tpg, m, t, part, ys, ys + 64); break;
+    case 4: pool_slice<4, false>(rows, ps.G, ps.tpg, m, t, part, ys, ys + 64); break;
+    case 8: pool_slice<8, false>(rows, ps.G, ps.tpg, m, t, part, ys, ys + 64); break;
+    case -2: pool_slice<2, true>(rows, ps.G, ps.tpg, m, t, part, ys, ys + 64); break;
+    case -4: pool_slice<4, true>(rows, ps.G, ps.tpg, m, t, part, ys, ys + 64); break;
+    default: pool_slice<8, true>(rows, ps.G, ps.tpg, m, t, part, ys, ys + 64); break;
+  }
+  __syncthreads();
+  // the entry's dims, 8 to a thread as every other pooling kernel writes them
+  const bool has = t < 8;
   float y[8] = {}, y2[8] = {};
-  pool_team(rows, ps, m, t, active, part, y, y2);
-  const bool has = active && t < 8;
+  if (has)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      y[k] = ys[8 * t + k];
+      y2[k] = ys[64 + 8 * t + k];
+    }
   const int c8 = cbase / 8 + t;   // the thread's channel group in the row
   if (has && 8 * c8 < a.d_nope) {
     atomicMax(&words[2], __float_as_uint(entry_amax(y, has, c8, a.d_nope)));

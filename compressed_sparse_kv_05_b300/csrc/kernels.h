@@ -55,6 +55,10 @@ __host__ __device__ inline PoolShape pool_shape(int m, int C) {
   p.tpg = (m + G - 1) / G;
   return p;
 }
+// channels a thread takes when a 64-channel slice of a block with G token
+// groups is pooled from shared memory (pool_cluster_kernel): 64 / CPT x G
+// threads, at most 256
+__host__ __device__ inline int slice_cpt(int G) { return G <= 8 ? 2 : (G <= 16 ? 4 : 8); }
 // shared-memory floats a team needs to combine its token groups (0 when G == 1)
 __host__ __device__ inline int pool_part_floats(PoolShape p, bool two) {
   return p.G > 1 ? p.G * p.cg * (two ? 24 : 16) : 0;
