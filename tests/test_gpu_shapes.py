@@ -188,6 +188,40 @@ def test_long_block_chunk_invariance_bytes(base):
                 assert torch.equal(getattr(ref, name)[:, :open_slots], getattr(c, name)[:, :open_slots]), (chunks, name)
 
 
+@pytest.mark.parametrize("ratio,sep", [(16, True), (256, False)], ids=["ratio16_sep_v", "ratio256"])
+def test_long_block_other_token_groups(ratio, sep):
+    """The clustered pooling at its other team shapes: 2 token groups at ratio
+    16 (2 channels a thread, separate V) and 32 at ratio 256 (8 channels a
+    thread), 128-dim entries (clusters of 2): chunked appends whose blocks
+    straddle calls against the oracle, and byte-identical to single-token
+    appends."""
+    n = ratio * 6 + 5
+    layer = W.Layer("hca", 2, n, 8, 64, 64, sep, ratio, 128)
+    desc, cache = gpu_stream_cache(layer, "lbgroups", 0, n, (2 * ratio + 3,))
+    assert dsv4.dsv4_read_status(cache) == 0
+    _check_stream_cache(layer, cache, n, "lbgroups")
+    one = gpu_stream_cache(layer, "lbgroups", 0, n, (1,))[1]
+    for name in ("k_nope", "k_scale", "k_rope", "v_nope", "v_scale", "v_rope", "win_k", "win_v", "n_tokens"):
+        if getattr(cache, name) is not None:
+            assert torch.equal(getattr(cache, name), getattr(one, name)), name
+
+
+def test_long_block_capacity_overflow_sets_status_and_changes_nothing():
+    """A chunk that would complete more ratio-128 blocks than the cache holds
+    (the clustered path) sets the capacity bit and writes nothing."""
+    layer = W.scaled(W.STACK_HCA, batch=2, n_tokens=256, cache_source="stream")
+    desc, cache = gpu_stream_cache(layer, "lbcap", 0, 256, (256,), capacity=3)
+    assert dsv4.dsv4_read_status(cache) == 0
+    before = {n: getattr(cache, n).clone() for n in ("k_nope", "k_scale", "k_rope", "n_tokens", "win_k", "pend_k")}
+    toks = {k: to_dev(v) for k, v in synth.token_stream("lbcap", 0, layer, 2, 256, 512).items()}
+    b = to_dev(synth.position_bias("lbcap", 0, layer, "b"))
+    dsv4.dsv4_compress_append(desc, cache, 256, toks["k"], None, toks["z"], b)
+    assert dsv4.dsv4_read_status(cache) == dsv4.STATUS_CAPACITY
+    for n_, t in before.items():
+        assert torch.equal(t, getattr(cache, n_)), n_
+    assert dsv4.dsv4_read_status(cache) == 0
+
+
 # ----------------------------------------------------------------------------- other declared shapes
 
 
