@@ -10,14 +10,16 @@
 // sliding window is a ring of window_size tokens overwritten cyclically.
 //
 // Per block j and channel c: y[c] = sum_i e_i x_i / sum_i e_i with
-// e_i = exp(z_i + b_i - max_i(z_i + b_i)), in fp32, shared out among a team of
-// threads the same way in every kernel (see pool_team). An append of T > 1
-// tokens is two kernels on the caller's stream: pool_chunk_kernel reads the
-// old pending tokens and the new tokens of every block this call completes and
-// writes its entry; append_tail_kernel then writes the window ring and the new
-// pending tokens and advances n_tokens. Splitting them keeps the pending reads
-// of the first kernel ahead of the pending writes of the second. A single
-// token is one kernel (append_one_kernel).
+// e_i = exp(z_i + b_i - max_i(z_i + b_i)), in fp32, split into the same token
+// groups and summed in the same order in every kernel (pool_team, pool_slice),
+// so a block's bits do not depend on how its tokens arrived. An append of T > 1
+// tokens is two kernels on the caller's stream: pool_chunk_kernel (or, for
+// long blocks, pool_cluster_kernel) reads the old pending tokens and the new
+// tokens of every block this call completes, writes its entry and writes the
+// window ring; append_tail_kernel then writes the new pending tokens and
+// advances n_tokens. Splitting them keeps the pending reads of the first
+// kernel ahead of the pending writes of the second. A single token is one
+// kernel (append_one_kernel).
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
