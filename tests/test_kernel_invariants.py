@@ -1,7 +1,8 @@
-"""Index arithmetic the tensor-core attention kernel relies on, checked on the host.
+"""Index arithmetic the kernels rely on, checked on the host.
 
-These are properties of the kernel's own layouts (compressed_sparse_kv_05_b300/csrc/
-attention_tc.cu), not of the method: the constants below restate that file's.
+These are properties of the kernels' own layouts (compressed_sparse_kv_05_b300/csrc/
+attention_tc.cu, and compress.cu's clustered pooling), not of the method: the
+constants and shape rules below restate those files' (and kernels.h's).
 """
 import math
 
@@ -47,3 +48,56 @@ def test_code_chunk_dequantisation_is_warp_local(rc):
     for byte, ws in writers.items():
         assert len(ws) == 1
         assert readers.get(byte, set()) <= ws
+
+
+# ----------------------------------------------------------------------------- clustered pooling
+
+
+def _pool_shape(m, C):
+    """kernels.h pool_shape: channel groups of 8, up to 512 threads a team."""
+    cg = C // 8
+    G = (m + 7) // 8
+    gmax = 512 // cg if cg <= 512 else 1
+    G = max(1, min(G, gmax))
+    return cg, G, -(-m // G)
+
+
+def _slice_cpt(G):
+    return 2 if G <= 8 else (4 if G <= 16 else 8)
+
+
+@pytest.mark.parametrize("D", range(64, 513, 64))
+@pytest.mark.parametrize("two", [False, True])
+def test_cluster_pooling_fits_and_covers(D, two):
+    """For every ratio the clustered pooling takes (9..256) and every D it takes
+    (multiples of 64 up to 512): the CTA has 64 to 256 threads;
+    its shared memory (bias, z, x (, v), the combine buffer, four words, the
+    pooled slice) fits the 200 KB the launch allows; pool_slice's threads cover
+    every (channel, token group) of the 64-channel slice exactly once; the
+    combine buffer's largest index is inside its G x 8 x (16 | 24) floats; the
+    token groups tile [0, ratio); cp.async sources stay 16-byte aligned."""
+    S = 3 if two else 2
+    for m in range(9, 257):
+        _, G, tpg = _pool_shape(m, D)
+        cpt = _slice_cpt(G)
+        threads = 64 * G // cpt
+        assert 64 <= threads <= 256 and 64 * G % cpt == 0, (m, G)
+        part = G * 8 * (24 if two else 16)
+        smem = m * 64 * (4 + 2 * (3 if two else 2)) + part * 4 + 4 * 4 + 128 * 4
+        assert smem <= 200 * 1024, (m, smem)
+        seen = set()
+        top = -1
+        for t in range(threads):
+            q, g = t % (64 // cpt), t // (64 // cpt)
+            assert g < G
+            for k in range(cpt):
+                c = q * cpt + k
+                assert (c, g) not in seen
+                seen.add((c, g))
+                top = max(top, (g * 64 + c) * S + S - 1)
+        assert len(seen) == 64 * G
+        assert top < part
+        toks = [i for g in range(G) for i in range(g * tpg, min(g * tpg + tpg, m))]
+        assert toks == list(range(m))
+        assert (D * 2) % 16 == 0 and (64 * 2) % 16 == 0 and (D * 4) % 16 == 0
+
