@@ -188,15 +188,16 @@ def test_long_block_chunk_invariance_bytes(base):
                 assert torch.equal(getattr(ref, name)[:, :open_slots], getattr(c, name)[:, :open_slots]), (chunks, name)
 
 
-@pytest.mark.parametrize("ratio,sep", [(16, True), (256, False)], ids=["ratio16_sep_v", "ratio256"])
-def test_long_block_other_token_groups(ratio, sep):
+@pytest.mark.parametrize("ratio,sep,d_nope", [(16, True, 64), (256, False, 64), (128, False, 128), (64, True, 256)],
+                         ids=["ratio16_sep_v", "ratio256", "d192_cs3", "d320_cs5_sep_v"])
+def test_long_block_other_token_groups(ratio, sep, d_nope):
     """The clustered pooling at its other team shapes: 2 token groups at ratio
     16 (2 channels a thread, separate V) and 32 at ratio 256 (8 channels a
-    thread), 128-dim entries (clusters of 2): chunked appends whose blocks
-    straddle calls against the oracle, and byte-identical to single-token
-    appends."""
+    thread) with 128-dim entries (clusters of 2), and clusters of 3 and 5 CTAs
+    (192- and 320-dim entries): chunked appends whose blocks straddle calls
+    against the oracle, and byte-identical to single-token appends."""
     n = ratio * 6 + 5
-    layer = W.Layer("hca", 2, n, 8, 64, 64, sep, ratio, 128)
+    layer = W.Layer("hca", 2, n, 8, d_nope, 64, sep, ratio, 128)
     desc, cache = gpu_stream_cache(layer, "lbgroups", 0, n, (2 * ratio + 3,))
     assert dsv4.dsv4_read_status(cache) == 0
     _check_stream_cache(layer, cache, n, "lbgroups")
