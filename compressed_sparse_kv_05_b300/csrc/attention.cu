@@ -367,8 +367,6 @@ __global__ void __launch_bounds__(256, KS <= 8 ? 4 : 2) attn_merge_tc_kernel(Att
 }
 
 namespace {
-int launch_status() { return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA; }
-
 template <int HP, int ACC>
 int launch_split(const AttnArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
   static std::once_flag flag;
